@@ -1,0 +1,292 @@
+"""Plain fp64 CPU oracle for kernelized linear attention.
+
+TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the
+benchmark's CPU-baseline leg may import or run this module.  It shares no code
+with the CUDA library and the library never calls it.
+
+Everything is computed in float64 with numpy, straight from the definitions on
+the source pages, one sequence and one head at a time:
+
+* feature maps: identity and ELU+1 ("The Kernel Zoo", running example and
+  §2.5 table; "Linear attention & kernelized approximations", item 2) and the
+  FAVOR+ positive random features phi+(x) = exp(Omega x - |x|^2/2)/sqrt(m)
+  ("The Kernel Zoo", §4.2 boxed map and §5.4; "Performer", §2 Step 3 and the
+  §3 sketch);
+* orthogonal random features by Gram-Schmidt on Gaussian blocks, rows scaled
+  to Gaussian (chi) lengths ("The Kernel Zoo", §5.1 and §5.3 Steps 1-4;
+  "Performer", §2 Step 4);
+* bidirectional attention S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j),
+  out_i = phi(q_i)^T S / max(phi(q_i)^T z, eps) ("Reassociate a feature-map
+  kernel", ¶1-2; "Performer", §2 Step 5 and §3 sketch, whose denominator is
+  clamped from below at 1e-6);
+* causal attention by the prefix recurrence S_i = S_{i-1} + phi(k_i) v_i^T,
+  z_i = z_{i-1} + phi(k_i), with the diagonal included ("The Kernel Zoo",
+  §1.3 and §5.4; "Reassociate a feature-map kernel", ¶4), with the state reset
+  at every packed-sequence boundary (same paragraph);
+* the quadratic rescan form, for cross-checks on tiny inputs ("Linear
+  attention & kernelized approximations", "The naive way").
+
+Every function here is pinned by tests against values the pages print,
+closed forms or brute force (see tests/test_oracle_pins.py).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MAPS = ("identity", "elu1", "favor")
+
+
+# ----------------------------------------------------------------------------
+# Feature maps
+# ----------------------------------------------------------------------------
+def feature_map(x, kind: str, omega=None) -> np.ndarray:
+    """phi(x) over the last axis, in float64.
+
+    identity: phi(x) = x                      ("The Kernel Zoo", §1.3, FWP baseline)
+    elu1:     phi(x) = elu(x) + 1 = x + 1 for x > 0, exp(x) for x <= 0
+              (ELU with alpha = 1; "The Kernel Zoo", running example)
+    favor:    phi(x) = exp(omega x - |x|^2 / 2) / sqrt(m), omega of shape [m, d]
+              ("The Kernel Zoo", §4.2 boxed feature map)
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if kind == "identity":
+        return x.copy()
+    if kind == "elu1":
+        return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+    if kind == "favor":
+        if omega is None:
+            raise ValueError("favor map needs omega")
+        om = np.asarray(omega, dtype=np.float64)
+        m = om.shape[0]
+        proj = x @ om.T                                    # omega_i^T x for every i
+        half_sq = 0.5 * np.sum(x * x, axis=-1, keepdims=True)   # |x|^2 / 2
+        return np.exp(proj - half_sq) / np.sqrt(m)
+    raise ValueError(f"unknown feature map {kind!r}")
+
+
+def feature_dim(kind: str, d: int, omega=None) -> int:
+    return int(np.asarray(omega).shape[0]) if kind == "favor" else d
+
+
+# ----------------------------------------------------------------------------
+# Orthogonal random features
+# ----------------------------------------------------------------------------
+def gram_schmidt(rows) -> np.ndarray:
+    """Orthonormalise the rows of one or a batch of square blocks, in order.
+
+    Row i has its components along the already finished rows 0..i-1 removed
+    (the projection step of "The Kernel Zoo" §5.3 Step 2) and is then scaled
+    to unit length (Steps 1 and 3).  The removal is applied twice, which
+    leaves the exact-arithmetic result unchanged and keeps fp64 rounding from
+    eroding orthogonality for ill-conditioned Gaussian draws.
+    """
+    Q = np.array(rows, dtype=np.float64, copy=True)
+    squeeze = Q.ndim == 2
+    if squeeze:
+        Q = Q[None]
+    n = Q.shape[1]
+    for i in range(n):
+        row = Q[:, i, :]
+        if i > 0:
+            prev = Q[:, :i, :]
+            for _ in range(2):
+                coef = prev @ row[:, :, None]                  # [b, i, 1]: q_j . row
+                row = row - (coef.transpose(0, 2, 1) @ prev)[:, 0, :]
+        row = row / np.linalg.norm(row, axis=-1, keepdims=True)
+        Q[:, i, :] = row
+    return Q[0] if squeeze else Q
+
+
+def orthogonal_random_features(blocks, norm_vectors=None, r=None, norm: str = "chi") -> np.ndarray:
+    """Orthogonal random projection matrix Omega of shape [r, d].
+
+    blocks: [nb, d, d] iid N(0,1).  Each block's rows are orthonormalised by
+    Gram-Schmidt ("The Kernel Zoo" §5.1: m <= d orthogonal rows per draw);
+    the blocks are stacked and the first r rows kept (r > d is reached by
+    stacking independent orthogonal blocks).
+    norm = "chi":   row i is scaled to |norm_vectors[i]|, the length of a
+                    fresh N(0, I_d) vector, so every row has the length
+                    distribution of a Gaussian vector ("Performer" §2 Step 4).
+    norm = "sqrt_d": every row scaled to sqrt(d) ("The Kernel Zoo" §5.3 Step 4).
+    """
+    B = np.asarray(blocks, dtype=np.float64)
+    if B.ndim == 2:
+        B = B[None]
+    nb, d, d2 = B.shape
+    assert d == d2
+    if r is None:
+        r = nb * d if norm_vectors is None else np.asarray(norm_vectors).shape[0]
+    Q = gram_schmidt(B).reshape(nb * d, d)[:r]
+    if norm == "chi":
+        lengths = np.linalg.norm(np.asarray(norm_vectors, dtype=np.float64)[:r], axis=-1)
+    elif norm == "sqrt_d":
+        lengths = np.full(r, np.sqrt(d))
+    else:
+        raise ValueError(norm)
+    return Q * lengths[:, None]
+
+
+# ----------------------------------------------------------------------------
+# Attention
+# ----------------------------------------------------------------------------
+def _bounds(cu_seqlens, T):
+    if cu_seqlens is None:
+        return [0, T]
+    cu = [int(c) for c in np.asarray(cu_seqlens).ravel()]
+    if cu[0] != 0 or cu[-1] != T or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0, end at T and not decrease")
+    return cu
+
+
+def normalise(num, den, eps: float, eps_mode: str = "clamp"):
+    """out = num / max(den, eps) (clamp, as the "Performer" §3 sketch does).
+
+    eps_mode "add" gives num / (den + eps) and "none" returns the numerator
+    alone (the unnormalised fast-weight output of "The Kernel Zoo" §1.2).
+    """
+    num = np.asarray(num, dtype=np.float64)
+    den = np.asarray(den, dtype=np.float64)
+    if eps_mode == "none":
+        return num
+    if eps_mode == "clamp":
+        d = np.maximum(den, eps)
+    elif eps_mode == "add":
+        d = den + eps
+    else:
+        raise ValueError(eps_mode)
+    return num / d[..., None]
+
+
+def bidir(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
+          return_parts=False):
+    """Bidirectional kernelized attention over packed sequences.
+
+    q, k: [T, H, dk]; v: [T, H, dv].  For each sequence and head:
+    S = Phi_K^T V, z = Phi_K^T 1, num = Phi_Q S, den = Phi_Q z,
+    out = num / max(den, eps)   ("Performer" §2 Step 5 and §3 sketch;
+    "Linear attention & kernelized approximations", "Build the state once").
+    Returns out [T, H, dv] (and num, den, per-(sequence, head) S and z).
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    T, H, _ = q.shape
+    dv = v.shape[2]
+    cu = _bounds(cu_seqlens, T)
+    num = np.zeros((T, H, dv)); den = np.zeros((T, H))
+    states = {}
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        for h in range(H):
+            pq = feature_map(q[a:b, h], kind, omega)
+            pk = feature_map(k[a:b, h], kind, omega)
+            S = pk.T @ v[a:b, h]          # sum_j phi(k_j) v_j^T   [r, dv]
+            z = pk.sum(axis=0)            # sum_j phi(k_j)         [r]
+            num[a:b, h] = pq @ S
+            den[a:b, h] = pq @ z
+            states[(s, h)] = (S, z)
+    out = normalise(num, den, eps, eps_mode)
+    if return_parts:
+        return out, num, den, states
+    return out
+
+
+def causal(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
+           return_parts=False):
+    """Causal kernelized attention by the prefix recurrence, token by token.
+
+    For each sequence and head, starting from S = 0, z = 0 at the sequence's
+    first token:  S += phi(k_i) v_i^T;  z += phi(k_i);  num_i = phi(q_i)^T S;
+    den_i = phi(q_i)^T z; out_i = num_i / max(den_i, eps).  Key i is added
+    before query i reads the state (inclusive prefix, "The Kernel Zoo" §1.3
+    sum over j = 1..i; "Reassociate a feature-map kernel" ¶4).
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    T, H, _ = q.shape
+    dv = v.shape[2]
+    cu = _bounds(cu_seqlens, T)
+    num = np.zeros((T, H, dv)); den = np.zeros((T, H))
+    finals = {}
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        for h in range(H):
+            pq = feature_map(q[a:b, h], kind, omega)   # phi acts on one token at a time
+            pk = feature_map(k[a:b, h], kind, omega)
+            r = pk.shape[1]
+            S = np.zeros((r, dv)); z = np.zeros(r)
+            for i in range(b - a):
+                S += np.outer(pk[i], v[a + i, h])
+                z += pk[i]
+                num[a + i, h] = pq[i] @ S
+                den[a + i, h] = pq[i] @ z
+            finals[(s, h)] = (S.copy(), z.copy())
+    out = normalise(num, den, eps, eps_mode)
+    if return_parts:
+        return out, num, den, finals
+    return out
+
+
+def rescan(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
+           causal_mask=True):
+    """Quadratic form: every query rescans its keys ("Linear attention &
+    kernelized approximations", "The naive way: rescan every key").
+
+    out_i = sum_j w_ij v_j / max(sum_j w_ij, eps), w_ij = phi(q_i) . phi(k_j),
+    j over the whole sequence (bidirectional) or j <= i (causal).
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    T, H, _ = q.shape
+    dv = v.shape[2]
+    cu = _bounds(cu_seqlens, T)
+    num = np.zeros((T, H, dv)); den = np.zeros((T, H))
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        for h in range(H):
+            pq = feature_map(q[a:b, h], kind, omega)
+            pk = feature_map(k[a:b, h], kind, omega)
+            for i in range(b - a):
+                last = i + 1 if causal_mask else b - a
+                w = np.array([pq[i] @ pk[j] for j in range(last)])
+                num[a + i, h] = w @ v[a:a + last, h]
+                den[a + i, h] = w.sum()
+    return normalise(num, den, eps, eps_mode)
+
+
+def causal_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp"):
+    """Causal outputs of selected rows of one sequence [start, end) and head.
+
+    Each requested row i gets S_i = sum_{start <= j <= i} phi(k_j) v_j^T and
+    z_i = sum phi(k_j) computed directly from its definition, so single rows of
+    very long sequences can be checked without running the whole recurrence.
+    Returns an array [len(rows), dv].
+    """
+    kk = np.asarray(k[start:end, head], np.float64)
+    vv = np.asarray(v[start:end, head], np.float64)
+    pk = feature_map(kk, kind, omega)
+    outs = []
+    for i in rows:
+        j = int(i) - start
+        assert 0 <= j < end - start
+        S = pk[: j + 1].T @ vv[: j + 1]
+        z = pk[: j + 1].sum(axis=0)
+        pq = feature_map(np.asarray(q[int(i), head], np.float64), kind, omega)
+        outs.append(normalise(pq @ S, np.asarray(pq @ z), eps, eps_mode))
+    return np.array(outs)
+
+
+def bidir_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp"):
+    """Bidirectional outputs of selected rows of one sequence and head."""
+    pk = feature_map(np.asarray(k[start:end, head], np.float64), kind, omega)
+    S = pk.T @ np.asarray(v[start:end, head], np.float64)
+    z = pk.sum(axis=0)
+    pq = feature_map(np.asarray(q[np.asarray(rows, int), head], np.float64), kind, omega)
+    return normalise(pq @ S, pq @ z, eps, eps_mode)
+
+
+def forward(q, k, v, kind, causal_form, omega=None, cu_seqlens=None, eps=1e-6):
+    """Dispatch to the bidirectional or causal oracle."""
+    f = causal if causal_form else bidir
+    return f(q, k, v, kind, omega=omega, cu_seqlens=cu_seqlens, eps=eps)
+
+
+def softmax_kernel_estimate(x, y, omega):
+    """phi+(x)^T phi+(y), the FAVOR+ estimate of exp(x^T y) ("The Kernel Zoo" §4.2)."""
+    return float(feature_map(x, "favor", omega) @ feature_map(y, "favor", omega))

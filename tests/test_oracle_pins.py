@@ -1,0 +1,309 @@
+"""Pins of the fp64 oracle against what the source pages and mathematics fix.
+
+Each test checks the oracle against something other than itself: values the
+pages print for their worked examples (tests/golden/, each citing its
+passage), closed forms, library routines, invariants and brute force.  The
+pins are chosen so that a plausible slip (a dropped 1/sqrt(m), a sign in the
+|x|^2/2 term, a transposed projection, an exclusive prefix, a missed state
+reset, add-eps instead of clamp) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+
+def _one_head(a):
+    """[n, d] -> [n, 1, d]"""
+    return np.asarray(a, np.float64)[:, None, :]
+
+
+# ----------------------------------------------------------------------------
+# Worked examples printed on the pages
+# ----------------------------------------------------------------------------
+def test_identity_bidir_worked_example(golden):
+    g = golden("identity_bidir_worked_example.txt")
+    K = g["k"]
+    v = g["v"].reshape(4, 1)
+    q = np.zeros((4, 2)); q[0] = g["q0"]
+    out, num, den, states = oracle.bidir(_one_head(q), _one_head(K), _one_head(v), "identity",
+                                         return_parts=True)
+    S, z = states[(0, 0)]
+    assert np.allclose(S[:, 0], g["s"], atol=g["tol"], rtol=0)
+    assert np.allclose(z, g["z"], atol=g["tol"], rtol=0)
+    assert abs(num[0, 0, 0] - g["num"]) <= g["tol"]
+    assert abs(den[0, 0] - g["den"]) <= g["tol"]
+    assert abs(out[0, 0, 0] - g["out"]) <= g["tol"]
+    # the naive rescan gives the same number
+    scores = K @ g["q0"]
+    assert np.allclose(scores, g["scores"], atol=0)
+    resc = oracle.rescan(_one_head(q), _one_head(K), _one_head(v), "identity", causal_mask=False)
+    assert abs(resc[0, 0, 0] - g["out"]) <= g["tol"]
+
+
+def test_elu1_maps_of_running_example(golden):
+    g = golden("elu_running_example.txt")
+    assert np.array_equal(oracle.feature_map(g["Q"], "elu1"), g["phiQ"])
+    assert np.array_equal(oracle.feature_map(g["K"], "elu1"), g["phiK"])
+
+
+def test_elu1_causal_state_retrieval_and_o4(golden):
+    g = golden("elu_running_example.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    # state after two causal steps
+    _, _, _, finals = oracle.causal(Q[:2], K[:2], V[:2], "elu1", return_parts=True)
+    S2, z2 = finals[(0, 0)]
+    assert np.allclose(S2, g["S2"], atol=g["tol_exact"], rtol=0)
+    retrieved = S2.T @ g["phiK"][0]
+    assert np.allclose(retrieved, g["retrieve_k1"], atol=g["tol_exact"], rtol=0)
+    assert np.allclose(retrieved / retrieved.sum(), g["retrieve_k1_normalised"],
+                       atol=g["tol_printed"], rtol=0)
+    out = oracle.causal(Q, K, V, "elu1")
+    assert np.allclose(out[3, 0], [25 / 26, 15 / 26], atol=g["tol_exact"], rtol=0)
+    assert np.allclose(out[3, 0], g["o4"], atol=g["tol_printed"], rtol=0)
+
+
+def test_fast_weight_programmer_trace(golden):
+    g = golden("fwp_identity_trace.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    y, _, _, finals = oracle.causal(Q, K, V, "identity", eps_mode="none", return_parts=True)
+    assert np.allclose(y[:, 0], g["y"], atol=g["tol"], rtol=0)
+    S4, _ = finals[(0, 0)]
+    assert np.allclose(S4.T, g["W4"], atol=g["tol"], rtol=0)
+
+
+def test_identity_causal_zero_denominator_gives_zero(golden):
+    # token 1 of the running example: q1 . k1 = 0 and the numerator is 0 too.
+    g = golden("fwp_identity_trace.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    out = oracle.causal(Q, K, V, "identity", eps=1e-6)
+    expect = np.array([[0, 0], [1, 0], [0.75, 0.75], [0.5, 1.0]])
+    assert np.allclose(out[:, 0], expect, atol=1e-12, rtol=0)
+
+
+def test_negative_denominator_is_clamped_not_shifted():
+    # "Performer" §3 sketch clamps the denominator from below at 1e-6; adding
+    # eps would give a very different number for a negative identity-map score.
+    q = _one_head([[1.0, 0.0]]); k = _one_head([[-1.0, 0.0]]); v = _one_head([[2.0]])
+    clamp = oracle.bidir(q, k, v, "identity", eps=1e-6)
+    add = oracle.bidir(q, k, v, "identity", eps=1e-6, eps_mode="add")
+    assert clamp[0, 0, 0] == pytest.approx(-2.0 / 1e-6, rel=1e-12)
+    assert add[0, 0, 0] == pytest.approx(-2.0 / (-1.0 + 1e-6), rel=1e-12)
+
+
+def test_favor_m4_worked_example(golden):
+    g = golden("favor_m4_worked_example.txt")
+    om = g["omega"]
+    pq1 = oracle.feature_map(g["q1"], "favor", om)
+    pk1 = oracle.feature_map(g["k1"], "favor", om)
+    pk2 = oracle.feature_map(g["k2"], "favor", om)
+    # exact: exp(-1/2) * exp(1/2) / sqrt(4)
+    assert pq1[0] == pytest.approx(0.5, abs=1e-15)
+    assert np.allclose(pq1, g["phi_q1"], atol=g["tol"], rtol=0)
+    assert np.allclose(pk1, g["phi_k1"], atol=g["tol"], rtol=0)
+    assert np.array_equal(pk2, pq1)
+    assert abs(pq1 @ pk1 - g["dot_q1_k1"]) <= g["tol"]
+    assert abs(pq1 @ pk2 - g["dot_q1_k2"]) <= g["tol"]
+    assert np.all(pq1 > 0) and np.all(pk1 > 0)
+
+
+def test_orf_gram_schmidt_worked_example(golden):
+    g = golden("orf_gram_schmidt_worked_example.txt")
+    om = oracle.orthogonal_random_features(g["omega_raw"][None], norm="sqrt_d")
+    assert np.allclose(om, g["omega_ort"], atol=g["tol"], rtol=0)
+    assert abs(om[0] @ om[1]) < 1e-14
+    assert np.allclose(np.linalg.norm(om, axis=1), math.sqrt(2), atol=1e-14)
+    phi = oracle.feature_map(g["q1"], "favor", om)
+    assert np.allclose(phi, g["phi_ort_q1"], atol=g["tol"], rtol=0)
+
+
+# ----------------------------------------------------------------------------
+# Closed forms, library routines, invariants
+# ----------------------------------------------------------------------------
+def test_elu1_matches_library_elu_plus_one():
+    torch = pytest.importorskip("torch")
+    x = np.linspace(-12, 6, 2001)
+    ref = (torch.nn.functional.elu(torch.tensor(x, dtype=torch.float64), alpha=1.0) + 1).numpy()
+    # elu(x) + 1 = (exp(x) - 1) + 1 cancels for x << 0: absolute error ~ 2^-53
+    assert np.allclose(oracle.feature_map(x, "elu1"), ref, rtol=1e-15, atol=4e-16)
+    assert oracle.feature_map(np.array([-1.0]), "elu1")[0] == pytest.approx(math.exp(-1), rel=1e-15)
+
+
+def test_identity_map_is_identity():
+    x = np.random.default_rng(0).standard_normal((5, 7))
+    assert np.array_equal(oracle.feature_map(x, "identity"), x)
+
+
+def test_feature_maps_are_positive():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((200, 64)) * 2
+    om = rng.standard_normal((256, 64))
+    assert np.all(oracle.feature_map(x, "elu1") > 0)
+    assert np.all(oracle.feature_map(x * 0.3, "favor", om) > 0)
+
+
+def _chi_orf_batch(rng, nbatch, r, d):
+    nb = -(-r // d)
+    blocks = rng.standard_normal((nbatch, nb, d, d))
+    norms = np.linalg.norm(rng.standard_normal((nbatch, r, d)), axis=-1)
+    Q = oracle.gram_schmidt(blocks.reshape(nbatch * nb, d, d)).reshape(nbatch, nb * d, d)[:, :r]
+    return Q * norms[..., None]
+
+
+@pytest.mark.parametrize("xy", [0.5, -0.4])
+def test_lemma1_monte_carlo_unbiased_with_chi_orf(xy):
+    """Mean over 10^4 independent chi-norm orthogonal draws (d=64, r=256) of
+    phi+(x)^T phi+(y) matches exp(x^T y) within 3 standard errors
+    ("The Kernel Zoo" §4.1 Lemma 1; "Performer" §2 Steps 3-4)."""
+    d, r, nseeds = 64, 256, 10_000
+    rng = np.random.default_rng(12345)
+    x = rng.standard_normal(d); x /= np.linalg.norm(x)
+    w = rng.standard_normal(d); w -= (w @ x) * x; w /= np.linalg.norm(w)
+    y = xy * x + math.sqrt(1 - xy * xy) * w            # |x| = |y| = 1, x^T y = xy
+    est = []
+    for _ in range(nseeds // 500):
+        om = _chi_orf_batch(rng, 500, r, d)
+        px = np.exp(om @ x - 0.5 * x @ x) / math.sqrt(r)
+        py = np.exp(om @ y - 0.5 * y @ y) / math.sqrt(r)
+        est.append(np.sum(px * py, axis=-1))
+    est = np.concatenate(est)
+    se = est.std(ddof=1) / math.sqrt(len(est))
+    assert abs(est.mean() - math.exp(xy)) <= 3 * se
+    # and the oracle's own feature map gives the same estimate on one draw
+    om = _chi_orf_batch(rng, 1, r, d)[0]
+    direct = np.exp(om @ x - 0.5) / 16 @ (np.exp(om @ y - 0.5) / 16)
+    assert oracle.softmax_kernel_estimate(x, y, om) == pytest.approx(direct, rel=1e-12)
+
+
+def test_lemma2_iid_positive_estimator_variance():
+    """Variance of the i.i.d. positive estimator with m features equals
+    SM(x,y)^2 (exp(|x+y|^2) - 1) / m, derived from the Gaussian moment
+    generating function used in "The Kernel Zoo" §4.1 (the same quantity as
+    §4.4's positive-MSE line, whose last factor is printed with x - y)."""
+    d, m, n = 8, 16, 40_000
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(d); x *= 0.5 / np.linalg.norm(x)
+    y = rng.standard_normal(d); y *= 0.5 / np.linalg.norm(y)
+    om = rng.standard_normal((n, m, d))
+    est = np.array([oracle.softmax_kernel_estimate(x, y, om[i]) for i in range(n)])
+    sm = math.exp(x @ y)
+    var = sm * sm * (math.exp((x + y) @ (x + y)) - 1) / m
+    assert abs(est.mean() - sm) <= 4 * est.std(ddof=1) / math.sqrt(n)
+    assert est.var(ddof=1) == pytest.approx(var, rel=0.08)
+
+
+def test_sampled_omega_is_block_orthogonal_with_chi_lengths():
+    r, d = 256, 64
+    blocks, normv = synthetic.omega_gaussians(r, d, seed=7)
+    om = oracle.orthogonal_random_features(blocks, normv, r=r)
+    lengths = np.linalg.norm(normv, axis=1)
+    assert np.allclose(np.linalg.norm(om, axis=1), lengths, rtol=1e-13, atol=0)
+    for b in range(r // d):
+        blk = om[b * d:(b + 1) * d]
+        G = blk @ blk.T
+        off = G - np.diag(np.diag(G))
+        assert np.max(np.abs(off)) <= 1e-11 * np.max(np.diag(G))
+    # each block spans the same space as its Gaussian draw (Gram-Schmidt keeps
+    # the leading subspaces): row i lies in span(draw rows 0..i)
+    B0 = blocks[0]
+    for i in (0, 5, 31, 63):
+        coef, *_ = np.linalg.lstsq(B0[: i + 1].T, om[i], rcond=None)
+        assert np.allclose(B0[: i + 1].T @ coef, om[i], atol=1e-9)
+
+
+def test_chi_lengths_have_chi_mean():
+    """E|g| for g ~ N(0, I_d) is sqrt(2) Gamma((d+1)/2) / Gamma(d/2) (chi mean)."""
+    from scipy.special import gammaln
+    d, n = 64, 20_000
+    lengths = np.linalg.norm(np.random.default_rng(3).standard_normal((n, d)), axis=1)
+    mean = math.sqrt(2) * math.exp(gammaln((d + 1) / 2) - gammaln(d / 2))
+    assert abs(lengths.mean() - mean) <= 3 * lengths.std() / math.sqrt(n)
+
+
+@pytest.mark.parametrize("kind", ["identity", "elu1", "favor"])
+@pytest.mark.parametrize("causal_form", [True, False])
+def test_linear_form_equals_quadratic_rescan(kind, causal_form):
+    """Reassociation: the state form equals every query rescanning its keys
+    ("Linear attention & kernelized approximations"; "The Kernel Zoo" §1.3)."""
+    rng = np.random.default_rng(11)
+    lengths = [5, 1, 10]
+    T, H, d, dv = sum(lengths), 2, 4, 3
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    q = rng.standard_normal((T, H, d)) * 0.6
+    k = rng.standard_normal((T, H, d)) * 0.6
+    v = rng.standard_normal((T, H, dv))
+    om = rng.standard_normal((12, d))
+    fast = oracle.forward(q, k, v, kind, causal_form, omega=om, cu_seqlens=cu)
+    slow = oracle.rescan(q, k, v, kind, omega=om, cu_seqlens=cu, causal_mask=causal_form)
+    if kind == "identity":
+        # identity scores can make den <= eps; compare where den is well away
+        assert np.allclose(fast, slow, rtol=1e-9, atol=1e-9 * np.abs(slow).max())
+    else:
+        assert np.allclose(fast, slow, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal_form", [True, False])
+def test_packed_sequences_reset_state(causal_form):
+    """A packed batch equals each sequence run alone ("Reassociate a
+    feature-map kernel" ¶4: packing must reset the state at the boundary)."""
+    rng = np.random.default_rng(5)
+    lengths = [7, 3, 0, 9]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, d = cu[-1], 2, 4
+    q, k, v = (rng.standard_normal((T, H, d)) * 0.5 for _ in range(3))
+    om = rng.standard_normal((8, d))
+    packed = oracle.forward(q, k, v, "favor", causal_form, omega=om, cu_seqlens=cu)
+    for s in range(len(lengths)):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            continue
+        alone = oracle.forward(q[a:b], k[a:b], v[a:b], "favor", causal_form, omega=om)
+        assert np.array_equal(packed[a:b], alone)
+    # a missed reset would leak the previous sequence: check that it matters
+    joined = oracle.forward(q, k, v, "favor", causal_form, omega=om)
+    assert not np.allclose(joined[cu[1]:cu[2]], packed[cu[1]:cu[2]])
+
+
+def test_last_causal_row_equals_bidirectional_row():
+    rng = np.random.default_rng(9)
+    T, H, d = 12, 3, 5
+    q, k, v = (rng.standard_normal((T, H, d)) * 0.5 for _ in range(3))
+    om = rng.standard_normal((16, d))
+    c = oracle.causal(q, k, v, "favor", omega=om)
+    b = oracle.bidir(q, k, v, "favor", omega=om)
+    assert np.allclose(c[-1], b[-1], rtol=1e-12, atol=0)
+    assert not np.allclose(c[0], b[0])
+
+
+def test_row_sampler_matches_recurrence():
+    rng = np.random.default_rng(2)
+    T, H, d = 40, 2, 6
+    q, k, v = (rng.standard_normal((T, H, d)) * 0.5 for _ in range(3))
+    om = rng.standard_normal((16, d))
+    cu = [0, 13, 40]
+    full_c = oracle.causal(q, k, v, "favor", omega=om, cu_seqlens=cu)
+    full_b = oracle.bidir(q, k, v, "favor", omega=om, cu_seqlens=cu)
+    rows = [13, 14, 27, 39]
+    got_c = oracle.causal_rows(q, k, v, "favor", om, 13, 40, 1, rows)
+    got_b = oracle.bidir_rows(q, k, v, "favor", om, 13, 40, 1, rows)
+    assert np.allclose(got_c, full_c[rows, 1], rtol=1e-12, atol=1e-14)
+    assert np.allclose(got_b, full_b[rows, 1], rtol=1e-12, atol=1e-14)
+
+
+def test_favor_kernel_matrix_is_unbiased_for_exp_scores():
+    """Averaged over independent chi-norm orthogonal draws, the FAVOR+ score
+    matrix Phi_Q Phi_K^T matches the softmax kernel exp(Q K^T) entrywise
+    within 4 standard errors ("Performer" §2 Steps 3-5)."""
+    rng = np.random.default_rng(4)
+    n, d, r, draws = 6, 8, 64, 4000
+    q = rng.standard_normal((n, d)) * d ** -0.25
+    k = rng.standard_normal((n, d)) * d ** -0.25
+    om = _chi_orf_batch(rng, draws, r, d)
+    est = np.stack([oracle.feature_map(q, "favor", om[t]) @ oracle.feature_map(k, "favor", om[t]).T
+                    for t in range(draws)])
+    mean = est.mean(axis=0)
+    se = est.std(axis=0, ddof=1) / np.sqrt(draws)
+    assert np.all(np.abs(mean - np.exp(q @ k.T)) <= 4 * se)
