@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the kernelized linear attention library on GB300.
+
+Metric: tokens/s/GPU of the causal FAVOR+ forward (r = 256, d = 64), with the
+dominant kernel's fraction of the tensor-core / HBM roofline.  Workload: the
+long causal FAVOR+ case, B=1, H=16, N=65536, d_k=d_v=64, r=256, bf16 q/k/v,
+fp32 state, eps 1e-6, synthetic seeded inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one forward call (every phase: plan, segment states, scan,
+outputs) over the whole batch with inputs resident in HBM.  The inputs (402
+MB) exceed the 126 MB L2, so no flush is needed between steps.  Under
+torchrun (N > 1) every rank runs an independent replica on its own GPU (the
+path has no exchange step); value = all ranks' tokens / max-over-ranks time.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+WORKLOAD = "favor_causal_b1h16n65536"
+METRIC = "tokens/s/GPU causal FAVOR+ r=256 d=64; % tensor-core / HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PHASE_NAMES = ["plan", "state", "scan", "output"]
+KERNEL_SOURCES = {"output": "simt.cu", "state": "simt.cu", "scan": "plan.cu", "plan": "plan.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic work (per token-head), from the method's definition
+# ----------------------------------------------------------------------------
+def algorithmic(w: synthetic.Workload) -> dict:
+    """FLOPs, bytes and exponentials one token of one head needs.
+
+    FAVOR+ projection of q and k: 2 * 2 * d_k * r; state update phi(k)[v|1]^T:
+    2 * r * (d_v + 1); readout phi(q)^T [S|z]: 2 * r * (d_v + 1).  HBM: q, k,
+    v read once, out written once.  Exponentials: r for q and r for k.
+    """
+    esz = 2 if w.dtype == "bf16" else 4
+    proj = 2 * 2 * w.dk * w.r if w.map == "favor" else 0
+    flops = proj + 2 * 2 * w.r * (w.dv + 1)
+    byts = (2 * w.dk + 2 * w.dv) * esz
+    exps = 2 * w.r if w.map == "favor" else (2 * w.dk if w.map == "elu1" else 0)
+    return {"flops": flops, "bytes": byts, "exps": exps}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash(phase: str) -> str:
+    p = os.path.join(ROOT, "kernelized_linear_attention_gb300", "csrc", KERNEL_SOURCES[phase])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(phase: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[workload][phase]
+        if e.get("source_sha256_16") == kernel_source_hash(phase):
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling (nvidia-smi, during the timed region)
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        smax = float(rows[0][2])
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if _isnum(r[3])) if any(
+                    _isnum(r[3]) for r in rows) else None}
+
+
+def _isnum(s):
+    try:
+        float(s)
+        return True
+    except Exception:
+        return False
+
+
+# ----------------------------------------------------------------------------
+# Distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity for one process)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(tokens_per_step_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step_per_rank * steps * world / (max_ms / 1e3)
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle, timed on a bounded sample of the workload
+# ----------------------------------------------------------------------------
+def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None) -> dict:
+    """Time the oracle, as it stands, on rows [0, n) of every head of the first
+    sequence (n sized from a calibration run so the sample takes ~`seconds`).
+    BLAS is limited to one thread; tokens/s = token-heads/s / H."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_limits
+        limiter = threadpool_limits(limits=1)
+    except Exception:
+        limiter = None
+    if inputs is None:
+        inputs = synthetic.make_qkv(w)
+    om = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
+    a, b = int(inputs.cu_seqlens[0]), int(inputs.cu_seqlens[1])
+    f = oracle.causal if w.causal else oracle.bidir
+
+    def run(h, n):
+        sl = slice(a, a + n)
+        f(inputs.q[sl, h:h + 1], inputs.k[sl, h:h + 1], inputs.v[sl, h:h + 1], w.map, omega=om, eps=w.eps)
+
+    n0 = min(2048, b - a)
+    t0 = time.perf_counter()
+    run(0, n0)
+    t_cal = time.perf_counter() - t0
+    n = int(min(b - a, max(n0, n0 * (seconds - t_cal) / max(1e-9, t_cal * max(1, w.H - 1)))))
+    t1 = time.perf_counter()
+    for h in range(1, w.H):
+        run(h, n)
+    el = time.perf_counter() - t1
+    th = n * (w.H - 1)
+    if el <= 0 or th == 0:
+        el, th = t_cal, n0
+    return {"value": th / w.H / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle ({'causal recurrence' if w.causal else 'bidirectional'}) on rows 0..{n - 1} "
+                      f"of heads 1..{w.H - 1} of sequence 0: {th} token-heads in {el:.1f} s, 1 BLAS thread; "
+                      f"tokens/s = token-heads/s / H"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import kernelized_linear_attention_gb300 as la
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    la.load_library()
+
+    w = synthetic.workloads()[args.workload]
+    inputs = synthetic.make_qkv(w)
+    T, H, dk, dv, r = w.T, w.H, w.dk, w.dv, w.r
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {}
+    for n in ("q", "k", "v"):
+        a = torch.from_numpy(np.ascontiguousarray(inputs.storage(n)))
+        if w.dtype == "bf16":
+            a = a.view(torch.bfloat16)
+        host[n] = a.pin_memory()
+    dq, dk_, dvv = (host[n].to(dev) for n in ("q", "k", "v"))
+    omega = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(r, dk)
+        omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), r)
+    cu = None if w.equal_lengths else torch.from_numpy(inputs.cu_seqlens).to(dev)
+    nseq = w.nseq
+    out = torch.empty((T, H, dv), dtype=tdt, device=dev)
+    ws_bytes = la.la_workspace_bytes(w.causal, w.map, tdt, cu is not None, nseq, T, H, dk, dv, r)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    call_args = (ptr(dq), ptr(dk_), ptr(dvv), ptr(omega), w.map, tdt, ptr(cu), nseq, T, H, dk, dv, r, w.eps,
+                 ptr(out), ptr(ws), ws_bytes, stream.cuda_stream)
+
+    def step(evs=None):
+        n = 0
+        for ph in range(4):
+            if evs is not None:
+                evs[ph].record(stream)
+            n += la.la_forward_phase(w.causal, ph, *call_args)
+        if evs is not None:
+            evs[4].record(stream)
+        return n
+
+    warmup = max(args.warmup, 3)      # timing rules: at least 3 untimed warm-up steps
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if la.la_workspace_error(ws) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    launches = 0
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        launches += step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total_max = max_over_ranks(ms_total, world, dev)
+    phase_ms = {PHASE_NAMES[p]: statistics.mean(evs[i][p].elapsed_time(evs[i][p + 1]) for i in range(K))
+                for p in range(4)}
+    if la.la_workspace_error(ws) != 0:
+        raise RuntimeError("device error during the timed steps")
+
+    tokens = T  # tokens per step per GPU (all heads)
+    value = aggregate_value(tokens, K, world, ms_total_max)
+    alg = algorithmic(w)
+    peaks = measured_peaks()
+    token_heads = T * H
+    dom = max(phase_ms, key=phase_ms.get)
+    dom_ms = phase_ms[dom]
+    # algorithmic work of one output-phase launch: the whole method for every
+    # token-head of the batch (it reads q, k, v, writes out, computes both
+    # projections, the state terms and the readout).
+    alg_flops = alg["flops"] * token_heads
+    alg_bytes = alg["bytes"] * token_heads
+    t_flop = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    t_byte = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if dom == "output":
+        if t_flop >= t_byte:
+            achieved = alg_flops / (dom_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        else:
+            achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        byts = alg["bytes"] * token_heads / 2 if dom == "state" else alg_bytes
+        achieved = byts / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")
+    roof["tensor_frac_of_output"] = alg_flops / (phase_ms["output"] * 1e-3) / 1e12 / peaks["bf16_tflops"]
+    roof["hbm_frac_of_output"] = alg_bytes / (phase_ms["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    roof["phase_ms"] = phase_ms
+
+    # end to end through the C ABI with host buffers: H2D q, k, v; forward; D2H out
+    out_host = torch.empty((T, H, dv), dtype=tdt).pin_memory()
+    Ke = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 20))
+    for _ in range(2):
+        dq.copy_(host["q"], non_blocking=True); dk_.copy_(host["k"], non_blocking=True)
+        dvv.copy_(host["v"], non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        dq.copy_(host["q"], non_blocking=True); dk_.copy_(host["k"], non_blocking=True)
+        dvv.copy_(host["v"], non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / Ke
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v"))
+    d2h = out_host.numel() * out_host.element_size()
+    e2e = {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": warmup, "ms_per_step": ms_total_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) q,k scaled by d^-1/4, v)",
+        "config": {"workload": w.name, "B": w.nseq, "H": H, "N": w.lengths[0], "d_k": dk, "d_v": dv, "r": r,
+                   "map": w.map, "causal": w.causal, "eps": w.eps, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: q, k, v (402 MB) exceed the 126 MB L2",
+                   "path": "tcgen05" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 else "cuda-core"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = synthetic.workloads()[args.workload]
+    inputs = synthetic.make_qkv(w)
+    import oracle
+    om = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
+    n_sample = 2048
+    sl = slice(0, n_sample)
+
+    def one():
+        if w.causal:
+            oracle.causal(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps)
+        else:
+            oracle.bidir(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = n_sample * args.steps / w.H / el
+    sample = (f"each step: fp64 oracle on the first {n_sample} tokens of head 0 of the "
+              f"{w.name} workload (1 of {w.H} heads); tokens/s = token-heads/s / H")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

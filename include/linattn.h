@@ -1,0 +1,213 @@
+/*
+ * linattn.h - C ABI of the GB300 kernelized linear attention library (liblinattn.so).
+ *
+ * The library computes kernelized (linear) attention
+ *
+ *     out_i = phi(q_i)^T S / max(phi(q_i)^T z, eps),
+ *     S = sum_j phi(k_j) v_j^T  in R^{r x d_v},   z = sum_j phi(k_j)  in R^r,
+ *
+ * ("Reassociate a feature-map kernel without claiming exact softmax", ¶1-2;
+ *  "Performer - Random Feature Softmax Approximation", §2 Step 5 and §3),
+ * in bidirectional form (j over the whole sequence) and causal form (j <= i,
+ * the inclusive prefix recurrence of "The Kernel Zoo", §1.3 and §5.4), over
+ * packed sequences whose state resets at every boundary ("Reassociate a
+ * feature-map kernel", ¶4).  The denominator is clamped from below at eps,
+ * as the "Performer" §3 sketch does (its .clamp(min=1e-6)).
+ *
+ * Feature maps phi:
+ *   LA_MAP_IDENTITY  phi(x) = x, r = d_k            ("The Kernel Zoo", §1.3)
+ *   LA_MAP_ELU1      phi(x) = elu(x) + 1, r = d_k   ("The Kernel Zoo", running example;
+ *                    x + 1 for x > 0, exp(x) otherwise)
+ *   LA_MAP_FAVOR     phi(x) = exp(Omega x - |x|^2/2) / sqrt(r), Omega in R^{r x d_k}
+ *                    ("The Kernel Zoo", §4.2 and §5.4; "Performer", §2 Step 3)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout.   q, k: [T, H, d_k]; v, out: [T, H, d_v]; all contiguous row-major
+ *           (d innermost), T = total packed tokens.  Omega: [r, d_k] fp32
+ *           row-major, shared by every head and sequence (the single omega of
+ *           the "Performer" §3 sketch).  Element type of q, k, v and out is
+ *           given by `dtype` (LA_F32: float, LA_BF16: bfloat16 bits).
+ * Packing.  cu_seqlens: device int32 [nseq + 1], cu_seqlens[0] = 0,
+ *           non-decreasing, cu_seqlens[nseq] = T.  Sequence s owns rows
+ *           cu_seqlens[s] .. cu_seqlens[s+1]-1.  NULL means nseq sequences of
+ *           T / nseq tokens each (a B x N batch).  Empty sequences are allowed.
+ * Memory.   Every pointer is device memory owned by the caller, except where
+ *           a call says "host".  The library allocates nothing and keeps no
+ *           state between calls; calls on different streams with different
+ *           workspaces may run concurrently.  Inputs are read only; `out` must
+ *           not alias them.  Pointers must be aligned to their element size;
+ *           16-byte aligned q/k/v/out/omega enable the tensor-core path.
+ * Streams.  `stream` is a cudaStream_t (NULL: the legacy default stream).
+ *           Compute calls only enqueue work and return; they never
+ *           synchronise, except la_check_cu_seqlens and la_workspace_error.
+ * Errors.   Argument checks run on the host before anything is enqueued and
+ *           return LA_ERR_INVALID_ARG / LA_ERR_UNSUPPORTED / LA_ERR_WORKSPACE;
+ *           nothing is written in that case.  A failed launch returns
+ *           LA_ERR_CUDA.  Problems only the device can see (cu_seqlens contents
+ *           that break the rules above, a bounded wait inside a kernel that ran
+ *           out) are recorded in the workspace's error word and the affected
+ *           work is skipped; read it with la_workspace_error.  No kernel traps.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(LA_BUILDING_LIBRARY)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size or a bad combination       */
+    LA_ERR_UNSUPPORTED = 2,   /* valid, but beyond the library's size limits           */
+    LA_ERR_WORKSPACE = 3,     /* workspace_bytes < la_workspace_bytes(...)             */
+    LA_ERR_CUDA = 4,          /* a CUDA call or kernel launch failed                   */
+    LA_ERR_DEVICE = 5         /* the device recorded an error (la_workspace_error)     */
+} la_status;
+
+typedef enum { LA_MAP_IDENTITY = 0, LA_MAP_ELU1 = 1, LA_MAP_FAVOR = 2 } la_map;
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Device error codes stored in the workspace error word. */
+#define LA_DEVERR_NONE 0
+#define LA_DEVERR_CU_SEQLENS 1    /* cu_seqlens broke the packing rules: nothing computed */
+#define LA_DEVERR_WAIT_TIMEOUT 2  /* a bounded in-kernel wait ran out: output incomplete */
+
+/* Size limits (checked on the host). */
+#define LA_MAX_DK 256
+#define LA_MAX_DV 256
+#define LA_MAX_R 512
+
+/*
+ * la_feature_map - phi applied to every row of x.
+ *   x:      [T, H, d] of dtype;  omega: [r, d] fp32 (FAVOR only, else may be NULL)
+ *   phi:    [T, H, r] fp32 output
+ *   map:    la_map;  r must equal d for identity and ELU+1.
+ * Defined by "The Kernel Zoo" §4.2 boxed map (FAVOR+), the running example
+ * (ELU+1) and §1.3 (identity).  For LA_BF16 input the values are those the
+ * forward calls use before they round phi to bf16 for the tensor cores.
+ */
+LA_API la_status la_feature_map(const void* x, const float* omega, int map, int dtype,
+                         int64_t T, int H, int d, int r, float* phi, void* stream);
+
+/*
+ * la_forward_bidir - bidirectional kernelized attention.
+ *   For every sequence and head: S = Phi_K^T V, z = Phi_K^T 1 over the whole
+ *   sequence, out_i = phi(q_i)^T S / max(phi(q_i)^T z, eps)
+ *   ("Performer" §2 Step 5 and the §3 sketch; "Linear attention & kernelized
+ *   approximations", "Build the state once").
+ *   q, k: [T, H, d_k]; v, out: [T, H, d_v] (dtype); omega: [r, d_k] fp32 or NULL.
+ *   eps >= 0.  workspace: device scratch of at least
+ *   la_workspace_bytes(0, ...) bytes, 256-byte aligned; its contents on entry
+ *   do not matter.  Sums over tokens are fp32 and run in a fixed order, so the
+ *   result is deterministic for a given device.
+ */
+LA_API la_status la_forward_bidir(const void* q, const void* k, const void* v, const float* omega,
+                           int map, int dtype, const int32_t* cu_seqlens, int nseq,
+                           int64_t T, int H, int d_k, int d_v, int r, float eps,
+                           void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * la_forward_causal - causal kernelized attention by prefix sums.
+ *   S_i = sum_{j<=i} phi(k_j) v_j^T, z_i = sum_{j<=i} phi(k_j) within each
+ *   sequence (key i is visible to query i), out_i = phi(q_i)^T S_i /
+ *   max(phi(q_i)^T z_i, eps) ("The Kernel Zoo" §1.3 and §5.4; "Reassociate a
+ *   feature-map kernel" ¶4; "Performer" §2, prefix-sum recurrence).  The state
+ *   is carried in fp32.  Arguments as for la_forward_bidir, with
+ *   la_workspace_bytes(1, ...).
+ */
+LA_API la_status la_forward_causal(const void* q, const void* k, const void* v, const float* omega,
+                            int map, int dtype, const int32_t* cu_seqlens, int nseq,
+                            int64_t T, int H, int d_k, int d_v, int r, float eps,
+                            void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * la_forward_phase - one phase of a forward call, for callers that time or
+ *   interleave the kernels.  la_forward_bidir / la_forward_causal are exactly
+ *   phases LA_PHASE_PLAN .. LA_PHASE_OUTPUT called in order with the same
+ *   arguments and workspace:
+ *     LA_PHASE_PLAN    split the packed sequences into segments (reads cu_seqlens)
+ *     LA_PHASE_STATE   per-segment state sum_j phi(k_j) [v_j | 1]^T
+ *     LA_PHASE_SCAN    state entering each segment (causal: exclusive prefix
+ *                      over the sequence's segments; bidirectional: the sum)
+ *     LA_PHASE_OUTPUT  outputs of every segment
+ *   A phase that the call does not need (STATE and SCAN when every causal
+ *   sequence is a single segment) enqueues nothing.  *launched (host, may be
+ *   NULL) receives the number of kernels the phase enqueued.
+ */
+#define LA_PHASE_PLAN 0
+#define LA_PHASE_STATE 1
+#define LA_PHASE_SCAN 2
+#define LA_PHASE_OUTPUT 3
+#define LA_NUM_PHASES 4
+LA_API la_status la_forward_phase(int causal, int phase, const void* q, const void* k, const void* v,
+                           const float* omega, int map, int dtype, const int32_t* cu_seqlens,
+                           int nseq, int64_t T, int H, int d_k, int d_v, int r, float eps,
+                           void* out, void* workspace, size_t workspace_bytes, void* stream,
+                           int* launched);
+
+/*
+ * la_workspace_bytes - scratch size for a forward call on the current device.
+ *   causal: 1 for la_forward_causal, 0 for la_forward_bidir; `has_cu_seqlens`:
+ *   1 when a cu_seqlens array will be passed.  Returns 0 for arguments the
+ *   forward call would reject.  The size depends on the device's SM count.
+ */
+LA_API size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq,
+                          int64_t T, int H, int d_k, int d_v, int r);
+
+/*
+ * la_check_cu_seqlens - validate cu_seqlens contents (device array).
+ *   Returns LA_OK when cu_seqlens[0] = 0, the array does not decrease and
+ *   cu_seqlens[nseq] = T; LA_ERR_INVALID_ARG otherwise.  Synchronises `stream`
+ *   (it copies nseq + 1 integers to the host).
+ */
+LA_API la_status la_check_cu_seqlens(const int32_t* cu_seqlens, int nseq, int64_t T, void* stream);
+
+/*
+ * la_workspace_error - read the device error word a forward call left in its
+ *   workspace.  Synchronises `stream`.  Returns LA_OK, or LA_ERR_DEVICE and the
+ *   LA_DEVERR_* code in *code (host pointer, may be NULL).
+ */
+LA_API la_status la_workspace_error(const void* workspace, int* code, void* stream);
+
+/*
+ * la_orthogonal_features - build the FAVOR+ projection matrix from Gaussian draws.
+ *   gauss_blocks:  [ceil(r/d), d, d] fp64, i.i.d. N(0,1) (device)
+ *   gauss_lengths: [r, d] fp64, i.i.d. N(0,1) (device)
+ *   omega:         [r, d] fp32 output (device)
+ *   Each block's rows are orthonormalised in order by Gram-Schmidt; row i of
+ *   the stacked result is scaled to the Euclidean length of gauss_lengths[i]
+ *   (a chi(d) draw), and the first r rows are kept ("The Kernel Zoo" §5.1 and
+ *   §5.3 Steps 1-3; "Performer" §2 Step 4, rows with Gaussian-distributed
+ *   norms).  Computed in fp64 and rounded to fp32.  1 <= d <= 128.
+ */
+LA_API la_status la_orthogonal_features(const double* gauss_blocks, const double* gauss_lengths,
+                                 int r, int d, float* omega, void* stream);
+
+/*
+ * la_selected_path - which kernels a forward call with these arguments runs:
+ *   0 = fp32 CUDA-core kernels, 1 = tcgen05 tensor-core kernels.  Assumes
+ *   16-byte aligned pointers.  Returns -1 for arguments a call would reject.
+ */
+LA_API int la_selected_path(int causal, int map, int dtype, int d_k, int d_v, int r);
+
+/* la_status_string - static description of a status code. */
+LA_API const char* la_status_string(la_status status);
+
+/* la_version - library version, major * 10000 + minor * 100 + patch. */
+LA_API int la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

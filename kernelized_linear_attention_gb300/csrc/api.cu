@@ -1,0 +1,249 @@
+// C ABI of liblinattn.so: argument checks, workspace layout, dispatch.
+// The operation each entry point computes is specified in include/linattn.h.
+#include <cmath>
+#include <vector>
+
+#include "internal.h"
+
+namespace la {
+
+namespace {
+
+constexpr int kPathSimt = 0;
+constexpr int kPathTensor = 1;
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// Shape checks shared by every forward entry point and the size queries.
+la_status check_dims(int map, int dtype, int nseq, int64_t T, int H, int dk, int dv, int r,
+                     bool has_cu) {
+    if (map < LA_MAP_IDENTITY || map > LA_MAP_FAVOR) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+    if (nseq < 1 || nseq > 65535 || H < 1 || H > 65535) return LA_ERR_INVALID_ARG;
+    if (T < 0 || T > (int64_t)INT32_MAX) return LA_ERR_INVALID_ARG;
+    if (dk < 1 || dv < 1 || r < 1) return LA_ERR_INVALID_ARG;
+    if (map != LA_MAP_FAVOR && r != dk) return LA_ERR_INVALID_ARG;
+    if (!has_cu && (T % nseq) != 0) return LA_ERR_INVALID_ARG;
+    if (dk > LA_MAX_DK || dv > LA_MAX_DV || r > LA_MAX_R) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+int select_path(int /*causal*/, int /*map*/, int /*dtype*/, int /*dk*/, int /*dv*/, int /*r*/) {
+    return kPathSimt;
+}
+
+int path_chunk(int path) { return path == kPathTensor ? 128 : simt_chunk(); }
+
+la_status path_supported(int path, int map, int dk, int dv, int r) {
+    if (path == kPathSimt && simt_smem_bytes(map, dk, dv, r) > kSmemLimitBytes) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+// Segment length and unit bound.  Equal-length batches split every sequence
+// into the same number of segments so that units * heads fills the SMs;
+// packed batches (lengths only known on the device) use one length for all.
+Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm) {
+    Layout lo{};
+    const int64_t C = path_chunk(path);
+    int64_t L, U;
+    if (!has_cu) {
+        const int64_t len = T / nseq;
+        const int64_t per = std::max<int64_t>(1, nsm / std::max<int64_t>(1, (int64_t)nseq * H));
+        L = std::max<int64_t>(C, ceil_div(ceil_div(len, per), C) * C);
+        U = (int64_t)nseq * ceil_div(len, L);
+    } else {
+        L = std::max<int64_t>(C, ceil_div(ceil_div(T * H, std::max(1, nsm)), C) * C);
+        U = nseq + ceil_div(T, L);
+    }
+    U = std::max<int64_t>(U, 1);
+    lo.L = (int)std::min<int64_t>(L, INT32_MAX);
+    lo.U = (int)U;
+    lo.dvx = dv + 1;
+    size_t o = align_up(sizeof(WsHeader), kAlign);
+    lo.units = o;     o = align_up(o + sizeof(Unit) * (size_t)U, kAlign);
+    lo.seq_first = o; o = align_up(o + sizeof(int) * (size_t)(nseq + 1), kAlign);
+    const size_t state_bytes = sizeof(float) * (size_t)U * H * r * lo.dvx;
+    lo.partial = o;   o = align_up(o + state_bytes, kAlign);
+    lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
+    lo.total = o;
+    return lo;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const void* k, const void* v,
+                  const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
+                  int H, int dk, int dv, int r, float eps, void* out, void* workspace,
+                  size_t workspace_bytes, void* stream, int* launched) {
+    if (launched) *launched = 0;
+    const bool has_cu = cu_seqlens != nullptr;
+    la_status st = check_dims(map, dtype, nseq, T, H, dk, dv, r, has_cu);
+    if (st != LA_OK) return st;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (map == LA_MAP_FAVOR && omega == nullptr) return LA_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned(workspace, kAlign)) return LA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID_ARG;
+    const size_t esz = dtype == LA_F32 ? 4 : 2;
+    if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(out, esz)) return LA_ERR_INVALID_ARG;
+    if (omega && !aligned(omega, 4)) return LA_ERR_INVALID_ARG;
+    const int path = select_path(causal, map, dtype, dk, dv, r);
+    if ((st = path_supported(path, map, dk, dv, r)) != LA_OK) return st;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return LA_ERR_CUDA;
+    const Layout lo = make_layout(path, has_cu, nseq, T, H, dv, r, nsm);
+    if (workspace_bytes < lo.total) return LA_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.omega = omega; p.out = out;
+    p.cu_seqlens = cu_seqlens; p.nseq = nseq; p.T = T;
+    p.H = H; p.dk = dk; p.dv = dv; p.r = r; p.dvx = lo.dvx;
+    p.map = map; p.causal = causal; p.eps = eps;
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.units = reinterpret_cast<Unit*>(ws + lo.units);
+    p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
+    p.partial = reinterpret_cast<float*>(ws + lo.partial);
+    p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
+    p.U = lo.U; p.L = lo.L;
+
+    // A causal call whose sequences are all single segments starts every unit
+    // from a zero state: the state pass and the scan are skipped.
+    const bool single_segments = !has_cu && lo.U == nseq;
+    const bool need_state = !causal || !single_segments;
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    for (int ph = phase_lo; ph <= phase_hi && e == cudaSuccess; ++ph) {
+        switch (ph) {
+            case LA_PHASE_PLAN:
+                e = launch_plan(p, s); ++n; break;
+            case LA_PHASE_STATE:
+                if (T > 0 && need_state) { e = simt_state(p, dtype, s); ++n; }
+                break;
+            case LA_PHASE_SCAN:
+                if (T > 0 && need_state) { e = launch_scan(p, s); ++n; }
+                break;
+            case LA_PHASE_OUTPUT:
+                if (T > 0) { e = simt_out(p, dtype, need_state ? 0 : 1, s); ++n; }
+                break;
+            default:
+                return LA_ERR_INVALID_ARG;
+        }
+    }
+    if (launched) *launched = n;
+    return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+la_status la_feature_map(const void* x, const float* omega, int map, int dtype, int64_t T, int H, int d,
+                         int r, float* phi, void* stream) {
+    la_status st = check_dims(map, dtype, 1, T, H, d, 1, r, true);
+    if (st != LA_OK) return st;
+    if (map == LA_MAP_FAVOR && omega == nullptr) return LA_ERR_INVALID_ARG;
+    if (T == 0) return LA_OK;
+    if (!x || !phi) return LA_ERR_INVALID_ARG;
+    const size_t esz = dtype == LA_F32 ? 4 : 2;
+    if (!aligned(x, esz) || !aligned(phi, 4) || (omega && !aligned(omega, 4))) return LA_ERR_INVALID_ARG;
+    if (simt_fmap_smem_bytes(map, d, r) > kSmemLimitBytes) return LA_ERR_UNSUPPORTED;
+    cudaError_t e = simt_feature_map(x, omega, map, dtype, T, H, d, r, phi, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+la_status la_forward_bidir(const void* q, const void* k, const void* v, const float* omega, int map, int dtype,
+                           const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k, int d_v, int r,
+                           float eps, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward(0, LA_PHASE_PLAN, LA_PHASE_OUTPUT, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k,
+                   d_v, r, eps, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+la_status la_forward_causal(const void* q, const void* k, const void* v, const float* omega, int map, int dtype,
+                            const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k, int d_v, int r,
+                            float eps, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward(1, LA_PHASE_PLAN, LA_PHASE_OUTPUT, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k,
+                   d_v, r, eps, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+la_status la_forward_phase(int causal, int phase, const void* q, const void* k, const void* v, const float* omega,
+                           int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k,
+                           int d_v, int r, float eps, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream, int* launched) {
+    if (phase < LA_PHASE_PLAN || phase > LA_PHASE_OUTPUT) return LA_ERR_INVALID_ARG;
+    return forward(causal != 0, phase, phase, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r,
+                   eps, out, workspace, workspace_bytes, stream, launched);
+}
+
+size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq, int64_t T, int H,
+                          int d_k, int d_v, int r) {
+    if (check_dims(map, dtype, nseq, T, H, d_k, d_v, r, has_cu_seqlens != 0) != LA_OK) return 0;
+    const int path = select_path(causal, map, dtype, d_k, d_v, r);
+    if (path_supported(path, map, d_k, d_v, r) != LA_OK) return 0;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return 0;
+    return make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm).total;
+}
+
+la_status la_check_cu_seqlens(const int32_t* cu_seqlens, int nseq, int64_t T, void* stream) {
+    if (cu_seqlens == nullptr || nseq < 1 || T < 0) return LA_ERR_INVALID_ARG;
+    std::vector<int32_t> h((size_t)nseq + 1);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(h.data(), cu_seqlens, sizeof(int32_t) * h.size(), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    if (h[0] != 0 || (int64_t)h[nseq] != T) return LA_ERR_INVALID_ARG;
+    for (int i = 0; i < nseq; ++i)
+        if (h[i + 1] < h[i]) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+la_status la_workspace_error(const void* workspace, int* code, void* stream) {
+    if (workspace == nullptr) return LA_ERR_INVALID_ARG;
+    int err = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    if (code) *code = err;
+    return err == LA_DEVERR_NONE ? LA_OK : LA_ERR_DEVICE;
+}
+
+la_status la_orthogonal_features(const double* gauss_blocks, const double* gauss_lengths, int r, int d,
+                                 float* omega, void* stream) {
+    if (!gauss_blocks || !gauss_lengths || !omega) return LA_ERR_INVALID_ARG;
+    if (r < 1 || d < 1) return LA_ERR_INVALID_ARG;
+    if (d > 128 || r > LA_MAX_R) return LA_ERR_UNSUPPORTED;
+    cudaError_t e = orf_build(gauss_blocks, gauss_lengths, r, d, omega, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+int la_selected_path(int causal, int map, int dtype, int d_k, int d_v, int r) {
+    if (check_dims(map, dtype, 1, 0, 1, d_k, d_v, r, true) != LA_OK) return -1;
+    const int path = select_path(causal, map, dtype, d_k, d_v, r);
+    if (path_supported(path, map, d_k, d_v, r) != LA_OK) return -1;
+    return path;
+}
+
+const char* la_status_string(la_status status) {
+    switch (status) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported size";
+        case LA_ERR_WORKSPACE: return "workspace too small";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_DEVICE: return "device-side error recorded in the workspace";
+    }
+    return "unknown status";
+}
+
+int la_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Shared definitions of the kernelized linear attention library: workspace
+// layout, work units, element access helpers.  Internal to liblinattn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "linattn.h"
+
+namespace la {
+
+// A work unit is one contiguous token range (a segment) of one packed
+// sequence; every unit is processed for every head (grid.y).  Segments of one
+// sequence are consecutive unit indices, in token order.
+struct Unit {
+    int seq;     // sequence index
+    int start;   // first token (global row)
+    int end;     // one past the last token
+    int first;   // unit index of the sequence's first segment
+};
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+    int error;     // LA_DEVERR_*; written with atomicMax, never cleared by kernels but the planner
+    int n_units;   // units the planner produced
+    int pad[62];
+};
+
+// Byte offsets of the workspace regions for one forward call.
+struct Layout {
+    size_t units;      // Unit[U]
+    size_t seq_first;  // int[nseq + 1]: first unit of each sequence (+ total)
+    size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
+    size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
+    size_t total;      // bytes
+    int U;             // upper bound on units
+    int L;             // segment length in tokens
+    int dvx;           // d_v + 1: the ones column carries z
+};
+
+constexpr int kAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Parameters of one forward call, as the kernels see them.
+struct FwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* omega;
+    void* out;
+    const int32_t* cu_seqlens;  // may be NULL
+    int nseq;
+    int64_t T;
+    int H, dk, dv, r, dvx;
+    int map;       // la_map
+    int causal;
+    float eps;
+    // workspace regions
+    WsHeader* hdr;
+    Unit* units;
+    int* seq_first;
+    float* partial;
+    float* prefix;
+    int U, L;
+};
+
+// ---------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_elem(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void record_error(WsHeader* hdr, int code) {
+    atomicMax(&hdr->error, code);
+}
+
+}  // namespace la

@@ -1,0 +1,30 @@
+// Launchers shared between the translation units of liblinattn.so.
+#pragma once
+
+#include "common.cuh"
+
+namespace la {
+
+// Work planning (plan.cu): fills the unit table and sequence index from
+// cu_seqlens (or equal lengths), clears the error word.
+cudaError_t launch_plan(const FwdParams& p, cudaStream_t s);
+// Combines per-unit partial states into the state each unit starts from:
+// exclusive prefix over the sequence's units (causal) or the whole-sequence
+// sum (bidirectional).  Fixed summation order.
+cudaError_t launch_scan(const FwdParams& p, cudaStream_t s);
+
+// fp32 CUDA-core path (simt.cu).
+size_t simt_smem_bytes(int map, int dk, int dv, int r);
+size_t simt_fmap_smem_bytes(int map, int d, int r);
+constexpr size_t kSmemLimitBytes = 227 * 1024;
+int simt_chunk();
+cudaError_t simt_feature_map(const void* x, const float* omega, int map, int dtype,
+                             int64_t T, int H, int d, int r, float* phi, cudaStream_t s);
+cudaError_t simt_state(const FwdParams& p, int dtype, cudaStream_t s);
+cudaError_t simt_out(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_t s);
+
+// Orthogonal random features (orf.cu).
+cudaError_t orf_build(const double* blocks, const double* lengths, int r, int d, float* omega,
+                      cudaStream_t s);
+
+}  // namespace la

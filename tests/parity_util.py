@@ -1,0 +1,67 @@
+"""Helpers shared by the GPU parity tests.
+
+Tolerances (written out here and asserted in the tests):
+* fp32 path: max over elements of |gpu - oracle| / max(|oracle|, RMS(oracle))
+  <= 1e-4 (relative error, with the output RMS as the floor below which an
+  element's size does not shrink the allowance);
+* bf16 inputs, fp32 accumulation: max |gpu - oracle| <= 2e-2 * RMS(oracle).
+"""
+import numpy as np
+
+import oracle
+import synthetic
+
+FP32_REL_TOL = 1e-4
+BF16_RMS_TOL = 2e-2
+
+
+def rel_err_rms_floor(got, ref):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    denom = np.maximum(np.abs(ref), rms)
+    denom = np.where(denom == 0, 1.0, denom)
+    return float(np.max(np.abs(got - ref) / denom)) if ref.size else 0.0
+
+
+def abs_err_over_rms(got, ref):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = np.sqrt(np.mean(ref * ref))
+    return float(np.max(np.abs(got - ref)) / (rms if rms > 0 else 1.0))
+
+
+def assert_close(got, ref, dtype, what=""):
+    if dtype == "f32":
+        e = rel_err_rms_floor(got, ref)
+        assert e <= FP32_REL_TOL, f"{what}: fp32 relative error {e:.3e} > {FP32_REL_TOL}"
+    else:
+        e = abs_err_over_rms(got, ref)
+        assert e <= BF16_RMS_TOL, f"{what}: bf16 abs error / RMS {e:.3e} > {BF16_RMS_TOL}"
+    return e
+
+
+def omega_for(r, d, seed=synthetic.OMEGA_SEED):
+    """fp32 orthogonal random features (chi lengths) drawn from the oracle."""
+    blocks, lengths = synthetic.omega_gaussians(r, d, seed)
+    return oracle.orthogonal_random_features(blocks, lengths, r=r).astype(np.float32)
+
+
+def to_torch(inputs, device="cuda"):
+    """Inputs -> (q, k, v) torch tensors on device, in storage dtype."""
+    import torch
+    out = []
+    for name in ("q", "k", "v"):
+        a = inputs.storage(name)
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if inputs.dtype == "bf16":
+            t = t.view(torch.bfloat16)
+        out.append(t.to(device))
+    return out
+
+
+def from_torch(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy()
+    return t.cpu().numpy()

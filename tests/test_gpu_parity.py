@@ -1,0 +1,250 @@
+"""GPU parity: the CUDA library against the fp64 oracle on identical seeded inputs.
+
+Every comparison goes through the C ABI (via the ctypes binding).  Sizes span
+several chunks and segments with ragged tails; the full-size workloads are
+checked on sampled rows in the same launch configuration the benchmark uses.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from parity_util import (BF16_RMS_TOL, FP32_REL_TOL, abs_err_over_rms, assert_close, from_torch,
+                         omega_for, rel_err_rms_floor, to_torch)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import kernelized_linear_attention_gb300 as m
+    m.load_library()   # raises if the library was not built: no fallback
+    return m
+
+
+def _tensor(a, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype == "bf16":
+        t = torch.from_numpy(synthetic.bf16_bits(np.asarray(a, np.float32)).view(np.int16)).view(torch.bfloat16)
+    return t.cuda()
+
+
+def _run(la, inputs, kind, causal, omega=None, eps=1e-6, cu=True):
+    q, k, v = to_torch(inputs)
+    om = torch.from_numpy(omega).cuda() if omega is not None else None
+    cu_t = torch.from_numpy(inputs.cu_seqlens).cuda() if cu else None
+    nseq = len(inputs.cu_seqlens) - 1
+    fn = la.la_forward_causal if causal else la.la_forward_bidir
+    out = fn(q, k, v, kind, omega=om, cu_seqlens=cu_t, nseq=nseq, eps=eps)
+    torch.cuda.synchronize()
+    return from_torch(out)
+
+
+def _oracle(inputs, kind, causal, omega=None, eps=1e-6):
+    return oracle.forward(inputs.q, inputs.k, inputs.v, kind, causal, omega=omega,
+                          cu_seqlens=inputs.cu_seqlens, eps=eps)
+
+
+# ----------------------------------------------------------------------------
+# Feature maps
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_feature_map_identity_and_elu1(la, dtype):
+    rng = np.random.default_rng(0)
+    x = synthetic.quantise(rng.standard_normal((300, 3, 64)).astype(np.float32) * 2, dtype)
+    xt = _tensor(x, dtype)
+    ident = la.la_feature_map(xt, "identity").cpu().numpy()
+    assert np.array_equal(ident, x)
+    elu = la.la_feature_map(xt, "elu1").cpu().numpy()
+    ref = oracle.feature_map(x, "elu1")
+    pos = x > 0
+    # x > 0: x + 1 rounded once to fp32, bit-exact
+    assert np.array_equal(elu[pos], ref[pos].astype(np.float32))
+    # x <= 0: exp(x) within a few fp32 ulps
+    assert np.max(np.abs(elu[~pos] - ref[~pos]) / ref[~pos]) < 4 * 2.0 ** -23
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_feature_map_favor(la, dtype):
+    rng = np.random.default_rng(1)
+    r, d = 256, 64
+    x = synthetic.quantise(rng.standard_normal((257, 2, d)).astype(np.float32) * d ** -0.25, dtype)
+    om = omega_for(r, d)
+    phi = la.la_feature_map(_tensor(x, dtype), "favor", omega=torch.from_numpy(om).cuda()).cpu().numpy()
+    ref = oracle.feature_map(x, "favor", om)
+    logerr = np.abs(np.log(phi.astype(np.float64)) - np.log(ref))
+    if la.la_selected_path(True, "favor", 1 if dtype == "bf16" else 0, d, d, r) == 1 and dtype == "bf16":
+        # tensor-core projection uses bf16(Omega * log2 e): the exponent error is
+        # bounded by 2^-9 * sum_i |omega_i x_i| plus fp32 accumulation
+        bound = 1.1 * 2.0 ** -9 * (np.abs(x)[..., None, :] * np.abs(om)[None, None]).sum(-1) + 1e-5
+        assert np.all(logerr <= bound)
+    else:
+        assert np.max(logerr) < 1e-5
+
+
+def test_orthogonal_features_match_oracle(la):
+    for r, d in ((256, 64), (100, 32), (4, 2)):
+        blocks, lengths = synthetic.omega_gaussians(r, d, seed=7 + r)
+        ref = oracle.orthogonal_random_features(blocks, lengths, r=r)
+        om = la.la_orthogonal_features(torch.from_numpy(blocks).cuda(), torch.from_numpy(lengths).cuda(), r)
+        got = om.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(got - ref)) <= 4 * 2.0 ** -24 * np.abs(ref).max()
+
+
+# ----------------------------------------------------------------------------
+# Worked examples through the GPU
+# ----------------------------------------------------------------------------
+def _small(q, k, v, dtype="f32"):
+    q, k, v = (np.asarray(a, np.float32)[:, None, :] for a in (q, k, v))
+    return synthetic.Inputs(q, k, v, np.array([0, q.shape[0]], np.int32), dtype)
+
+
+def test_identity_bidir_worked_example_on_gpu(la):
+    K = [[2, 1], [-1, 2], [1, -1], [0, 3]]
+    v = [[3], [-2], [1], [4]]
+    q = [[1, 0], [0, 0], [0, 0], [0, 0]]
+    out = _run(la, _small(q, K, v), "identity", causal=False)
+    assert out[0, 0, 0] == pytest.approx(4.5, abs=1e-6)
+
+
+def test_elu1_running_example_o4_on_gpu(la):
+    Q = [[1, 0], [0, 1], [1, 1], [2, 0]]
+    K = [[0, 1], [1, 0], [1, 1], [0, 2]]
+    V = [[1, 0], [0, 1], [1, 1], [2, 0]]
+    out = _run(la, _small(Q, K, V), "elu1", causal=True)
+    assert np.allclose(out[3, 0], [25 / 26, 15 / 26], atol=1e-6)
+    ident = _run(la, _small(Q, K, V), "identity", causal=True)
+    assert np.allclose(ident[:, 0], [[0, 0], [1, 0], [0.75, 0.75], [0.5, 1.0]], atol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# fp32 path: the single-head N=1024 workload (<= 1e-4 relative)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("kind", ["elu1", "favor"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_fp32_single_head_n1024(la, kind, causal):
+    w = synthetic.workloads()["fp32_n1024"]
+    inp = synthetic.make_qkv(w)
+    om = omega_for(256, 64) if kind == "favor" else None
+    got = _run(la, inp, kind, causal, om)
+    ref = _oracle(inp, kind, causal, om)
+    e = rel_err_rms_floor(got, ref)
+    assert e <= FP32_REL_TOL, e
+
+
+def test_fp32_identity_positive_inputs(la):
+    rng = np.random.default_rng(3)
+    lengths = [100, 37, 1, 200]
+    T = sum(lengths)
+    q, k = (np.abs(rng.standard_normal((T, 2, 16))).astype(np.float32) for _ in range(2))
+    v = rng.standard_normal((T, 2, 24)).astype(np.float32)
+    inp = synthetic.Inputs(q, k, v, np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), "f32")
+    for causal in (True, False):
+        assert_close(_run(la, inp, "identity", causal), _oracle(inp, "identity", causal), "f32")
+
+
+# ----------------------------------------------------------------------------
+# Ragged packed batches, both dtypes, all maps
+# ----------------------------------------------------------------------------
+RAGGED = [0, 1, 15, 16, 17, 127, 128, 129, 300, 0, 1000]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["elu1", "favor"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_packed(la, dtype, kind, causal):
+    inp = synthetic.random_inputs(RAGGED, H=3, dk=64, dv=64, dtype=dtype, seed=11,
+                                  qk_scale=(64 ** -0.25 if kind == "favor" else 1.0))
+    om = omega_for(256, 64) if kind == "favor" else None
+    got = _run(la, inp, kind, causal, om)
+    ref = _oracle(inp, kind, causal, om)
+    assert_close(got, ref, dtype, f"{kind} causal={causal}")
+
+
+@pytest.mark.parametrize("shape", [(32, 48, 96), (16, 16, 16), (64, 32, 128)])
+def test_other_head_sizes_fp32(la, shape):
+    dk, dv, r = shape
+    inp = synthetic.random_inputs([70, 5, 200], H=2, dk=dk, dv=dv, dtype="f32", seed=5, qk_scale=dk ** -0.25)
+    om = omega_for(r, dk)
+    for causal in (True, False):
+        assert_close(_run(la, inp, "favor", causal, om), _oracle(inp, "favor", causal, om), "f32")
+
+
+def test_equal_length_batch_without_cu_seqlens(la):
+    inp = synthetic.random_inputs([333] * 3, H=2, dk=64, dv=64, dtype="bf16", seed=8)
+    om = omega_for(256, 64)
+    for causal in (True, False):
+        got = _run(la, inp, "favor", causal, om, cu=False)
+        assert_close(got, _oracle(inp, "favor", causal, om), "bf16")
+
+
+def test_deterministic_and_workspace_contents_do_not_matter(la):
+    inp = synthetic.random_inputs([700, 300], H=2, dk=64, dv=64, dtype="bf16", seed=9)
+    q, k, v = to_torch(inp)
+    om = torch.from_numpy(omega_for(256, 64)).cuda()
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    o1, ws = la.attention(q, k, v, "favor", om, causal=True, cu_seqlens=cu, return_workspace=True)
+    ws.fill_(0xFF)
+    o2 = la.attention(q, k, v, "favor", om, causal=True, cu_seqlens=cu, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert la.la_workspace_error(ws) == 0
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted(la):
+    inp = synthetic.random_inputs([10, 20], H=1, dk=64, dv=64, dtype="f32", seed=1)
+    q, k, v = to_torch(inp)
+    good = torch.tensor([0, 10, 30], dtype=torch.int32, device="cuda")
+    assert la.la_check_cu_seqlens(good, 30)
+    for bad in ([0, 20, 10], [1, 10, 30], [0, 10, 29], [0, -5, 30], [0, 10, 40]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        assert not la.la_check_cu_seqlens(cu, 30)
+        out = torch.full_like(q, 7.0)
+        o, ws = la.attention(q, k, v, "elu1", causal=True, cu_seqlens=cu, out=out, return_workspace=True)
+        assert la.la_workspace_error(ws) == 1
+        assert torch.all(o == 7.0)     # nothing was computed
+
+
+def test_empty_batch(la):
+    z = torch.empty((0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    out = la.la_forward_causal(z, z, z, "elu1", nseq=1)
+    assert out.shape == (0, 2, 64)
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, sampled rows, benchmark launch configuration
+# ----------------------------------------------------------------------------
+def _sample_rows(start, end, rng, n=6):
+    L = end - start
+    cand = {start, end - 1, start + min(L - 1, 127), start + min(L - 1, 128), start + L // 2}
+    cand |= set(int(x) for x in rng.integers(start, end, size=n))
+    return sorted(c for c in cand if start <= c < end)
+
+
+@pytest.mark.parametrize("name", ["elu_causal_b8h8n4096", "favor_bidir_b4h8n16384",
+                                  "favor_causal_b1h16n65536", "favor_causal_varlen64_h8"])
+def test_full_size_workload_sampled_rows(la, name):
+    w = synthetic.workloads()[name]
+    inp = synthetic.make_qkv(w)
+    om = omega_for(w.r, w.dk) if w.map == "favor" else None
+    got = _run(la, inp, w.map, w.causal, om, cu=not w.equal_lengths)
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(0)
+    cu = inp.cu_seqlens
+    seqs = sorted(set([0, len(cu) - 2] + [int(s) for s in rng.integers(0, len(cu) - 1, size=2)]))
+    heads = sorted(set([0, w.H - 1, int(rng.integers(0, w.H))]))
+    worst = 0.0
+    for s in seqs:
+        a, b = int(cu[s]), int(cu[s + 1])
+        for h in heads:
+            rows = _sample_rows(a, b, rng)
+            f = oracle.causal_rows if w.causal else oracle.bidir_rows
+            ref = f(inp.q, inp.k, inp.v, w.map, om, a, b, h, rows, eps=w.eps)
+            e = abs_err_over_rms(got[rows, h], ref)
+            worst = max(worst, e)
+    assert worst <= BF16_RMS_TOL, worst
