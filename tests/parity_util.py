@@ -4,7 +4,11 @@ Tolerances (written out here and asserted in the tests):
 * fp32 path: max over elements of |gpu - oracle| / max(|oracle|, RMS(oracle))
   <= 1e-4 (relative error, with the output RMS as the floor below which an
   element's size does not shrink the allowance);
-* bf16 inputs, fp32 accumulation: max |gpu - oracle| <= 2e-2 * RMS(oracle).
+* bf16 inputs, fp32 accumulation, bf16 output: |gpu - oracle| <= 2e-2 * RMS(oracle)
+  + 2^-8 * |oracle| for every element.  The second term is the rounding of the
+  stored bf16 output itself (at most half an ulp, 2^-8 of the value): early
+  causal rows average few values and sit far above the RMS, so the storage
+  rounding alone can exceed 2e-2 * RMS there.
 """
 import numpy as np
 
@@ -23,12 +27,19 @@ def rel_err_rms_floor(got, ref):
     return float(np.max(np.abs(got - ref) / denom)) if ref.size else 0.0
 
 
-def abs_err_over_rms(got, ref):
+BF16_STORE_REL = 2.0 ** -8
+
+
+def abs_err_over_rms(got, ref, rms=None):
+    """max over elements of (|got - ref| - 2^-8 |ref|) / RMS(ref): the error
+    beyond the bf16 rounding of the stored output, in units of the RMS."""
     got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
     if ref.size == 0:
         return 0.0
-    rms = np.sqrt(np.mean(ref * ref))
-    return float(np.max(np.abs(got - ref)) / (rms if rms > 0 else 1.0))
+    if rms is None:
+        rms = np.sqrt(np.mean(ref * ref))
+    excess = np.abs(got - ref) - BF16_STORE_REL * np.abs(ref)
+    return float(max(0.0, np.max(excess)) / (rms if rms > 0 else 1.0))
 
 
 def assert_close(got, ref, dtype, what=""):
