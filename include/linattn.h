@@ -156,6 +156,41 @@ LA_API la_status la_forward_phase(int causal, int phase, const void* q, const vo
                            int* launched);
 
 /*
+ * la_forward_causal_noalloc - la_forward_causal for callers that cannot
+ *   allocate device memory.  The source pages have no counterpart: this is a
+ *   deployment variant of the same computation, not part of the method.
+ *
+ *   Who needs it: code that must not call cudaMalloc (or any allocator) on
+ *   its hot path - a real-time serving loop whose memory is budgeted up front,
+ *   a plug-in inside a host framework that owns all device memory, or a
+ *   caller whose allocator may not be entered while it issues work.  Such a
+ *   caller passes q, k, v, omega, cu_seqlens and out as usual but no
+ *   workspace.  The scratch lives in one fixed array of
+ *   LA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ *   loads the library keeps until the process exits.
+ *
+ *   Arguments and result are those of la_forward_causal without `workspace`
+ *   and `workspace_bytes`.  Returns LA_ERR_WORKSPACE, before enqueuing
+ *   anything, when the call would need more scratch than
+ *   LA_NOALLOC_SCRATCH_BYTES (la_workspace_bytes(1, ...) gives the need).
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  Every call on a device uses the same array and leaves
+ *   its contents behind; each call rewrites whatever it reads before reading
+ *   it, so nothing needs clearing, but calls whose work overlaps on the GPU
+ *   (different streams, or different host threads) race on the array and
+ *   must be serialised by the caller.  Device-side errors are not reported
+ *   (there is no workspace to read): check cu_seqlens with
+ *   la_check_cu_seqlens beforehand where its contents are not trusted.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
+LA_API la_status la_forward_causal_noalloc(const void* q, const void* k, const void* v,
+                                    const float* omega, int map, int dtype,
+                                    const int32_t* cu_seqlens, int nseq, int64_t T, int H,
+                                    int d_k, int d_v, int r, float eps, void* out, void* stream);
+
+/*
  * la_workspace_bytes - scratch size for a forward call on the current device.
  *   causal: 1 for la_forward_causal, 0 for la_forward_bidir; `has_cu_seqlens`:
  *   1 when a cu_seqlens array will be passed.  Returns 0 for arguments the

@@ -46,6 +46,7 @@ def load_library():
         "la_forward_bidir": (fwd_args, _c_int),
         "la_forward_causal": (fwd_args, _c_int),
         "la_forward_phase": ([_c_int, _c_int] + fwd_args + [ctypes.POINTER(_c_int)], _c_int),
+        "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
         "la_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_int],
                                _c_size),
         "la_check_cu_seqlens": ([_vp, _c_int, _c_i64, _vp], _c_int),
@@ -154,6 +155,30 @@ def la_forward_phase(causal: bool, phase: int, q, k, v, omega, map, dtype, cu_se
                                                     cu_seqlens, nseq, T, H, d_k, d_v, r, eps, out, workspace,
                                                     workspace_bytes, _stream(stream), ctypes.byref(n)))
     return n.value
+
+
+def la_forward_causal_noalloc(q, k, v, map, omega=None, cu_seqlens=None, nseq=None, eps=1e-6, out=None,
+                              stream=None) -> torch.Tensor:
+    """Causal forward whose scratch is the library's fixed device array (no
+    workspace, no device allocation inside the library); see
+    include/linattn.h for the sharing rules."""
+    _need(q, "q"); _need(k, "k"); _need(v, "v")
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    m = _map_id(map)
+    r = omega.shape[0] if m == MAP_IDS["favor"] else d_k
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        nseq = cu_seqlens.numel() - 1
+    elif nseq is None:
+        nseq = 1
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    _need(out, "out", q.dtype)
+    _check("la_forward_causal_noalloc", load_library().la_forward_causal_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype], _ptr(cu_seqlens), nseq, T, H, d_k, d_v, r,
+        eps, _ptr(out), _stream(stream)))
+    return out
 
 
 def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream):

@@ -140,6 +140,15 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
 }
 
 }  // namespace
+
+la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, const void* k, const void* v,
+                        const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
+                        int H, int dk, int dv, int r, float eps, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream, int* launched) {
+    return forward(causal, phase_lo, phase_hi, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, dk, dv, r, eps,
+                   out, workspace, workspace_bytes, stream, launched);
+}
+
 }  // namespace la
 
 using namespace la;

@@ -23,6 +23,13 @@ cudaError_t simt_feature_map(const void* x, const float* omega, int map, int dty
 cudaError_t simt_state(const FwdParams& p, int dtype, cudaStream_t s);
 cudaError_t simt_out(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_t s);
 
+// The forward dispatcher behind the C entry points (api.cu): phases
+// phase_lo..phase_hi of a bidirectional (causal = 0) or causal call.
+la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, const void* k, const void* v,
+                        const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
+                        int H, int dk, int dv, int r, float eps, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream, int* launched);
+
 // Orthogonal random features (orf.cu).
 cudaError_t orf_build(const double* blocks, const double* lengths, int r, int d, float* omega,
                       cudaStream_t s);
