@@ -33,8 +33,10 @@ la_status check_dims(int map, int dtype, int nseq, int64_t T, int H, int dk, int
     return LA_OK;
 }
 
-int select_path(int /*causal*/, int /*map*/, int /*dtype*/, int /*dk*/, int /*dv*/, int /*r*/) {
-    return kPathSimt;
+// Tensor cores for bf16 shapes the tcgen05 kernels cover; fp32 (exact
+// arithmetic) and every other shape on CUDA cores.
+int select_path(int /*causal*/, int map, int dtype, int dk, int dv, int r) {
+    return (dtype == LA_BF16 && tc_supported(map, dk, dv, r)) ? kPathTensor : kPathSimt;
 }
 
 int path_chunk(int path) { return path == kPathTensor ? 128 : simt_chunk(); }
@@ -91,7 +93,11 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     const size_t esz = dtype == LA_F32 ? 4 : 2;
     if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(out, esz)) return LA_ERR_INVALID_ARG;
     if (omega && !aligned(omega, 4)) return LA_ERR_INVALID_ARG;
-    const int path = select_path(causal, map, dtype, dk, dv, r);
+    int path = select_path(causal, map, dtype, dk, dv, r);
+    // TMA and vector loads need 16-byte aligned operands
+    if (path == kPathTensor && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) &&
+                                 (omega == nullptr || aligned(omega, 16))))
+        path = kPathSimt;
     if ((st = path_supported(path, map, dk, dv, r)) != LA_OK) return st;
     const int nsm = device_sm_count();
     if (nsm <= 0) return LA_ERR_CUDA;
@@ -123,13 +129,20 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
             case LA_PHASE_PLAN:
                 e = launch_plan(p, s); ++n; break;
             case LA_PHASE_STATE:
-                if (T > 0 && need_state) { e = simt_state(p, dtype, s); ++n; }
+                if (T > 0 && need_state) {
+                    e = path == kPathTensor ? tc_state(p, s) : simt_state(p, dtype, s);
+                    ++n;
+                }
                 break;
             case LA_PHASE_SCAN:
                 if (T > 0 && need_state) { e = launch_scan(p, s); ++n; }
                 break;
             case LA_PHASE_OUTPUT:
-                if (T > 0) { e = simt_out(p, dtype, need_state ? 0 : 1, s); ++n; }
+                if (T > 0) {
+                    e = path == kPathTensor ? tc_out(p, need_state ? 0 : 1, s)
+                                            : simt_out(p, dtype, need_state ? 0 : 1, s);
+                    ++n;
+                }
                 break;
             default:
                 return LA_ERR_INVALID_ARG;
@@ -164,8 +177,15 @@ la_status la_feature_map(const void* x, const float* omega, int map, int dtype, 
     if (!x || !phi) return LA_ERR_INVALID_ARG;
     const size_t esz = dtype == LA_F32 ? 4 : 2;
     if (!aligned(x, esz) || !aligned(phi, 4) || (omega && !aligned(omega, 4))) return LA_ERR_INVALID_ARG;
-    if (simt_fmap_smem_bytes(map, d, r) > kSmemLimitBytes) return LA_ERR_UNSUPPORTED;
-    cudaError_t e = simt_feature_map(x, omega, map, dtype, T, H, d, r, phi, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (dtype == LA_BF16 && map == LA_MAP_FAVOR && tc_supported(map, d, d, r) && aligned(x, 16) &&
+        aligned(omega, 16) && aligned(phi, 16)) {
+        // same projection and exponent as the forward's tensor-core path, before the bf16 rounding
+        e = tc_feature_map(x, omega, T, H, r, phi, nullptr, static_cast<cudaStream_t>(stream));
+    } else {
+        if (simt_fmap_smem_bytes(map, d, r) > kSmemLimitBytes) return LA_ERR_UNSUPPORTED;
+        e = simt_feature_map(x, omega, map, dtype, T, H, d, r, phi, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

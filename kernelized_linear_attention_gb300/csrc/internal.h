@@ -30,6 +30,14 @@ la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, c
                         int H, int dk, int dv, int r, float eps, void* out, void* workspace,
                         size_t workspace_bytes, void* stream, int* launched);
 
+// tcgen05 tensor-core path (tc.cu): bf16, d_k = d_v = 64, r in {64, 128, 256}
+// (FAVOR+) or r = 64 (ELU+1, identity); 16-byte aligned operands.
+bool tc_supported(int map, int dk, int dv, int r);
+cudaError_t tc_state(const FwdParams& p, cudaStream_t s);
+cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
+cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
+                           cudaStream_t s);
+
 // Orthogonal random features (orf.cu).
 cudaError_t orf_build(const double* blocks, const double* lengths, int r, int d, float* omega,
                       cudaStream_t s);

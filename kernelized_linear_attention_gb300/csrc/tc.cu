@@ -1,0 +1,853 @@
+// Tensor-core (tcgen05) kernels for bf16 inputs with d_k = d_v = 64.
+//
+// A chunk is 128 consecutive tokens of one head; one CTA owns one unit (a
+// segment of a sequence) of one head and walks its chunks in order:
+//
+//   FAVOR+ projection   P = X Omega'^T with Omega' = log2(e) Omega held as two
+//                       bf16 parts (hi + lo, ~16 significant bits), so the
+//                       exponent carries no bf16 rounding of Omega; epilogue
+//                       phi = 2^(P - c), c = log2(e) |x|^2/2 + log2(sqrt r)
+//                       ("The Kernel Zoo" §4.2, "Performer" §2 Step 3), rounded
+//                       to bf16 as the operand of the next products
+//   ELU+1 / identity    phi computed element-wise from the staged tile
+//   causal scores       A (+)= Phi_Q Phi_K^T                  (TMEM, fp32)
+//   cross-chunk readout O (+)= Phi_Q [S|z]  (state before this chunk, bf16;
+//                       hi + lo parts in the bidirectional kernel)
+//   state update        [S|z] += Phi_K^T [V|1]                (TMEM, fp32, carried)
+//   causal in-chunk     O += tril(A) [V|1]  (diagonal included, "The Kernel Zoo" §1.3),
+//                       A as bf16 hi + lo parts from tensor memory
+//   store               out = O[:, :64] / max(O[:, 64], eps)  ("Performer" §3 sketch clamp)
+//
+// The ones column of [V|1] makes column 64 of every state z and of every
+// numerator the denominator, so numerator and denominator see the same
+// rounded weights.  The causal kernel processes the feature dimension in
+// halves of 128 (keys) and quarters of 64 (queries) so that its operands fit
+// in shared memory; the bidirectional output kernel reads the whole-sequence
+// state; the state kernel only projects k and updates the state.
+//
+// Shared-memory operands use the 128-byte-swizzled [rows][64] layout of
+// tc_ptx.cuh.  One thread issues TMA and MMA; all 4 warps run the epilogues
+// (warp w owns TMEM lanes 32w..32w+31).  Waits are bounded: a wait that runs
+// out records LA_DEVERR_WAIT_TIMEOUT in the workspace, drains outstanding
+// MMAs, frees TMEM and returns.
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;                          // tokens per chunk
+constexpr int kThreads = 128;
+constexpr uint32_t kTile = kC * 64 * 2;          // [128][64] bf16 = 16 KB
+constexpr uint32_t kOmgBytes = 256 * 128;        // Omega' part [256][64] bf16 = 32 KB
+constexpr int kNX = 80;                          // d_v + ones column, padded to a multiple of 16
+constexpr uint32_t kSbfBlock = kNX * 128;        // [80][64] bf16 = 10 KB
+
+// Tensor-memory columns (512 allocated).
+constexpr uint32_t kColS = 0;     // state, one 80-column block per feature half (lanes = features)
+constexpr uint32_t kColA = 160;   // causal scores [128 q][128 k]
+constexpr uint32_t kColO = 288;   // numerator | denominator [128][80]
+constexpr uint32_t kColP = 368;   // projection of up to 128 features [128][128]
+constexpr uint32_t kTmemCols = 512;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+typedef unsigned char Tile[kTile];
+
+struct Bars {
+    uint64_t load;
+    uint64_t mma;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int pad;
+};
+
+// Causal output kernel: 216 KB.
+struct __align__(1024) CausalSmem {
+    unsigned char omg_hi[kOmgBytes];
+    unsigned char omg_lo[kOmgBytes];
+    Tile tq, tk, tv;
+    Tile ones;                        // second MN atom of [V|1]: column 0 = 1
+    Tile phq;                         // Phi_Q of one 64-feature quarter
+    Tile phk[2];                      // Phi_K of one 128-feature half
+    unsigned char sbf[4][kSbfBlock];  // [S|z]^T bf16: block j = features 64j..64j+63, rows n < 80
+    Bars b;
+};
+
+// Bidirectional output kernel: 192 KB.
+struct __align__(1024) BidirSmem {
+    unsigned char omg_hi[kOmgBytes];
+    unsigned char omg_lo[kOmgBytes];
+    Tile tq;
+    Tile phq[2];                      // Phi_Q of one 128-feature half
+    unsigned char shi[4][kSbfBlock];  // whole-sequence [S|z]^T, bf16 high part
+    unsigned char slo[4][kSbfBlock];  // and the bf16 rounding remainder
+    Bars b;
+};
+
+// Segment-state kernel: 144 KB.
+struct __align__(1024) StateSmem {
+    unsigned char omg_hi[kOmgBytes];
+    unsigned char omg_lo[kOmgBytes];
+    Tile tk, tv, ones;
+    Tile phk[2];
+    Bars b;
+};
+
+// Feature-map kernel: 80 KB.
+struct __align__(1024) FmapSmem {
+    unsigned char omg_hi[kOmgBytes];
+    unsigned char omg_lo[kOmgBytes];
+    Tile tq;
+    Bars b;
+};
+
+template <typename S>
+constexpr size_t smem_bytes() { return sizeof(S) + 1024; }
+
+template <typename S>
+__device__ __forceinline__ S& smem_ref() {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    return *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+}
+
+struct TcParams {
+    FwdParams p;
+    int prefix_is_zero;
+};
+
+// ---------------------------------------------------------------------------
+// Set-up helpers
+// ---------------------------------------------------------------------------
+// Omega' = log2(e) * Omega as bf16 hi + lo, [r][64] each, K-major swizzled
+// (the B operand of the projection).  lo = bf16(Omega' - hi).
+__device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* omega, int r) {
+    for (int i = threadIdx.x; i < r * 8; i += kThreads) {
+        const int row = i >> 3, c = i & 7;
+        const float4* src = reinterpret_cast<const float4*>(omega + row * 64 + c * 8);
+        const float4 a = src[0], b = src[1];
+        const float x[8] = {a.x * kLog2e, a.y * kLog2e, a.z * kLog2e, a.w * kLog2e,
+                            b.x * kLog2e, b.y * kLog2e, b.z * kLog2e, b.w * kLog2e};
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            wh[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+            wl[j] = pack_bf16x2(x[2 * j] - bf16lo(wh[j]), x[2 * j + 1] - bf16hi(wh[j]));
+        }
+        *reinterpret_cast<uint4*>(hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+}
+
+__device__ void fill_ones(unsigned char* blk) {
+    for (int i = threadIdx.x; i < kC * 8; i += kThreads) {
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(blk + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+    }
+}
+
+__device__ __forceinline__ void zero_row(unsigned char* blk, int t) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(blk + sw128_chunk(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// |x_t|^2 of row t of a staged [128][64] bf16 tile.
+__device__ float row_sq_norm(const unsigned char* tile, int t) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = bf16lo(ws[j]), hi = bf16hi(ws[j]);
+            s = fmaf(lo, lo, s);
+            s = fmaf(hi, hi, s);
+        }
+    }
+    return s;
+}
+
+// Exponent offset of the FAVOR+ epilogue for row t: log2(e) |x|^2 / 2 + log2(sqrt r).
+__device__ __forceinline__ float favor_offset(const unsigned char* tile, int t, int r) {
+    return row_sq_norm(tile, t) * (0.5f * kLog2e) + 0.5f * __log2f((float)r);
+}
+
+// Element-wise phi (ELU+1 or identity) of row t of a tile into the same
+// position of dst (row t; zero when the row is past the unit's end).
+__device__ void elementwise_phi_row(const unsigned char* tile, unsigned char* dst, int t, bool valid, int map) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo = bf16lo(ws[j]), hi = bf16hi(ws[j]);
+                if (map == LA_MAP_ELU1) {
+                    lo = lo > 0.f ? lo + 1.f : ex2_approx(lo * kLog2e);
+                    hi = hi > 0.f ? hi + 1.f : ex2_approx(hi * kLog2e);
+                }
+                ws[j] = pack_bf16x2(lo, hi);
+            }
+            o = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, c)) = o;
+    }
+}
+
+// 32 fp32 values of row t, columns f0..f0+31 -> bf16 into 64-wide blocks blk[f0 / 64].
+__device__ __forceinline__ void store_row32_bf16(unsigned char* blk0, int t, int f0, const uint32_t (&w)[16]) {
+    unsigned char* blk = blk0 + kTile * (f0 >> 6);
+    const int cb = (f0 & 63) >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(blk + sw128_chunk(t, cb + q)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Projection epilogue: P (TMEM columns kColP.., lane = token) -> phi = 2^(p - c)
+// -> bf16 K-major blocks starting at dst (nf features, a multiple of 32).
+__device__ void projection_epilogue(uint32_t tbase, int nf, float c, bool valid, unsigned char* dst) {
+    const int warp = threadIdx.x >> 5, t = threadIdx.x;
+    for (int f0 = 0; f0 < nf; f0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tbase, warp * 32, kColP + f0), v);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float a = valid ? ex2_approx(__uint_as_float(v[2 * j]) - c) : 0.f;
+            const float b = valid ? ex2_approx(__uint_as_float(v[2 * j + 1]) - c) : 0.f;
+            w[j] = pack_bf16x2(a, b);
+        }
+        store_row32_bf16(dst, t, f0, w);
+    }
+}
+
+// fp32 projection epilogue for la_feature_map: phi = 2^(p - c) to global fp32.
+__device__ void projection_to_global(uint32_t tbase, int nf, float c, bool valid, float* dst) {
+    const int warp = threadIdx.x >> 5;
+    for (int f0 = 0; f0 < nf; f0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tbase, warp * 32, kColP + f0), v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 o = make_float4(ex2_approx(__uint_as_float(v[j]) - c),
+                                             ex2_approx(__uint_as_float(v[j + 1]) - c),
+                                             ex2_approx(__uint_as_float(v[j + 2]) - c),
+                                             ex2_approx(__uint_as_float(v[j + 3]) - c));
+                *reinterpret_cast<float4*>(dst + f0 + j) = o;
+            }
+        }
+    }
+}
+
+// State of one feature half (TMEM lanes = features, 80 columns) -> bf16 rows n of
+// the K-major readout blocks sbf[2 half], sbf[2 half + 1] (thread f owns feature 128 half + f).
+__device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, int half) {
+    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+    unsigned char* blk = sbf[2 * half + (f >> 6)];
+    const uint32_t col = f & 63;
+#pragma unroll 1
+    for (int n0 = 0; n0 < kNX; n0 += 16) {
+        uint32_t w[16];
+        tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<__nv_bfloat16*>(blk + sw128_off(n0 + j, col)) =
+                __float2bfloat16_rn(__uint_as_float(w[j]));
+    }
+}
+
+// The fp32 state a unit starts from ([r][65] in global; zero if `zero`):
+// into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
+// rounding remainder into lo when lo != nullptr).
+__device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[kSbfBlock], uint32_t tbase,
+                           bool to_tmem, const float* src, int r, int nhalves, bool zero) {
+    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+    for (int half = 0; half < nhalves; ++half) {
+        const int feat = 128 * half + f;
+        const bool have = !zero && feat < r;
+        const int blk = 2 * half + (f >> 6);
+        for (int n0 = 0; n0 < kNX; n0 += 16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                const float x = (have && n < 65) ? src[(int64_t)feat * 65 + n] : 0.f;
+                w[j] = __float_as_uint(x);
+                const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+                *reinterpret_cast<__nv_bfloat16*>(hi[blk] + sw128_off(n, f & 63)) = xh;
+                if (lo != nullptr)
+                    *reinterpret_cast<__nv_bfloat16*>(lo[blk] + sw128_off(n, f & 63)) =
+                        __float2bfloat16_rn(x - __bfloat162float(xh));
+            }
+            if (to_tmem) tmem_st16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
+        }
+    }
+    if (to_tmem) tmem_st_wait();
+}
+
+// Writes the fp32 state held in TMEM (features < r, 65 columns) to global [r][65].
+__device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves) {
+    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+    for (int half = 0; half < nhalves; ++half) {
+        const int feat = 128 * half + f;
+        for (int n0 = 0; n0 < kNX; n0 += 16) {
+            uint32_t w[16];
+            tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
+            tmem_ld_wait();
+            if (feat < r) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (n0 + j < 65) dst[(int64_t)feat * 65 + n0 + j] = __uint_as_float(w[j]);
+            }
+        }
+    }
+}
+
+// out row t = O[t][0..63] / max(O[t][64], eps), bf16, to global (when valid).
+__device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat16* dst_row) {
+    const int warp = threadIdx.x >> 5;
+    uint32_t a[32], b[32], c[16];
+    tmem_ld32(tmem_addr(tbase, warp * 32, kColO), a);
+    tmem_ld32(tmem_addr(tbase, warp * 32, kColO + 32), b);
+    tmem_ld16(tmem_addr(tbase, warp * 32, kColO + 64), c);
+    tmem_ld_wait();
+    if (!valid) return;
+    const float inv = 1.0f / fmaxf(__uint_as_float(c[0]), eps);
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]) * inv, __uint_as_float(a[8 * q + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(a[8 * q + 2]) * inv, __uint_as_float(a[8 * q + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(a[8 * q + 4]) * inv, __uint_as_float(a[8 * q + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(a[8 * q + 6]) * inv, __uint_as_float(a[8 * q + 7]) * inv));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        dst[4 + q] = make_uint4(pack_bf16x2(__uint_as_float(b[8 * q]) * inv, __uint_as_float(b[8 * q + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(b[8 * q + 2]) * inv, __uint_as_float(b[8 * q + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(b[8 * q + 4]) * inv, __uint_as_float(b[8 * q + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(b[8 * q + 6]) * inv, __uint_as_float(b[8 * q + 7]) * inv));
+}
+
+// ---------------------------------------------------------------------------
+// Synchronisation and MMA helpers
+// ---------------------------------------------------------------------------
+// Every thread waits for the phase; returns false for all threads if any timed out.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __syncthreads_or(!ok) == 0;
+}
+// Shared-memory writes and TMEM reads of all threads are done before the MMA issuer proceeds.
+__device__ __forceinline__ void handoff_to_mma() {
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// D (+)= A B^T, both K-major in 64-wide blocks: A blocks a0 + a_stride*j, B blocks b0 + b_stride*j.
+__device__ __forceinline__ void mma_kk(uint32_t d, const unsigned char* a0, uint32_t a_stride, const unsigned char* b0,
+                                       uint32_t b_stride, int ksteps, uint32_t idesc, bool accumulate) {
+    for (int k = 0; k < ksteps; ++k) {
+        const uint64_t ad = sdesc_sw128(smem_u32(a0) + a_stride * (k >> 2) + 32u * (k & 3), 16, 1024);
+        const uint64_t bd = sdesc_sw128(smem_u32(b0) + b_stride * (k >> 2) + 32u * (k & 3), 16, 1024);
+        mma_ss(d, ad, bd, idesc, (accumulate || k > 0) ? 1u : 0u);
+    }
+}
+
+// P = X Omega'^T for `nf` features starting at feature f0: X tile (K = 64) times
+// the hi part, then the lo part accumulated.
+__device__ __forceinline__ void mma_projection(uint32_t tbase, const unsigned char* x, const unsigned char* omg_hi,
+                                               const unsigned char* omg_lo, int f0, int nf) {
+    const uint32_t idesc = idesc_bf16(128, nf, false, false);
+    mma_kk(tbase + kColP, x, 0, omg_hi + 128u * f0, 0, 4, idesc, false);
+    mma_kk(tbase + kColP, x, 0, omg_lo + 128u * f0, 0, 4, idesc, true);
+}
+
+// [S|z] (+)= Phi_K^T [V|1]: A MN-major (features contiguous, blocks phk0, phk0 + kTile),
+// B MN-major (tv | ones at tv + lbo).
+__device__ __forceinline__ void mma_state_update(uint32_t d, const unsigned char* phk0, const unsigned char* tv,
+                                                 const unsigned char* ones) {
+    const uint32_t idesc = idesc_bf16(128, kNX, true, true);
+    const uint32_t lbo_b = smem_u32(ones) - smem_u32(tv);
+    for (int k = 0; k < kC / 16; ++k)
+        mma_ss(d, sdesc_sw128(smem_u32(phk0) + 2048u * k, kTile, 1024),
+               sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
+}
+
+// O += tril(A) [V|1] with the masked scores as two bf16 parts in tensor memory
+// (a_hi, a_lo: 64 columns each, two keys per column), B MN-major.
+__device__ __forceinline__ void mma_in_chunk(uint32_t d, uint32_t a_hi, uint32_t a_lo, const unsigned char* tv,
+                                             const unsigned char* ones) {
+    const uint32_t idesc = idesc_bf16(128, kNX, false, true);
+    const uint32_t lbo_b = smem_u32(ones) - smem_u32(tv);
+    for (int k = 0; k < kC / 16; ++k)
+        mma_ts(d, a_hi + 8u * k, sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
+    for (int k = 0; k < kC / 16; ++k)
+        mma_ts(d, a_lo + 8u * k, sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
+}
+
+__device__ void setup_bars(Bars& b) {
+    if (threadIdx.x == 0) {
+        mbar_init(&b.load, 1);
+        mbar_init(&b.mma, 1);
+        mbar_init(&b.drain, 1);
+        fence_mbar_init();
+    }
+    if ((threadIdx.x >> 5) == 0) {
+        tmem_alloc(&b.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+}
+
+// After a timed-out wait: record it, wait (bounded) for this CTA's MMAs to finish.
+__device__ void drain_after_timeout(Bars& b, int* err) {
+    if (threadIdx.x == 0) {
+        if (err) atomicMax(err, LA_DEVERR_WAIT_TIMEOUT);
+        mma_commit(&b.drain);
+        mbar_wait(&b.drain, 0, 500000000ull);
+    }
+    __syncthreads();
+}
+
+__device__ void teardown(Bars& b) {
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(b.tmem_base, kTmemCols);
+}
+
+// Pending-phase tracker for one mbarrier (all threads keep the same copy).
+struct Phase {
+    uint32_t bit = 0;
+    __device__ __forceinline__ bool wait(uint64_t* bar) {
+        const bool ok = wait_all(bar, bit);
+        bit ^= 1u;
+        return ok;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Causal output kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_v, const TcParams tp) {
+    const FwdParams& p = tp.p;
+    const int u = blockIdx.x, head = blockIdx.y;
+    if (u >= p.hdr->n_units) return;
+    const Unit un = p.units[u];
+    CausalSmem& s = smem_ref<CausalSmem>();
+    const int t = threadIdx.x, warp = t >> 5;
+    const int r = p.r;
+    const bool favor = p.map == LA_MAP_FAVOR;
+    const int fh = r < 128 ? r : 128;             // key features per half
+    const int nhalves = (r + 127) / 128;
+    const int nq = fh / 64;                       // query quarters per half
+
+    if (t == 0) { prefetch_tensormap(&map_q); prefetch_tensormap(&map_k); prefetch_tensormap(&map_v); }
+    setup_bars(s.b);
+    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+    fill_ones(s.ones);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = s.b.tmem_base;
+    const int64_t E = (int64_t)r * 65;
+    load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
+               tp.prefix_is_zero != 0);
+    handoff_to_mma();
+
+    if (t == 0) {
+        mbar_arrive_expect_tx(&s.b.load, 3 * kTile);
+        tma_load_3d(s.tq, &map_q, 0, head, un.start, &s.b.load);
+        tma_load_3d(s.tk, &map_k, 0, head, un.start, &s.b.load);
+        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load);
+    }
+    const uint32_t id_scores = idesc_bf16(128, 128, false, false);
+    const uint32_t id_read = idesc_bf16(128, kNX, false, false);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    Phase lp, mp;
+    bool ok = true;
+
+    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
+        const bool valid = t < min(kC, un.end - t0);
+        if (!(ok = lp.wait(&s.b.load))) break;
+        const float cq = favor ? favor_offset(s.tq, t, r) : 0.f;
+        const float ck = favor ? favor_offset(s.tk, t, r) : 0.f;
+        for (int half = 0; half < nhalves && ok; ++half) {
+            // Phi_K of this half of the features
+            if (favor) {
+                if (t == 0) {
+                    mma_projection(tb, s.tk, s.omg_hi, s.omg_lo, 128 * half, fh);
+                    mma_commit(&s.b.mma);
+                }
+                if (!(ok = mp.wait(&s.b.mma))) break;
+                tc_fence_after();
+                projection_epilogue(tb, fh, ck, valid, s.phk[0]);
+            } else {
+                elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
+            }
+            if (fh < 128) zero_row(s.phk[1], t);   // unused feature rows of the update stay zero
+            for (int jq = 0; jq < nq; ++jq) {
+                // Phi_Q of one quarter (64 features)
+                if (favor) {
+                    tc_fence_before();
+                    __syncthreads();
+                    tc_fence_after();
+                    if (t == 0) {
+                        mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half + 64 * jq, 64);
+                        mma_commit(&s.b.mma);
+                    }
+                    if (!(ok = mp.wait(&s.b.mma))) break;
+                    tc_fence_after();
+                    projection_epilogue(tb, 64, cq, valid, s.phq);
+                } else {
+                    elementwise_phi_row(s.tq, s.phq, t, valid, p.map);
+                }
+                handoff_to_mma();
+                if (t == 0) {
+                    const bool first = half == 0 && jq == 0;
+                    mma_kk(tb + kColA, s.phq, 0, s.phk[jq], 0, 4, id_scores, !first);
+                    mma_kk(tb + kColO, s.phq, 0, s.sbf[2 * half + jq], 0, 4, id_read, !first);
+                    if (jq == nq - 1) mma_state_update(tb + kColS + 80 * half, s.phk[0], s.tv, s.ones);
+                    mma_commit(&s.b.mma);
+                }
+                if (!(ok = mp.wait(&s.b.mma))) break;
+                tc_fence_after();
+            }
+        }
+        if (!ok) break;
+        // masked scores (key j <= query t) as bf16 hi + lo parts in tensor memory: the
+        // hi part replaces the fp32 scores in place (keys 2c, 2c+1 in column c; every
+        // column written has been read), the lo part goes to the free projection columns
+        for (int j0 = 0; j0 < kC; j0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem_addr(tb, warp * 32, kColA + j0), v);
+            tmem_ld_wait();
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int c0 = j0 + 2 * j;
+                const float a = c0 <= t ? __uint_as_float(v[2 * j]) : 0.f;
+                const float b = c0 + 1 <= t ? __uint_as_float(v[2 * j + 1]) : 0.f;
+                hi[j] = pack_bf16x2(a, b);
+                lo[j] = pack_bf16x2(a - bf16lo(hi[j]), b - bf16hi(hi[j]));
+            }
+            tmem_st16(tmem_addr(tb, warp * 32, kColA + j0 / 2), hi);
+            tmem_st16(tmem_addr(tb, warp * 32, kColP + j0 / 2), lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (t == 0) {
+            mma_in_chunk(tb + kColO, tb + kColA, tb + kColP, s.tv, s.ones);
+            mma_commit(&s.b.mma);
+        }
+        if (!(ok = mp.wait(&s.b.mma))) break;
+        tc_fence_after();
+        // every tile of this chunk has been consumed: prefetch the next chunk
+        if (t == 0 && t0 + kC < un.end) {
+            mbar_arrive_expect_tx(&s.b.load, 3 * kTile);
+            tma_load_3d(s.tq, &map_q, 0, head, t0 + kC, &s.b.load);
+            tma_load_3d(s.tk, &map_k, 0, head, t0 + kC, &s.b.load);
+            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load);
+        }
+        store_output(tb, p.eps, valid, out + ((int64_t)(t0 + t) * p.H + head) * 64);
+        for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half);
+        handoff_to_mma();
+    }
+    if (!ok) drain_after_timeout(s.b, &p.hdr->error);
+    teardown(s.b);
+}
+
+// ---------------------------------------------------------------------------
+// Bidirectional output kernel: out = Phi_Q [S|z] / ..., [S|z] the whole-sequence state
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp) {
+    const FwdParams& p = tp.p;
+    const int u = blockIdx.x, head = blockIdx.y;
+    if (u >= p.hdr->n_units) return;
+    const Unit un = p.units[u];
+    BidirSmem& s = smem_ref<BidirSmem>();
+    const int t = threadIdx.x;
+    const int r = p.r;
+    const bool favor = p.map == LA_MAP_FAVOR;
+    const int fh = r < 128 ? r : 128;
+    const int nhalves = (r + 127) / 128;
+
+    if (t == 0) prefetch_tensormap(&map_q);
+    setup_bars(s.b);
+    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = s.b.tmem_base;
+    load_state(s.shi, s.slo, tb, false, p.prefix + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves, false);
+    handoff_to_mma();
+    if (t == 0) {
+        mbar_arrive_expect_tx(&s.b.load, kTile);
+        tma_load_3d(s.tq, &map_q, 0, head, un.start, &s.b.load);
+    }
+    const uint32_t id_read = idesc_bf16(128, kNX, false, false);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    Phase lp, mp;
+    bool ok = true;
+    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
+        const bool valid = t < min(kC, un.end - t0);
+        if (!(ok = lp.wait(&s.b.load))) break;
+        const float cq = favor ? favor_offset(s.tq, t, r) : 0.f;
+        for (int half = 0; half < nhalves && ok; ++half) {
+            if (favor) {
+                if (t == 0) {
+                    mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
+                    mma_commit(&s.b.mma);
+                }
+                if (!(ok = mp.wait(&s.b.mma))) break;
+                tc_fence_after();
+                projection_epilogue(tb, fh, cq, valid, s.phq[0]);
+            } else {
+                elementwise_phi_row(s.tq, s.phq[0], t, valid, p.map);
+            }
+            handoff_to_mma();
+            if (t == 0) {
+                const int ks = fh / 16;
+                mma_kk(tb + kColO, s.phq[0], kTile, s.shi[2 * half], kSbfBlock, ks, id_read, half > 0);
+                mma_kk(tb + kColO, s.phq[0], kTile, s.slo[2 * half], kSbfBlock, ks, id_read, true);
+                mma_commit(&s.b.mma);
+            }
+            if (!(ok = mp.wait(&s.b.mma))) break;
+            tc_fence_after();
+        }
+        if (!ok) break;
+        if (t == 0 && t0 + kC < un.end) {
+            mbar_arrive_expect_tx(&s.b.load, kTile);
+            tma_load_3d(s.tq, &map_q, 0, head, t0 + kC, &s.b.load);
+        }
+        store_output(tb, p.eps, valid, out + ((int64_t)(t0 + t) * p.H + head) * 64);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!ok) drain_after_timeout(s.b, &p.hdr->error);
+    teardown(s.b);
+}
+
+// ---------------------------------------------------------------------------
+// Segment-state kernel: sum over the unit of phi(k) [v | 1]^T
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                const TcParams tp) {
+    const FwdParams& p = tp.p;
+    const int u = blockIdx.x, head = blockIdx.y;
+    if (u >= p.hdr->n_units) return;
+    const Unit un = p.units[u];
+    StateSmem& s = smem_ref<StateSmem>();
+    const int t = threadIdx.x, warp = t >> 5;
+    const int r = p.r;
+    const bool favor = p.map == LA_MAP_FAVOR;
+    const int fh = r < 128 ? r : 128;
+    const int nhalves = (r + 127) / 128;
+    if (t == 0) { prefetch_tensormap(&map_k); prefetch_tensormap(&map_v); }
+    setup_bars(s.b);
+    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+    fill_ones(s.ones);
+    zero_row(s.phk[1], t);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = s.b.tmem_base;
+    {
+        uint32_t z[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] = 0u;
+        for (int half = 0; half < nhalves; ++half)
+            for (int n0 = 0; n0 < kNX; n0 += 16) tmem_st16(tmem_addr(tb, warp * 32, kColS + 80 * half + n0), z);
+        tmem_st_wait();
+    }
+    handoff_to_mma();
+    if (t == 0) {
+        mbar_arrive_expect_tx(&s.b.load, 2 * kTile);
+        tma_load_3d(s.tk, &map_k, 0, head, un.start, &s.b.load);
+        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load);
+    }
+    Phase lp, mp;
+    bool ok = true;
+    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
+        const bool valid = t < min(kC, un.end - t0);
+        if (!(ok = lp.wait(&s.b.load))) break;
+        const float ck = favor ? favor_offset(s.tk, t, r) : 0.f;
+        for (int half = 0; half < nhalves && ok; ++half) {
+            if (favor) {
+                if (t == 0) {
+                    mma_projection(tb, s.tk, s.omg_hi, s.omg_lo, 128 * half, fh);
+                    mma_commit(&s.b.mma);
+                }
+                if (!(ok = mp.wait(&s.b.mma))) break;
+                tc_fence_after();
+                projection_epilogue(tb, fh, ck, valid, s.phk[0]);
+            } else {
+                elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
+            }
+            handoff_to_mma();
+            if (t == 0) {
+                mma_state_update(tb + kColS + 80 * half, s.phk[0], s.tv, s.ones);
+                mma_commit(&s.b.mma);
+            }
+            if (!(ok = mp.wait(&s.b.mma))) break;
+            tc_fence_after();
+        }
+        if (!ok) break;
+        if (t == 0 && t0 + kC < un.end) {
+            mbar_arrive_expect_tx(&s.b.load, 2 * kTile);
+            tma_load_3d(s.tk, &map_k, 0, head, t0 + kC, &s.b.load);
+            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load);
+        }
+    }
+    if (ok) store_state(tb, p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves);
+    else drain_after_timeout(s.b, &p.hdr->error);
+    teardown(s.b);
+}
+
+// ---------------------------------------------------------------------------
+// FAVOR+ feature map to global fp32 (la_feature_map for bf16 input)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+tc_fmap_kernel(const __grid_constant__ CUtensorMap map_x, const float* omega, int T, int H, int r, float* phi,
+               int* err) {
+    FmapSmem& s = smem_ref<FmapSmem>();
+    const int t = threadIdx.x, head = blockIdx.y;
+    const int t0 = blockIdx.x * kC;
+    const int fh = r < 128 ? r : 128;
+    const int nhalves = (r + 127) / 128;
+    if (t == 0) prefetch_tensormap(&map_x);
+    setup_bars(s.b);
+    stage_omega(s.omg_hi, s.omg_lo, omega, r);
+    handoff_to_mma();
+    const uint32_t tb = s.b.tmem_base;
+    if (t == 0) {
+        mbar_arrive_expect_tx(&s.b.load, kTile);
+        tma_load_3d(s.tq, &map_x, 0, head, t0, &s.b.load);
+    }
+    Phase lp, mp;
+    bool ok = lp.wait(&s.b.load);
+    if (ok) {
+        const float c = favor_offset(s.tq, t, r);
+        const bool valid = t0 + t < T;
+        for (int half = 0; half < nhalves; ++half) {
+            if (t == 0) {
+                mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
+                mma_commit(&s.b.mma);
+            }
+            if (!(ok = mp.wait(&s.b.mma))) break;
+            tc_fence_after();
+            projection_to_global(tb, fh, c, valid, phi + ((int64_t)(t0 + t) * H + head) * r + 128 * half);
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+    }
+    if (!ok) drain_after_timeout(s.b, err);
+    teardown(s.b);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// [T, H, 64] bf16 -> boxes of 128 tokens x 64 features of one head, 128-byte swizzle.
+bool make_row_map(CUtensorMap* m, const void* base, int64_t T, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {64 * 2, (cuuint64_t)H * 64 * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kC};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+bool tc_supported(int map, int dk, int dv, int r) {
+    if (dk != 64 || dv != 64) return false;
+    if (map == LA_MAP_FAVOR) return r == 64 || r == 128 || r == 256;
+    return r == 64;
+}
+
+cudaError_t tc_state(const FwdParams& p, cudaStream_t s) {
+    CUtensorMap mk, mv;
+    if (!make_row_map(&mk, p.k, p.T, p.H) || !make_row_map(&mv, p.v, p.T, p.H)) return cudaErrorInvalidValue;
+    const size_t bytes = smem_bytes<StateSmem>();
+    cudaError_t e = set_smem(tc_state_kernel, bytes);
+    if (e != cudaSuccess) return e;
+    tc_state_kernel<<<dim3((unsigned)p.U, (unsigned)p.H), kThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    return cudaGetLastError();
+}
+
+cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
+    const dim3 grid((unsigned)p.U, (unsigned)p.H);
+    const TcParams tp{p, prefix_is_zero};
+    CUtensorMap mq;
+    if (!make_row_map(&mq, p.q, p.T, p.H)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (p.causal) {
+        CUtensorMap mk, mv;
+        if (!make_row_map(&mk, p.k, p.T, p.H) || !make_row_map(&mv, p.v, p.T, p.H)) return cudaErrorInvalidValue;
+        const size_t bytes = smem_bytes<CausalSmem>();
+        if ((e = set_smem(tc_causal_out_kernel, bytes)) != cudaSuccess) return e;
+        tc_causal_out_kernel<<<grid, kThreads, bytes, s>>>(mq, mk, mv, tp);
+    } else {
+        const size_t bytes = smem_bytes<BidirSmem>();
+        if ((e = set_smem(tc_bidir_out_kernel, bytes)) != cudaSuccess) return e;
+        tc_bidir_out_kernel<<<grid, kThreads, bytes, s>>>(mq, tp);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
+                           cudaStream_t s) {
+    CUtensorMap mx;
+    if (!make_row_map(&mx, x, T, H)) return cudaErrorInvalidValue;
+    const size_t bytes = smem_bytes<FmapSmem>();
+    cudaError_t e = set_smem(tc_fmap_kernel, bytes);
+    if (e != cudaSuccess) return e;
+    tc_fmap_kernel<<<dim3((unsigned)ceil_div(T, kC), (unsigned)H), kThreads, bytes, s>>>(mx, omega, (int)T, H, r,
+                                                                                        phi, err);
+    return cudaGetLastError();
+}
+
+}  // namespace la
