@@ -58,23 +58,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 typedef unsigned char Tile[kTile];
 
 struct Bars {
-    uint64_t load;
-    uint64_t mma;
+    uint64_t load;       // q (and k) tiles
+    uint64_t load_v;     // v tile
+    uint64_t mma;        // score / readout / update / in-chunk products
+    uint64_t proj[2];    // projection into TMEM buffer 0 / 1
     uint64_t drain;
     uint32_t tmem_base;
     int pad;
-};
-
-// Causal output kernel: 216 KB.
-struct __align__(1024) CausalSmem {
-    unsigned char omg_hi[kOmgBytes];
-    unsigned char omg_lo[kOmgBytes];
-    Tile tq, tk, tv;
-    Tile ones;                        // second MN atom of [V|1]: column 0 = 1
-    Tile phq;                         // Phi_Q of one 64-feature quarter
-    Tile phk[2];                      // Phi_K of one 128-feature half
-    unsigned char sbf[4][kSbfBlock];  // [S|z]^T bf16: block j = features 64j..64j+63, rows n < 80
-    Bars b;
 };
 
 // Bidirectional output kernel: 192 KB.
@@ -210,13 +200,13 @@ __device__ __forceinline__ void store_row32_bf16(unsigned char* blk0, int t, int
             make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
-// Projection epilogue: P (TMEM columns kColP.., lane = token) -> phi = 2^(p - c)
+// Projection epilogue: P (TMEM columns col.., lane = token) -> phi = 2^(p - c)
 // -> bf16 K-major blocks starting at dst (nf features, a multiple of 32).
-__device__ void projection_epilogue(uint32_t tbase, int nf, float c, bool valid, unsigned char* dst) {
+__device__ void projection_epilogue(uint32_t tbase, uint32_t col, int nf, float c, bool valid, unsigned char* dst) {
     const int warp = threadIdx.x >> 5, t = threadIdx.x;
     for (int f0 = 0; f0 < nf; f0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem_addr(tbase, warp * 32, kColP + f0), v);
+        tmem_ld32(tmem_addr(tbase, warp * 32, col + f0), v);
         tmem_ld_wait();
         uint32_t w[16];
 #pragma unroll
@@ -251,8 +241,8 @@ __device__ void projection_to_global(uint32_t tbase, int nf, float c, bool valid
 
 // State of one feature half (TMEM lanes = features, 80 columns) -> bf16 rows n of
 // the K-major readout blocks sbf[2 half], sbf[2 half + 1] (thread f owns feature 128 half + f).
-__device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, int half) {
-    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+__device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, int half, int f = threadIdx.x) {
+    const int warp = f >> 5;
     unsigned char* blk = sbf[2 * half + (f >> 6)];
     const uint32_t col = f & 63;
 #pragma unroll 1
@@ -271,8 +261,8 @@ __device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, in
 // into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
 // rounding remainder into lo when lo != nullptr).
 __device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[kSbfBlock], uint32_t tbase,
-                           bool to_tmem, const float* src, int r, int nhalves, bool zero) {
-    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+                           bool to_tmem, const float* src, int r, int nhalves, bool zero, int f = threadIdx.x) {
+    const int warp = f >> 5;
     for (int half = 0; half < nhalves; ++half) {
         const int feat = 128 * half + f;
         const bool have = !zero && feat < r;
@@ -315,8 +305,8 @@ __device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves) {
 }
 
 // out row t = O[t][0..63] / max(O[t][64], eps), bf16, to global (when valid).
-__device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat16* dst_row) {
-    const int warp = threadIdx.x >> 5;
+__device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat16* dst_row, int f = threadIdx.x) {
+    const int warp = f >> 5;
     uint32_t a[32], b[32], c[16];
     tmem_ld32(tmem_addr(tbase, warp * 32, kColO), a);
     tmem_ld32(tmem_addr(tbase, warp * 32, kColO + 32), b);
@@ -365,13 +355,13 @@ __device__ __forceinline__ void mma_kk(uint32_t d, const unsigned char* a0, uint
     }
 }
 
-// P = X Omega'^T for `nf` features starting at feature f0: X tile (K = 64) times
-// the hi part, then the lo part accumulated.
-__device__ __forceinline__ void mma_projection(uint32_t tbase, const unsigned char* x, const unsigned char* omg_hi,
+// P = X Omega'^T for `nf` features starting at feature f0 into TMEM address d:
+// X tile (K = 64) times the hi part, then the lo part accumulated.
+__device__ __forceinline__ void mma_projection(uint32_t d, const unsigned char* x, const unsigned char* omg_hi,
                                                const unsigned char* omg_lo, int f0, int nf) {
     const uint32_t idesc = idesc_bf16(128, nf, false, false);
-    mma_kk(tbase + kColP, x, 0, omg_hi + 128u * f0, 0, 4, idesc, false);
-    mma_kk(tbase + kColP, x, 0, omg_lo + 128u * f0, 0, 4, idesc, true);
+    mma_kk(d, x, 0, omg_hi + 128u * f0, 0, 4, idesc, false);
+    mma_kk(d, x, 0, omg_lo + 128u * f0, 0, 4, idesc, true);
 }
 
 // [S|z] (+)= Phi_K^T [V|1]: A MN-major (features contiguous, blocks phk0, phk0 + kTile),
@@ -400,7 +390,10 @@ __device__ __forceinline__ void mma_in_chunk(uint32_t d, uint32_t a_hi, uint32_t
 __device__ void setup_bars(Bars& b) {
     if (threadIdx.x == 0) {
         mbar_init(&b.load, 1);
+        mbar_init(&b.load_v, 1);
         mbar_init(&b.mma, 1);
+        mbar_init(&b.proj[0], 1);
+        mbar_init(&b.proj[1], 1);
         mbar_init(&b.drain, 1);
         fence_mbar_init();
     }
@@ -436,10 +429,82 @@ struct Phase {
     }
 };
 
+// Completion counter of the MMA groups committed to one barrier, one commit at
+// a time outstanding at most two phases apart: wait_for(n) returns once n
+// commits have completed (all threads call it with the same n).
+struct Commits {
+    uint32_t issued = 0, done = 0;
+    __device__ __forceinline__ bool wait_for(uint64_t* bar, uint32_t n) {
+        while (done < n) {
+            if (!wait_all(bar, done & 1u)) return false;
+            ++done;
+        }
+        return true;
+    }
+};
+
 // ---------------------------------------------------------------------------
-// Causal output kernel
+// Causal output kernel (warp-specialised)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+// Roles (384 threads):
+//   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
+//   warp 1 lane 0      MMA issue (warp 1 also owns the TMEM allocation)
+//   warps 4..7  (PE)   projection epilogue: phi(k), phi(q) of each quarter of the
+//                      features into shared memory (token t = TMEM lane t)
+//   warps 8..11 (TE)   chunk tail: masked scores as bf16 hi + lo in TMEM, the
+//                      output rows, the bf16 copy of the state for the next readout
+// Per chunk the MMA warp runs, for each quarter q of the features, the
+// projections of k and q (Omega hi + lo) into two alternating TMEM buffers and,
+// once the PE has written phi, the products of that quarter:
+//   A (+)= Phi_Q Phi_K^T,  O (+)= Phi_Q [S|z]_bf16,  and after the last quarter
+//   of each half [S|z] += Phi_K^T [V|1];
+// then, once the TE has split A, O += tril(A) [V|1].  All hand-offs are
+// mbarriers; the next chunk's projections overlap this chunk's tail.
+constexpr int kCausalThreads = 384;
+constexpr uint32_t kBarPE = 1, kBarTE = 2;   // named barriers of the two epilogue warpgroups
+
+struct CausalBars {
+    uint64_t qk_full, qk_empty;     // TMA -> (MMA, PE);  (MMA commit + PE) -> TMA
+    uint64_t v_full, v_empty;       // TMA -> MMA;        MMA commit -> TMA
+    uint64_t p_full[2];             // MMA commit -> PE: projection in TMEM buffer b
+    uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
+    uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
+    uint64_t phiq_full;             // PE (4 warps) -> MMA: phi(q) in smem
+    uint64_t cons[2];               // MMA commit -> PE: products of global quarter g done (g & 1)
+    uint64_t a_full;                // MMA commit -> TE: scores of the chunk complete
+    uint64_t ahl_full;              // TE (4 warps) -> MMA: masked scores hi/lo in TMEM
+    uint64_t o_full;                // MMA commit -> TE: numerator/denominator and state complete
+    uint64_t tail_done;             // TE (4 warps) -> MMA: O, state read; bf16 state written
+    uint64_t drain;
+    uint32_t tmem_base;
+    int pad;
+};
+
+struct __align__(1024) CausalSmem {
+    unsigned char omg_hi[kOmgBytes];
+    unsigned char omg_lo[kOmgBytes];
+    Tile tq, tk, tv;
+    Tile ones;                        // second MN atom of [V|1]: column 0 = 1
+    Tile phq;                         // Phi_Q of one quarter (64 features)
+    Tile phk[2];                      // Phi_K of one half (two quarters)
+    unsigned char sbf[4][kSbfBlock];  // [S|z]^T bf16: block j = features 64j..64j+63, rows n < 80
+    CausalBars b;
+};
+
+// Bounded wait of every thread of a named group; false for all if any timed out.
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint32_t bar_id) {
+    const bool ok = mbar_wait(bar, parity);
+    return !named_sync_or(bar_id, 128, !ok);
+}
+// A warp's threads are done with shared-memory writes / TMEM accesses: lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, bool smem_written) {
+    if (smem_written) fence_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+__global__ void __launch_bounds__(kCausalThreads, 1)
 tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, const TcParams tp) {
     const FwdParams& p = tp.p;
@@ -447,133 +512,296 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
     CausalSmem& s = smem_ref<CausalSmem>();
-    const int t = threadIdx.x, warp = t >> 5;
+    CausalBars& B = s.b;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
     const bool favor = p.map == LA_MAP_FAVOR;
-    const int fh = r < 128 ? r : 128;             // key features per half
+    const int nq = r / 64;                        // feature quarters (1, 2 or 4)
     const int nhalves = (r + 127) / 128;
-    const int nq = fh / 64;                       // query quarters per half
+    const int nchunks = (un.end - un.start + kC - 1) / kC;
 
-    if (t == 0) { prefetch_tensormap(&map_q); prefetch_tensormap(&map_k); prefetch_tensormap(&map_v); }
-    setup_bars(s.b);
-    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
-    fill_ones(s.ones);
+    if (t == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+        mbar_init(&B.qk_full, 1);
+        mbar_init(&B.qk_empty, 2);
+        mbar_init(&B.v_full, 1);
+        mbar_init(&B.v_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B.p_full[i], 1);
+            mbar_init(&B.p_empty[i], 4);
+            mbar_init(&B.phik_full[i], 4);
+            mbar_init(&B.cons[i], 1);
+        }
+        mbar_init(&B.phiq_full, 4);
+        mbar_init(&B.a_full, 1);
+        mbar_init(&B.ahl_full, 4);
+        mbar_init(&B.o_full, 1);
+        mbar_init(&B.tail_done, 4);
+        mbar_init(&B.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&B.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    for (int i = t; i < (favor ? r * 8 : 0); i += kCausalThreads) {
+        // Omega' = log2(e) Omega as bf16 hi + lo (one 16-byte chunk per iteration)
+        const int row = i >> 3, c = i & 7;
+        const float4* src = reinterpret_cast<const float4*>(p.omega + row * 64 + c * 8);
+        const float4 a = src[0], b = src[1];
+        const float x[8] = {a.x * kLog2e, a.y * kLog2e, a.z * kLog2e, a.w * kLog2e,
+                            b.x * kLog2e, b.y * kLog2e, b.z * kLog2e, b.w * kLog2e};
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            wh[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+            wl[j] = pack_bf16x2(x[2 * j] - bf16lo(wh[j]), x[2 * j + 1] - bf16hi(wh[j]));
+        }
+        *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(s.omg_lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+    for (int i = t; i < kC * 8; i += kCausalThreads) {
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+        if (nq == 1)   // feature rows 64..127 of the state update stay zero
+            *reinterpret_cast<uint4*>(s.phk[1] + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tb = s.b.tmem_base;
-    const int64_t E = (int64_t)r * 65;
-    load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
-               tp.prefix_is_zero != 0);
-    handoff_to_mma();
+    const uint32_t tb = B.tmem_base;
 
-    if (t == 0) {
-        mbar_arrive_expect_tx(&s.b.load, 3 * kTile);
-        tma_load_3d(s.tq, &map_q, 0, head, un.start, &s.b.load);
-        tma_load_3d(s.tk, &map_k, 0, head, un.start, &s.b.load);
-        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load);
-    }
-    const uint32_t id_scores = idesc_bf16(128, 128, false, false);
-    const uint32_t id_read = idesc_bf16(128, kNX, false, false);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    Phase lp, mp;
-    bool ok = true;
-
-    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
-        const bool valid = t < min(kC, un.end - t0);
-        if (!(ok = lp.wait(&s.b.load))) break;
-        const float cq = favor ? favor_offset(s.tq, t, r) : 0.f;
-        const float ck = favor ? favor_offset(s.tk, t, r) : 0.f;
-        for (int half = 0; half < nhalves && ok; ++half) {
-            // Phi_K of this half of the features
-            if (favor) {
-                if (t == 0) {
-                    mma_projection(tb, s.tk, s.omg_hi, s.omg_lo, 128 * half, fh);
-                    mma_commit(&s.b.mma);
-                }
-                if (!(ok = mp.wait(&s.b.mma))) break;
-                tc_fence_after();
-                projection_epilogue(tb, fh, ck, valid, s.phk[0]);
-            } else {
-                elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
-            }
-            if (fh < 128) zero_row(s.phk[1], t);   // unused feature rows of the update stay zero
-            for (int jq = 0; jq < nq; ++jq) {
-                // Phi_Q of one quarter (64 features)
-                if (favor) {
-                    tc_fence_before();
-                    __syncthreads();
-                    tc_fence_after();
-                    if (t == 0) {
-                        mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half + 64 * jq, 64);
-                        mma_commit(&s.b.mma);
-                    }
-                    if (!(ok = mp.wait(&s.b.mma))) break;
-                    tc_fence_after();
-                    projection_epilogue(tb, 64, cq, valid, s.phq);
-                } else {
-                    elementwise_phi_row(s.tq, s.phq, t, valid, p.map);
-                }
-                handoff_to_mma();
-                if (t == 0) {
-                    const bool first = half == 0 && jq == 0;
-                    mma_kk(tb + kColA, s.phq, 0, s.phk[jq], 0, 4, id_scores, !first);
-                    mma_kk(tb + kColO, s.phq, 0, s.sbf[2 * half + jq], 0, 4, id_read, !first);
-                    if (jq == nq - 1) mma_state_update(tb + kColS + 80 * half, s.phk[0], s.tv, s.ones);
-                    mma_commit(&s.b.mma);
-                }
-                if (!(ok = mp.wait(&s.b.mma))) break;
-                tc_fence_after();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int t0 = un.start + c * kC;
+                if (c > 0 && !mbar_wait(&B.qk_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
+                mbar_arrive_expect_tx(&B.qk_full, 2 * kTile);
+                tma_load_3d(s.tq, &map_q, 0, head, t0, &B.qk_full);
+                tma_load_3d(s.tk, &map_k, 0, head, t0, &B.qk_full);
+                if (c > 0 && !mbar_wait(&B.v_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
+                mbar_arrive_expect_tx(&B.v_full, kTile);
+                tma_load_3d(s.tv, &map_v, 0, head, t0, &B.v_full);
             }
         }
-        if (!ok) break;
-        // masked scores (key j <= query t) as bf16 hi + lo parts in tensor memory: the
-        // hi part replaces the fp32 scores in place (keys 2c, 2c+1 in column c; every
-        // column written has been read), the lo part goes to the free projection columns
-        for (int j0 = 0; j0 < kC; j0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem_addr(tb, warp * 32, kColA + j0), v);
-            tmem_ld_wait();
-            uint32_t hi[16], lo[16];
+    }
+    else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
+            const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
+            const uint64_t d_tq = sdesc_sw128(smem_u32(s.tq), 16, 1024);
+            const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk), 16, 1024);
+            const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq), 16, 1024);
+            const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
+            const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), 16, 1024);
+            const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
+            const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones) - smem_u32(s.tv), 1024);
+            const uint32_t id_proj = idesc_bf16(128, 64, false, false);
+            const uint32_t id_scores = idesc_bf16(128, 128, false, false);
+            const uint32_t id_read = idesc_bf16(128, kNX, false, false);
+            const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
+            const uint32_t id_av = idesc_bf16(128, kNX, false, true);
+            uint32_t jobs[2] = {0u, 0u};
+            bool ok = true;
+            // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b
+            auto issue_job = [&](int b, int quarter) -> bool {
+                if (!mbar_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
+                ++jobs[b];
+                tc_fence_after();
+                const uint64_t dx = b ? d_tq : d_tk;
+                const uint32_t d = tb + kColP + 64 * b, fo = 8192u * quarter;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int c0 = j0 + 2 * j;
-                const float a = c0 <= t ? __uint_as_float(v[2 * j]) : 0.f;
-                const float b = c0 + 1 <= t ? __uint_as_float(v[2 * j + 1]) : 0.f;
-                hi[j] = pack_bf16x2(a, b);
-                lo[j] = pack_bf16x2(a - bf16lo(hi[j]), b - bf16hi(hi[j]));
+                for (int k = 0; k < 4; ++k) mma_ss(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_ss(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+                mma_commit(&B.p_full[b]);
+                return true;
+            };
+            for (int c = 0; c < nchunks && ok; ++c) {
+                if (!(ok = mbar_wait(&B.qk_full, c & 1))) break;
+                if (favor) {
+                    if (!(ok = issue_job(0, 0) && issue_job(1, 0))) break;
+                }
+                bool v_ready = false;
+                for (int q = 0; q < nq; ++q) {
+                    if (favor && q + 1 < nq) {
+                        if (!(ok = issue_job(0, q + 1) && issue_job(1, q + 1))) break;
+                    }
+                    if (q == nq - 1) mma_commit(&B.qk_empty);   // every projection of this chunk issued
+                    const int g = c * nq + q;
+                    if (!(ok = mbar_wait(&B.phik_full[g & 1], (g >> 1) & 1) && mbar_wait(&B.phiq_full, g & 1))) break;
+                    if (q == 0) {
+                        if (!(ok = mbar_wait(&B.tail_done, c & 1))) break;
+                        tc_fence_after();
+                    }
+                    const bool update_now = (q & 1) || q == nq - 1;
+                    if (update_now && !v_ready) {
+                        if (!(ok = mbar_wait(&B.v_full, c & 1))) break;
+                        v_ready = true;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
+                               (q > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, kSbfBlock * q + 32 * k), id_read,
+                               (q > 0 || k > 0) ? 1u : 0u);
+                    if (update_now) {
+#pragma unroll
+                        for (int k = 0; k < kC / 16; ++k)
+                            mma_ss(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
+                    }
+                    mma_commit(&B.cons[g & 1]);
+                }
+                if (!ok) break;
+                mma_commit(&B.a_full);
+                if (!(ok = mbar_wait(&B.ahl_full, c & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kC / 16; ++k) mma_ts(tb + kColO, tb + kColA + 8 * k, sdesc_add(d_vx, 2048 * k), id_av, 1u);
+#pragma unroll
+                for (int k = 0; k < kC / 16; ++k) mma_ts(tb + kColO, tb + kColA + 64 + 8 * k, sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                mma_commit(&B.o_full);
+                mma_commit(&B.v_empty);
             }
-            tmem_st16(tmem_addr(tb, warp * 32, kColA + j0 / 2), hi);
-            tmem_st16(tmem_addr(tb, warp * 32, kColP + j0 / 2), lo);
+            if (!ok) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (t == 0) {
-            mma_in_chunk(tb + kColO, tb + kColA, tb + kColP, s.tv, s.ones);
-            mma_commit(&s.b.mma);
-        }
-        if (!(ok = mp.wait(&s.b.mma))) break;
-        tc_fence_after();
-        // every tile of this chunk has been consumed: prefetch the next chunk
-        if (t == 0 && t0 + kC < un.end) {
-            mbar_arrive_expect_tx(&s.b.load, 3 * kTile);
-            tma_load_3d(s.tq, &map_q, 0, head, t0 + kC, &s.b.load);
-            tma_load_3d(s.tk, &map_k, 0, head, t0 + kC, &s.b.load);
-            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load);
-        }
-        store_output(tb, p.eps, valid, out + ((int64_t)(t0 + t) * p.H + head) * 64);
-        for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half);
-        handoff_to_mma();
     }
-    if (!ok) drain_after_timeout(s.b, &p.hdr->error);
-    teardown(s.b);
+    else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ PE: phi(k), phi(q)
+        const int tr = t - 128;                   // token row of the chunk = TMEM lane
+        const int wl = (warp & 3) * 32;           // this warp's TMEM lane base
+        if (favor) {                              // both projection buffers start empty
+            warp_arrive(&B.p_empty[0], false);
+            warp_arrive(&B.p_empty[1], false);
+        }
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int t0 = un.start + c * kC;
+            const bool valid = tr < min(kC, un.end - t0);
+            if (!(ok = group_wait(&B.qk_full, c & 1, kBarPE))) break;
+            const float cq = favor ? favor_offset(s.tq, tr, r) : 0.f;
+            const float ck = favor ? favor_offset(s.tk, tr, r) : 0.f;
+            if (favor) {                          // the tiles are no longer read by this group
+                named_sync(kBarPE, 128);
+                if (tr == 0) mbar_arrive(&B.qk_empty);
+            }
+            for (int q = 0; q < nq && ok; ++q) {
+                const int g = c * nq + q;
+                for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
+                    if (favor) {
+                        if (!(ok = group_wait(&B.p_full[kind], g & 1, kBarPE))) break;
+                        tc_fence_after();
+                    }
+                    // the products that read the destination buffer last must be done
+                    const int gw = (kind == 0 && (q & 1)) ? g - 2 : g - 1;
+                    if (gw >= 0 && !(ok = group_wait(&B.cons[gw & 1], (gw >> 1) & 1, kBarPE))) break;
+                    unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq;
+                    if (favor) {
+                        uint32_t v0[32], v1[32];
+                        const uint32_t col = kColP + 64 * kind;
+                        tmem_ld32(tmem_addr(tb, wl, col), v0);
+                        tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
+                        tmem_ld_wait();
+                        warp_arrive(&B.p_empty[kind], false);
+                        const float cx = kind == 0 ? ck : cq;
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_bf16x2(valid ? ex2_approx(__uint_as_float(v0[2 * j]) - cx) : 0.f,
+                                               valid ? ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx) : 0.f);
+                        store_row32_bf16(dst, tr, 0, w);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_bf16x2(valid ? ex2_approx(__uint_as_float(v1[2 * j]) - cx) : 0.f,
+                                               valid ? ex2_approx(__uint_as_float(v1[2 * j + 1]) - cx) : 0.f);
+                        store_row32_bf16(dst, tr, 32, w);
+                    } else {
+                        elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
+                    }
+                    warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full, true);
+                }
+            }
+            if (ok && !favor) {
+                named_sync(kBarPE, 128);
+                if (tr == 0) mbar_arrive(&B.qk_empty);
+            }
+        }
+        if (!ok && tr == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ TE: tail of each chunk
+        const int tr = t - 256;                   // query row / state feature = TMEM lane
+        const int wl = (warp & 3) * 32;
+        const int64_t E = (int64_t)r * 65;
+        load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
+                   tp.prefix_is_zero != 0, tr);
+        warp_arrive(&B.tail_done, true);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int t0 = un.start + c * kC;
+            const bool valid = tr < min(kC, un.end - t0);
+            if (!(ok = group_wait(&B.a_full, c & 1, kBarTE))) break;
+            tc_fence_after();
+            // masked scores (key j <= query tr) as bf16 hi (columns 0..63) + lo (64..127),
+            // written in place: every column is read before it is overwritten
+            uint32_t hi_keys[64];
+            tmem_ld32(tmem_addr(tb, wl, kColA + 64), *reinterpret_cast<uint32_t(*)[32]>(hi_keys));
+            tmem_ld32(tmem_addr(tb, wl, kColA + 96), *reinterpret_cast<uint32_t(*)[32]>(hi_keys + 32));
+            tmem_ld_wait();
+            for (int j0 = 0; j0 < kC; j0 += 32) {
+                uint32_t v[32];
+                if (j0 < 64) {
+                    tmem_ld32(tmem_addr(tb, wl, kColA + j0), v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = hi_keys[j0 - 64 + j];
+                }
+                uint32_t hv[16], lv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = j0 + 2 * j;
+                    const float a = c0 <= tr ? __uint_as_float(v[2 * j]) : 0.f;
+                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v[2 * j + 1]) : 0.f;
+                    hv[j] = pack_bf16x2(a, b2);
+                    lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
+                }
+                tmem_st16(tmem_addr(tb, wl, kColA + j0 / 2), hv);
+                tmem_st16(tmem_addr(tb, wl, kColA + 64 + j0 / 2), lv);
+            }
+            tmem_st_wait();
+            warp_arrive(&B.ahl_full, false);
+            if (!(ok = group_wait(&B.o_full, c & 1, kBarTE))) break;
+            tc_fence_after();
+            store_output(tb, p.eps, valid, out + ((int64_t)(t0 + tr) * p.H + head) * 64, tr);
+            for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half, tr);
+            warp_arrive(&B.tail_done, true);
+        }
+        if (!ok && tr == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    }
+    // ---------------------------------------------------------------- exit
+    tc_fence_before();
+    __syncthreads();
+    if (t == 32) {   // all MMAs of this CTA finished before TMEM is freed (bounded)
+        mma_commit(&B.drain);
+        mbar_wait(&B.drain, 0, 500000000ull);
+    }
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
 // Bidirectional output kernel: out = Phi_Q [S|z] / ..., [S|z] the whole-sequence state
 // ---------------------------------------------------------------------------
+// Jobs are the projections of q for each quarter of the features, into two
+// alternating TMEM buffers; each quarter's readout uses the state's hi and lo parts.
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp) {
     const FwdParams& p = tp.p;
@@ -584,7 +812,7 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
     const int t = threadIdx.x;
     const int r = p.r;
     const bool favor = p.map == LA_MAP_FAVOR;
-    const int fh = r < 128 ? r : 128;
+    const int nq = r / 64;
     const int nhalves = (r + 127) / 128;
 
     if (t == 0) prefetch_tensormap(&map_q);
@@ -602,35 +830,43 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
     }
     const uint32_t id_read = idesc_bf16(128, kNX, false, false);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    Phase lp, mp;
+    auto issue_job = [&](int q) {   // thread 0 only
+        mma_projection(tb + kColP + 64 * (q & 1), s.tq, s.omg_hi, s.omg_lo, 64 * q, 64);
+        mma_commit(&s.b.proj[q & 1]);
+    };
+    Phase lp, pp0, pp1;
+    Commits cm;
     bool ok = true;
     for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
         const bool valid = t < min(kC, un.end - t0);
         if (!(ok = lp.wait(&s.b.load))) break;
         const float cq = favor ? favor_offset(s.tq, t, r) : 0.f;
-        for (int half = 0; half < nhalves && ok; ++half) {
+        const uint32_t base = cm.issued;
+        if (favor && t == 0) {
+            issue_job(0);
+            if (nq > 1) issue_job(1);
+        }
+        for (int q = 0; q < nq; ++q) {
+            const int b = q & 1;
             if (favor) {
-                if (t == 0) {
-                    mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
-                    mma_commit(&s.b.mma);
-                }
-                if (!(ok = mp.wait(&s.b.mma))) break;
+                if (!(ok = (b ? pp1 : pp0).wait(&s.b.proj[b]))) break;
                 tc_fence_after();
-                projection_epilogue(tb, fh, cq, valid, s.phq[0]);
-            } else {
-                elementwise_phi_row(s.tq, s.phq[0], t, valid, p.map);
             }
+            if (q > 0 && !(ok = cm.wait_for(&s.b.mma, base + q))) break;   // readout q-1 done
+            if (favor) projection_epilogue(tb, kColP + 64 * b, 64, cq, valid, s.phq[b]);
+            else elementwise_phi_row(s.tq, s.phq[b], t, valid, p.map);
             handoff_to_mma();
             if (t == 0) {
-                const int ks = fh / 16;
-                mma_kk(tb + kColO, s.phq[0], kTile, s.shi[2 * half], kSbfBlock, ks, id_read, half > 0);
-                mma_kk(tb + kColO, s.phq[0], kTile, s.slo[2 * half], kSbfBlock, ks, id_read, true);
+                if (favor && q + 2 < nq) issue_job(q + 2);
+                mma_kk(tb + kColO, s.phq[b], 0, s.shi[q], 0, 4, id_read, q > 0);
+                mma_kk(tb + kColO, s.phq[b], 0, s.slo[q], 0, 4, id_read, true);
                 mma_commit(&s.b.mma);
             }
-            if (!(ok = mp.wait(&s.b.mma))) break;
-            tc_fence_after();
+            ++cm.issued;
         }
         if (!ok) break;
+        if (!(ok = cm.wait_for(&s.b.mma, base + nq))) break;
+        tc_fence_after();
         if (t == 0 && t0 + kC < un.end) {
             mbar_arrive_expect_tx(&s.b.load, kTile);
             tma_load_3d(s.tq, &map_q, 0, head, t0 + kC, &s.b.load);
@@ -658,13 +894,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int t = threadIdx.x, warp = t >> 5;
     const int r = p.r;
     const bool favor = p.map == LA_MAP_FAVOR;
-    const int fh = r < 128 ? r : 128;
+    const int nq = r / 64;
     const int nhalves = (r + 127) / 128;
     if (t == 0) { prefetch_tensormap(&map_k); prefetch_tensormap(&map_v); }
     setup_bars(s.b);
     if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
     fill_ones(s.ones);
-    zero_row(s.phk[1], t);
+    if (nq == 1) zero_row(s.phk[1], t);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -679,41 +915,63 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     handoff_to_mma();
     if (t == 0) {
-        mbar_arrive_expect_tx(&s.b.load, 2 * kTile);
+        mbar_arrive_expect_tx(&s.b.load, kTile);
         tma_load_3d(s.tk, &map_k, 0, head, un.start, &s.b.load);
-        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load);
+        mbar_arrive_expect_tx(&s.b.load_v, kTile);
+        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load_v);
     }
-    Phase lp, mp;
+    auto issue_job = [&](int q) {   // thread 0 only
+        mma_projection(tb + kColP + 64 * (q & 1), s.tk, s.omg_hi, s.omg_lo, 64 * q, 64);
+        mma_commit(&s.b.proj[q & 1]);
+    };
+    Phase lk, lv, pp0, pp1;
+    Commits cm;
     bool ok = true;
     for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
         const bool valid = t < min(kC, un.end - t0);
-        if (!(ok = lp.wait(&s.b.load))) break;
+        if (!(ok = lk.wait(&s.b.load))) break;
         const float ck = favor ? favor_offset(s.tk, t, r) : 0.f;
-        for (int half = 0; half < nhalves && ok; ++half) {
+        const uint32_t base = cm.issued;
+        bool v_ready = false;
+        if (favor && t == 0) {
+            issue_job(0);
+            if (nq > 1) issue_job(1);
+        }
+        for (int q = 0; q < nq; ++q) {
+            const int b = q & 1;
             if (favor) {
-                if (t == 0) {
-                    mma_projection(tb, s.tk, s.omg_hi, s.omg_lo, 128 * half, fh);
-                    mma_commit(&s.b.mma);
-                }
-                if (!(ok = mp.wait(&s.b.mma))) break;
+                if (!(ok = (b ? pp1 : pp0).wait(&s.b.proj[b]))) break;
                 tc_fence_after();
-                projection_epilogue(tb, fh, ck, valid, s.phk[0]);
-            } else {
-                elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
+            }
+            // the first phi(k) of a half overwrites the previous half's update operand
+            if (q > 0 && (q & 1) == 0 && !(ok = cm.wait_for(&s.b.mma, base + (q >> 1)))) break;
+            if (favor) projection_epilogue(tb, kColP + 64 * b, 64, ck, valid, s.phk[b]);
+            else elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
+            const bool update_now = (q & 1) || q == nq - 1;
+            if (update_now && !v_ready) {
+                if (!(ok = lv.wait(&s.b.load_v))) break;
+                v_ready = true;
             }
             handoff_to_mma();
             if (t == 0) {
-                mma_state_update(tb + kColS + 80 * half, s.phk[0], s.tv, s.ones);
-                mma_commit(&s.b.mma);
+                if (favor && q + 2 < nq) issue_job(q + 2);
+                if (update_now) {
+                    mma_state_update(tb + kColS + 80 * (q >> 1), s.phk[0], s.tv, s.ones);
+                    mma_commit(&s.b.mma);
+                }
             }
-            if (!(ok = mp.wait(&s.b.mma))) break;
-            tc_fence_after();
+            if (update_now) ++cm.issued;
         }
         if (!ok) break;
-        if (t == 0 && t0 + kC < un.end) {
-            mbar_arrive_expect_tx(&s.b.load, 2 * kTile);
+        if (t == 0 && t0 + kC < un.end) {   // every projection has read tk
+            mbar_arrive_expect_tx(&s.b.load, kTile);
             tma_load_3d(s.tk, &map_k, 0, head, t0 + kC, &s.b.load);
-            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load);
+        }
+        if (!(ok = cm.wait_for(&s.b.mma, cm.issued))) break;
+        tc_fence_after();
+        if (t == 0 && t0 + kC < un.end) {   // every update has read tv
+            mbar_arrive_expect_tx(&s.b.load_v, kTile);
+            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load_v);
         }
     }
     if (ok) store_state(tb, p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves);
@@ -748,7 +1006,7 @@ tc_fmap_kernel(const __grid_constant__ CUtensorMap map_x, const float* omega, in
         const bool valid = t0 + t < T;
         for (int half = 0; half < nhalves; ++half) {
             if (t == 0) {
-                mma_projection(tb, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
+                mma_projection(tb + kColP, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
                 mma_commit(&s.b.mma);
             }
             if (!(ok = mp.wait(&s.b.mma))) break;
@@ -829,7 +1087,7 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
         if (!make_row_map(&mk, p.k, p.T, p.H) || !make_row_map(&mv, p.v, p.T, p.H)) return cudaErrorInvalidValue;
         const size_t bytes = smem_bytes<CausalSmem>();
         if ((e = set_smem(tc_causal_out_kernel, bytes)) != cudaSuccess) return e;
-        tc_causal_out_kernel<<<grid, kThreads, bytes, s>>>(mq, mk, mv, tp);
+        tc_causal_out_kernel<<<grid, kCausalThreads, bytes, s>>>(mq, mk, mv, tp);
     } else {
         const size_t bytes = smem_bytes<BidirSmem>();
         if ((e = set_smem(tc_bidir_out_kernel, bytes)) != cudaSuccess) return e;

@@ -213,6 +213,29 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 // ---------------------------------------------------------------------------
+// Named barriers (a subset of the CTA's warps)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Synchronises the named group and returns the OR of `pred` over its threads.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
+// Shared-memory descriptor advanced by `bytes` (start address field only).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
+// ---------------------------------------------------------------------------
 // Arithmetic helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
