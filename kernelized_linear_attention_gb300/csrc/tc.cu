@@ -261,9 +261,11 @@ __device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, in
 // into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
 // rounding remainder into lo when lo != nullptr).
 __device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[kSbfBlock], uint32_t tbase,
-                           bool to_tmem, const float* src, int r, int nhalves, bool zero, int f = threadIdx.x) {
+                           bool to_tmem, const float* src, int r, int nhalves, bool zero, int f = threadIdx.x,
+                           int only_half = -1) {
     const int warp = f >> 5;
     for (int half = 0; half < nhalves; ++half) {
+        if (only_half >= 0 && half != only_half) continue;
         const int feat = 128 * half + f;
         const bool have = !zero && feat < r;
         const int blk = 2 * half + (f >> 6);
@@ -327,6 +329,21 @@ __device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat1
                                 pack_bf16x2(__uint_as_float(b[8 * q + 2]) * inv, __uint_as_float(b[8 * q + 3]) * inv),
                                 pack_bf16x2(__uint_as_float(b[8 * q + 4]) * inv, __uint_as_float(b[8 * q + 5]) * inv),
                                 pack_bf16x2(__uint_as_float(b[8 * q + 6]) * inv, __uint_as_float(b[8 * q + 7]) * inv));
+}
+
+// One output row from registers: O[0..63] / max(den, eps) as bf16 to global.
+__device__ __forceinline__ void store_output_row(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t den,
+                                                 float eps, __nv_bfloat16* dst_row) {
+    const float inv = 1.0f / fmaxf(__uint_as_float(den), eps);
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t* x = q < 4 ? a + 8 * q : b + 8 * (q - 4);
+        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                            pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                            pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                            pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -446,12 +463,13 @@ struct Commits {
 // ---------------------------------------------------------------------------
 // Causal output kernel (warp-specialised)
 // ---------------------------------------------------------------------------
-// Roles (384 threads):
+// Roles (512 threads):
 //   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
 //   warp 1 lane 0      MMA issue (warp 1 also owns the TMEM allocation)
-//   warps 4..7  (PE)   projection epilogue: phi(k), phi(q) of each quarter of the
-//                      features into shared memory (token t = TMEM lane t)
-//   warps 8..11 (TE)   chunk tail: masked scores as bf16 hi + lo in TMEM, the
+//   warps 4..11 (PE)   projection epilogue in two warpgroups, each converting 32 of
+//                      the 64 columns of every job: phi(k), phi(q) of each quarter
+//                      of the features into shared memory (token t = TMEM lane t)
+//   warps 12..15 (TE)  chunk tail: masked scores as bf16 hi + lo in TMEM, the
 //                      output rows, the bf16 copy of the state for the next readout
 // Per chunk the MMA warp runs, for each quarter q of the features, the
 // projections of k and q (Omega hi + lo) into two alternating TMEM buffers and,
@@ -460,21 +478,22 @@ struct Commits {
 //   of each half [S|z] += Phi_K^T [V|1];
 // then, once the TE has split A, O += tril(A) [V|1].  All hand-offs are
 // mbarriers; the next chunk's projections overlap this chunk's tail.
-constexpr int kCausalThreads = 384;
-constexpr uint32_t kBarPE = 1, kBarTE = 2;   // named barriers of the two epilogue warpgroups
+constexpr int kCausalThreads = 512;
 
 struct CausalBars {
-    uint64_t qk_full, qk_empty;     // TMA -> (MMA, PE);  (MMA commit + PE) -> TMA
+    uint64_t qk_full, qk_empty;     // TMA -> (MMA, PE);  (MMA commit + 4 PE warps) -> TMA
     uint64_t v_full, v_empty;       // TMA -> MMA;        MMA commit -> TMA
     uint64_t p_full[2];             // MMA commit -> PE: projection in TMEM buffer b
     uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
     uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
     uint64_t phiq_full;             // PE (4 warps) -> MMA: phi(q) in smem
     uint64_t cons[2];               // MMA commit -> PE: products of global quarter g done (g & 1)
-    uint64_t a_full;                // MMA commit -> TE: scores of the chunk complete
-    uint64_t ahl_full;              // TE (4 warps) -> MMA: masked scores hi/lo in TMEM
-    uint64_t o_full;                // MMA commit -> TE: numerator/denominator and state complete
-    uint64_t tail_done;             // TE (4 warps) -> MMA: O, state read; bf16 state written
+    uint64_t phq_free;              // MMA commit -> PE: scores and readout of quarter g done
+    uint64_t a_full;                // MMA commit -> SE, OE: scores, readout, state update of the chunk done
+    uint64_t ahl_full;              // OE (4 warps) -> MMA: masked scores hi/lo in TMEM
+    uint64_t o_full;                // MMA commit -> OE: numerator/denominator complete
+    uint64_t o_empty;               // OE (4 warps) -> MMA: O read out of TMEM
+    uint64_t sbf_full;              // SE (4 warps) -> MMA: bf16 state of the previous chunks in smem
     uint64_t drain;
     uint32_t tmem_base;
     int pad;
@@ -491,10 +510,11 @@ struct __align__(1024) CausalSmem {
     CausalBars b;
 };
 
-// Bounded wait of every thread of a named group; false for all if any timed out.
-__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint32_t bar_id) {
+// Bounded wait of every lane of a warp; false for the whole warp if any lane timed out.
+// Epilogue warps proceed independently and meet only through mbarriers.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     const bool ok = mbar_wait(bar, parity);
-    return !named_sync_or(bar_id, 128, !ok);
+    return !__any_sync(0xffffffffu, !ok);
 }
 // A warp's threads are done with shared-memory writes / TMEM accesses: lane 0 arrives.
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, bool smem_written) {
@@ -525,7 +545,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
         mbar_init(&B.qk_full, 1);
-        mbar_init(&B.qk_empty, 2);
+        mbar_init(&B.qk_empty, 5);      // MMA commit + one arrival per projection-epilogue warp
         mbar_init(&B.v_full, 1);
         mbar_init(&B.v_empty, 1);
         for (int i = 0; i < 2; ++i) {
@@ -535,10 +555,12 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(&B.cons[i], 1);
         }
         mbar_init(&B.phiq_full, 4);
+        mbar_init(&B.phq_free, 1);
         mbar_init(&B.a_full, 1);
         mbar_init(&B.ahl_full, 4);
         mbar_init(&B.o_full, 1);
-        mbar_init(&B.tail_done, 4);
+        mbar_init(&B.o_empty, 4);
+        mbar_init(&B.sbf_full, 4);
         mbar_init(&B.drain, 1);
         fence_mbar_init();
     }
@@ -622,11 +644,13 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 mma_commit(&B.p_full[b]);
                 return true;
             };
+            bool started = false;   // first projection jobs of chunk c already issued
             for (int c = 0; c < nchunks && ok; ++c) {
-                if (!(ok = mbar_wait(&B.qk_full, c & 1))) break;
-                if (favor) {
-                    if (!(ok = issue_job(0, 0) && issue_job(1, 0))) break;
+                if (!started) {
+                    if (!(ok = mbar_wait(&B.qk_full, c & 1))) break;
+                    if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
                 }
+                started = false;
                 bool v_ready = false;
                 for (int q = 0; q < nq; ++q) {
                     if (favor && q + 1 < nq) {
@@ -635,8 +659,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     if (q == nq - 1) mma_commit(&B.qk_empty);   // every projection of this chunk issued
                     const int g = c * nq + q;
                     if (!(ok = mbar_wait(&B.phik_full[g & 1], (g >> 1) & 1) && mbar_wait(&B.phiq_full, g & 1))) break;
-                    if (q == 0) {
-                        if (!(ok = mbar_wait(&B.tail_done, c & 1))) break;
+                    if (q == 0) {   // O and the scores of chunk c-1 read out; bf16 state of chunks < c ready
+                        if (!(ok = (c == 0 || mbar_wait(&B.o_empty, (c - 1) & 1)) && mbar_wait(&B.sbf_full, c & 1))) break;
                         tc_fence_after();
                     }
                     const bool update_now = (q & 1) || q == nq - 1;
@@ -652,6 +676,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     for (int k = 0; k < 4; ++k)
                         mma_ss(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, kSbfBlock * q + 32 * k), id_read,
                                (q > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(&B.phq_free);   // phi(q) of the next quarter waits only for these
                     if (update_now) {
 #pragma unroll
                         for (int k = 0; k < kC / 16; ++k)
@@ -661,12 +686,21 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 }
                 if (!ok) break;
                 mma_commit(&B.a_full);
+                // overlap: if the next chunk's q and k have landed, start its projections
+                // now, while the output warps split this chunk's scores
+                if (c + 1 < nchunks && mbar_test_wait(&B.qk_full, (c + 1) & 1)) {
+                    if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
+                    started = true;
+                }
                 if (!(ok = mbar_wait(&B.ahl_full, c & 1))) break;
                 tc_fence_after();
+                // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
 #pragma unroll
-                for (int k = 0; k < kC / 16; ++k) mma_ts(tb + kColO, tb + kColA + 8 * k, sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                for (int k = 0; k < kC / 16; ++k)
+                    mma_ts(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
 #pragma unroll
-                for (int k = 0; k < kC / 16; ++k) mma_ts(tb + kColO, tb + kColA + 64 + 8 * k, sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                for (int k = 0; k < kC / 16; ++k)
+                    mma_ts(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
                 mma_commit(&B.o_full);
                 mma_commit(&B.v_empty);
             }
@@ -685,42 +719,40 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             const bool valid = tr < min(kC, un.end - t0);
-            if (!(ok = group_wait(&B.qk_full, c & 1, kBarPE))) break;
+            if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
             const float cq = favor ? favor_offset(s.tq, tr, r) : 0.f;
             const float ck = favor ? favor_offset(s.tk, tr, r) : 0.f;
-            if (favor) {                          // the tiles are no longer read by this group
-                named_sync(kBarPE, 128);
-                if (tr == 0) mbar_arrive(&B.qk_empty);
-            }
+            if (favor) warp_arrive(&B.qk_empty, false);   // this warp no longer reads the tiles
             for (int q = 0; q < nq && ok; ++q) {
                 const int g = c * nq + q;
                 for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
+                    uint32_t v0[32], v1[32];
                     if (favor) {
-                        if (!(ok = group_wait(&B.p_full[kind], g & 1, kBarPE))) break;
+                        if (!(ok = warp_wait(&B.p_full[kind], g & 1))) break;
                         tc_fence_after();
+                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind), v0);
+                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind + 32), v1);
+                        tmem_ld_wait();
+                        warp_arrive(&B.p_empty[kind], false);
                     }
                     // the products that read the destination buffer last must be done
                     const int gw = (kind == 0 && (q & 1)) ? g - 2 : g - 1;
-                    if (gw >= 0 && !(ok = group_wait(&B.cons[gw & 1], (gw >> 1) & 1, kBarPE))) break;
+                    if (gw >= 0 && !(ok = kind == 0 ? warp_wait(&B.cons[gw & 1], (gw >> 1) & 1)
+                                                    : warp_wait(&B.phq_free, gw & 1))) break;
                     unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq;
                     if (favor) {
-                        uint32_t v0[32], v1[32];
-                        const uint32_t col = kColP + 64 * kind;
-                        tmem_ld32(tmem_addr(tb, wl, col), v0);
-                        tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
-                        tmem_ld_wait();
-                        warp_arrive(&B.p_empty[kind], false);
-                        const float cx = kind == 0 ? ck : cq;
+                        // rows past the unit's end: 2^(p - inf) = 0
+                        const float cx = valid ? (kind == 0 ? ck : cq) : __int_as_float(0x7f800000);
                         uint32_t w[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            w[j] = pack_bf16x2(valid ? ex2_approx(__uint_as_float(v0[2 * j]) - cx) : 0.f,
-                                               valid ? ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx) : 0.f);
+                            w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * j]) - cx),
+                                               ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx));
                         store_row32_bf16(dst, tr, 0, w);
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            w[j] = pack_bf16x2(valid ? ex2_approx(__uint_as_float(v1[2 * j]) - cx) : 0.f,
-                                               valid ? ex2_approx(__uint_as_float(v1[2 * j + 1]) - cx) : 0.f);
+                            w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * j]) - cx),
+                                               ex2_approx(__uint_as_float(v1[2 * j + 1]) - cx));
                         store_row32_bf16(dst, tr, 32, w);
                     } else {
                         elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
@@ -728,63 +760,79 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full, true);
                 }
             }
-            if (ok && !favor) {
-                named_sync(kBarPE, 128);
-                if (tr == 0) mbar_arrive(&B.qk_empty);
-            }
+            if (ok && !favor) warp_arrive(&B.qk_empty, false);
         }
-        if (!ok && tr == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ TE: tail of each chunk
-        const int tr = t - 256;                   // query row / state feature = TMEM lane
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------ OE: scores split, output
+        const int tr = t - 256;                   // query row = TMEM lane
         const int wl = (warp & 3) * 32;
-        const int64_t E = (int64_t)r * 65;
-        load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
-                   tp.prefix_is_zero != 0, tr);
-        warp_arrive(&B.tail_done, true);
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             const bool valid = tr < min(kC, un.end - t0);
-            if (!(ok = group_wait(&B.a_full, c & 1, kBarTE))) break;
+            if (!(ok = warp_wait(&B.a_full, c & 1))) break;
             tc_fence_after();
-            // masked scores (key j <= query tr) as bf16 hi (columns 0..63) + lo (64..127),
-            // written in place: every column is read before it is overwritten
-            uint32_t hi_keys[64];
-            tmem_ld32(tmem_addr(tb, wl, kColA + 64), *reinterpret_cast<uint32_t(*)[32]>(hi_keys));
-            tmem_ld32(tmem_addr(tb, wl, kColA + 96), *reinterpret_cast<uint32_t(*)[32]>(hi_keys + 32));
-            tmem_ld_wait();
-            for (int j0 = 0; j0 < kC; j0 += 32) {
-                uint32_t v[32];
-                if (j0 < 64) {
-                    tmem_ld32(tmem_addr(tb, wl, kColA + j0), v);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = hi_keys[j0 - 64 + j];
-                }
+            // masked scores (key j <= query tr) as bf16 hi + lo, two keys per column, in
+            // TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127]: each group of
+            // 64 keys is read whole before its 64 columns are overwritten
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t cb = kColA + 64 * part;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem_addr(tb, wl, cb), v0);
+                tmem_ld32(tmem_addr(tb, wl, cb + 32), v1);
+                tmem_ld_wait();
                 uint32_t hv[16], lv[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int c0 = j0 + 2 * j;
-                    const float a = c0 <= tr ? __uint_as_float(v[2 * j]) : 0.f;
-                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v[2 * j + 1]) : 0.f;
+                    const int c0 = 64 * part + 2 * j;
+                    const float a = c0 <= tr ? __uint_as_float(v0[2 * j]) : 0.f;
+                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v0[2 * j + 1]) : 0.f;
                     hv[j] = pack_bf16x2(a, b2);
                     lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
                 }
-                tmem_st16(tmem_addr(tb, wl, kColA + j0 / 2), hv);
-                tmem_st16(tmem_addr(tb, wl, kColA + 64 + j0 / 2), lv);
+                tmem_st16(tmem_addr(tb, wl, cb), hv);
+                tmem_st16(tmem_addr(tb, wl, cb + 32), lv);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = 64 * part + 32 + 2 * j;
+                    const float a = c0 <= tr ? __uint_as_float(v1[2 * j]) : 0.f;
+                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v1[2 * j + 1]) : 0.f;
+                    hv[j] = pack_bf16x2(a, b2);
+                    lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
+                }
+                tmem_st16(tmem_addr(tb, wl, cb + 16), hv);
+                tmem_st16(tmem_addr(tb, wl, cb + 48), lv);
             }
             tmem_st_wait();
             warp_arrive(&B.ahl_full, false);
-            if (!(ok = group_wait(&B.o_full, c & 1, kBarTE))) break;
+            if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            store_output(tb, p.eps, valid, out + ((int64_t)(t0 + tr) * p.H + head) * 64, tr);
-            for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half, tr);
-            warp_arrive(&B.tail_done, true);
+            uint32_t o0[32], o1[32], den;
+            tmem_ld32(tmem_addr(tb, wl, kColO), o0);
+            tmem_ld32(tmem_addr(tb, wl, kColO + 32), o1);
+            tmem_ld1(tmem_addr(tb, wl, kColO + 64), den);
+            tmem_ld_wait();
+            warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
+            if (valid) store_output_row(o0, o1, den, p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
         }
-        if (!ok && tr == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ SE: state of the chunks so far
+        const int tr = t - 384;                   // state feature (within a half) = TMEM lane
+        const int64_t E = (int64_t)r * 65;
+        load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
+                   tp.prefix_is_zero != 0, tr);
+        warp_arrive(&B.sbf_full, true);
+        bool ok = true;
+        for (int c = 0; c + 1 < nchunks && ok; ++c) {   // the last chunk's state is not read again
+            if (!(ok = warp_wait(&B.a_full, c & 1))) break;
+            tc_fence_after();
+            for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half, tr);
+            warp_arrive(&B.sbf_full, true);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     // ---------------------------------------------------------------- exit
     tc_fence_before();
