@@ -78,13 +78,24 @@ struct __align__(1024) BidirSmem {
     Bars b;
 };
 
-// Segment-state kernel: 144 KB.
+// Segment-state kernel: 209 KB.
+struct StateBars {
+    uint64_t k_full[2], k_empty[2];     // TMA -> all;  (MMA commit + 8 PE warps) -> TMA
+    uint64_t v_full[2], v_empty[2];     // TMA -> MMA;  MMA commit -> TMA
+    uint64_t p_full[2], p_empty[2];     // MMA commit -> PE: projection of a feature half;  PE (8 warps) -> MMA
+    uint64_t h_full[2], h_empty[2];     // PE (8 warps) -> MMA: phi(k) of one feature half; MMA commit -> PE
+    uint64_t drain;
+    uint32_t tmem_base;
+    int pad;
+};
+
 struct __align__(1024) StateSmem {
     unsigned char omg_hi[kOmgBytes];
     unsigned char omg_lo[kOmgBytes];
-    Tile tk, tv, ones;
-    Tile phk[2];
-    Bars b;
+    Tile tk[2], tv[2];                  // two stages
+    Tile ones;
+    Tile phk[2][2];                     // [buffer][quarter of the half]: phi(k) of 128 features
+    StateBars b;
 };
 
 // Feature-map kernel: 80 KB.
@@ -115,7 +126,7 @@ struct TcParams {
 // Omega' = log2(e) * Omega as bf16 hi + lo, [r][64] each, K-major swizzled
 // (the B operand of the projection).  lo = bf16(Omega' - hi).
 __device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* omega, int r) {
-    for (int i = threadIdx.x; i < r * 8; i += kThreads) {
+    for (int i = threadIdx.x; i < r * 8; i += blockDim.x) {
         const int row = i >> 3, c = i & 7;
         const float4* src = reinterpret_cast<const float4*>(omega + row * 64 + c * 8);
         const float4 a = src[0], b = src[1];
@@ -133,7 +144,7 @@ __device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* o
 }
 
 __device__ void fill_ones(unsigned char* blk) {
-    for (int i = threadIdx.x; i < kC * 8; i += kThreads) {
+    for (int i = threadIdx.x; i < kC * 8; i += blockDim.x) {
         const int row = i >> 3, c = i & 7;
         *reinterpret_cast<uint4*>(blk + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
     }
@@ -289,14 +300,17 @@ __device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[k
 }
 
 // Writes the fp32 state held in TMEM (features < r, 65 columns) to global [r][65].
-__device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves) {
-    const int warp = threadIdx.x >> 5, f = threadIdx.x;
+// Zeros instead when `zero` (a unit without tokens); thread f = TMEM lane f.
+__device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves, int f = threadIdx.x, bool zero = false) {
+    const int warp = f >> 5;
     for (int half = 0; half < nhalves; ++half) {
         const int feat = 128 * half + f;
         for (int n0 = 0; n0 < kNX; n0 += 16) {
-            uint32_t w[16];
-            tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
-            tmem_ld_wait();
+            uint32_t w[16] = {};
+            if (!zero) {
+                tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
+                tmem_ld_wait();
+            }
             if (feat < r) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
@@ -466,18 +480,19 @@ struct Commits {
 // Roles (512 threads):
 //   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
 //   warp 1 lane 0      MMA issue (warp 1 also owns the TMEM allocation)
-//   warps 4..11 (PE)   projection epilogue in two warpgroups, each converting 32 of
-//                      the 64 columns of every job: phi(k), phi(q) of each quarter
-//                      of the features into shared memory (token t = TMEM lane t)
-//   warps 12..15 (TE)  chunk tail: masked scores as bf16 hi + lo in TMEM, the
-//                      output rows, the bf16 copy of the state for the next readout
+//   warps 4..7 (PE)    projection epilogue: phi(k), phi(q) of each quarter of the
+//                      features into shared memory (token t = TMEM lane t)
+//   warps 8..11 (OE)   masked scores as bf16 hi + lo in TMEM; the output rows
+//   warps 12..15 (SE)  the bf16 copy of the state for the next chunk's readout
 // Per chunk the MMA warp runs, for each quarter q of the features, the
-// projections of k and q (Omega hi + lo) into two alternating TMEM buffers and,
-// once the PE has written phi, the products of that quarter:
+// projections of k and q (Omega hi + lo) into two TMEM buffers and, once the
+// PE has written phi, the products of that quarter:
 //   A (+)= Phi_Q Phi_K^T,  O (+)= Phi_Q [S|z]_bf16,  and after the last quarter
 //   of each half [S|z] += Phi_K^T [V|1];
-// then, once the TE has split A, O += tril(A) [V|1].  All hand-offs are
-// mbarriers; the next chunk's projections overlap this chunk's tail.
+// then, once the OE has split A, O += tril(A) [V|1].  All hand-offs are
+// mbarriers.  The next chunk's projections overlap this chunk's tail; its
+// first products wait only until O has been read out and the SE has written
+// the state of the chunks so far.
 constexpr int kCausalThreads = 512;
 
 struct CausalBars {
@@ -929,9 +944,22 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 }
 
 // ---------------------------------------------------------------------------
-// Segment-state kernel: sum over the unit of phi(k) [v | 1]^T
+// Segment-state kernel (warp-specialised): [S|z] = sum over the unit of phi(k) [v | 1]^T
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+// Roles (384 threads):
+//   warp 0 lane 0     TMA: the k and v tiles of each chunk into two alternating stages
+//   warp 1            MMA issue (one elected lane; warp 1 owns the TMEM allocation).
+//                     For each 128-feature half h of chunk c: the state update of
+//                     (c, h), then the projection of (c + 1, h) into one of two TMEM
+//                     buffers, so the projections run one chunk ahead of the updates
+//   warps 4..11       two warpgroups; warpgroup w converts features 64w..64w+63 of
+//                     every half into phi(k) (one of two alternating 128-feature
+//                     buffers in shared memory)
+// The state accumulates in TMEM over the unit and is written once at the end.
+constexpr int kStateThreads = 384;
+constexpr uint32_t kColPS = 256;   // two 128-column projection buffers
+
+__global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const TcParams tp) {
     const FwdParams& p = tp.p;
@@ -939,92 +967,188 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
     StateSmem& s = smem_ref<StateSmem>();
-    const int t = threadIdx.x, warp = t >> 5;
+    StateBars& B = s.b;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
     const bool favor = p.map == LA_MAP_FAVOR;
-    const int nq = r / 64;
+    const int nq = r / 64;                        // feature quarters (1, 2 or 4)
     const int nhalves = (r + 127) / 128;
-    if (t == 0) { prefetch_tensormap(&map_k); prefetch_tensormap(&map_v); }
-    setup_bars(s.b);
+    const int nchunks = (un.end - un.start + kC - 1) / kC;
+
+    if (t == 0) {
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B.k_full[i], 1);
+            mbar_init(&B.k_empty[i], favor ? 9 : 8);   // (MMA commit) + one arrival per PE warp
+            mbar_init(&B.v_full[i], 1);
+            mbar_init(&B.v_empty[i], 1);
+            mbar_init(&B.p_full[i], 1);
+            mbar_init(&B.p_empty[i], 8);
+            mbar_init(&B.h_full[i], 8);
+            mbar_init(&B.h_empty[i], 1);
+        }
+        mbar_init(&B.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&B.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
     if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
     fill_ones(s.ones);
-    if (nq == 1) zero_row(s.phk[1], t);
+    if (nq == 1) {   // feature rows 64..127 of the update operand stay zero
+        for (int i = t; i < kC; i += kStateThreads) {
+            zero_row(s.phk[0][1], i);
+            zero_row(s.phk[1][1], i);
+        }
+    }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tb = s.b.tmem_base;
-    {
-        uint32_t z[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = 0u;
-        for (int half = 0; half < nhalves; ++half)
-            for (int n0 = 0; n0 < kNX; n0 += 16) tmem_st16(tmem_addr(tb, warp * 32, kColS + 80 * half + n0), z);
-        tmem_st_wait();
-    }
-    handoff_to_mma();
-    if (t == 0) {
-        mbar_arrive_expect_tx(&s.b.load, kTile);
-        tma_load_3d(s.tk, &map_k, 0, head, un.start, &s.b.load);
-        mbar_arrive_expect_tx(&s.b.load_v, kTile);
-        tma_load_3d(s.tv, &map_v, 0, head, un.start, &s.b.load_v);
-    }
-    auto issue_job = [&](int q) {   // thread 0 only
-        mma_projection(tb + kColP + 64 * (q & 1), s.tk, s.omg_hi, s.omg_lo, 64 * q, 64);
-        mma_commit(&s.b.proj[q & 1]);
-    };
-    Phase lk, lv, pp0, pp1;
-    Commits cm;
-    bool ok = true;
-    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
-        const bool valid = t < min(kC, un.end - t0);
-        if (!(ok = lk.wait(&s.b.load))) break;
-        const float ck = favor ? favor_offset(s.tk, t, r) : 0.f;
-        const uint32_t base = cm.issued;
-        bool v_ready = false;
-        if (favor && t == 0) {
-            issue_job(0);
-            if (nq > 1) issue_job(1);
+    const uint32_t tb = B.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1, t0 = un.start + c * kC;
+                if (c >= 2 && !mbar_wait(&B.k_empty[st], ((c >> 1) - 1) & 1)) {
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&B.k_full[st], kTile);
+                tma_load_3d(s.tk[st], &map_k, 0, head, t0, &B.k_full[st]);
+                if (c >= 2 && !mbar_wait(&B.v_empty[st], ((c >> 1) - 1) & 1)) {
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&B.v_full[st], kTile);
+                tma_load_3d(s.tv[st], &map_v, 0, head, t0, &B.v_full[st]);
+            }
         }
-        for (int q = 0; q < nq; ++q) {
-            const int b = q & 1;
-            if (favor) {
-                if (!(ok = (b ? pp1 : pp0).wait(&s.b.proj[b]))) break;
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue (whole warp, elected lane issues)
+        const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
+        const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
+        const uint32_t id_proj = idesc_bf16(128, min(r, 128), false, false);
+        const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
+        // projection of k (chunk c) onto features 128h.. into buffer (c nhalves + h) & 1
+        auto issue_proj = [&](int c, int h) -> bool {
+            const int j = c * nhalves + h, b = j & 1;
+            if (j >= 2 && !warp_wait(&B.p_empty[b], ((j >> 1) - 1) & 1)) return false;
+            tc_fence_after();
+            const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk[c & 1]), 16, 1024);
+            const uint32_t d = tb + kColPS + 128 * b, fo = 16384u * h;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_ss_w(d, sdesc_add(d_tk, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_ss_w(d, sdesc_add(d_tk, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+            mma_commit_w(&B.p_full[b]);
+            return true;
+        };
+        bool ok = true;
+        if (favor && nchunks > 0) {
+            ok = warp_wait(&B.k_full[0], 0);
+            tc_fence_after();
+            for (int h = 0; h < nhalves && ok; ++h) ok = issue_proj(0, h);
+            if (ok) mma_commit_w(&B.k_empty[0]);
+        }
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            const bool next = favor && c + 1 < nchunks;
+            if (!(ok = warp_wait(&B.v_full[st], (c >> 1) & 1))) break;
+            const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv[st]), smem_u32(s.ones) - smem_u32(s.tv[st]), 1024);
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int hh = c * nhalves + h, hb = hh & 1;
+                if (!(ok = warp_wait(&B.h_full[hb], (hh >> 1) & 1))) break;
                 tc_fence_after();
-            }
-            // the first phi(k) of a half overwrites the previous half's update operand
-            if (q > 0 && (q & 1) == 0 && !(ok = cm.wait_for(&s.b.mma, base + (q >> 1)))) break;
-            if (favor) projection_epilogue(tb, kColP + 64 * b, 64, ck, valid, s.phk[b]);
-            else elementwise_phi_row(s.tk, s.phk[0], t, valid, p.map);
-            const bool update_now = (q & 1) || q == nq - 1;
-            if (update_now && !v_ready) {
-                if (!(ok = lv.wait(&s.b.load_v))) break;
-                v_ready = true;
-            }
-            handoff_to_mma();
-            if (t == 0) {
-                if (favor && q + 2 < nq) issue_job(q + 2);
-                if (update_now) {
-                    mma_state_update(tb + kColS + 80 * (q >> 1), s.phk[0], s.tv, s.ones);
-                    mma_commit(&s.b.mma);
+                const uint64_t d_a = sdesc_sw128(smem_u32(s.phk[hb][0]), kTile, 1024);   // MN-major
+#pragma unroll
+                for (int k = 0; k < kC / 16; ++k)
+                    mma_ss_w(tb + kColS + 80 * h, sdesc_add(d_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd,
+                             (c > 0 || k > 0) ? 1u : 0u);
+                mma_commit_w(&B.h_empty[hb]);
+                if (next) {
+                    if (h == 0 && !(ok = warp_wait(&B.k_full[(c + 1) & 1], ((c + 1) >> 1) & 1))) break;
+                    tc_fence_after();
+                    if (!(ok = issue_proj(c + 1, h))) break;
                 }
             }
-            if (update_now) ++cm.issued;
+            if (!ok) break;
+            mma_commit_w(&B.v_empty[st]);
+            if (next) mma_commit_w(&B.k_empty[(c + 1) & 1]);
         }
-        if (!ok) break;
-        if (t == 0 && t0 + kC < un.end) {   // every projection has read tk
-            mbar_arrive_expect_tx(&s.b.load, kTile);
-            tma_load_3d(s.tk, &map_k, 0, head, t0 + kC, &s.b.load);
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ PE: phi(k)
+        const int wg = (warp - 4) >> 2;           // converts features 64 wg .. of every half
+        const int tr = (t - 128) & 127;           // token row of the chunk = TMEM lane
+        const int wl = (warp & 3) * 32;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            const bool valid = tr < min(kC, un.end - (un.start + c * kC));
+            if (!(ok = warp_wait(&B.k_full[st], (c >> 1) & 1))) break;
+            const float ck = favor ? favor_offset(s.tk[st], tr, r) : 0.f;
+            if (favor) warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int hh = c * nhalves + h, hb = hh & 1;
+                const bool job = favor && 2 * h + wg < nq;
+                uint32_t v0[32], v1[32];
+                if (favor) {
+                    if (!(ok = warp_wait(&B.p_full[hb], (hh >> 1) & 1))) break;
+                    tc_fence_after();
+                    if (job) {
+                        tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * hb + 64 * wg), v0);
+                        tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * hb + 64 * wg + 32), v1);
+                        tmem_ld_wait();
+                    }
+                    warp_arrive(&B.p_empty[hb], false);
+                }
+                // the update that read this buffer last must be done
+                if (hh >= 2 && !(ok = warp_wait(&B.h_empty[hb], ((hh >> 1) - 1) & 1))) break;
+                unsigned char* dst = s.phk[hb][wg];
+                if (job) {
+                    // rows past the unit's end: 2^(p - inf) = 0
+                    const float cx = valid ? ck : __int_as_float(0x7f800000);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * i]) - cx),
+                                           ex2_approx(__uint_as_float(v0[2 * i + 1]) - cx));
+                    store_row32_bf16(dst, tr, 0, w);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * i]) - cx),
+                                           ex2_approx(__uint_as_float(v1[2 * i + 1]) - cx));
+                    store_row32_bf16(dst, tr, 32, w);
+                } else if (!favor && wg == 0) {
+                    elementwise_phi_row(s.tk[st], dst, tr, valid, p.map);
+                }
+                warp_arrive(&B.h_full[hb], true);
+            }
+            if (ok && !favor) warp_arrive(&B.k_empty[st], false);
         }
-        if (!(ok = cm.wait_for(&s.b.mma, cm.issued))) break;
-        tc_fence_after();
-        if (t == 0 && t0 + kC < un.end) {   // every update has read tv
-            mbar_arrive_expect_tx(&s.b.load_v, kTile);
-            tma_load_3d(s.tv, &map_v, 0, head, t0 + kC, &s.b.load_v);
-        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
-    if (ok) store_state(tb, p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves);
-    else drain_after_timeout(s.b, &p.hdr->error);
-    teardown(s.b);
+    // ---------------------------------------------------------------- state out
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {   // every update finished (bounded)
+        mma_commit_w(&B.drain);
+        if (!warp_wait(&B.drain, 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp >= 4 && warp < 8)
+        store_state(tb, p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves, t - 128, nchunks == 0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1120,7 +1244,7 @@ cudaError_t tc_state(const FwdParams& p, cudaStream_t s) {
     const size_t bytes = smem_bytes<StateSmem>();
     cudaError_t e = set_smem(tc_state_kernel, bytes);
     if (e != cudaSuccess) return e;
-    tc_state_kernel<<<dim3((unsigned)p.U, (unsigned)p.H), kThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    tc_state_kernel<<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
     return cudaGetLastError();
 }
 
