@@ -78,13 +78,17 @@ struct __align__(1024) BidirSmem {
     Bars b;
 };
 
-// Segment-state kernel: 209 KB.
+// Segment-state kernel: 226 KB.
+constexpr int kStateStages = 4;
 struct StateBars {
-    uint64_t k_full[2], k_empty[2];     // TMA -> all;  (MMA commit + 8 PE warps) -> TMA
-    uint64_t v_full[2], v_empty[2];     // TMA -> MMA;  MMA commit -> TMA
-    uint64_t p_full[2], p_empty[2];     // MMA commit -> PE: projection of a feature half;  PE (8 warps) -> MMA
-    uint64_t h_full[2], h_empty[2];     // PE (8 warps) -> MMA: phi(k) of one feature half; MMA commit -> PE
-    uint64_t drain;
+    uint64_t k_full[kStateStages], k_empty[kStateStages];   // TMA -> NE / PE;  (projection commit + NE) / 8 PE warps -> TMA
+    uint64_t v_full[kStateStages], v_empty[kStateStages];   // TMA -> update issuer;  its commit -> TMA
+    uint64_t cx_full[kStateStages];   // NE -> projection issuer: exponent offsets of the stage's tokens staged
+    uint64_t p_full[2];      // MMA commit -> PE: phi exponent of a feature half in fp32 buffer b
+    uint64_t p_empty[2];     // PE (8 warps) -> MMA: buffer b read out
+    uint64_t a_full[2];      // PE (8 warps) -> MMA: phi(k)^T of a half in bf16 buffer a
+    uint64_t a_empty[2];     // MMA commit -> PE: the update has read buffer a
+    uint64_t drain[2];
     uint32_t tmem_base;
     int pad;
 };
@@ -92,9 +96,10 @@ struct StateBars {
 struct __align__(1024) StateSmem {
     unsigned char omg_hi[kOmgBytes];
     unsigned char omg_lo[kOmgBytes];
-    Tile tk[2], tv[2];                  // two stages
-    Tile ones;
-    Tile phk[2][2];                     // [buffer][quarter of the half]: phi(k) of 128 features
+    Tile tk[kStateStages], tv[kStateStages];
+    Tile bias;                    // K-major [token][64]: columns 16 st, 16 st + 1 = -offset (hi, lo) of stage st
+    Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1
+    float zsum[256];              // normaliser column: second warpgroup's share
     StateBars b;
 };
 
@@ -946,18 +951,39 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // ---------------------------------------------------------------------------
 // Segment-state kernel (warp-specialised): [S|z] = sum over the unit of phi(k) [v | 1]^T
 // ---------------------------------------------------------------------------
+// The projection is computed transposed, P^T = Omega' K^T (TMEM lanes = features,
+// columns = tokens); one more K step adds each token's exponent offset -(log2(e)
+// |k|^2 / 2 + log2(sqrt r)) as bf16 hi + lo, so that phi = 2^P^T element-wise.
+// The PE warps turn it into phi(k)^T, write it to tensor memory
+// as bf16 and keep the normaliser z = sum_t phi(k_t) in registers (from the same
+// bf16 values); S += phi(k)^T V takes its A operand from tensor memory.  Neither
+// phi(k) nor the update's A operand passes through shared memory.
+// TMEM: S [0, 128) (64 columns per 128-feature half), two fp32 projection buffers
+// [128, 384), two bf16 phi(k)^T buffers [384, 512).
 // Roles (384 threads):
-//   warp 0 lane 0     TMA: the k and v tiles of each chunk into two alternating stages
-//   warp 1            MMA issue (one elected lane; warp 1 owns the TMEM allocation).
-//                     For each 128-feature half h of chunk c: the state update of
-//                     (c, h), then the projection of (c + 1, h) into one of two TMEM
-//                     buffers, so the projections run one chunk ahead of the updates
-//   warps 4..11       two warpgroups; warpgroup w converts features 64w..64w+63 of
-//                     every half into phi(k) (one of two alternating 128-feature
-//                     buffers in shared memory)
-// The state accumulates in TMEM over the unit and is written once at the end.
+//   warp 0 lane 0     TMA: k and v tiles of each chunk into four stages (and L2 prefetch)
+//   warp 1            projection MMAs (one elected lane; warp 1 owns the TMEM
+//                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the PE
+//                     has read that buffer out
+//   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T.
+//                     The two issuers touch disjoint tensor memory and never wait
+//                     on each other
+//   warp 3 (NE)       the exponent offset of every token of a stage (FAVOR+), into
+//                     the bias operand of the projection
+//   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
+//                     every half (lane = feature)
+// The state accumulates in TMEM and registers over the unit and is written once.
 constexpr int kStateThreads = 384;
-constexpr uint32_t kColPS = 256;   // two 128-column projection buffers
+constexpr int kPrefetchAhead = 4;  // chunks of k and v requested into L2 ahead of the loads
+constexpr uint32_t kColSS = 0;     // S, 64 columns per half
+constexpr uint32_t kColPS = 128;   // two 128-column fp32 projection buffers
+constexpr uint32_t kColAS = 384;   // two 64-column bf16 phi(k)^T buffers
+
+// phi of one element for the element-wise maps.
+__device__ __forceinline__ float phi_elementwise(float x, int map) {
+    if (map == LA_MAP_ELU1) return x > 0.f ? x + 1.f : ex2_approx(x * kLog2e);
+    return x;
+}
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -971,56 +997,72 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
     const bool favor = p.map == LA_MAP_FAVOR;
-    const int nq = r / 64;                        // feature quarters (1, 2 or 4)
     const int nhalves = (r + 127) / 128;
     const int nchunks = (un.end - un.start + kC - 1) / kC;
 
     if (t == 0) {
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStateStages; ++i) {
             mbar_init(&B.k_full[i], 1);
-            mbar_init(&B.k_empty[i], favor ? 9 : 8);   // (MMA commit) + one arrival per PE warp
+            mbar_init(&B.k_empty[i], favor ? 2 : 8);   // projection commit + NE (FAVOR+) or the PE warps
             mbar_init(&B.v_full[i], 1);
             mbar_init(&B.v_empty[i], 1);
+            mbar_init(&B.cx_full[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
             mbar_init(&B.p_empty[i], 8);
-            mbar_init(&B.h_full[i], 8);
-            mbar_init(&B.h_empty[i], 1);
+            mbar_init(&B.a_full[i], 8);
+            mbar_init(&B.a_empty[i], 1);
         }
-        mbar_init(&B.drain, 1);
+        mbar_init(&B.drain[0], 1);
+        mbar_init(&B.drain[1], 1);
         fence_mbar_init();
     }
     if (warp == 1) {
         tmem_alloc(&B.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
-    fill_ones(s.ones);
-    if (nq == 1) {   // feature rows 64..127 of the update operand stay zero
-        for (int i = t; i < kC; i += kStateThreads) {
-            zero_row(s.phk[0][1], i);
-            zero_row(s.phk[1][1], i);
+    if (favor) {
+        stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+        for (int i = t; i < (128 - r) * 8 && r < 128; i += kStateThreads) {   // features r..127 of half 0: zero
+            const int row = r + (i >> 3), c = i & 7;
+            *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(s.omg_lo + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    for (int i = t; i < kC * 8; i += kStateThreads) {   // bias columns start at zero; ones at 16 i, 16 i + 1
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(s.bias + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) =
+            make_uint4((c & 1) == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = B.tmem_base;
+    float z0 = 0.f, z1 = 0.f;     // PE: this thread's share of z for its feature in halves 0 and 1
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1, t0 = un.start + c * kC;
-                if (c >= 2 && !mbar_wait(&B.k_empty[st], ((c >> 1) - 1) & 1)) {
+                const int st = c % kStateStages, ph = ((c / kStateStages) - 1) & 1, t0 = un.start + c * kC;
+                // into L2 ahead of the stages: the loads below then wait on L2, not DRAM
+                for (int a = (c == 0 ? 0 : kPrefetchAhead); a <= kPrefetchAhead; ++a)
+                    if (c + a < nchunks) {
+                        tma_prefetch_3d(&map_k, 0, head, t0 + a * kC);
+                        tma_prefetch_3d(&map_v, 0, head, t0 + a * kC);
+                    }
+                if (c >= kStateStages && !mbar_wait(&B.k_empty[st], ph)) {
                     record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
                 mbar_arrive_expect_tx(&B.k_full[st], kTile);
                 tma_load_3d(s.tk[st], &map_k, 0, head, t0, &B.k_full[st]);
-                if (c >= 2 && !mbar_wait(&B.v_empty[st], ((c >> 1) - 1) & 1)) {
+                if (c >= kStateStages && !mbar_wait(&B.v_empty[st], ph)) {
                     record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -1029,123 +1071,171 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue (whole warp, elected lane issues)
+        // ------------------------------------------------------------ projection MMAs (elected lane issues)
         const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
         const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
-        const uint32_t id_proj = idesc_bf16(128, min(r, 128), false, false);
-        const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
-        // projection of k (chunk c) onto features 128h.. into buffer (c nhalves + h) & 1
-        auto issue_proj = [&](int c, int h) -> bool {
-            const int j = c * nhalves + h, b = j & 1;
-            if (j >= 2 && !warp_wait(&B.p_empty[b], ((j >> 1) - 1) & 1)) return false;
-            tc_fence_after();
-            const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk[c & 1]), 16, 1024);
-            const uint32_t d = tb + kColPS + 128 * b, fo = 16384u * h;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_ss_w(d, sdesc_add(d_tk, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_ss_w(d, sdesc_add(d_tk, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
-            mma_commit_w(&B.p_full[b]);
-            return true;
-        };
+        const uint64_t d_bias = sdesc_sw128(smem_u32(s.bias), 16, 1024);
+        const uint64_t d_ones = sdesc_sw128(smem_u32(s.ones), 16, 1024);
+        const uint32_t id_proj = idesc_bf16(128, kC, false, false);   // M = features, N = tokens
         bool ok = true;
-        if (favor && nchunks > 0) {
-            ok = warp_wait(&B.k_full[0], 0);
-            tc_fence_after();
-            for (int h = 0; h < nhalves && ok; ++h) ok = issue_proj(0, h);
-            if (ok) mma_commit_w(&B.k_empty[0]);
-        }
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1;
-            const bool next = favor && c + 1 < nchunks;
-            if (!(ok = warp_wait(&B.v_full[st], (c >> 1) & 1))) break;
-            const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv[st]), smem_u32(s.ones) - smem_u32(s.tv[st]), 1024);
+        for (int c = 0; favor && c < nchunks && ok; ++c) {
+            const int st = c % kStateStages;
+            if (!(ok = warp_wait(&B.cx_full[st], (c / kStateStages) & 1))) break;   // tile and offsets staged
+            const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk[st]), 16, 1024);
             for (int h = 0; h < nhalves && ok; ++h) {
-                const int hh = c * nhalves + h, hb = hh & 1;
-                if (!(ok = warp_wait(&B.h_full[hb], (hh >> 1) & 1))) break;
+                // exponent of phi(k)^T, features 128h..: Omega' K^T, then one K step of
+                // ones x (-offset hi, -offset lo) per token
+                const int j = c * nhalves + h, b = j & 1;
+                if (j >= 2 && !(ok = warp_wait(&B.p_empty[b], ((j >> 1) - 1) & 1))) break;
                 tc_fence_after();
-                const uint64_t d_a = sdesc_sw128(smem_u32(s.phk[hb][0]), kTile, 1024);   // MN-major
+                const uint32_t d = tb + kColPS + 128 * b, fo = 16384u * h;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(d, sdesc_add(d_omg_hi, fo + 32 * k), sdesc_add(d_tk, 32 * k), id_proj, k > 0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(d, sdesc_add(d_omg_lo, fo + 32 * k), sdesc_add(d_tk, 32 * k), id_proj, 1u);
+                mma_ss_w(d, sdesc_add(d_ones, 32 * st), sdesc_add(d_bias, 32 * st), id_proj, 1u);
+                mma_commit_w(&B.p_full[b]);
+            }
+            if (ok) mma_commit_w(&B.k_empty[st]);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ state-update MMAs (elected lane issues)
+        const uint32_t id_upd = idesc_bf16(128, 64, false, true);     // A from TMEM, B = V MN-major
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c % kStateStages;
+            if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
+            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv[st]), 16, 1024);   // MN-major, one 64-wide atom
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int j = c * nhalves + h, b = j & 1;
+                if (!(ok = warp_wait(&B.a_full[b], (j >> 1) & 1))) break;
+                tc_fence_after();
+                const uint32_t a0 = tb + kColAS + 64 * b;
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ss_w(tb + kColS + 80 * h, sdesc_add(d_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd,
+                    mma_ts_w(tb + kColSS + 64 * h, a0 + 8 * k, sdesc_add(d_v, 2048 * k), id_upd,
                              (c > 0 || k > 0) ? 1u : 0u);
-                mma_commit_w(&B.h_empty[hb]);
-                if (next) {
-                    if (h == 0 && !(ok = warp_wait(&B.k_full[(c + 1) & 1], ((c + 1) >> 1) & 1))) break;
-                    tc_fence_after();
-                    if (!(ok = issue_proj(c + 1, h))) break;
-                }
+                mma_commit_w(&B.a_empty[b]);
             }
-            if (!ok) break;
-            mma_commit_w(&B.v_empty[st]);
-            if (next) mma_commit_w(&B.k_empty[(c + 1) & 1]);
+            if (ok) mma_commit_w(&B.v_empty[st]);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ PE: phi(k)
-        const int wg = (warp - 4) >> 2;           // converts features 64 wg .. of every half
-        const int tr = (t - 128) & 127;           // token row of the chunk = TMEM lane
-        const int wl = (warp & 3) * 32;
+        // ------------------------------------------------------------ PE: phi(k)^T
+        const int wg = (warp - 4) >> 2;           // tokens 64 wg .. 64 wg + 63
+        const int wl = (warp & 3) * 32;           // TMEM lane base: features wl .. wl + 31 of a half
+        const int f = wl + lane;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1;
-            const bool valid = tr < min(kC, un.end - (un.start + c * kC));
-            if (!(ok = warp_wait(&B.k_full[st], (c >> 1) & 1))) break;
-            const float ck = favor ? favor_offset(s.tk[st], tr, r) : 0.f;
-            if (favor) warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
+            const int st = c % kStateStages;
+            const int nvalid = min(kC, un.end - (un.start + c * kC));
+            if (!favor && !(ok = warp_wait(&B.k_full[st], (c / kStateStages) & 1))) break;
             for (int h = 0; h < nhalves && ok; ++h) {
-                const int hh = c * nhalves + h, hb = hh & 1;
-                const bool job = favor && 2 * h + wg < nq;
-                uint32_t v0[32], v1[32];
+                const int j = c * nhalves + h, b = j & 1;
+                const bool live = 128 * h + f < r;
+                uint32_t w[32];
                 if (favor) {
-                    if (!(ok = warp_wait(&B.p_full[hb], (hh >> 1) & 1))) break;
+                    if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
                     tc_fence_after();
-                    if (job) {
-                        tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * hb + 64 * wg), v0);
-                        tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * hb + 64 * wg + 32), v1);
-                        tmem_ld_wait();
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg), v0);
+                    tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg + 32), v1);
+                    tmem_ld_wait();
+                    warp_arrive(&B.p_empty[b], false);
+                    // the update that read this phi buffer last must be done
+                    if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * e])),
+                                                  ex2_approx(__uint_as_float(v0[2 * e + 1]))) : 0u;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[16 + e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * e])),
+                                                       ex2_approx(__uint_as_float(v1[2 * e + 1]))) : 0u;
+                } else {
+                    if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int t0 = 64 * wg + 2 * e;
+                        float x0 = 0.f, x1 = 0.f;
+                        if (live && t0 < nvalid)
+                            x0 = phi_elementwise(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                                     s.tk[st] + sw128_off(t0, f))), p.map);
+                        if (live && t0 + 1 < nvalid)
+                            x1 = phi_elementwise(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                                     s.tk[st] + sw128_off(t0 + 1, f))), p.map);
+                        w[e] = pack_bf16x2(x0, x1);
                     }
-                    warp_arrive(&B.p_empty[hb], false);
                 }
-                // the update that read this buffer last must be done
-                if (hh >= 2 && !(ok = warp_wait(&B.h_empty[hb], ((hh >> 1) - 1) & 1))) break;
-                unsigned char* dst = s.phk[hb][wg];
-                if (job) {
-                    // rows past the unit's end: 2^(p - inf) = 0
-                    const float cx = valid ? ck : __int_as_float(0x7f800000);
-                    uint32_t w[16];
+                tmem_st32(tmem_addr(tb, wl, kColAS + 64 * b + 32 * wg), w);
+                float zs = 0.f;   // z from the same bf16 values the update multiplies
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * i]) - cx),
-                                           ex2_approx(__uint_as_float(v0[2 * i + 1]) - cx));
-                    store_row32_bf16(dst, tr, 0, w);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * i]) - cx),
-                                           ex2_approx(__uint_as_float(v1[2 * i + 1]) - cx));
-                    store_row32_bf16(dst, tr, 32, w);
-                } else if (!favor && wg == 0) {
-                    elementwise_phi_row(s.tk[st], dst, tr, valid, p.map);
-                }
-                warp_arrive(&B.h_full[hb], true);
+                for (int e = 0; e < 32; ++e) zs += bf16lo(w[e]) + bf16hi(w[e]);
+                if (h == 0) z0 += zs;
+                else z1 += zs;
+                tmem_st_wait();
+                warp_arrive(&B.a_full[b], false);
             }
-            if (ok && !favor) warp_arrive(&B.k_empty[st], false);
+            if (ok && !favor) warp_arrive(&B.k_empty[st], false);   // done with the tile
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+        if (wg == 1) {
+            s.zsum[f] = z0;
+            s.zsum[128 + f] = z1;
+        }
+    } else if (favor) {
+        // ------------------------------------------------------------ NE: exponent offsets (warp 3)
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c % kStateStages;
+            const int nvalid = min(kC, un.end - (un.start + c * kC));
+            if (!(ok = warp_wait(&B.k_full[st], (c / kStateStages) & 1))) break;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int tok = lane + 32 * x;
+                // -offset as bf16 hi + lo into the stage's bias columns; past the unit's
+                // end a large negative exponent makes phi = 0
+                const float o = tok < nvalid ? -(row_sq_norm(s.tk[st], tok) * (0.5f * kLog2e) + 0.5f * __log2f((float)r))
+                                             : -32768.f;
+                const uint32_t hl = pack_bf16x2(o, 0.f);
+                *reinterpret_cast<uint32_t*>(s.bias + sw128_off(tok, 16 * st)) = pack_bf16x2(o, o - bf16lo(hl));
+            }
+            warp_arrive(&B.cx_full[st], true);
+            warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     // ---------------------------------------------------------------- state out
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {   // every update finished (bounded)
-        mma_commit_w(&B.drain);
-        if (!warp_wait(&B.drain, 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    if (warp == 1 || warp == 2) {   // every MMA of both issuers finished (bounded)
+        mma_commit_w(&B.drain[warp - 1]);
+        if (!warp_wait(&B.drain[warp - 1], 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     __syncthreads();
     tc_fence_after();
-    if (warp >= 4 && warp < 8)
-        store_state(tb, p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves, t - 128, nchunks == 0);
+    if (warp >= 4 && warp < 8) {   // [S|z] rows of this thread's feature in each half
+        const int f = t - 128;
+        float* dst = p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65;
+        for (int h = 0; h < nhalves; ++h) {
+            const int feat = 128 * h + f;
+            for (int n0 = 0; n0 < 64; n0 += 16) {
+                uint32_t w[16] = {};
+                if (nchunks > 0) {
+                    tmem_ld16(tmem_addr(tb, (warp & 3) * 32, kColSS + 64 * h + n0), w);
+                    tmem_ld_wait();
+                }
+                if (feat < r) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dst[(int64_t)feat * 65 + n0 + e] = __uint_as_float(w[e]);
+                }
+            }
+            if (feat < r) dst[(int64_t)feat * 65 + 64] = (h == 0 ? z0 : z1) + s.zsum[128 * h + f];
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tb, kTmemCols);
