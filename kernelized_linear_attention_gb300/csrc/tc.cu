@@ -484,7 +484,7 @@ struct Commits {
 // ---------------------------------------------------------------------------
 // Roles (512 threads):
 //   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
-//   warp 1 lane 0      MMA issue (warp 1 also owns the TMEM allocation)
+//   warp 1             MMA issue, one elected lane (warp 1 also owns the TMEM allocation)
 //   warps 4..7 (PE)    projection epilogue: phi(k), phi(q) of each quarter of the
 //                      features into shared memory (token t = TMEM lane t)
 //   warps 8..11 (OE)   masked scores as bf16 hi + lo in TMEM; the output rows
@@ -632,8 +632,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         }
     }
     else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issue (whole warp, elected lane issues)
+        {
             const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
             const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
             const uint64_t d_tq = sdesc_sw128(smem_u32(s.tq), 16, 1024);
@@ -652,22 +652,22 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             bool ok = true;
             // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b
             auto issue_job = [&](int b, int quarter) -> bool {
-                if (!mbar_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
+                if (!warp_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
                 ++jobs[b];
                 tc_fence_after();
                 const uint64_t dx = b ? d_tq : d_tk;
                 const uint32_t d = tb + kColP + 64 * b, fo = 8192u * quarter;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_ss(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+                for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_ss(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
-                mma_commit(&B.p_full[b]);
+                for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+                mma_commit_w(&B.p_full[b]);
                 return true;
             };
             bool started = false;   // first projection jobs of chunk c already issued
             for (int c = 0; c < nchunks && ok; ++c) {
                 if (!started) {
-                    if (!(ok = mbar_wait(&B.qk_full, c & 1))) break;
+                    if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
                     if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
                 }
                 started = false;
@@ -676,55 +676,55 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     if (favor && q + 1 < nq) {
                         if (!(ok = issue_job(0, q + 1) && issue_job(1, q + 1))) break;
                     }
-                    if (q == nq - 1) mma_commit(&B.qk_empty);   // every projection of this chunk issued
+                    if (q == nq - 1) mma_commit_w(&B.qk_empty);   // every projection of this chunk issued
                     const int g = c * nq + q;
-                    if (!(ok = mbar_wait(&B.phik_full[g & 1], (g >> 1) & 1) && mbar_wait(&B.phiq_full, g & 1))) break;
+                    if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1) && warp_wait(&B.phiq_full, g & 1))) break;
                     if (q == 0) {   // O and the scores of chunk c-1 read out; bf16 state of chunks < c ready
-                        if (!(ok = (c == 0 || mbar_wait(&B.o_empty, (c - 1) & 1)) && mbar_wait(&B.sbf_full, c & 1))) break;
+                        if (!(ok = (c == 0 || warp_wait(&B.o_empty, (c - 1) & 1)) && warp_wait(&B.sbf_full, c & 1))) break;
                         tc_fence_after();
                     }
                     const bool update_now = (q & 1) || q == nq - 1;
                     if (update_now && !v_ready) {
-                        if (!(ok = mbar_wait(&B.v_full, c & 1))) break;
+                        if (!(ok = warp_wait(&B.v_full, c & 1))) break;
                         v_ready = true;
                     }
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
+                        mma_ss_w(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
                                (q > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, kSbfBlock * q + 32 * k), id_read,
+                        mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, kSbfBlock * q + 32 * k), id_read,
                                (q > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(&B.phq_free);   // phi(q) of the next quarter waits only for these
+                    mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
                     if (update_now) {
 #pragma unroll
                         for (int k = 0; k < kC / 16; ++k)
-                            mma_ss(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
+                            mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
                     }
-                    mma_commit(&B.cons[g & 1]);
+                    mma_commit_w(&B.cons[g & 1]);
                 }
                 if (!ok) break;
-                mma_commit(&B.a_full);
+                mma_commit_w(&B.a_full);
                 // overlap: if the next chunk's q and k have landed, start its projections
                 // now, while the output warps split this chunk's scores
-                if (c + 1 < nchunks && mbar_test_wait(&B.qk_full, (c + 1) & 1)) {
+                if (c + 1 < nchunks && __any_sync(0xffffffffu, mbar_test_wait(&B.qk_full, (c + 1) & 1))) {
                     if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
                     started = true;
                 }
-                if (!(ok = mbar_wait(&B.ahl_full, c & 1))) break;
+                if (!(ok = warp_wait(&B.ahl_full, c & 1))) break;
                 tc_fence_after();
                 // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ts(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ts(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
-                mma_commit(&B.o_full);
-                mma_commit(&B.v_empty);
+                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                mma_commit_w(&B.o_full);
+                mma_commit_w(&B.v_empty);
             }
-            if (!ok) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+            if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
         }
     }
     else if (warp >= 4 && warp < 8) {
@@ -857,9 +857,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     // ---------------------------------------------------------------- exit
     tc_fence_before();
     __syncthreads();
-    if (t == 32) {   // all MMAs of this CTA finished before TMEM is freed (bounded)
-        mma_commit(&B.drain);
-        mbar_wait(&B.drain, 0, 500000000ull);
+    if (warp == 1) {   // all MMAs of this CTA finished before TMEM is freed (bounded)
+        mma_commit_w(&B.drain);
+        if (!warp_wait(&B.drain, 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     __syncthreads();
     if (warp == 1) tmem_dealloc(tb, kTmemCols);
