@@ -38,7 +38,11 @@ WORKLOAD = "favor_causal_b1h16n65536"
 METRIC = "tokens/s/GPU causal FAVOR+ r=256 d=64; % tensor-core / HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PHASE_NAMES = ["plan", "state", "scan", "output"]
-KERNEL_SOURCES = {"output": "simt.cu", "state": "simt.cu", "scan": "plan.cu", "plan": "plan.cu"}
+# source file of each phase's kernel on the tensor-core (tc) and CUDA-core (simt) paths
+KERNEL_SOURCES = {"tc": {"output": "tc.cu", "state": "tc.cu", "scan": "plan.cu", "plan": "plan.cu"},
+                  "simt": {"output": "simt.cu", "state": "simt.cu", "scan": "plan.cu", "plan": "plan.cu"}}
+# second measured line: the bidirectional state pass (phi(k)^T [v|1] over every token)
+BIDIR_WORKLOAD = "favor_bidir_b4h8n16384"
 
 
 def parse_args(argv=None):
@@ -51,6 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the bidirectional state-pass line")
     return ap.parse_args(argv)
 
 
@@ -84,21 +89,21 @@ def measured_peaks() -> dict:
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_source_hash(phase: str) -> str:
-    p = os.path.join(ROOT, "kernelized_linear_attention_gb300", "csrc", KERNEL_SOURCES[phase])
+def kernel_source_hash(path: str, phase: str) -> str:
+    p = os.path.join(ROOT, "kernelized_linear_attention_gb300", "csrc", KERNEL_SOURCES[path][phase])
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(phase: str, workload: str):
+def recorded_traffic(path: str, phase: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on
-    the current source of that kernel (else None)."""
+    the current source of that kernel on this path (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d[workload][phase]
-        if e.get("source_sha256_16") == kernel_source_hash(phase):
+        e = d[workload][path][phase]
+        if e.get("source_sha256_16") == kernel_source_hash(path, phase):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -344,8 +349,9 @@ def run_ours(args):
         byts = alg["bytes"] * token_heads / 2 if dom == "state" else alg_bytes
         achieved = byts / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 else "simt"
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["traffic"] = recorded_traffic(path, dom, w.name)
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")
     roof["tensor_frac_of_output"] = alg_flops / (phase_ms["output"] * 1e-3) / 1e12 / peaks["bf16_tflops"]
@@ -383,15 +389,61 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.nseq, "H": H, "N": w.lengths[0], "d_k": dk, "d_v": dv, "r": r,
                    "map": w.map, "causal": w.causal, "eps": w.eps, "parallelism": f"replicas x{world}",
                    "l2": "no flush: q, k, v (402 MB) exceed the 126 MB L2",
-                   "path": "tcgen05" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 else "cuda-core"},
+                   "path": "tcgen05" if path == "tc" else "cuda-core"},
         "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
+    if not args.no_secondary:
+        line["bidir_state_pass"] = bidir_state_pass(la, dev, stream, peaks, K)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def bidir_state_pass(la, dev, stream, peaks, steps: int) -> dict:
+    """The state phase of the bidirectional FAVOR+ forward (the per-segment
+    sum of phi(k_j) [v_j | 1]^T over every token) on its own workload, timed
+    with CUDA events on the launching stream after warm-up.  Algorithmic
+    bytes: k and v read once (2 * d * 2 B per token-head; the state written is
+    negligible).  q, k, v (100 MB) are below L2, so L2 is flushed between
+    launches by writing a 256 MB buffer (outside the timed intervals)."""
+    import torch
+    w = synthetic.workloads()[BIDIR_WORKLOAD]
+    inputs = synthetic.make_qkv(w)
+    dev_t = {n: torch.from_numpy(np.ascontiguousarray(inputs.storage(n))).view(torch.bfloat16).to(dev)
+             for n in ("q", "k", "v")}
+    blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+    omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), w.r)
+    out = torch.empty((w.T, w.H, w.dv), dtype=torch.bfloat16, device=dev)
+    nb = la.la_workspace_bytes(False, w.map, torch.bfloat16, False, w.nseq, w.T, w.H, w.dk, w.dv, w.r)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    args = (dev_t["q"].data_ptr(), dev_t["k"].data_ptr(), dev_t["v"].data_ptr(), omega.data_ptr(), w.map,
+            torch.bfloat16, None, w.nseq, w.T, w.H, w.dk, w.dv, w.r, w.eps, out.data_ptr(), ws.data_ptr(), nb,
+            stream.cuda_stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    la.la_forward_phase(False, 0, *args)
+    for _ in range(3):
+        la.la_forward_phase(False, 1, *args)
+    times = []
+    for _ in range(max(3, steps)):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        la.la_forward_phase(False, 1, *args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if la.la_workspace_error(ws) != 0:
+        raise RuntimeError("device error in the bidirectional state pass")
+    ms = statistics.mean(times)
+    byts = w.T * w.H * 2 * w.dk * 2
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "kernel": "state (tc_state_kernel)", "ms": ms, "bound": "hbm",
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "alg_bytes": byts, "l2": "flushed (256 MB write) before each timed launch",
+            "traffic": recorded_traffic("tc", "state", w.name)}
 
 
 def run_reference(args):
