@@ -255,24 +255,6 @@ __device__ void projection_to_global(uint32_t tbase, int nf, float c, bool valid
     }
 }
 
-// State of one feature half (TMEM lanes = features, 80 columns) -> bf16 rows n of
-// the K-major readout blocks sbf[2 half], sbf[2 half + 1] (thread f owns feature 128 half + f).
-__device__ void state_to_sbf(unsigned char (*sbf)[kSbfBlock], uint32_t tbase, int half, int f = threadIdx.x) {
-    const int warp = f >> 5;
-    unsigned char* blk = sbf[2 * half + (f >> 6)];
-    const uint32_t col = f & 63;
-#pragma unroll 1
-    for (int n0 = 0; n0 < kNX; n0 += 16) {
-        uint32_t w[16];
-        tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<__nv_bfloat16*>(blk + sw128_off(n0 + j, col)) =
-                __float2bfloat16_rn(__uint_as_float(w[j]));
-    }
-}
-
 // The fp32 state a unit starts from ([r][65] in global; zero if `zero`):
 // into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
 // rounding remainder into lo when lo != nullptr).
@@ -348,6 +330,13 @@ __device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat1
                                 pack_bf16x2(__uint_as_float(b[8 * q + 2]) * inv, __uint_as_float(b[8 * q + 3]) * inv),
                                 pack_bf16x2(__uint_as_float(b[8 * q + 4]) * inv, __uint_as_float(b[8 * q + 5]) * inv),
                                 pack_bf16x2(__uint_as_float(b[8 * q + 6]) * inv, __uint_as_float(b[8 * q + 7]) * inv));
+}
+
+// 64 bf16 (packed in pairs) as row `row` of a 128-byte-swizzled tile.
+__device__ __forceinline__ void state_row_bf16(unsigned char* tile, int row, const uint32_t (&w)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, c)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // One output row from registers: O[0..63] / max(den, eps) as bf16 to global.
@@ -513,7 +502,7 @@ struct CausalBars {
     uint64_t ahl_full;              // OE (4 warps) -> MMA: masked scores hi/lo in TMEM
     uint64_t o_full;                // MMA commit -> OE: numerator/denominator complete
     uint64_t o_empty;               // OE (4 warps) -> MMA: O read out of TMEM
-    uint64_t sbf_full;              // SE (4 warps) -> MMA: bf16 state of the previous chunks in smem
+    uint64_t sbf_full;              // SE (4 warps) -> MMA, PE: bf16 state and fp32 z of the previous chunks in smem
     uint64_t drain;
     uint32_t tmem_base;
     int pad;
@@ -526,7 +515,8 @@ struct __align__(1024) CausalSmem {
     Tile ones;                        // second MN atom of [V|1]: column 0 = 1
     Tile phq;                         // Phi_Q of one quarter (64 features)
     Tile phk[2];                      // Phi_K of one half (two quarters)
-    unsigned char sbf[4][kSbfBlock];  // [S|z]^T bf16: block j = features 64j..64j+63, rows n < 80
+    Tile sbf[2];                      // S bf16, MN-major [feature][v]: features 128h.. in sbf[h]
+    unsigned char zrow[4][2048];      // per quarter: K-major [16][64], row 0 = z bf16, rows 1..15 = 0
     CausalBars b;
 };
 
@@ -604,6 +594,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(s.omg_lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
     }
+    for (int i = t; i < 4 * 2048 / 16; i += kCausalThreads)
+        reinterpret_cast<uint4*>(s.zrow)[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int i = t; i < kC * 8; i += kCausalThreads) {
         const int row = i >> 3, c = i & 7;
         *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
@@ -640,14 +632,17 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk), 16, 1024);
             const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq), 16, 1024);
             const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
-            const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), 16, 1024);
+            const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), kTile, 1024);                 // MN-major
+            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv), kTile, 1024);                       // MN-major, V only
+            const uint64_t d_zrow = sdesc_sw128(smem_u32(s.zrow[0]), 16, 1024);
+            const uint32_t id_den = idesc_bf16(128, 16, false, false);
             const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
             const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones) - smem_u32(s.tv), 1024);
             const uint32_t id_proj = idesc_bf16(128, 64, false, false);
             const uint32_t id_scores = idesc_bf16(128, 128, false, false);
-            const uint32_t id_read = idesc_bf16(128, kNX, false, false);
+            const uint32_t id_read = idesc_bf16(128, 64, false, true);
             const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
-            const uint32_t id_av = idesc_bf16(128, kNX, false, true);
+            const uint32_t id_av = idesc_bf16(128, 64, false, true);
             uint32_t jobs[2] = {0u, 0u};
             bool ok = true;
             // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b
@@ -694,7 +689,13 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                                (q > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, kSbfBlock * q + 32 * k), id_read,
+                        mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
+                               (q > 0 || k > 0) ? 1u : 0u);
+                    // denominator term phi(q) . z into column 64 of O (z as the only
+                    // non-zero row of a 16-row operand)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
                                (q > 0 || k > 0) ? 1u : 0u);
                     mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
                     if (update_now) {
@@ -717,10 +718,10 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_vx, 2048 * k), id_av, 1u);
+                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
                 mma_commit_w(&B.o_full);
                 mma_commit_w(&B.v_empty);
             }
@@ -797,6 +798,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             // masked scores (key j <= query tr) as bf16 hi + lo, two keys per column, in
             // TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127]: each group of
             // 64 keys is read whole before its 64 columns are overwritten
+            float dsum = 0.f;   // sum_{j <= i} A_ij: the in-chunk part of the denominator
             for (int part = 0; part < 2; ++part) {
                 const uint32_t cb = kColA + 64 * part;
                 uint32_t v0[32], v1[32];
@@ -809,6 +811,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     const int c0 = 64 * part + 2 * j;
                     const float a = c0 <= tr ? __uint_as_float(v0[2 * j]) : 0.f;
                     const float b2 = c0 + 1 <= tr ? __uint_as_float(v0[2 * j + 1]) : 0.f;
+                    dsum += a + b2;
                     hv[j] = pack_bf16x2(a, b2);
                     lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
                 }
@@ -819,6 +822,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     const int c0 = 64 * part + 32 + 2 * j;
                     const float a = c0 <= tr ? __uint_as_float(v1[2 * j]) : 0.f;
                     const float b2 = c0 + 1 <= tr ? __uint_as_float(v1[2 * j + 1]) : 0.f;
+                    dsum += a + b2;
                     hv[j] = pack_bf16x2(a, b2);
                     lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
                 }
@@ -829,27 +833,67 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             warp_arrive(&B.ahl_full, false);
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            uint32_t o0[32], o1[32], den;
+            uint32_t o0[32], o1[32], dz;
             tmem_ld32(tmem_addr(tb, wl, kColO), o0);
             tmem_ld32(tmem_addr(tb, wl, kColO + 32), o1);
-            tmem_ld1(tmem_addr(tb, wl, kColO + 64), den);
+            tmem_ld1(tmem_addr(tb, wl, kColO + 64), dz);
             tmem_ld_wait();
+            const float den = dsum + __uint_as_float(dz);
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
-            if (valid) store_output_row(o0, o1, den, p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+            if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp >= 12) {
         // ------------------------------------------------------------ SE: state of the chunks so far
         const int tr = t - 384;                   // state feature (within a half) = TMEM lane
         const int64_t E = (int64_t)r * 65;
-        load_state(s.sbf, nullptr, tb, true, p.prefix + ((int64_t)u * p.H + head) * E, r, nhalves,
-                   tp.prefix_is_zero != 0, tr);
+        const float* src = p.prefix + ((int64_t)u * p.H + head) * E;
+        const bool zero = tp.prefix_is_zero != 0;
+        for (int half = 0; half < nhalves; ++half) {   // the entering state: TMEM, bf16 rows, z
+            const int feat = 128 * half + tr;
+            const bool have = !zero && feat < r;
+            uint32_t w[32];
+#pragma unroll
+            for (int n0 = 0; n0 < kNX; n0 += 16) {
+                uint32_t x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    x[j] = __float_as_uint((have && n0 + j < 65) ? src[(int64_t)feat * 65 + n0 + j] : 0.f);
+                tmem_st16(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + n0), x);
+                if (n0 < 64) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w[n0 / 2 + j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                } else if (feat < r) {
+                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
+                        __float2bfloat16_rn(__uint_as_float(x[0]));
+                }
+            }
+            state_row_bf16(s.sbf[half], tr, w);
+        }
+        tmem_st_wait();
         warp_arrive(&B.sbf_full, true);
         bool ok = true;
         for (int c = 0; c + 1 < nchunks && ok; ++c) {   // the last chunk's state is not read again
             if (!(ok = warp_wait(&B.a_full, c & 1))) break;
             tc_fence_after();
-            for (int half = 0; half < nhalves; ++half) state_to_sbf(s.sbf, tb, half, tr);
+            for (int half = 0; half < nhalves; ++half) {
+                uint32_t a0[32], a1[32], zc;
+                tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half), a0);
+                tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 32), a1);
+                tmem_ld1(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 64), zc);
+                tmem_ld_wait();
+                uint32_t w[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    w[j] = pack_bf16x2(__uint_as_float(a0[2 * j]), __uint_as_float(a0[2 * j + 1]));
+                    w[16 + j] = pack_bf16x2(__uint_as_float(a1[2 * j]), __uint_as_float(a1[2 * j + 1]));
+                }
+                state_row_bf16(s.sbf[half], tr, w);
+                const int feat = 128 * half + tr;
+                if (feat < r)
+                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
+                        __float2bfloat16_rn(__uint_as_float(zc));
+            }
             warp_arrive(&B.sbf_full, true);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
