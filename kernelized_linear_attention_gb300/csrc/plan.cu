@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
                 const int64_t e = e0 + j * kScanThreads;
                 if (e < E) {
                     p.prefix[base + e] = acc[j];
-                    acc[j] += p.partial[base + e];
+                    acc[j] += p.partial[base + e];   // (the last unit's sum is never stored)
                 }
             }
         }

@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(NT) state_kernel(FwdParams p, int om_in_smem) 
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
+    // causal: no later segment adds the last segment of a sequence to its prefix
+    if (p.causal && u + 1 == p.seq_first[un.seq + 1]) return;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const SmemPlan sp = plan_smem(p.map, p.dk, p.dv, p.r, om_in_smem);
     float* sm = reinterpret_cast<float*>(smem_raw);

@@ -194,9 +194,10 @@ __device__ void elementwise_phi_row(const unsigned char* tile, unsigned char* ds
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float lo = bf16lo(ws[j]), hi = bf16hi(ws[j]);
-                if (map == LA_MAP_ELU1) {
-                    lo = lo > 0.f ? lo + 1.f : ex2_approx(lo * kLog2e);
-                    hi = hi > 0.f ? hi + 1.f : ex2_approx(hi * kLog2e);
+                if (map == LA_MAP_ELU1) {   // exponentials unconditional, so that the choices are selects
+                    const float el = ex2_approx(lo * kLog2e), eh = ex2_approx(hi * kLog2e);
+                    lo = lo > 0.f ? lo + 1.f : el;
+                    hi = hi > 0.f ? hi + 1.f : eh;
                 }
                 ws[j] = pack_bf16x2(lo, hi);
             }
@@ -1004,7 +1005,7 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // phi(k) nor the update's A operand passes through shared memory.
 // TMEM: S [0, 128) (64 columns per 128-feature half), two fp32 projection buffers
 // [128, 384), two bf16 phi(k)^T buffers [384, 512).
-// Roles (384 threads):
+// Roles (416 threads):
 //   warp 0 lane 0     TMA: k and v tiles of each chunk into four stages (and L2 prefetch)
 //   warp 1            projection MMAs (one elected lane; warp 1 owns the TMEM
 //                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the PE
@@ -1012,12 +1013,13 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 //   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T.
 //                     The two issuers touch disjoint tensor memory and never wait
 //                     on each other
-//   warp 3 (NE)       the exponent offset of every token of a stage (FAVOR+), into
-//                     the bias operand of the projection
+//   warps 3, 12 (NE)  the exponent offset of every token of a stage (FAVOR+), into
+//                     the bias operand of the projection (64 tokens each, on two
+//                     different SM sub-partitions)
 //   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
 //                     every half (lane = feature)
 // The state accumulates in TMEM and registers over the unit and is written once.
-constexpr int kStateThreads = 384;
+constexpr int kStateThreads = 416;
 constexpr int kPrefetchAhead = 4;  // chunks of k and v requested into L2 ahead of the loads
 constexpr uint32_t kColSS = 0;     // S, 64 columns per half
 constexpr uint32_t kColPS = 128;   // two 128-column fp32 projection buffers
@@ -1025,10 +1027,14 @@ constexpr uint32_t kColAS = 384;   // two 64-column bf16 phi(k)^T buffers
 
 // phi of one element for the element-wise maps.
 __device__ __forceinline__ float phi_elementwise(float x, int map) {
-    if (map == LA_MAP_ELU1) return x > 0.f ? x + 1.f : ex2_approx(x * kLog2e);
+    const float e = ex2_approx(x * kLog2e);   // unconditional, so that the choice is a select
+    if (map == LA_MAP_ELU1) return x > 0.f ? x + 1.f : e;
     return x;
 }
 
+// kFavor: FAVOR+ (projection by Omega' hi + lo and the offset step), else an
+// element-wise map of k (identity projection); one instantiation per kind.
+template <bool kFavor>
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const TcParams tp) {
@@ -1036,11 +1042,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int u = blockIdx.x, head = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
+    // causal: no later segment adds the last segment of a sequence to its prefix
+    if (p.causal && u + 1 == p.seq_first[un.seq + 1]) return;
     StateSmem& s = smem_ref<StateSmem>();
     StateBars& B = s.b;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
-    const bool favor = p.map == LA_MAP_FAVOR;
+    constexpr bool favor = kFavor;
     const int nhalves = (r + 127) / 128;
     const int nchunks = (un.end - un.start + kC - 1) / kC;
 
@@ -1049,10 +1057,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         prefetch_tensormap(&map_v);
         for (int i = 0; i < kStateStages; ++i) {
             mbar_init(&B.k_full[i], 1);
-            mbar_init(&B.k_empty[i], favor ? 2 : 8);   // projection commit + NE (FAVOR+) or the PE warps
+            mbar_init(&B.k_empty[i], 3);   // projection commit + 2 NE warps
             mbar_init(&B.v_full[i], 1);
             mbar_init(&B.v_empty[i], 1);
-            mbar_init(&B.cx_full[i], 1);
+            mbar_init(&B.cx_full[i], 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
@@ -1074,6 +1082,17 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             const int row = r + (i >> 3), c = i & 7;
             *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(s.omg_lo + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    } else {
+        // element-wise maps (r = d = 64): the "projection" is the identity, so that
+        // k^T reaches tensor memory by the same exact MMA (rows 64..127 zero)
+        for (int i = t; i < 128 * 8; i += kStateThreads) {
+            const int row = i >> 3, c = i & 7;
+            const bool one = row < r && (row >> 3) == c;
+            const uint32_t w = one ? (0x3F80u << (16 * (row & 1))) : 0u;
+            const int e = (row & 7) >> 1;   // 32-bit word of the chunk holding column row
+            *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) =
+                make_uint4(e == 0 ? w : 0u, e == 1 ? w : 0u, e == 2 ? w : 0u, e == 3 ? w : 0u);
         }
     }
     for (int i = t; i < kC * 8; i += kStateThreads) {   // bias columns start at zero; ones at 16 i, 16 i + 1
@@ -1122,7 +1141,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const uint64_t d_ones = sdesc_sw128(smem_u32(s.ones), 16, 1024);
         const uint32_t id_proj = idesc_bf16(128, kC, false, false);   // M = features, N = tokens
         bool ok = true;
-        for (int c = 0; favor && c < nchunks && ok; ++c) {
+        for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
             if (!(ok = warp_wait(&B.cx_full[st], (c / kStateStages) & 1))) break;   // tile and offsets staged
             const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk[st]), 16, 1024);
@@ -1136,10 +1155,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss_w(d, sdesc_add(d_omg_hi, fo + 32 * k), sdesc_add(d_tk, 32 * k), id_proj, k > 0);
+                if (favor) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_ss_w(d, sdesc_add(d_omg_lo, fo + 32 * k), sdesc_add(d_tk, 32 * k), id_proj, 1u);
-                mma_ss_w(d, sdesc_add(d_ones, 32 * st), sdesc_add(d_bias, 32 * st), id_proj, 1u);
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss_w(d, sdesc_add(d_omg_lo, fo + 32 * k), sdesc_add(d_tk, 32 * k), id_proj, 1u);
+                    mma_ss_w(d, sdesc_add(d_ones, 32 * st), sdesc_add(d_bias, 32 * st), id_proj, 1u);
+                }
                 mma_commit_w(&B.p_full[b]);
             }
             if (ok) mma_commit_w(&B.k_empty[st]);
@@ -1167,7 +1188,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             if (ok) mma_commit_w(&B.v_empty[st]);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ PE: phi(k)^T
         const int wg = (warp - 4) >> 2;           // tokens 64 wg .. 64 wg + 63
         const int wl = (warp & 3) * 32;           // TMEM lane base: features wl .. wl + 31 of a half
@@ -1176,21 +1197,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
             const int nvalid = min(kC, un.end - (un.start + c * kC));
-            if (!favor && !(ok = warp_wait(&B.k_full[st], (c / kStateStages) & 1))) break;
             for (int h = 0; h < nhalves && ok; ++h) {
                 const int j = c * nhalves + h, b = j & 1;
                 const bool live = 128 * h + f < r;
                 uint32_t w[32];
+                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
+                tc_fence_after();
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg), v0);
+                tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg + 32), v1);
+                tmem_ld_wait();
+                warp_arrive(&B.p_empty[b], false);
+                // the update that read this phi buffer last must be done
+                if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
                 if (favor) {
-                    if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
-                    tc_fence_after();
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg), v0);
-                    tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg + 32), v1);
-                    tmem_ld_wait();
-                    warp_arrive(&B.p_empty[b], false);
-                    // the update that read this phi buffer last must be done
-                    if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         w[e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * e])),
@@ -1200,18 +1220,19 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                         w[16 + e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * e])),
                                                        ex2_approx(__uint_as_float(v1[2 * e + 1]))) : 0u;
                 } else {
-                    if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
+                    // k^T element-wise; tokens past the unit's end give phi = 0
+                    const int tbase = 64 * wg;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int t0 = 64 * wg + 2 * e;
-                        float x0 = 0.f, x1 = 0.f;
-                        if (live && t0 < nvalid)
-                            x0 = phi_elementwise(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                                                     s.tk[st] + sw128_off(t0, f))), p.map);
-                        if (live && t0 + 1 < nvalid)
-                            x1 = phi_elementwise(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                                                     s.tk[st] + sw128_off(t0 + 1, f))), p.map);
-                        w[e] = pack_bf16x2(x0, x1);
+                    for (int e = 0; e < 16; ++e) {
+                        const float x0 = tbase + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v0[2 * e]), p.map) : 0.f;
+                        const float x1 = tbase + 2 * e + 1 < nvalid ? phi_elementwise(__uint_as_float(v0[2 * e + 1]), p.map) : 0.f;
+                        w[e] = live ? pack_bf16x2(x0, x1) : 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float x0 = tbase + 32 + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v1[2 * e]), p.map) : 0.f;
+                        const float x1 = tbase + 33 + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v1[2 * e + 1]), p.map) : 0.f;
+                        w[16 + e] = live ? pack_bf16x2(x0, x1) : 0u;
                     }
                 }
                 tmem_st32(tmem_addr(tb, wl, kColAS + 64 * b + 32 * wg), w);
@@ -1223,23 +1244,23 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 tmem_st_wait();
                 warp_arrive(&B.a_full[b], false);
             }
-            if (ok && !favor) warp_arrive(&B.k_empty[st], false);   // done with the tile
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
         if (wg == 1) {
             s.zsum[f] = z0;
             s.zsum[128 + f] = z1;
         }
-    } else if (favor) {
-        // ------------------------------------------------------------ NE: exponent offsets (warp 3)
+    } else {
+        // ------------------------------------------------------------ NE: exponent offsets (warps 3, 12)
+        const int tok0 = warp == 3 ? 0 : 64;      // this warp's 64 tokens
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
             const int nvalid = min(kC, un.end - (un.start + c * kC));
             if (!(ok = warp_wait(&B.k_full[st], (c / kStateStages) & 1))) break;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int tok = lane + 32 * x;
+            for (int x = 0; x < 2 && favor; ++x) {
+                const int tok = tok0 + lane + 32 * x;
                 // -offset as bf16 hi + lo into the stage's bias columns; past the unit's
                 // end a large negative exponent makes phi = 0
                 const float o = tok < nvalid ? -(row_sq_norm(s.tk[st], tok) * (0.5f * kLog2e) + 0.5f * __log2f((float)r))
@@ -1376,9 +1397,11 @@ cudaError_t tc_state(const FwdParams& p, cudaStream_t s) {
     CUtensorMap mk, mv;
     if (!make_row_map(&mk, p.k, p.T, p.H) || !make_row_map(&mv, p.v, p.T, p.H)) return cudaErrorInvalidValue;
     const size_t bytes = smem_bytes<StateSmem>();
-    cudaError_t e = set_smem(tc_state_kernel, bytes);
+    const bool favor = p.map == LA_MAP_FAVOR;
+    cudaError_t e = favor ? set_smem(tc_state_kernel<true>, bytes) : set_smem(tc_state_kernel<false>, bytes);
     if (e != cudaSuccess) return e;
-    tc_state_kernel<<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    if (favor) tc_state_kernel<true><<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    else tc_state_kernel<false><<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
     return cudaGetLastError();
 }
 
