@@ -535,6 +535,8 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, bool smem_written) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// kFavor: FAVOR+ projections, else element-wise maps of q and k; one instantiation per kind.
+template <bool kFavor>
 __global__ void __launch_bounds__(kCausalThreads, 1)
 tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, const TcParams tp) {
@@ -546,7 +548,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     CausalBars& B = s.b;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
-    const bool favor = p.map == LA_MAP_FAVOR;
+    constexpr bool favor = kFavor;
     const int nq = r / 64;                        // feature quarters (1, 2 or 4)
     const int nhalves = (r + 127) / 128;
     const int nchunks = (un.end - un.start + kC - 1) / kC;
@@ -1415,8 +1417,13 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
         CUtensorMap mk, mv;
         if (!make_row_map(&mk, p.k, p.T, p.H) || !make_row_map(&mv, p.v, p.T, p.H)) return cudaErrorInvalidValue;
         const size_t bytes = smem_bytes<CausalSmem>();
-        if ((e = set_smem(tc_causal_out_kernel, bytes)) != cudaSuccess) return e;
-        tc_causal_out_kernel<<<grid, kCausalThreads, bytes, s>>>(mq, mk, mv, tp);
+        if (p.map == LA_MAP_FAVOR) {
+            if ((e = set_smem(tc_causal_out_kernel<true>, bytes)) != cudaSuccess) return e;
+            tc_causal_out_kernel<true><<<grid, kCausalThreads, bytes, s>>>(mq, mk, mv, tp);
+        } else {
+            if ((e = set_smem(tc_causal_out_kernel<false>, bytes)) != cudaSuccess) return e;
+            tc_causal_out_kernel<false><<<grid, kCausalThreads, bytes, s>>>(mq, mk, mv, tp);
+        }
     } else {
         const size_t bytes = smem_bytes<BidirSmem>();
         if ((e = set_smem(tc_bidir_out_kernel, bytes)) != cudaSuccess) return e;
