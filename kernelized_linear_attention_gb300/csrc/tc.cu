@@ -67,15 +67,27 @@ struct Bars {
     int pad;
 };
 
-// Bidirectional output kernel: 192 KB.
+// Bidirectional output kernel: 208 KB.
+struct BidirBars {
+    uint64_t q_full[2], q_empty[2];   // TMA -> NE, projection issuer;  (projection commit + 2 NE) -> TMA
+    uint64_t cx_full[2];              // NE (2 warps) -> projection issuer: offsets of the stage's queries staged
+    uint64_t p_full[2], p_empty[2];   // projection commit -> PE: exponent of a feature half;  PE (8 warps) -> issuer
+    uint64_t a_full[2], a_empty[2];   // PE (8 warps) -> readout issuer: phi(q) bf16 in TMEM;  readout commit -> PE
+    uint64_t o_full, o_empty;         // readout commit -> OE: numerator/denominator;  OE (4 warps) -> readout issuer
+    uint64_t drain[2];
+    uint32_t tmem_base;
+    int pad;
+};
+
 struct __align__(1024) BidirSmem {
     unsigned char omg_hi[kOmgBytes];
     unsigned char omg_lo[kOmgBytes];
-    Tile tq;
-    Tile phq[2];                      // Phi_Q of one 128-feature half
+    Tile tq[2];                       // two stages
+    Tile bias;                        // K-major [query][64]: columns 16 st, 16 st + 1 = -offset (hi, lo)
+    Tile ones;                        // K-major [feature][64]: columns 16 i, 16 i + 1 = 1
     unsigned char shi[4][kSbfBlock];  // whole-sequence [S|z]^T, bf16 high part
     unsigned char slo[4][kSbfBlock];  // and the bf16 rounding remainder
-    Bars b;
+    BidirBars b;
 };
 
 // Segment-state kernel: 226 KB.
@@ -912,87 +924,258 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
+constexpr int kPrefetchAhead = 4;  // chunks of the streamed tiles requested into L2 ahead of the loads
+
+// phi of one element for the element-wise maps.
+__device__ __forceinline__ float phi_elementwise(float x, int map) {
+    const float e = ex2_approx(x * kLog2e);   // unconditional, so that the choice is a select
+    if (map == LA_MAP_ELU1) return x > 0.f ? x + 1.f : e;
+    return x;
+}
+
 // ---------------------------------------------------------------------------
-// Bidirectional output kernel: out = Phi_Q [S|z] / ..., [S|z] the whole-sequence state
+// Bidirectional output kernel (warp-specialised): out = phi(q)^T [S|z] / max(phi(q)^T z, eps)
+// with [S|z] the whole-sequence state (bf16 hi + lo in shared memory)
 // ---------------------------------------------------------------------------
-// Jobs are the projections of q for each quarter of the features, into two
-// alternating TMEM buffers; each quarter's readout uses the state's hi and lo parts.
-__global__ void __launch_bounds__(kThreads, 1)
+// TMEM: two fp32 projection buffers [0, 256) (one 128-feature half each), two bf16
+// phi(q) buffers [256, 384), O = numerator | denominator [384, 464).
+// Roles (544 threads):
+//   warp 0 lane 0      TMA: the q tile of each chunk into two stages (and L2 prefetch)
+//   warp 1             projection MMAs (elected lane; warp 1 owns the TMEM allocation):
+//                      Q Omega'^T (hi, lo) plus one K step adding each query's
+//                      exponent offset (FAVOR+), or Q itself (identity, element-wise maps)
+//   warp 2             readout MMAs: O (+)= phi(q) [S|z]_hi + phi(q) [S|z]_lo, A from TMEM
+//   warps 3, 12 (NE)   per-query exponent offsets into the bias operand (FAVOR+)
+//   warps 4..11 (PE)   phi(q) of each half: warpgroup w converts features 64w.. (lane = query)
+//   warps 13..16 (OE)  out rows = O[0..63] / max(O[64], eps), after releasing O
+constexpr int kBidirThreads = 544;
+constexpr uint32_t kColBP = 0, kColBA = 256, kColBO = 384;
+
+template <bool kFavor>
+__global__ void __launch_bounds__(kBidirThreads, 1)
 tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp) {
     const FwdParams& p = tp.p;
     const int u = blockIdx.x, head = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
     BidirSmem& s = smem_ref<BidirSmem>();
-    const int t = threadIdx.x;
+    BidirBars& B = s.b;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int r = p.r;
-    const bool favor = p.map == LA_MAP_FAVOR;
-    const int nq = r / 64;
+    constexpr bool favor = kFavor;
     const int nhalves = (r + 127) / 128;
+    const int nchunks = (un.end - un.start + kC - 1) / kC;
 
-    if (t == 0) prefetch_tensormap(&map_q);
-    setup_bars(s.b);
-    if (favor) stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+    if (t == 0) {
+        prefetch_tensormap(&map_q);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B.q_full[i], 1);
+            mbar_init(&B.q_empty[i], 3);
+            mbar_init(&B.cx_full[i], 2);
+            mbar_init(&B.p_full[i], 1);
+            mbar_init(&B.p_empty[i], 8);
+            mbar_init(&B.a_full[i], 8);
+            mbar_init(&B.a_empty[i], 1);
+            mbar_init(&B.drain[i], 1);
+        }
+        mbar_init(&B.o_full, 1);
+        mbar_init(&B.o_empty, 4);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&B.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (favor) {
+        stage_omega(s.omg_hi, s.omg_lo, p.omega, r);
+        for (int i = t; i < (128 - r) * 8 && r < 128; i += kBidirThreads) {   // features r..127: zero
+            const int row = r + (i >> 3), c = i & 7;
+            *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(s.omg_lo + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    } else {
+        // element-wise maps (r = d = 64): the projection is the identity, so that q
+        // reaches tensor memory by the same exact MMA (features 64..127 zero)
+        for (int i = t; i < 128 * 8; i += kBidirThreads) {
+            const int row = i >> 3, c = i & 7;
+            const bool one = row < r && (row >> 3) == c;
+            const uint32_t w = one ? (0x3F80u << (16 * (row & 1))) : 0u;
+            const int e = (row & 7) >> 1;
+            *reinterpret_cast<uint4*>(s.omg_hi + sw128_chunk(row, c)) =
+                make_uint4(e == 0 ? w : 0u, e == 1 ? w : 0u, e == 2 ? w : 0u, e == 3 ? w : 0u);
+        }
+    }
+    for (int i = t; i < kC * 8; i += kBidirThreads) {   // bias columns start at zero; ones at 16 i, 16 i + 1
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(s.bias + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) =
+            make_uint4((c & 1) == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
+    }
+    if (t < 128)   // the whole-sequence state as bf16 hi + lo readout blocks
+        load_state(s.shi, s.slo, 0u, false, p.prefix + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves,
+                   false, t);
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tb = s.b.tmem_base;
-    load_state(s.shi, s.slo, tb, false, p.prefix + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves, false);
-    handoff_to_mma();
-    if (t == 0) {
-        mbar_arrive_expect_tx(&s.b.load, kTile);
-        tma_load_3d(s.tq, &map_q, 0, head, un.start, &s.b.load);
-    }
-    const uint32_t id_read = idesc_bf16(128, kNX, false, false);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    auto issue_job = [&](int q) {   // thread 0 only
-        mma_projection(tb + kColP + 64 * (q & 1), s.tq, s.omg_hi, s.omg_lo, 64 * q, 64);
-        mma_commit(&s.b.proj[q & 1]);
-    };
-    Phase lp, pp0, pp1;
-    Commits cm;
-    bool ok = true;
-    for (int t0 = un.start; t0 < un.end && ok; t0 += kC) {
-        const bool valid = t < min(kC, un.end - t0);
-        if (!(ok = lp.wait(&s.b.load))) break;
-        const float cq = favor ? favor_offset(s.tq, t, r) : 0.f;
-        const uint32_t base = cm.issued;
-        if (favor && t == 0) {
-            issue_job(0);
-            if (nq > 1) issue_job(1);
+    const uint32_t tb = B.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1, t0 = un.start + c * kC;
+                for (int a = (c == 0 ? 0 : kPrefetchAhead); a <= kPrefetchAhead; ++a)
+                    if (c + a < nchunks) tma_prefetch_3d(&map_q, 0, head, t0 + a * kC);
+                if (c >= 2 && !mbar_wait(&B.q_empty[st], ((c >> 1) - 1) & 1)) {
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&B.q_full[st], kTile);
+                tma_load_3d(s.tq[st], &map_q, 0, head, t0, &B.q_full[st]);
+            }
         }
-        for (int q = 0; q < nq; ++q) {
-            const int b = q & 1;
-            if (favor) {
-                if (!(ok = (b ? pp1 : pp0).wait(&s.b.proj[b]))) break;
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ projection MMAs (elected lane issues)
+        const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
+        const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
+        const uint64_t d_bias = sdesc_sw128(smem_u32(s.bias), 16, 1024);
+        const uint64_t d_ones = sdesc_sw128(smem_u32(s.ones), 16, 1024);
+        const uint32_t id_proj = idesc_bf16(128, min(r, 128), false, false);   // M = queries, N = features
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            if (!(ok = warp_wait(&B.cx_full[st], (c >> 1) & 1))) break;   // tile and offsets staged
+            const uint64_t d_tq = sdesc_sw128(smem_u32(s.tq[st]), 16, 1024);
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int j = c * nhalves + h, b = j & 1;
+                if (j >= 2 && !(ok = warp_wait(&B.p_empty[b], ((j >> 1) - 1) & 1))) break;
                 tc_fence_after();
+                const uint32_t d = tb + kColBP + 128 * b, fo = 16384u * h;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(d, sdesc_add(d_tq, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+                if (favor) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss_w(d, sdesc_add(d_tq, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+                    mma_ss_w(d, sdesc_add(d_bias, 32 * st), sdesc_add(d_ones, 32 * st), id_proj, 1u);
+                }
+                mma_commit_w(&B.p_full[b]);
             }
-            if (q > 0 && !(ok = cm.wait_for(&s.b.mma, base + q))) break;   // readout q-1 done
-            if (favor) projection_epilogue(tb, kColP + 64 * b, 64, cq, valid, s.phq[b]);
-            else elementwise_phi_row(s.tq, s.phq[b], t, valid, p.map);
-            handoff_to_mma();
-            if (t == 0) {
-                if (favor && q + 2 < nq) issue_job(q + 2);
-                mma_kk(tb + kColO, s.phq[b], 0, s.shi[q], 0, 4, id_read, q > 0);
-                mma_kk(tb + kColO, s.phq[b], 0, s.slo[q], 0, 4, id_read, true);
-                mma_commit(&s.b.mma);
+            if (ok) mma_commit_w(&B.q_empty[st]);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ readout MMAs (elected lane issues)
+        const uint32_t id_read = idesc_bf16(128, kNX, false, false);   // A from TMEM, B K-major
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int j = c * nhalves + h, b = j & 1;
+                if (!(ok = warp_wait(&B.a_full[b], (j >> 1) & 1))) break;
+                if (h == 0 && c > 0 && !(ok = warp_wait(&B.o_empty, (c - 1) & 1))) break;   // O read out
+                tc_fence_after();
+                const uint32_t a0 = tb + kColBA + 64 * b;
+                const int nk = min(r - 128 * h, 128) / 16;
+                for (int k = 0; k < nk; ++k) {
+                    const int blk = 2 * h + (k >> 2);
+                    mma_ts_w(tb + kColBO, a0 + 8 * k, sdesc_sw128(smem_u32(s.shi[blk]) + 32u * (k & 3), 16, 1024),
+                             id_read, (h > 0 || k > 0) ? 1u : 0u);
+                    mma_ts_w(tb + kColBO, a0 + 8 * k, sdesc_sw128(smem_u32(s.slo[blk]) + 32u * (k & 3), 16, 1024),
+                             id_read, 1u);
+                }
+                mma_commit_w(&B.a_empty[b]);
             }
-            ++cm.issued;
+            if (ok) mma_commit_w(&B.o_full);
         }
-        if (!ok) break;
-        if (!(ok = cm.wait_for(&s.b.mma, base + nq))) break;
-        tc_fence_after();
-        if (t == 0 && t0 + kC < un.end) {
-            mbar_arrive_expect_tx(&s.b.load, kTile);
-            tma_load_3d(s.tq, &map_q, 0, head, t0 + kC, &s.b.load);
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ PE: phi(q)
+        const int wg = (warp - 4) >> 2;           // features 64 wg .. of every half
+        const int wl = (warp & 3) * 32;           // TMEM lane base: queries wl ..
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int j = c * nhalves + h, b = j & 1;
+                const bool live = 128 * h + 64 * wg < r;   // these 64 features exist
+                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
+                tc_fence_after();
+                uint32_t v0[32], v1[32], w[32];
+                tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg), v0);
+                tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg + 32), v1);
+                tmem_ld_wait();
+                warp_arrive(&B.p_empty[b], false);
+                // the readout that read this phi buffer last must be done
+                if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float a0 = __uint_as_float(v0[2 * e]), a1 = __uint_as_float(v0[2 * e + 1]);
+                    w[e] = live ? (favor ? pack_bf16x2(ex2_approx(a0), ex2_approx(a1))
+                                         : pack_bf16x2(phi_elementwise(a0, p.map), phi_elementwise(a1, p.map)))
+                                : 0u;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float a0 = __uint_as_float(v1[2 * e]), a1 = __uint_as_float(v1[2 * e + 1]);
+                    w[16 + e] = live ? (favor ? pack_bf16x2(ex2_approx(a0), ex2_approx(a1))
+                                              : pack_bf16x2(phi_elementwise(a0, p.map), phi_elementwise(a1, p.map)))
+                                     : 0u;
+                }
+                tmem_st32(tmem_addr(tb, wl, kColBA + 64 * b + 32 * wg), w);
+                tmem_st_wait();
+                warp_arrive(&B.a_full[b], false);
+            }
         }
-        store_output(tb, p.eps, valid, out + ((int64_t)(t0 + t) * p.H + head) * 64);
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else if (warp == 3 || warp == 12) {
+        // ------------------------------------------------------------ NE: exponent offsets (warps 3, 12)
+        const int tok0 = warp == 3 ? 0 : 64;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            if (!(ok = warp_wait(&B.q_full[st], (c >> 1) & 1))) break;
+#pragma unroll
+            for (int x = 0; x < 2 && favor; ++x) {
+                const int tok = tok0 + lane + 32 * x;
+                const float o = -(row_sq_norm(s.tq[st], tok) * (0.5f * kLog2e) + 0.5f * __log2f((float)r));
+                const uint32_t hl = pack_bf16x2(o, 0.f);
+                *reinterpret_cast<uint32_t*>(s.bias + sw128_off(tok, 16 * st)) = pack_bf16x2(o, o - bf16lo(hl));
+            }
+            warp_arrive(&B.cx_full[st], true);
+            warp_arrive(&B.q_empty[st], false);   // this warp no longer reads the tile
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    } else {
+        // ------------------------------------------------------------ OE: output rows (warps 13..16)
+        const int wl = (warp & 3) * 32;
+        const int tr = wl + lane;                 // query row = TMEM lane
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int t0 = un.start + c * kC;
+            if (!(ok = warp_wait(&B.o_full, c & 1))) break;
+            tc_fence_after();
+            uint32_t o0[32], o1[32], den;
+            tmem_ld32(tmem_addr(tb, wl, kColBO), o0);
+            tmem_ld32(tmem_addr(tb, wl, kColBO + 32), o1);
+            tmem_ld1(tmem_addr(tb, wl, kColBO + 64), den);
+            tmem_ld_wait();
+            warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O
+            if (tr < min(kC, un.end - t0))
+                store_output_row(o0, o1, den, p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
-    if (!ok) drain_after_timeout(s.b, &p.hdr->error);
-    teardown(s.b);
+    // ---------------------------------------------------------------- exit
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1 || warp == 2) {   // every MMA of both issuers finished (bounded)
+        mma_commit_w(&B.drain[warp - 1]);
+        if (!warp_wait(&B.drain[warp - 1], 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    }
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1022,17 +1205,10 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 //                     every half (lane = feature)
 // The state accumulates in TMEM and registers over the unit and is written once.
 constexpr int kStateThreads = 416;
-constexpr int kPrefetchAhead = 4;  // chunks of k and v requested into L2 ahead of the loads
 constexpr uint32_t kColSS = 0;     // S, 64 columns per half
 constexpr uint32_t kColPS = 128;   // two 128-column fp32 projection buffers
 constexpr uint32_t kColAS = 384;   // two 64-column bf16 phi(k)^T buffers
 
-// phi of one element for the element-wise maps.
-__device__ __forceinline__ float phi_elementwise(float x, int map) {
-    const float e = ex2_approx(x * kLog2e);   // unconditional, so that the choice is a select
-    if (map == LA_MAP_ELU1) return x > 0.f ? x + 1.f : e;
-    return x;
-}
 
 // kFavor: FAVOR+ (projection by Omega' hi + lo and the offset step), else an
 // element-wise map of k (identity projection); one instantiation per kind.
@@ -1426,8 +1602,13 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
         }
     } else {
         const size_t bytes = smem_bytes<BidirSmem>();
-        if ((e = set_smem(tc_bidir_out_kernel, bytes)) != cudaSuccess) return e;
-        tc_bidir_out_kernel<<<grid, kThreads, bytes, s>>>(mq, tp);
+        if (p.map == LA_MAP_FAVOR) {
+            if ((e = set_smem(tc_bidir_out_kernel<true>, bytes)) != cudaSuccess) return e;
+            tc_bidir_out_kernel<true><<<grid, kBidirThreads, bytes, s>>>(mq, tp);
+        } else {
+            if ((e = set_smem(tc_bidir_out_kernel<false>, bytes)) != cudaSuccess) return e;
+            tc_bidir_out_kernel<false><<<grid, kBidirThreads, bytes, s>>>(mq, tp);
+        }
     }
     return cudaGetLastError();
 }
