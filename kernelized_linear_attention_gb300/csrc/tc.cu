@@ -486,14 +486,16 @@ struct Commits {
 // ---------------------------------------------------------------------------
 // Roles (512 threads):
 //   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
-//   warp 1             MMA issue, one elected lane (warp 1 also owns the TMEM allocation)
+//   warp 1             projection MMAs, one elected lane (warp 1 also owns the TMEM
+//                      allocation); runs ahead, throttled by the two projection buffers
+//   warp 2             product MMAs (scores, readout, denominator, state update, A V)
 //   warps 4..7 (PE)    projection epilogue: phi(k), phi(q) of each quarter of the
 //                      features into shared memory (token t = TMEM lane t)
 //   warps 8..11 (OE)   masked scores as bf16 hi + lo in TMEM; the output rows
 //   warps 12..15 (SE)  the bf16 copy of the state for the next chunk's readout
-// Per chunk the MMA warp runs, for each quarter q of the features, the
-// projections of k and q (Omega hi + lo) into two TMEM buffers and, once the
-// PE has written phi, the products of that quarter:
+// Per chunk the projection warp runs, for each quarter q of the features, the
+// projections of k and q (Omega hi + lo) into two TMEM buffers; once the PE has
+// written phi, the product warp runs the products of that quarter:
 //   A (+)= Phi_Q Phi_K^T,  O (+)= Phi_Q [S|z]_bf16,  and after the last quarter
 //   of each half [S|z] += Phi_K^T [V|1];
 // then, once the OE has split A, O += tril(A) [V|1].  All hand-offs are
@@ -516,7 +518,7 @@ struct CausalBars {
     uint64_t o_full;                // MMA commit -> OE: numerator/denominator complete
     uint64_t o_empty;               // OE (4 warps) -> MMA: O read out of TMEM
     uint64_t sbf_full;              // SE (4 warps) -> MMA, PE: bf16 state and fp32 z of the previous chunks in smem
-    uint64_t drain;
+    uint64_t drain[2];              // one per MMA-issuing warp
     uint32_t tmem_base;
     int pad;
 };
@@ -586,7 +588,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         mbar_init(&B.o_full, 1);
         mbar_init(&B.o_empty, 4);
         mbar_init(&B.sbf_full, 4);
-        mbar_init(&B.drain, 1);
+        mbar_init(&B.drain[0], 1);
+        mbar_init(&B.drain[1], 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -639,109 +642,102 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         }
     }
     else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue (whole warp, elected lane issues)
-        {
-            const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
-            const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
-            const uint64_t d_tq = sdesc_sw128(smem_u32(s.tq), 16, 1024);
-            const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk), 16, 1024);
-            const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq), 16, 1024);
-            const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
-            const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), kTile, 1024);                 // MN-major
-            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv), kTile, 1024);                       // MN-major, V only
-            const uint64_t d_zrow = sdesc_sw128(smem_u32(s.zrow[0]), 16, 1024);
-            const uint32_t id_den = idesc_bf16(128, 16, false, false);
-            const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
-            const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones) - smem_u32(s.tv), 1024);
-            const uint32_t id_proj = idesc_bf16(128, 64, false, false);
-            const uint32_t id_scores = idesc_bf16(128, 128, false, false);
-            const uint32_t id_read = idesc_bf16(128, 64, false, true);
-            const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
-            const uint32_t id_av = idesc_bf16(128, 64, false, true);
-            uint32_t jobs[2] = {0u, 0u};
-            bool ok = true;
-            // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b
-            auto issue_job = [&](int b, int quarter) -> bool {
-                if (!warp_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
-                ++jobs[b];
-                tc_fence_after();
-                const uint64_t dx = b ? d_tq : d_tk;
-                const uint32_t d = tb + kColP + 64 * b, fo = 8192u * quarter;
+        // ------------------------------------------------------------ projection MMAs (elected lane issues)
+        const uint64_t d_omg_hi = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
+        const uint64_t d_omg_lo = sdesc_sw128(smem_u32(s.omg_lo), 16, 1024);
+        const uint64_t d_tq = sdesc_sw128(smem_u32(s.tq), 16, 1024);
+        const uint64_t d_tk = sdesc_sw128(smem_u32(s.tk), 16, 1024);
+        const uint32_t id_proj = idesc_bf16(128, 64, false, false);
+        uint32_t jobs[2] = {0u, 0u};
+        bool ok = true;
+        // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b;
+        // runs ahead of the products, throttled by the epilogue draining each buffer
+        auto issue_job = [&](int b, int quarter) -> bool {
+            if (!warp_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
+            ++jobs[b];
+            tc_fence_after();
+            const uint64_t dx = b ? d_tq : d_tk;
+            const uint32_t d = tb + kColP + 64 * b, fo = 8192u * quarter;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+            for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
-                mma_commit_w(&B.p_full[b]);
-                return true;
-            };
-            bool started = false;   // first projection jobs of chunk c already issued
-            for (int c = 0; c < nchunks && ok; ++c) {
-                if (!started) {
-                    if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
-                    if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
-                }
-                started = false;
-                bool v_ready = false;
-                for (int q = 0; q < nq; ++q) {
-                    if (favor && q + 1 < nq) {
-                        if (!(ok = issue_job(0, q + 1) && issue_job(1, q + 1))) break;
-                    }
-                    if (q == nq - 1) mma_commit_w(&B.qk_empty);   // every projection of this chunk issued
-                    const int g = c * nq + q;
-                    if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1) && warp_wait(&B.phiq_full, g & 1))) break;
-                    if (q == 0) {   // O and the scores of chunk c-1 read out; bf16 state of chunks < c ready
-                        if (!(ok = (c == 0 || warp_wait(&B.o_empty, (c - 1) & 1)) && warp_wait(&B.sbf_full, c & 1))) break;
-                        tc_fence_after();
-                    }
-                    const bool update_now = (q & 1) || q == nq - 1;
-                    if (update_now && !v_ready) {
-                        if (!(ok = warp_wait(&B.v_full, c & 1))) break;
-                        v_ready = true;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss_w(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
-                               (q > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
-                               (q > 0 || k > 0) ? 1u : 0u);
-                    // denominator term phi(q) . z into column 64 of O (z as the only
-                    // non-zero row of a 16-row operand)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
-                               (q > 0 || k > 0) ? 1u : 0u);
-                    mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
-                    if (update_now) {
-#pragma unroll
-                        for (int k = 0; k < kC / 16; ++k)
-                            mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
-                    }
-                    mma_commit_w(&B.cons[g & 1]);
-                }
-                if (!ok) break;
-                mma_commit_w(&B.a_full);
-                // overlap: if the next chunk's q and k have landed, start its projections
-                // now, while the output warps split this chunk's scores
-                if (c + 1 < nchunks && __any_sync(0xffffffffu, mbar_test_wait(&B.qk_full, (c + 1) & 1))) {
-                    if (favor && !(ok = issue_job(0, 0) && issue_job(1, 0))) break;
-                    started = true;
-                }
-                if (!(ok = warp_wait(&B.ahl_full, c & 1))) break;
-                tc_fence_after();
-                // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
-#pragma unroll
-                for (int k = 0; k < kC / 16; ++k)
-                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
-#pragma unroll
-                for (int k = 0; k < kC / 16; ++k)
-                    mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
-                mma_commit_w(&B.o_full);
-                mma_commit_w(&B.v_empty);
-            }
-            if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+            for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+            mma_commit_w(&B.p_full[b]);
+            return true;
+        };
+        for (int c = 0; c < nchunks && ok; ++c) {
+            if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
+            for (int q = 0; favor && q < nq && ok; ++q) ok = issue_job(0, q) && issue_job(1, q);
+            if (ok) mma_commit_w(&B.qk_empty);   // every projection of this chunk issued
         }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    }
+    else if (warp == 2) {
+        // ------------------------------------------------------------ product MMAs (elected lane issues)
+        const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq), 16, 1024);
+        const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
+        const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), kTile, 1024);                 // MN-major
+        const uint64_t d_v = sdesc_sw128(smem_u32(s.tv), kTile, 1024);                       // MN-major, V only
+        const uint64_t d_zrow = sdesc_sw128(smem_u32(s.zrow[0]), 16, 1024);
+        const uint32_t id_den = idesc_bf16(128, 16, false, false);
+        const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
+        const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones) - smem_u32(s.tv), 1024);
+        const uint32_t id_scores = idesc_bf16(128, 128, false, false);
+        const uint32_t id_read = idesc_bf16(128, 64, false, true);
+        const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
+        const uint32_t id_av = idesc_bf16(128, 64, false, true);
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            bool v_ready = false;
+            for (int q = 0; q < nq; ++q) {
+                const int g = c * nq + q;
+                if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1) && warp_wait(&B.phiq_full, g & 1))) break;
+                if (q == 0) {   // O and the scores of chunk c-1 read out; bf16 state of chunks < c ready
+                    if (!(ok = (c == 0 || warp_wait(&B.o_empty, (c - 1) & 1)) && warp_wait(&B.sbf_full, c & 1))) break;
+                }
+                tc_fence_after();
+                const bool update_now = (q & 1) || q == nq - 1;
+                if (update_now && !v_ready) {
+                    if (!(ok = warp_wait(&B.v_full, c & 1))) break;
+                    v_ready = true;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
+                             (q > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
+                             (q > 0 || k > 0) ? 1u : 0u);
+                // denominator term phi(q) . z into column 64 of O (z as the only
+                // non-zero row of a 16-row operand)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
+                             (q > 0 || k > 0) ? 1u : 0u);
+                mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
+                if (update_now) {
+#pragma unroll
+                    for (int k = 0; k < kC / 16; ++k)
+                        mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
+                }
+                mma_commit_w(&B.cons[g & 1]);
+            }
+            if (!ok) break;
+            mma_commit_w(&B.a_full);
+            if (!(ok = warp_wait(&B.ahl_full, c & 1))) break;
+            tc_fence_after();
+            // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)
+                mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)
+                mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
+            mma_commit_w(&B.o_full);
+            mma_commit_w(&B.v_empty);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ PE: phi(k), phi(q)
@@ -916,9 +912,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     // ---------------------------------------------------------------- exit
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {   // all MMAs of this CTA finished before TMEM is freed (bounded)
-        mma_commit_w(&B.drain);
-        if (!warp_wait(&B.drain, 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    if (warp == 1 || warp == 2) {   // all MMAs of this CTA finished before TMEM is freed (bounded)
+        mma_commit_w(&B.drain[warp - 1]);
+        if (!warp_wait(&B.drain[warp - 1], 0) && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     __syncthreads();
     if (warp == 1) tmem_dealloc(tb, kTmemCols);
