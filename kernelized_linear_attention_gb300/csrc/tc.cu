@@ -511,7 +511,7 @@ struct CausalBars {
     uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
     uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
     uint64_t phiq_full;             // PE (4 warps) -> MMA: phi(q) in smem
-    uint64_t cons[2];               // MMA commit -> PE: products of global quarter g done (g & 1)
+    uint64_t upd_done;              // MMA commit -> PE: a state update has read phi(k) of its half
     uint64_t phq_free;              // MMA commit -> PE: scores and readout of quarter g done
     uint64_t a_full;                // MMA commit -> SE, OE: scores, readout, state update of the chunk done
     uint64_t ahl_full;              // OE (4 warps) -> MMA: masked scores hi/lo in TMEM
@@ -579,10 +579,10 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(&B.p_full[i], 1);
             mbar_init(&B.p_empty[i], 4);
             mbar_init(&B.phik_full[i], 4);
-            mbar_init(&B.cons[i], 1);
         }
         mbar_init(&B.phiq_full, 4);
         mbar_init(&B.phq_free, 1);
+        mbar_init(&B.upd_done, 1);
         mbar_init(&B.a_full, 1);
         mbar_init(&B.ahl_full, 4);
         mbar_init(&B.o_full, 1);
@@ -691,16 +691,21 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             bool v_ready = false;
             for (int q = 0; q < nq; ++q) {
                 const int g = c * nq + q;
-                if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1) && warp_wait(&B.phiq_full, g & 1))) break;
-                if (q == 0) {   // O and the scores of chunk c-1 read out; bf16 state of chunks < c ready
+                if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1))) break;
+                if (q == 0) {   // O and the scores of chunk c-1 read out; the state of chunks < c copied
                     if (!(ok = (c == 0 || warp_wait(&B.o_empty, (c - 1) & 1)) && warp_wait(&B.sbf_full, c & 1))) break;
                 }
                 tc_fence_after();
-                const bool update_now = (q & 1) || q == nq - 1;
-                if (update_now && !v_ready) {
-                    if (!(ok = warp_wait(&B.v_full, c & 1))) break;
+                if ((q & 1) || q == nq - 1) {   // phi(k) of the half complete: update now, ahead of the scores
+                    if (!v_ready && !(ok = warp_wait(&B.v_full, c & 1))) break;
                     v_ready = true;
+#pragma unroll
+                    for (int k = 0; k < kC / 16; ++k)
+                        mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
+                    mma_commit_w(&B.upd_done);
                 }
+                if (!(ok = warp_wait(&B.phiq_full, g & 1))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss_w(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
@@ -716,12 +721,6 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
                              (q > 0 || k > 0) ? 1u : 0u);
                 mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
-                if (update_now) {
-#pragma unroll
-                    for (int k = 0; k < kC / 16; ++k)
-                        mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
-                }
-                mma_commit_w(&B.cons[g & 1]);
             }
             if (!ok) break;
             mma_commit_w(&B.a_full);
@@ -767,10 +766,17 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         tmem_ld_wait();
                         warp_arrive(&B.p_empty[kind], false);
                     }
-                    // the products that read the destination buffer last must be done
-                    const int gw = (kind == 0 && (q & 1)) ? g - 2 : g - 1;
-                    if (gw >= 0 && !(ok = kind == 0 ? warp_wait(&B.cons[gw & 1], (gw >> 1) & 1)
-                                                    : warp_wait(&B.phq_free, gw & 1))) break;
+                    // the MMAs that read the destination buffer last must be done: for phi(q) the
+                    // products of the previous quarter; for phi(k) the update of the half of the
+                    // previous quarter using this buffer (its scores finished before the phi(q)
+                    // wait of the quarter in between)
+                    if (kind == 1) {
+                        if (g >= 1 && !(ok = warp_wait(&B.phq_free, (g - 1) & 1))) break;
+                    } else {
+                        const int gw = g - (nq >= 2 ? 2 : 1);
+                        const int uw = (gw / nq) * nhalves + ((gw % nq) >> 1);   // that update's index
+                        if (gw >= 0 && !(ok = warp_wait(&B.upd_done, uw & 1))) break;
+                    }
                     unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq;
                     if (favor) {
                         // rows past the unit's end: 2^(p - inf) = 0
