@@ -489,10 +489,12 @@ struct Commits {
 //   warp 1             projection MMAs, one elected lane (warp 1 also owns the TMEM
 //                      allocation); runs ahead, throttled by the two projection buffers
 //   warp 2             product MMAs (scores, readout, denominator, state update, A V)
-//   warps 4..7 (PE)    projection epilogue: phi(k), phi(q) of each quarter of the
-//                      features into shared memory (token t = TMEM lane t)
-//   warps 8..11 (OE)   masked scores as bf16 hi + lo in TMEM; the output rows
-//   warps 12..15 (SE)  the bf16 copy of the state for the next chunk's readout
+//   warps 4..11 (PE)   projection epilogue in two warpgroups, each converting 32 of
+//                      the 64 columns of every job: phi(k), phi(q) of each quarter
+//                      of the features into shared memory (token t = TMEM lane t)
+//   warps 12..15 (TE)  chunk tail: masked scores as bf16 hi + lo in TMEM, then (while
+//                      A V runs) the bf16 copy of the state for the next chunk's
+//                      readout, then the output rows
 // Per chunk the projection warp runs, for each quarter q of the features, the
 // projections of k and q (Omega hi + lo) into two TMEM buffers; once the PE has
 // written phi, the product warp runs the products of that quarter:
@@ -572,15 +574,15 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
         mbar_init(&B.qk_full, 1);
-        mbar_init(&B.qk_empty, 5);      // MMA commit + one arrival per projection-epilogue warp
+        mbar_init(&B.qk_empty, 9);      // MMA commit + one arrival per projection-epilogue warp
         mbar_init(&B.v_full, 1);
         mbar_init(&B.v_empty, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
-            mbar_init(&B.p_empty[i], 4);
-            mbar_init(&B.phik_full[i], 4);
+            mbar_init(&B.p_empty[i], 8);
+            mbar_init(&B.phik_full[i], 8);
         }
-        mbar_init(&B.phiq_full, 4);
+        mbar_init(&B.phiq_full, 8);
         mbar_init(&B.phq_free, 1);
         mbar_init(&B.upd_done, 1);
         mbar_init(&B.a_full, 1);
@@ -738,10 +740,11 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
-    else if (warp >= 4 && warp < 8) {
+    else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ PE: phi(k), phi(q)
-        const int tr = t - 128;                   // token row of the chunk = TMEM lane
+        const int tr = (t - 128) & 127;           // token row of the chunk = TMEM lane
         const int wl = (warp & 3) * 32;           // this warp's TMEM lane base
+        const int half_cols = (warp - 4) >> 2;    // columns 32 half_cols .. + 31 of every job
         if (favor) {                              // both projection buffers start empty
             warp_arrive(&B.p_empty[0], false);
             warp_arrive(&B.p_empty[1], false);
@@ -757,12 +760,11 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             for (int q = 0; q < nq && ok; ++q) {
                 const int g = c * nq + q;
                 for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
-                    uint32_t v0[32], v1[32];
+                    uint32_t v0[32];
                     if (favor) {
                         if (!(ok = warp_wait(&B.p_full[kind], g & 1))) break;
                         tc_fence_after();
-                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind), v0);
-                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind + 32), v1);
+                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind + 32 * half_cols), v0);
                         tmem_ld_wait();
                         warp_arrive(&B.p_empty[kind], false);
                     }
@@ -786,13 +788,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         for (int j = 0; j < 16; ++j)
                             w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * j]) - cx),
                                                ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx));
-                        store_row32_bf16(dst, tr, 0, w);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * j]) - cx),
-                                               ex2_approx(__uint_as_float(v1[2 * j + 1]) - cx));
-                        store_row32_bf16(dst, tr, 32, w);
-                    } else {
+                        store_row32_bf16(dst, tr, 32 * half_cols, w);
+                    } else if (half_cols == 0) {
                         elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
                     }
                     warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full, true);
@@ -801,10 +798,36 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             if (ok && !favor) warp_arrive(&B.qk_empty, false);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
-    } else if (warp >= 8 && warp < 12) {
-        // ------------------------------------------------------------ OE: scores split, output
-        const int tr = t - 256;                   // query row = TMEM lane
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ TE: chunk tail
+        const int tr = t - 384;                   // query row / state feature = TMEM lane
         const int wl = (warp & 3) * 32;
+        const int64_t E = (int64_t)r * 65;
+        const float* src = p.prefix + ((int64_t)u * p.H + head) * E;
+        const bool zero = tp.prefix_is_zero != 0;
+        for (int half = 0; half < nhalves; ++half) {   // the entering state: TMEM, bf16 rows, z
+            const int feat = 128 * half + tr;
+            const bool have = !zero && feat < r;
+            uint32_t w[32];
+#pragma unroll
+            for (int n0 = 0; n0 < kNX; n0 += 16) {
+                uint32_t x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    x[j] = __float_as_uint((have && n0 + j < 65) ? src[(int64_t)feat * 65 + n0 + j] : 0.f);
+                tmem_st16(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + n0), x);
+                if (n0 < 64) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w[n0 / 2 + j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                } else if (feat < r) {
+                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
+                        __float2bfloat16_rn(__uint_as_float(x[0]));
+                }
+            }
+            state_row_bf16(s.sbf[half], tr, w);
+        }
+        tmem_st_wait();
+        warp_arrive(&B.sbf_full, true);
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -848,6 +871,27 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             }
             tmem_st_wait();
             warp_arrive(&B.ahl_full, false);
+            if (c + 1 < nchunks) {   // the state after this chunk, while A V runs
+                for (int half = 0; half < nhalves; ++half) {
+                    uint32_t a0[32], a1[32], zc;
+                    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half), a0);
+                    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 32), a1);
+                    tmem_ld1(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 64), zc);
+                    tmem_ld_wait();
+                    uint32_t w[32];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        w[j] = pack_bf16x2(__uint_as_float(a0[2 * j]), __uint_as_float(a0[2 * j + 1]));
+                        w[16 + j] = pack_bf16x2(__uint_as_float(a1[2 * j]), __uint_as_float(a1[2 * j + 1]));
+                    }
+                    state_row_bf16(s.sbf[half], tr, w);
+                    const int feat = 128 * half + tr;
+                    if (feat < r)
+                        *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
+                            __float2bfloat16_rn(__uint_as_float(zc));
+                }
+                warp_arrive(&B.sbf_full, true);
+            }
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
             uint32_t o0[32], o1[32], dz;
@@ -858,60 +902,6 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             const float den = dsum + __uint_as_float(dz);
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
             if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
-        }
-        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
-    } else if (warp >= 12) {
-        // ------------------------------------------------------------ SE: state of the chunks so far
-        const int tr = t - 384;                   // state feature (within a half) = TMEM lane
-        const int64_t E = (int64_t)r * 65;
-        const float* src = p.prefix + ((int64_t)u * p.H + head) * E;
-        const bool zero = tp.prefix_is_zero != 0;
-        for (int half = 0; half < nhalves; ++half) {   // the entering state: TMEM, bf16 rows, z
-            const int feat = 128 * half + tr;
-            const bool have = !zero && feat < r;
-            uint32_t w[32];
-#pragma unroll
-            for (int n0 = 0; n0 < kNX; n0 += 16) {
-                uint32_t x[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    x[j] = __float_as_uint((have && n0 + j < 65) ? src[(int64_t)feat * 65 + n0 + j] : 0.f);
-                tmem_st16(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + n0), x);
-                if (n0 < 64) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) w[n0 / 2 + j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-                } else if (feat < r) {
-                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
-                        __float2bfloat16_rn(__uint_as_float(x[0]));
-                }
-            }
-            state_row_bf16(s.sbf[half], tr, w);
-        }
-        tmem_st_wait();
-        warp_arrive(&B.sbf_full, true);
-        bool ok = true;
-        for (int c = 0; c + 1 < nchunks && ok; ++c) {   // the last chunk's state is not read again
-            if (!(ok = warp_wait(&B.a_full, c & 1))) break;
-            tc_fence_after();
-            for (int half = 0; half < nhalves; ++half) {
-                uint32_t a0[32], a1[32], zc;
-                tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half), a0);
-                tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 32), a1);
-                tmem_ld1(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 64), zc);
-                tmem_ld_wait();
-                uint32_t w[32];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    w[j] = pack_bf16x2(__uint_as_float(a0[2 * j]), __uint_as_float(a0[2 * j + 1]));
-                    w[16 + j] = pack_bf16x2(__uint_as_float(a1[2 * j]), __uint_as_float(a1[2 * j + 1]));
-                }
-                state_row_bf16(s.sbf[half], tr, w);
-                const int feat = 128 * half + tr;
-                if (feat < r)
-                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
-                        __float2bfloat16_rn(__uint_as_float(zc));
-            }
-            warp_arrive(&B.sbf_full, true);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
