@@ -345,6 +345,22 @@ __device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat1
                                 pack_bf16x2(__uint_as_float(b[8 * q + 6]) * inv, __uint_as_float(b[8 * q + 7]) * inv));
 }
 
+// 32 scores of one row (keys key0 .. key0 + 31) as bf16 hi + lo, two keys per word;
+// keys after `row` are zeroed when the block is on the diagonal.  Adds the kept
+// scores to dsum.
+__device__ __forceinline__ void split_scores32(const uint32_t (&v)[32], int key0, bool diag, int row, float& dsum,
+                                               uint32_t (&hv)[16], uint32_t (&lv)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int c0 = key0 + 2 * j;
+        const float a = (!diag || c0 <= row) ? __uint_as_float(v[2 * j]) : 0.f;
+        const float b = (!diag || c0 + 1 <= row) ? __uint_as_float(v[2 * j + 1]) : 0.f;
+        dsum += a + b;
+        hv[j] = pack_bf16x2(a, b);
+        lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b - bf16hi(hv[j]));
+    }
+}
+
 // 64 bf16 (packed in pairs) as row `row` of a 128-byte-swizzled tile.
 __device__ __forceinline__ void state_row_bf16(unsigned char* tile, int row, const uint32_t (&w)[32]) {
 #pragma unroll
@@ -839,35 +855,27 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             // TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127]: each group of
             // 64 keys is read whole before its 64 columns are overwritten
             float dsum = 0.f;   // sum_{j <= i} A_ij: the in-chunk part of the denominator
+            // key blocks of 32: above this warp's rows all masked (no load), below kept
+            // whole, on the diagonal masked per element
+            const int wq = warp & 3;                  // rows 32 wq .. 32 wq + 31
             for (int part = 0; part < 2; ++part) {
                 const uint32_t cb = kColA + 64 * part;
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tmem_addr(tb, wl, cb), v0);
-                tmem_ld32(tmem_addr(tb, wl, cb + 32), v1);
-                tmem_ld_wait();
-                uint32_t hv[16], lv[16];
+                const int x0 = 2 * part, x1 = 2 * part + 1;
+                uint32_t hv0[16], lv0[16], hv1[16], lv1[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c0 = 64 * part + 2 * j;
-                    const float a = c0 <= tr ? __uint_as_float(v0[2 * j]) : 0.f;
-                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v0[2 * j + 1]) : 0.f;
-                    dsum += a + b2;
-                    hv[j] = pack_bf16x2(a, b2);
-                    lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
+                for (int j = 0; j < 16; ++j) hv0[j] = lv0[j] = hv1[j] = lv1[j] = 0u;
+                if (x0 <= wq) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem_addr(tb, wl, cb), v0);
+                    if (x1 <= wq) tmem_ld32(tmem_addr(tb, wl, cb + 32), v1);
+                    tmem_ld_wait();
+                    split_scores32(v0, 32 * x0, x0 == wq, tr, dsum, hv0, lv0);
+                    if (x1 <= wq) split_scores32(v1, 32 * x1, x1 == wq, tr, dsum, hv1, lv1);
                 }
-                tmem_st16(tmem_addr(tb, wl, cb), hv);
-                tmem_st16(tmem_addr(tb, wl, cb + 32), lv);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c0 = 64 * part + 32 + 2 * j;
-                    const float a = c0 <= tr ? __uint_as_float(v1[2 * j]) : 0.f;
-                    const float b2 = c0 + 1 <= tr ? __uint_as_float(v1[2 * j + 1]) : 0.f;
-                    dsum += a + b2;
-                    hv[j] = pack_bf16x2(a, b2);
-                    lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b2 - bf16hi(hv[j]));
-                }
-                tmem_st16(tmem_addr(tb, wl, cb + 16), hv);
-                tmem_st16(tmem_addr(tb, wl, cb + 48), lv);
+                tmem_st16(tmem_addr(tb, wl, cb), hv0);
+                tmem_st16(tmem_addr(tb, wl, cb + 32), lv0);
+                tmem_st16(tmem_addr(tb, wl, cb + 16), hv1);
+                tmem_st16(tmem_addr(tb, wl, cb + 48), lv1);
             }
             tmem_st_wait();
             warp_arrive(&B.ahl_full, false);
