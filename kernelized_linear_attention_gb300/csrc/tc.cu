@@ -528,9 +528,9 @@ struct CausalBars {
     uint64_t p_full[2];             // MMA commit -> PE: projection in TMEM buffer b
     uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
     uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
-    uint64_t phiq_full;             // PE (4 warps) -> MMA: phi(q) in smem
+    uint64_t phiq_full[2];          // PE (8 warps) -> MMA: phi(q) of global quarter g in smem (g & 1)
     uint64_t upd_done;              // MMA commit -> PE: a state update has read phi(k) of its half
-    uint64_t phq_free;              // MMA commit -> PE: scores and readout of quarter g done
+    uint64_t phq_free[2];           // MMA commit -> PE: products of global quarter g done (g & 1)
     uint64_t a_full;                // MMA commit -> SE, OE: scores, readout, state update of the chunk done
     uint64_t ahl_full;              // OE (4 warps) -> MMA: masked scores hi/lo in TMEM
     uint64_t o_full;                // MMA commit -> OE: numerator/denominator complete
@@ -545,11 +545,11 @@ struct __align__(1024) CausalSmem {
     unsigned char omg_hi[kOmgBytes];
     unsigned char omg_lo[kOmgBytes];
     Tile tq, tk, tv;
-    Tile ones;                        // second MN atom of [V|1]: column 0 = 1
-    Tile phq;                         // Phi_Q of one quarter (64 features)
+    Tile phq[2];                      // Phi_Q of one quarter (64 features), two buffers
     Tile phk[2];                      // Phi_K of one half (two quarters)
     Tile sbf[2];                      // S bf16, MN-major [feature][v]: features 128h.. in sbf[h]
     unsigned char zrow[4][2048];      // per quarter: K-major [16][64], row 0 = z bf16, rows 1..15 = 0
+    unsigned char zones[2][2048];     // K-major [16][64] x 2 (tokens 0..63, 64..127): row 0 = 1, rest 0
     CausalBars b;
 };
 
@@ -598,8 +598,10 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(&B.p_empty[i], 8);
             mbar_init(&B.phik_full[i], 8);
         }
-        mbar_init(&B.phiq_full, 8);
-        mbar_init(&B.phq_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B.phiq_full[i], 8);
+            mbar_init(&B.phq_free[i], 1);
+        }
         mbar_init(&B.upd_done, 1);
         mbar_init(&B.a_full, 1);
         mbar_init(&B.ahl_full, 4);
@@ -632,9 +634,13 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     }
     for (int i = t; i < 4 * 2048 / 16; i += kCausalThreads)
         reinterpret_cast<uint4*>(s.zrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = t; i < 2 * 16 * 8; i += kCausalThreads) {   // row 0 of both 16 x 64 ones blocks = 1
+        const int blk = i >> 7, row = (i >> 3) & 15, c = i & 7;
+        *reinterpret_cast<uint4*>(s.zones[blk] + sw128_chunk(row, c)) =
+            row == 0 ? make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u) : make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int i = t; i < kC * 8; i += kCausalThreads) {
         const int row = i >> 3, c = i & 7;
-        *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
         if (nq == 1)   // feature rows 64..127 of the state update stay zero
             *reinterpret_cast<uint4*>(s.phk[1] + sw128_chunk(row, c)) = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -692,17 +698,18 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     }
     else if (warp == 2) {
         // ------------------------------------------------------------ product MMAs (elected lane issues)
-        const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq), 16, 1024);
+        const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq[0]), 16, 1024);
+        const uint64_t d_zones = sdesc_sw128(smem_u32(s.zones[0]), 16, 1024);
+        const uint32_t id_z = idesc_bf16(128, 16, true, false);
         const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
         const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), kTile, 1024);                 // MN-major
         const uint64_t d_v = sdesc_sw128(smem_u32(s.tv), kTile, 1024);                       // MN-major, V only
         const uint64_t d_zrow = sdesc_sw128(smem_u32(s.zrow[0]), 16, 1024);
         const uint32_t id_den = idesc_bf16(128, 16, false, false);
         const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
-        const uint64_t d_vx = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones) - smem_u32(s.tv), 1024);
         const uint32_t id_scores = idesc_bf16(128, 128, false, false);
         const uint32_t id_read = idesc_bf16(128, 64, false, true);
-        const uint32_t id_upd = idesc_bf16(128, kNX, true, true);
+        const uint32_t id_upd = idesc_bf16(128, 64, true, true);
         const uint32_t id_av = idesc_bf16(128, 64, false, true);
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -717,28 +724,33 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 if ((q & 1) || q == nq - 1) {   // phi(k) of the half complete: update now, ahead of the scores
                     if (!v_ready && !(ok = warp_wait(&B.v_full, c & 1))) break;
                     v_ready = true;
+                    const uint32_t ds = tb + kColS + 80 * (q >> 1);
 #pragma unroll
                     for (int k = 0; k < kC / 16; ++k)
-                        mma_ss_w(tb + kColS + 80 * (q >> 1), sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_vx, 2048 * k), id_upd, 1u);
+                        mma_ss_w(ds, sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_v, 2048 * k), id_upd, 1u);
+                    // z += phi(k)^T 1 into column 64 (the only non-zero row of a 16-row operand)
+#pragma unroll
+                    for (int k = 0; k < kC / 16; ++k)
+                        mma_ss_w(ds + 64, sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_zones, 2048 * (k >> 2) + 32 * (k & 3)), id_z, 1u);
                     mma_commit_w(&B.upd_done);
                 }
-                if (!(ok = warp_wait(&B.phiq_full, g & 1))) break;
+                if (!(ok = warp_wait(&B.phiq_full[g & 1], (g >> 1) & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColA, sdesc_add(d_phq, 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
+                    mma_ss_w(tb + kColA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
                              (q > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColO, sdesc_add(d_phq, 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
+                    mma_ss_w(tb + kColO, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
                              (q > 0 || k > 0) ? 1u : 0u);
                 // denominator term phi(q) . z into column 64 of O (z as the only
                 // non-zero row of a 16-row operand)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
+                    mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
                              (q > 0 || k > 0) ? 1u : 0u);
-                mma_commit_w(&B.phq_free);   // phi(q) of the next quarter waits only for these
+                mma_commit_w(&B.phq_free[g & 1]);   // this phi(q) buffer may be rewritten
             }
             if (!ok) break;
             mma_commit_w(&B.a_full);
@@ -785,17 +797,17 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         warp_arrive(&B.p_empty[kind], false);
                     }
                     // the MMAs that read the destination buffer last must be done: for phi(q) the
-                    // products of the previous quarter; for phi(k) the update of the half of the
-                    // previous quarter using this buffer (its scores finished before the phi(q)
-                    // wait of the quarter in between)
+                    // products of the quarter two before (same buffer); for phi(k) the scores of
+                    // the previous quarter using this buffer and the update of its half
                     if (kind == 1) {
-                        if (g >= 1 && !(ok = warp_wait(&B.phq_free, (g - 1) & 1))) break;
+                        if (g >= 2 && !(ok = warp_wait(&B.phq_free[g & 1], ((g >> 1) - 1) & 1))) break;
                     } else {
                         const int gw = g - (nq >= 2 ? 2 : 1);
                         const int uw = (gw / nq) * nhalves + ((gw % nq) >> 1);   // that update's index
-                        if (gw >= 0 && !(ok = warp_wait(&B.upd_done, uw & 1))) break;
+                        if (gw >= 0 && !(ok = warp_wait(&B.upd_done, uw & 1) &&
+                                              warp_wait(&B.phq_free[gw & 1], (gw >> 1) & 1))) break;
                     }
-                    unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq;
+                    unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq[g & 1];
                     if (favor) {
                         // rows past the unit's end: 2^(p - inf) = 0
                         const float cx = valid ? (kind == 0 ? ck : cq) : __int_as_float(0x7f800000);
@@ -808,7 +820,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     } else if (half_cols == 0) {
                         elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
                     }
-                    warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full, true);
+                    warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full[g & 1], true);
                 }
             }
             if (ok && !favor) warp_arrive(&B.qk_empty, false);
