@@ -12,6 +12,9 @@ the source pages, one sequence and one head at a time:
   FAVOR+ positive random features phi+(x) = exp(Omega x - |x|^2/2)/sqrt(m)
   ("The Kernel Zoo", §4.2 boxed map and §5.4; "Performer", §2 Step 3 and the
   §3 sketch);
+* the DPFP-nu map phi(x) = concat_s (x~ * x~^(s)), x~ = relu([x, -x]),
+  x~^(s)_i = x~_{(i+s) mod 2d}, s = 1..nu ("The Kernel Zoo", §6.3 boxed map and
+  the §6.5 worked examples; map names "dpfp1", "dpfp2", ... give nu);
 * orthogonal random features by Gram-Schmidt on Gaussian blocks, rows scaled
   to Gaussian (chi) lengths ("The Kernel Zoo", §5.1 and §5.3 Steps 1-4;
   "Performer", §2 Step 4);
@@ -33,7 +36,14 @@ from __future__ import annotations
 
 import numpy as np
 
-MAPS = ("identity", "elu1", "favor")
+MAPS = ("identity", "elu1", "favor", "dpfp1")
+
+
+def dpfp_nu(kind: str):
+    """nu of a "dpfp<nu>" map name, else None."""
+    if isinstance(kind, str) and kind.startswith("dpfp") and kind[4:].isdigit():
+        return int(kind[4:])
+    return None
 
 
 # ----------------------------------------------------------------------------
@@ -47,6 +57,10 @@ def feature_map(x, kind: str, omega=None) -> np.ndarray:
               (ELU with alpha = 1; "The Kernel Zoo", running example)
     favor:    phi(x) = exp(omega x - |x|^2 / 2) / sqrt(m), omega of shape [m, d]
               ("The Kernel Zoo", §4.2 boxed feature map)
+    dpfp<nu>: x~ = relu([x, -x]) in R^{2d}; for s = 1..nu the products
+              x~_i * x~_{(i+s) mod 2d}, i = 0..2d-1; the nu blocks concatenated in
+              order of s, so feature (s-1) * 2d + i ("The Kernel Zoo", §6.3, the
+              DPFP-nu boxed map, d_dot = 2 d nu)
     """
     x = np.asarray(x, dtype=np.float64)
     if kind == "identity":
@@ -61,11 +75,22 @@ def feature_map(x, kind: str, omega=None) -> np.ndarray:
         proj = x @ om.T                                    # omega_i^T x for every i
         half_sq = 0.5 * np.sum(x * x, axis=-1, keepdims=True)   # |x|^2 / 2
         return np.exp(proj - half_sq) / np.sqrt(m)
+    nu = dpfp_nu(kind)
+    if nu is not None:
+        d = x.shape[-1]
+        if not 1 <= nu <= 2 * d - 1:
+            raise ValueError(f"DPFP needs 1 <= nu <= 2d - 1, got nu = {nu}, d = {d}")
+        xt = np.maximum(np.concatenate([x, -x], axis=-1), 0.0)          # step 1: relu([x, -x])
+        blocks = [xt * np.roll(xt, -s, axis=-1) for s in range(1, nu + 1)]   # step 2: x~ * x~^(s)
+        return np.concatenate(blocks, axis=-1)
     raise ValueError(f"unknown feature map {kind!r}")
 
 
 def feature_dim(kind: str, d: int, omega=None) -> int:
-    return int(np.asarray(omega).shape[0]) if kind == "favor" else d
+    if kind == "favor":
+        return int(np.asarray(omega).shape[0])
+    nu = dpfp_nu(kind)
+    return 2 * d * nu if nu is not None else d
 
 
 # ----------------------------------------------------------------------------

@@ -132,6 +132,42 @@ def test_elu1_matches_library_elu_plus_one():
     assert oracle.feature_map(np.array([-1.0]), "elu1")[0] == pytest.approx(math.exp(-1), rel=1e-15)
 
 
+def test_dpfp1_worked_examples(golden):
+    """DPFP-1 of the running example's keys and of the mixed-sign keys k_A,
+    k_B ("The Kernel Zoo", §6.5-6.6)."""
+    g = golden("dpfp_worked_example.txt")
+    phi = oracle.feature_map(g["K"], "dpfp1")
+    assert phi.shape == (6, 4)
+    assert np.allclose(phi, g["phiK"], rtol=0, atol=g["tol_exact"])
+    assert abs(g["K"][4] @ g["K"][5] - g["kA_dot_kB"]) < g["tol_exact"]
+    assert abs(phi[4] @ phi[5] - g["phikA_dot_phikB"]) < g["tol_exact"]
+    assert oracle.feature_dim("dpfp1", 2) == 4
+
+
+def test_dpfp_invariants():
+    """Properties the DPFP-nu construction fixes ("The Kernel Zoo", §6.3-6.4):
+    d_dot = 2 d nu, non-negative features, the shift-d block is zero (it pairs
+    relu(x_i) with relu(-x_i)), degree-2 homogeneity, and phi(-x) equals phi(x)
+    with every 2d block rotated by d (x~(-x) is x~(x) rotated by d)."""
+    rng = np.random.default_rng(21)
+    d, nu = 3, 4
+    x = rng.standard_normal((50, d))
+    phi = oracle.feature_map(x, f"dpfp{nu}")
+    assert phi.shape == (50, 2 * d * nu) and oracle.feature_dim(f"dpfp{nu}", d) == 2 * d * nu
+    assert np.all(phi >= 0) and np.count_nonzero(phi) > phi.size // 8
+    blocks = phi.reshape(50, nu, 2 * d)
+    assert np.array_equal(blocks[:, d - 1], np.zeros((50, 2 * d)))          # s = d
+    assert np.count_nonzero(blocks[:, :d - 1]) > 0 and np.count_nonzero(blocks[:, d:]) > 0
+    assert np.allclose(oracle.feature_map(2.5 * x, f"dpfp{nu}"), 6.25 * phi, rtol=1e-14, atol=0)
+    neg = oracle.feature_map(-x, f"dpfp{nu}").reshape(50, nu, 2 * d)
+    assert np.array_equal(neg, np.roll(blocks, d, axis=-1))
+    # shift s pairs element i with element i + s: a plausible off-by-one (i - s,
+    # or s from 0) breaks the printed k_A / k_B values, pinned above, and this:
+    e = np.zeros((1, d)); e[0, 0] = 1.0; e[0, 1] = 1.0                  # x~ = e_0 + e_1
+    f1 = oracle.feature_map(e, "dpfp1")[0]
+    assert f1[0] == 1.0 and np.count_nonzero(f1) == 1
+
+
 def test_identity_map_is_identity():
     x = np.random.default_rng(0).standard_normal((5, 7))
     assert np.array_equal(oracle.feature_map(x, "identity"), x)
@@ -223,7 +259,7 @@ def test_chi_lengths_have_chi_mean():
     assert abs(lengths.mean() - mean) <= 3 * lengths.std() / math.sqrt(n)
 
 
-@pytest.mark.parametrize("kind", ["identity", "elu1", "favor"])
+@pytest.mark.parametrize("kind", ["identity", "elu1", "favor", "dpfp2"])
 @pytest.mark.parametrize("causal_form", [True, False])
 def test_linear_form_equals_quadratic_rescan(kind, causal_form):
     """Reassociation: the state form equals every query rescanning its keys
@@ -238,8 +274,9 @@ def test_linear_form_equals_quadratic_rescan(kind, causal_form):
     om = rng.standard_normal((12, d))
     fast = oracle.forward(q, k, v, kind, causal_form, omega=om, cu_seqlens=cu)
     slow = oracle.rescan(q, k, v, kind, omega=om, cu_seqlens=cu, causal_mask=causal_form)
-    if kind == "identity":
-        # identity scores can make den <= eps; compare where den is well away
+    if kind in ("identity", "dpfp2"):
+        # identity scores can make den <= eps (and DPFP features can all vanish);
+        # compare with a tolerance relative to the largest output
         assert np.allclose(fast, slow, rtol=1e-9, atol=1e-9 * np.abs(slow).max())
     else:
         assert np.allclose(fast, slow, rtol=1e-12, atol=1e-14)
