@@ -20,6 +20,10 @@
  *                    x + 1 for x > 0, exp(x) otherwise)
  *   LA_MAP_FAVOR     phi(x) = exp(Omega x - |x|^2/2) / sqrt(r), Omega in R^{r x d_k}
  *                    ("The Kernel Zoo", §4.2 and §5.4; "Performer", §2 Step 3)
+ *   LA_MAP_DPFP      DPFP-nu: x~ = relu([x, -x]) in R^{2 d_k}; feature (s-1) 2 d_k + i
+ *                    = x~_i x~_{(i+s) mod 2 d_k} for s = 1..nu; r = 2 d_k nu with
+ *                    1 <= nu <= 2 d_k - 1 ("The Kernel Zoo", §6.3; Omega unused).
+ *                    Computed on CUDA cores for every dtype.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -74,7 +78,7 @@ typedef enum {
     LA_ERR_DEVICE = 5         /* the device recorded an error (la_workspace_error)     */
 } la_status;
 
-typedef enum { LA_MAP_IDENTITY = 0, LA_MAP_ELU1 = 1, LA_MAP_FAVOR = 2 } la_map;
+typedef enum { LA_MAP_IDENTITY = 0, LA_MAP_ELU1 = 1, LA_MAP_FAVOR = 2, LA_MAP_DPFP = 3 } la_map;
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 
 /* Device error codes stored in the workspace error word. */
@@ -91,9 +95,10 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
  * la_feature_map - phi applied to every row of x.
  *   x:      [T, H, d] of dtype;  omega: [r, d] fp32 (FAVOR only, else may be NULL)
  *   phi:    [T, H, r] fp32 output
- *   map:    la_map;  r must equal d for identity and ELU+1.
+ *   map:    la_map;  r must equal d for identity and ELU+1, and be 2 d nu with
+ *           1 <= nu <= 2d - 1 for DPFP (LA_ERR_INVALID_ARG otherwise).
  * Defined by "The Kernel Zoo" §4.2 boxed map (FAVOR+), the running example
- * (ELU+1) and §1.3 (identity).  For LA_BF16 input the values are those the
+ * (ELU+1), §1.3 (identity) and §6.3 boxed map (DPFP-nu).  For LA_BF16 input the values are those the
  * forward calls use before they round phi to bf16 for the tensor cores.
  */
 LA_API la_status la_feature_map(const void* x, const float* omega, int map, int dtype,

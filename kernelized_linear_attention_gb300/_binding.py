@@ -10,7 +10,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "liblinattn.so")
 
-MAP_IDS = {"identity": 0, "elu1": 1, "favor": 2}
+MAP_IDS = {"identity": 0, "elu1": 1, "favor": 2, "dpfp": 3}
 DTYPE_IDS = {torch.float32: 0, torch.bfloat16: 1}
 
 LA_OK = 0
@@ -93,7 +93,21 @@ def _need(t: torch.Tensor, name: str, dtype=None, cuda=True):
 
 
 def _map_id(m) -> int:
-    return MAP_IDS[m] if isinstance(m, str) else int(m)
+    """Map id from a name ("identity", "elu1", "favor", "dpfp<nu>") or an id."""
+    if isinstance(m, str):
+        return MAP_IDS["dpfp"] if m.startswith("dpfp") else MAP_IDS[m]
+    return int(m)
+
+
+def _feature_dim(m, d_k: int, omega) -> int:
+    """r of a map: Omega's rows (FAVOR+), 2 d_k nu (DPFP-nu, named "dpfp<nu>"), else d_k."""
+    if _map_id(m) == MAP_IDS["favor"]:
+        return omega.shape[0]
+    if _map_id(m) == MAP_IDS["dpfp"]:
+        if not (isinstance(m, str) and m[4:].isdigit()):
+            raise ValueError('the DPFP map is named "dpfp<nu>", e.g. "dpfp2"')
+        return 2 * d_k * int(m[4:])
+    return d_k
 
 
 def la_status_string(status: int) -> str:
@@ -123,7 +137,7 @@ def la_feature_map(x: torch.Tensor, map, omega: Optional[torch.Tensor] = None,
     _need(x, "x")
     m = _map_id(map)
     T, H, d = x.shape
-    r = omega.shape[0] if m == MAP_IDS["favor"] else d
+    r = _feature_dim(map, d, omega)
     if omega is not None:
         _need(omega, "omega", torch.float32)
     if phi is None:
@@ -166,7 +180,7 @@ def la_forward_causal_noalloc(q, k, v, map, omega=None, cu_seqlens=None, nseq=No
     T, H, d_k = q.shape
     d_v = v.shape[2]
     m = _map_id(map)
-    r = omega.shape[0] if m == MAP_IDS["favor"] else d_k
+    r = _feature_dim(map, d_k, omega)
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int32)
         nseq = cu_seqlens.numel() - 1
@@ -188,7 +202,7 @@ def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace,
     T, H, d_k = q.shape
     d_v = v.shape[2]
     m = _map_id(map)
-    r = omega.shape[0] if m == MAP_IDS["favor"] else d_k
+    r = _feature_dim(map, d_k, omega)
     if omega is not None:
         _need(omega, "omega", torch.float32)
     if cu_seqlens is not None:

@@ -22,12 +22,13 @@ int device_sm_count() {
 // Shape checks shared by every forward entry point and the size queries.
 la_status check_dims(int map, int dtype, int nseq, int64_t T, int H, int dk, int dv, int r,
                      bool has_cu) {
-    if (map < LA_MAP_IDENTITY || map > LA_MAP_FAVOR) return LA_ERR_INVALID_ARG;
+    if (map < LA_MAP_IDENTITY || map > LA_MAP_DPFP) return LA_ERR_INVALID_ARG;
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
     if (nseq < 1 || nseq > 65535 || H < 1 || H > 65535) return LA_ERR_INVALID_ARG;
     if (T < 0 || T > (int64_t)INT32_MAX) return LA_ERR_INVALID_ARG;
     if (dk < 1 || dv < 1 || r < 1) return LA_ERR_INVALID_ARG;
-    if (map != LA_MAP_FAVOR && r != dk) return LA_ERR_INVALID_ARG;
+    if ((map == LA_MAP_IDENTITY || map == LA_MAP_ELU1) && r != dk) return LA_ERR_INVALID_ARG;
+    if (map == LA_MAP_DPFP && (r % (2 * dk) != 0 || r / (2 * dk) > 2 * dk - 1)) return LA_ERR_INVALID_ARG;
     if (!has_cu && (T % nseq) != 0) return LA_ERR_INVALID_ARG;
     if (dk > LA_MAX_DK || dv > LA_MAX_DV || r > LA_MAX_R) return LA_ERR_UNSUPPORTED;
     return LA_OK;

@@ -68,6 +68,21 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
             }
             phi[i] = val;
         }
+    } else if (map == LA_MAP_DPFP) {
+        // x~ = relu([x, -x]); feature (s-1) 2d + i = x~_i x~_{(i+s) mod 2d}, s = 1..r / 2d
+        const int d2 = 2 * d;
+        for (int i = threadIdx.x; i < CS * r; i += NT) {
+            const int row = i / r, f = i - row * r;
+            float val = 0.f;
+            if (row < nrows) {
+                const int s = f / d2 + 1, a = f - (s - 1) * d2, b = (a + s) % d2;
+                const float* xr = x + row * d;
+                const float xa = a < d ? fmaxf(xr[a], 0.f) : fmaxf(-xr[a - d], 0.f);
+                const float xb = b < d ? fmaxf(xr[b], 0.f) : fmaxf(-xr[b - d], 0.f);
+                val = xa * xb;
+            }
+            phi[i] = val;
+        }
     } else {
         for (int i = threadIdx.x; i < CS * r; i += NT) {
             const int row = i / r;

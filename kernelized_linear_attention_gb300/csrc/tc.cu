@@ -1578,7 +1578,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }  // namespace
 
 bool tc_supported(int map, int dk, int dv, int r) {
-    if (dk != 64 || dv != 64) return false;
+    if (dk != 64 || dv != 64 || map == LA_MAP_DPFP) return false;
     if (map == LA_MAP_FAVOR) return r == 64 || r == 128 || r == 256;
     return r == 64;
 }

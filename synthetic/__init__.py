@@ -127,6 +127,10 @@ def workloads() -> dict:
         H=8, dk=64, dv=64, r=256, map="favor", causal=True, dtype="bf16",
         lengths=varlen_lengths(64, 128, 8192, DATA_SEED_BASE + 4), qk_scale=s,
         equal_lengths=False, seed=DATA_SEED_BASE + 4)
+    w["dpfp2_causal_b8h8n4096"] = Workload(
+        "dpfp2_causal_b8h8n4096", "causal DPFP-2 (r = 256), B=8, H=8, N=4096, d=64, bf16",
+        H=8, dk=64, dv=64, r=256, map="dpfp2", causal=True, dtype="bf16",
+        lengths=[4096] * 8, qk_scale=1.0, seed=DATA_SEED_BASE + 5)
     return w
 
 

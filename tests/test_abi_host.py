@@ -84,6 +84,9 @@ def _fwd(lib, name, **kw):
     (dict(q=None), 1), (dict(out=None), 1),
     (dict(q=(1 << 20) + 1), 1),                         # misaligned for bf16
     (dict(dk=300, r=300, map=1), 2), (dict(r=1024), 2), (dict(dv=512), 2),
+    (dict(map=3, r=100), 1),                            # DPFP needs r = 2 d_k nu
+    (dict(map=3, dk=2, dv=2, r=16), 1),                 # and nu <= 2 d_k - 1
+    (dict(map=4), 1),
 ])
 def test_forward_rejects_bad_arguments_on_host(lib, name, bad, code):
     assert _fwd(lib, name, **bad) == code
@@ -95,6 +98,9 @@ def test_selected_path_and_workspace_queries_reject_bad_shapes(lib):
     assert la.la_selected_path(True, "favor", 1, 64, 64, 256) in (0, 1)
     assert la.la_selected_path(True, "favor", 0, 64, 64, 256) == 0        # fp32 always on CUDA cores
     assert la.la_workspace_bytes(True, "elu1", 1, False, 3, 100, 2, 64, 64, 64) == 0   # 3 does not divide 100
+    assert la.la_selected_path(True, "dpfp2", 1, 64, 64, 256) == 0      # DPFP on CUDA cores for bf16 too
+    assert la.la_selected_path(False, "dpfp1", 0, 64, 64, 128) == 0
+    assert la.la_selected_path(True, "dpfp1", 1, 64, 64, 64) == -1      # r = 2 d_k nu
 
 
 def test_feature_map_rejects_bad_arguments(lib):
@@ -103,6 +109,8 @@ def test_feature_map_rejects_bad_arguments(lib):
     assert fn(1 << 20, None, 1, 1, 128, 2, 64, 32, 1 << 21, None) == 1      # ELU+1 with r != d
     assert fn(None, None, 1, 1, 128, 2, 64, 64, 1 << 21, None) == 1
     assert fn(1 << 20, None, 1, 1, 0, 2, 64, 64, None, None) == 0           # T = 0: nothing to do
+    assert fn(1 << 20, None, 3, 1, 128, 2, 64, 192, 1 << 21, None) == 1     # DPFP: r not 2 d nu
+    assert fn(1 << 20, None, 3, 1, 0, 2, 64, 256, None, None) == 0          # DPFP-2, T = 0
 
 
 def test_orthogonal_features_rejects_bad_arguments(lib):

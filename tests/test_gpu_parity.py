@@ -122,6 +122,35 @@ def test_elu1_running_example_o4_on_gpu(la):
     assert np.allclose(ident[:, 0], [[0, 0], [1, 0], [0.75, 0.75], [0.5, 1.0]], atol=1e-6)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,nu", [(64, 1), (64, 2), (16, 5)])
+def test_feature_map_dpfp(la, dtype, d, nu):
+    """DPFP-nu: each feature is one product of two rectified inputs, rounded
+    once to fp32, so the library matches the fp64 oracle bit for bit."""
+    rng = np.random.default_rng(7)
+    x = synthetic.quantise(rng.standard_normal((300, 3, d)).astype(np.float32), dtype)
+    got = la.la_feature_map(_tensor(x, dtype), f"dpfp{nu}").cpu().numpy()
+    ref = oracle.feature_map(x, f"dpfp{nu}")
+    assert got.shape == ref.shape == (300, 3, 2 * d * nu)
+    assert np.array_equal(got, ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("nu", [1, 2])
+def test_dpfp_ragged_packed(la, dtype, causal, nu):
+    inp = synthetic.random_inputs(RAGGED, H=2, dk=64, dv=64, dtype=dtype, seed=13)
+    got = _run(la, inp, f"dpfp{nu}", causal)
+    ref = _oracle(inp, f"dpfp{nu}", causal)
+    assert_close(got, ref, dtype, f"dpfp{nu} causal={causal}")
+
+
+def test_dpfp_small_head_fp32(la):
+    inp = synthetic.random_inputs([70, 5, 200], H=2, dk=16, dv=24, dtype="f32", seed=17)
+    for causal in (True, False):
+        assert_close(_run(la, inp, "dpfp5", causal), _oracle(inp, "dpfp5", causal), "f32")
+
+
 # ----------------------------------------------------------------------------
 # fp32 path: the single-head N=1024 workload (<= 1e-4 relative)
 # ----------------------------------------------------------------------------
@@ -227,7 +256,8 @@ def _sample_rows(start, end, rng, n=6):
 
 
 @pytest.mark.parametrize("name", ["elu_causal_b8h8n4096", "favor_bidir_b4h8n16384",
-                                  "favor_causal_b1h16n65536", "favor_causal_varlen64_h8"])
+                                  "favor_causal_b1h16n65536", "favor_causal_varlen64_h8",
+                                  "dpfp2_causal_b8h8n4096"])
 def test_full_size_workload_sampled_rows(la, name):
     w = synthetic.workloads()[name]
     inp = synthetic.make_qkv(w)
