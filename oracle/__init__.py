@@ -6,7 +6,7 @@ oracle/linear_attention.py for what each function computes and which passage
 of the source pages it follows.
 """
 from .linear_attention import (  # noqa: F401
-    MAPS, feature_map, feature_dim, gram_schmidt, orthogonal_random_features,
-    normalise, bidir, causal, rescan, causal_rows, bidir_rows, forward,
-    softmax_kernel_estimate,
+    MAPS, NORMS, dpfp_nu, feature_map, feature_dim, sum_normalise, features, gram_schmidt,
+    orthogonal_random_features, normalise, bidir, causal, decode_step, rescan, causal_rows, bidir_rows,
+    forward, softmax_kernel_estimate,
 )

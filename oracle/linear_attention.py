@@ -27,7 +27,16 @@ the source pages, one sequence and one head at a time:
   §1.3 and §5.4; "Reassociate a feature-map kernel", ¶4), with the state reset
   at every packed-sequence boundary (same paragraph);
 * the quadratic rescan form, for cross-checks on tiny inputs ("Linear
-  attention & kernelized approximations", "The naive way").
+  attention & kernelized approximations", "The naive way");
+* normalisation variants: attention normalisation (the default above), none
+  (the unnormalised fast-weight output of "The Kernel Zoo" §1.2-1.4) and sum
+  normalisation phi'(x) = phi(x) / sum_f phi(x)_f applied to every query and
+  key feature vector, with no attention denominator ("The Kernel Zoo",
+  §7.2-7.4);
+* a state carried in from an earlier segment of each sequence and out to the
+  next ("The Kernel Zoo" §9.3, fast weights carried across training segments),
+  and the one-token decode step of the recurrence ("Reassociate a feature-map
+  kernel", ¶4).
 
 Every function here is pinned by tests against values the pages print,
 closed forms or brute force (see tests/test_oracle_pins.py).
@@ -37,6 +46,7 @@ from __future__ import annotations
 import numpy as np
 
 MAPS = ("identity", "elu1", "favor", "dpfp1")
+NORMS = ("attention", "none", "sum")
 
 
 def dpfp_nu(kind: str):
@@ -96,6 +106,26 @@ def feature_dim(kind: str, d: int, omega=None) -> int:
 # ----------------------------------------------------------------------------
 # Orthogonal random features
 # ----------------------------------------------------------------------------
+def sum_normalise(phi, eps: float = 1e-6) -> np.ndarray:
+    """phi'(x) = phi(x) / sum_f phi(x)_f over the last axis ("The Kernel Zoo"
+    §7.2), so that the components of every row sum to 1.
+
+    The pages assume non-negative features with a positive sum.  A sum below
+    eps (a DPFP vector of an all-zero input, or underflow) is clamped to eps,
+    the same floor the attention denominator gets, so such a row stays finite.
+    """
+    phi = np.asarray(phi, np.float64)
+    return phi / np.maximum(phi.sum(axis=-1, keepdims=True), eps)
+
+
+def features(x, kind: str, omega=None, norm: str = "attention", eps: float = 1e-6) -> np.ndarray:
+    """The feature vectors attention uses: phi(x), sum-normalised under norm "sum"."""
+    if norm not in NORMS:
+        raise ValueError(norm)
+    p = feature_map(x, kind, omega)
+    return sum_normalise(p, eps) if norm == "sum" else p
+
+
 def gram_schmidt(rows) -> np.ndarray:
     """Orthonormalise the rows of one or a batch of square blocks, in order.
 
@@ -182,80 +212,131 @@ def normalise(num, den, eps: float, eps_mode: str = "clamp"):
     return num / d[..., None]
 
 
+def _out(num, den, eps, eps_mode, norm):
+    """Attention normalisation divides by the denominator; "none" and "sum" return the numerator."""
+    if norm == "attention":
+        return normalise(num, den, eps, eps_mode)
+    if norm in ("none", "sum"):
+        return np.asarray(num, np.float64)
+    raise ValueError(norm)
+
+
+def _state_in(state_in, s, h, r, dv):
+    """(S, z) that sequence s, head h starts from: zero, or copies of state_in[0][s, h], state_in[1][s, h]."""
+    if state_in is None:
+        return np.zeros((r, dv)), np.zeros(r)
+    S0, z0 = state_in
+    return np.array(S0[s, h], np.float64), np.array(z0[s, h], np.float64)
+
+
 def bidir(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
-          return_parts=False):
+          return_parts=False, norm="attention", state_in=None):
     """Bidirectional kernelized attention over packed sequences.
 
     q, k: [T, H, dk]; v: [T, H, dv].  For each sequence and head:
     S = Phi_K^T V, z = Phi_K^T 1, num = Phi_Q S, den = Phi_Q z,
     out = num / max(den, eps)   ("Performer" §2 Step 5 and §3 sketch;
     "Linear attention & kernelized approximations", "Build the state once").
+    norm "none" returns num, norm "sum" uses sum-normalised features and
+    returns num ("The Kernel Zoo" §7.2-7.4).  state_in = (S0 [nseq, H, r, dv],
+    z0 [nseq, H, r]) is added to every sequence's sums (memory from earlier
+    segments, all of it visible).
     Returns out [T, H, dv] (and num, den, per-(sequence, head) S and z).
     """
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
-    T, H, _ = q.shape
+    T, H, dk = q.shape
     dv = v.shape[2]
     cu = _bounds(cu_seqlens, T)
+    r = feature_dim(kind, dk, omega)
     num = np.zeros((T, H, dv)); den = np.zeros((T, H))
     states = {}
     for s in range(len(cu) - 1):
         a, b = cu[s], cu[s + 1]
         for h in range(H):
-            pq = feature_map(q[a:b, h], kind, omega)
-            pk = feature_map(k[a:b, h], kind, omega)
-            S = pk.T @ v[a:b, h]          # sum_j phi(k_j) v_j^T   [r, dv]
-            z = pk.sum(axis=0)            # sum_j phi(k_j)         [r]
+            pq = features(q[a:b, h], kind, omega, norm, eps).reshape(b - a, r)
+            pk = features(k[a:b, h], kind, omega, norm, eps).reshape(b - a, r)
+            S, z = _state_in(state_in, s, h, r, dv)
+            S = S + pk.T @ v[a:b, h]      # sum_j phi(k_j) v_j^T   [r, dv]
+            z = z + pk.sum(axis=0)        # sum_j phi(k_j)         [r]
             num[a:b, h] = pq @ S
             den[a:b, h] = pq @ z
             states[(s, h)] = (S, z)
-    out = normalise(num, den, eps, eps_mode)
+    out = _out(num, den, eps, eps_mode, norm)
     if return_parts:
         return out, num, den, states
     return out
 
 
 def causal(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
-           return_parts=False):
+           return_parts=False, norm="attention", state_in=None):
     """Causal kernelized attention by the prefix recurrence, token by token.
 
     For each sequence and head, starting from S = 0, z = 0 at the sequence's
-    first token:  S += phi(k_i) v_i^T;  z += phi(k_i);  num_i = phi(q_i)^T S;
+    first token (or from state_in = (S0 [nseq, H, r, dv], z0 [nseq, H, r])):
+    S += phi(k_i) v_i^T;  z += phi(k_i);  num_i = phi(q_i)^T S;
     den_i = phi(q_i)^T z; out_i = num_i / max(den_i, eps).  Key i is added
     before query i reads the state (inclusive prefix, "The Kernel Zoo" §1.3
-    sum over j = 1..i; "Reassociate a feature-map kernel" ¶4).
+    sum over j = 1..i; "Reassociate a feature-map kernel" ¶4).  norm as for
+    bidir.  The parts include each (sequence, head)'s final (S, z).
     """
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
-    T, H, _ = q.shape
+    T, H, dk = q.shape
     dv = v.shape[2]
     cu = _bounds(cu_seqlens, T)
+    r = feature_dim(kind, dk, omega)
     num = np.zeros((T, H, dv)); den = np.zeros((T, H))
     finals = {}
     for s in range(len(cu) - 1):
         a, b = cu[s], cu[s + 1]
         for h in range(H):
-            pq = feature_map(q[a:b, h], kind, omega)   # phi acts on one token at a time
-            pk = feature_map(k[a:b, h], kind, omega)
-            r = pk.shape[1]
-            S = np.zeros((r, dv)); z = np.zeros(r)
+            pq = features(q[a:b, h], kind, omega, norm, eps).reshape(b - a, r)   # one token at a time
+            pk = features(k[a:b, h], kind, omega, norm, eps).reshape(b - a, r)
+            S, z = _state_in(state_in, s, h, r, dv)
             for i in range(b - a):
                 S += np.outer(pk[i], v[a + i, h])
                 z += pk[i]
                 num[a + i, h] = pq[i] @ S
                 den[a + i, h] = pq[i] @ z
             finals[(s, h)] = (S.copy(), z.copy())
-    out = normalise(num, den, eps, eps_mode)
+    out = _out(num, den, eps, eps_mode, norm)
     if return_parts:
         return out, num, den, finals
     return out
 
 
+def decode_step(q, k, v, kind, S, z, omega=None, eps=1e-6, norm="attention"):
+    """One token of causal attention for each of B independent sequences.
+
+    q, k: [B, H, dk]; v: [B, H, dv]; S: [B, H, r, dv]; z: [B, H, r].  The
+    recurrence's single step ("Reassociate a feature-map kernel" ¶4; "The
+    Kernel Zoo" §1.3): S' = S + phi(k) v^T, z' = z + phi(k), then the query
+    reads the updated state: out = phi(q)^T S' / max(phi(q)^T z', eps)
+    (numerator alone under norm "none" and "sum").  Returns (out, S', z');
+    the inputs are not modified.
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    B, H, _ = q.shape
+    S2 = np.array(S, np.float64); z2 = np.array(z, np.float64)
+    out = np.zeros(v.shape)
+    for b in range(B):
+        for h in range(H):
+            pq = features(q[b, h], kind, omega, norm, eps)
+            pk = features(k[b, h], kind, omega, norm, eps)
+            S2[b, h] += np.outer(pk, v[b, h])
+            z2[b, h] += pk
+            num = pq @ S2[b, h]
+            out[b, h] = num / max(pq @ z2[b, h], eps) if norm == "attention" else num
+    return out, S2, z2
+
+
 def rescan(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp",
-           causal_mask=True):
+           causal_mask=True, norm="attention"):
     """Quadratic form: every query rescans its keys ("Linear attention &
     kernelized approximations", "The naive way: rescan every key").
 
     out_i = sum_j w_ij v_j / max(sum_j w_ij, eps), w_ij = phi(q_i) . phi(k_j),
-    j over the whole sequence (bidirectional) or j <= i (causal).
+    j over the whole sequence (bidirectional) or j <= i (causal); norm as
+    for bidir.
     """
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
     T, H, _ = q.shape
@@ -265,17 +346,18 @@ def rescan(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp
     for s in range(len(cu) - 1):
         a, b = cu[s], cu[s + 1]
         for h in range(H):
-            pq = feature_map(q[a:b, h], kind, omega)
-            pk = feature_map(k[a:b, h], kind, omega)
+            pq = features(q[a:b, h], kind, omega, norm, eps)
+            pk = features(k[a:b, h], kind, omega, norm, eps)
             for i in range(b - a):
                 last = i + 1 if causal_mask else b - a
                 w = np.array([pq[i] @ pk[j] for j in range(last)])
                 num[a + i, h] = w @ v[a:a + last, h]
                 den[a + i, h] = w.sum()
-    return normalise(num, den, eps, eps_mode)
+    return _out(num, den, eps, eps_mode, norm)
 
 
-def causal_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp"):
+def causal_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp",
+                norm="attention"):
     """Causal outputs of selected rows of one sequence [start, end) and head.
 
     Each requested row i gets S_i = sum_{start <= j <= i} phi(k_j) v_j^T and
@@ -285,31 +367,33 @@ def causal_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode
     """
     kk = np.asarray(k[start:end, head], np.float64)
     vv = np.asarray(v[start:end, head], np.float64)
-    pk = feature_map(kk, kind, omega)
+    pk = features(kk, kind, omega, norm, eps)
     outs = []
     for i in rows:
         j = int(i) - start
         assert 0 <= j < end - start
         S = pk[: j + 1].T @ vv[: j + 1]
         z = pk[: j + 1].sum(axis=0)
-        pq = feature_map(np.asarray(q[int(i), head], np.float64), kind, omega)
-        outs.append(normalise(pq @ S, np.asarray(pq @ z), eps, eps_mode))
+        pq = features(np.asarray(q[int(i), head], np.float64), kind, omega, norm, eps)
+        outs.append(_out(pq @ S, np.asarray(pq @ z), eps, eps_mode, norm))
     return np.array(outs)
 
 
-def bidir_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp"):
+def bidir_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp",
+               norm="attention"):
     """Bidirectional outputs of selected rows of one sequence and head."""
-    pk = feature_map(np.asarray(k[start:end, head], np.float64), kind, omega)
+    pk = features(np.asarray(k[start:end, head], np.float64), kind, omega, norm, eps)
     S = pk.T @ np.asarray(v[start:end, head], np.float64)
     z = pk.sum(axis=0)
-    pq = feature_map(np.asarray(q[np.asarray(rows, int), head], np.float64), kind, omega)
-    return normalise(pq @ S, pq @ z, eps, eps_mode)
+    pq = features(np.asarray(q[np.asarray(rows, int), head], np.float64), kind, omega, norm, eps)
+    return _out(pq @ S, pq @ z, eps, eps_mode, norm)
 
 
-def forward(q, k, v, kind, causal_form, omega=None, cu_seqlens=None, eps=1e-6):
+def forward(q, k, v, kind, causal_form, omega=None, cu_seqlens=None, eps=1e-6, norm="attention",
+            state_in=None):
     """Dispatch to the bidirectional or causal oracle."""
     f = causal if causal_form else bidir
-    return f(q, k, v, kind, omega=omega, cu_seqlens=cu_seqlens, eps=eps)
+    return f(q, k, v, kind, omega=omega, cu_seqlens=cu_seqlens, eps=eps, norm=norm, state_in=state_in)
 
 
 def softmax_kernel_estimate(x, y, omega):

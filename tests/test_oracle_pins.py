@@ -344,3 +344,187 @@ def test_favor_kernel_matrix_is_unbiased_for_exp_scores():
     mean = est.mean(axis=0)
     se = est.std(axis=0, ddof=1) / np.sqrt(draws)
     assert np.all(np.abs(mean - np.exp(q @ k.T)) <= 4 * se)
+
+
+# ----------------------------------------------------------------------------
+# Normalisation variants, state carry and the decode step
+# ----------------------------------------------------------------------------
+def test_sum_normalisation_worked_example(golden):
+    g = golden("sum_normalisation_example.txt")
+    assert np.array_equal(oracle.feature_map(g["q1"], "elu1"), g["phi_q1"])
+    assert np.array_equal(oracle.feature_map(g["k1"], "elu1"), g["phi_k1"])
+    pq = oracle.features(g["q1"], "elu1", norm="sum")
+    pk = oracle.features(g["k1"], "elu1", norm="sum")
+    assert np.allclose(pq, g["phi_q1_sum"], atol=g["tol"], rtol=0)
+    assert np.allclose(pk, g["phi_k1_sum"], atol=g["tol"], rtol=0)
+    assert abs(pq @ pk - g["sim_sum"]) <= g["tol"]
+    assert abs(pq @ pk - g["sim_sum_printed"]) <= g["tol_printed"]
+    assert oracle.feature_map(g["q1"], "elu1") @ oracle.feature_map(g["k1"], "elu1") == g["sim"]
+    # the other norms leave the features alone
+    assert np.array_equal(oracle.features(g["q1"], "elu1", norm="none"), g["phi_q1"])
+
+
+@pytest.mark.parametrize("kind", ["elu1", "favor", "dpfp2"])
+def test_sum_normalised_features_sum_to_one(kind):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((9, 4)) * 0.7
+    om = rng.standard_normal((8, 4))
+    p = oracle.features(x, kind, om, norm="sum")
+    assert np.allclose(p.sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+    assert np.all(p >= 0)
+    # proportional to phi: the direction is unchanged
+    raw = oracle.feature_map(x, kind, om)
+    assert np.allclose(p * raw.sum(axis=-1, keepdims=True), raw, rtol=1e-13, atol=0)
+
+
+def test_sum_normalisation_of_a_zero_feature_vector_is_zero():
+    # DPFP of x = 0 has no positive part: every feature is 0 and the sum is
+    # clamped at eps instead of dividing 0 by 0.
+    p = oracle.features(np.zeros(3), "dpfp1", norm="sum", eps=1e-6)
+    assert np.array_equal(p, np.zeros(6))
+
+
+def test_sum_normalised_output_is_a_convex_combination():
+    """Under sum normalisation the output is phi'(q)-weighted columns of the
+    fast weights with weights summing to 1 ("The Kernel Zoo" §7.4): with one
+    stored pair (k, c) the output is (phi'(q) . phi'(k)) c, a weight strictly
+    between 0 and 1 for dense positive features, and no denominator."""
+    c = np.array([0.5, -2.0, 3.0])
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((1, 1, 2)); k = rng.standard_normal((1, 1, 2))
+    v = c[None, None, :]
+    out = oracle.causal(q, k, v, "elu1", norm="sum")
+    w = oracle.features(q[0, 0], "elu1", norm="sum") @ oracle.features(k[0, 0], "elu1", norm="sum")
+    assert 0 < w < 1
+    assert np.allclose(out[0, 0], w * c, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("norm", ["attention", "none", "sum"])
+@pytest.mark.parametrize("causal_form", [True, False])
+def test_norm_variants_equal_quadratic_rescan(norm, causal_form):
+    rng = np.random.default_rng(12)
+    lengths = [6, 0, 9]
+    T, H, d, dv = sum(lengths), 2, 4, 3
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    q, k = (rng.standard_normal((T, H, d)) * 0.6 for _ in range(2))
+    v = rng.standard_normal((T, H, dv))
+    om = rng.standard_normal((12, d))
+    for kind in ("elu1", "favor"):
+        fast = oracle.forward(q, k, v, kind, causal_form, omega=om, cu_seqlens=cu, norm=norm)
+        slow = oracle.rescan(q, k, v, kind, omega=om, cu_seqlens=cu, causal_mask=causal_form, norm=norm)
+        assert np.allclose(fast, slow, rtol=1e-12, atol=1e-14)
+
+
+def test_norm_none_is_the_fast_weight_trace(golden):
+    g = golden("fwp_identity_trace.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    y = oracle.causal(Q, K, V, "identity", norm="none")
+    assert np.allclose(y[:, 0], g["y"], atol=g["tol"], rtol=0)
+    # attention normalisation of the same trace differs (token 3: (0.75, 0.75))
+    assert not np.allclose(oracle.causal(Q, K, V, "identity")[:, 0], g["y"])
+
+
+def _state_pair(finals, nseq, H):
+    S = np.stack([np.stack([finals[(s, h)][0] for h in range(H)]) for s in range(nseq)])
+    z = np.stack([np.stack([finals[(s, h)][1] for h in range(H)]) for s in range(nseq)])
+    return S, z
+
+
+def test_state_carry_continues_the_running_example(golden):
+    """Carrying S_2 (printed) and z_2 = phi(k_1) + phi(k_2) (printed maps)
+    into a second segment of tokens 3-4 gives the page's o_4."""
+    g = golden("elu_running_example.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    S2 = np.asarray(g["S2"])[None, None]
+    z2 = (g["phiK"][0] + g["phiK"][1])[None, None]
+    out, _, _, finals = oracle.causal(Q[2:], K[2:], V[2:], "elu1", state_in=(S2, z2), return_parts=True)
+    assert np.allclose(out[1, 0], [25 / 26, 15 / 26], atol=g["tol_exact"], rtol=0)
+    assert np.allclose(out[1, 0], g["o4"], atol=g["tol_printed"], rtol=0)
+    # without the carried state the second segment starts from zero and differs
+    assert not np.allclose(oracle.causal(Q[2:], K[2:], V[2:], "elu1")[1, 0], g["o4"], atol=1e-2)
+
+
+def test_state_carry_reaches_the_printed_fast_weights(golden):
+    g = golden("fwp_identity_trace.txt")
+    Q, K, V = (_one_head(g[n]) for n in ("Q", "K", "V"))
+    _, _, _, f1 = oracle.causal(Q[:2], K[:2], V[:2], "identity", norm="none", return_parts=True)
+    y, _, _, f2 = oracle.causal(Q[2:], K[2:], V[2:], "identity", norm="none",
+                                state_in=_state_pair(f1, 1, 1), return_parts=True)
+    assert np.allclose(y[:, 0], g["y"][2:], atol=g["tol"], rtol=0)
+    assert np.allclose(f2[(0, 0)][0].T, g["W4"], atol=g["tol"], rtol=0)
+
+
+@pytest.mark.parametrize("norm", ["attention", "none", "sum"])
+@pytest.mark.parametrize("causal_form", [True, False])
+def test_split_segments_with_carried_state_equal_the_whole(norm, causal_form):
+    """Running every sequence in two segments, the second starting from the
+    first's final state, equals one run over the whole sequences (causal: the
+    recurrence continues; bidirectional: the sums add)."""
+    rng = np.random.default_rng(31)
+    first, second = [4, 0, 6], [5, 3, 0]
+    H, d, dv = 2, 3, 2
+    om = rng.standard_normal((8, d))
+    seqs = [(rng.standard_normal((a + b, H, d)) * 0.6, rng.standard_normal((a + b, H, d)) * 0.6,
+             rng.standard_normal((a + b, H, dv))) for a, b in zip(first, second)]
+    cat = lambda parts: np.concatenate(parts, axis=0)
+    cu1 = np.concatenate([[0], np.cumsum(first)]); cu2 = np.concatenate([[0], np.cumsum(second)])
+    cuw = np.concatenate([[0], np.cumsum(np.add(first, second))])
+    f = oracle.causal if causal_form else oracle.bidir
+    for kind in ("elu1", "favor"):
+        qw, kw, vw = (cat([s[i] for s in seqs]) for i in range(3))
+        q1, k1, v1 = (cat([s[i][:a] for s, a in zip(seqs, first)]) for i in range(3))
+        q2, k2, v2 = (cat([s[i][a:] for s, a in zip(seqs, first)]) for i in range(3))
+        _, _, _, f1 = f(q1, k1, v1, kind, omega=om, cu_seqlens=cu1, norm=norm, return_parts=True)
+        out2, _, _, f2 = f(q2, k2, v2, kind, omega=om, cu_seqlens=cu2, norm=norm,
+                           state_in=_state_pair(f1, 3, H), return_parts=True)
+        whole, _, _, fw = f(qw, kw, vw, kind, omega=om, cu_seqlens=cuw, norm=norm, return_parts=True)
+        for s, (a, b) in enumerate(zip(first, second)):
+            assert np.allclose(out2[cu2[s]:cu2[s + 1]], whole[cuw[s] + a:cuw[s + 1]], rtol=1e-12, atol=1e-14)
+            for h in range(H):
+                assert np.allclose(f2[(s, h)][0], fw[(s, h)][0], rtol=1e-12, atol=1e-14)
+                assert np.allclose(f2[(s, h)][1], fw[(s, h)][1], rtol=1e-12, atol=1e-14)
+
+
+def test_decode_steps_replay_the_running_example(golden):
+    """One decode step per token from a zero state gives the page's outputs:
+    the fast-weight trace y (identity, no normalisation), o_4 (ELU+1) and W_4."""
+    gy = golden("fwp_identity_trace.txt")
+    ge = golden("elu_running_example.txt")
+    for kind, norm, g, check in (("identity", "none", gy, "y"), ("elu1", "attention", ge, "o4")):
+        Q, K, V = g["Q"], g["K"], g["V"]
+        S = np.zeros((1, 1, 2, 2)); z = np.zeros((1, 1, 2))
+        outs = []
+        for t in range(4):
+            o, S, z = oracle.decode_step(Q[t][None, None], K[t][None, None], V[t][None, None], kind, S, z,
+                                         norm=norm)
+            outs.append(o[0, 0])
+        if check == "y":
+            assert np.allclose(outs, g["y"], atol=g["tol"], rtol=0)
+            assert np.allclose(S[0, 0].T, g["W4"], atol=g["tol"], rtol=0)
+        else:
+            assert np.allclose(outs[3], [25 / 26, 15 / 26], atol=g["tol_exact"], rtol=0)
+
+
+@pytest.mark.parametrize("norm", ["attention", "none", "sum"])
+def test_decode_steps_equal_the_causal_recurrence(norm):
+    rng = np.random.default_rng(17)
+    B, H, n, d, dv = 3, 2, 7, 4, 3
+    om = rng.standard_normal((8, d))
+    q, k = (rng.standard_normal((B, n, H, d)) * 0.6 for _ in range(2))
+    v = rng.standard_normal((B, n, H, dv))
+    for kind in ("elu1", "favor", "dpfp1"):
+        r = oracle.feature_dim(kind, d, om)
+        S = np.zeros((B, H, r, dv)); z = np.zeros((B, H, r))
+        steps = []
+        for t in range(n):
+            o, S2, z2 = oracle.decode_step(q[:, t], k[:, t], v[:, t], kind, S, z, omega=om, norm=norm)
+            assert not np.shares_memory(S2, S)
+            S, z = S2, z2
+            steps.append(o)
+        steps = np.stack(steps, axis=1)            # [B, n, H, dv]
+        cu = np.arange(B + 1) * n
+        ref, _, _, finals = oracle.causal(q.reshape(B * n, H, d), k.reshape(B * n, H, d), v.reshape(B * n, H, dv),
+                                          kind, omega=om, cu_seqlens=cu, norm=norm, return_parts=True)
+        assert np.allclose(steps.reshape(B * n, H, dv), ref, rtol=1e-12, atol=1e-13)
+        Sf, zf = _state_pair(finals, B, H)
+        assert np.allclose(S, Sf, rtol=1e-12, atol=1e-14) and np.allclose(z, zf, rtol=1e-12, atol=1e-14)
