@@ -36,13 +36,17 @@ import synthetic  # noqa: E402
 
 WORKLOAD = "favor_causal_b1h16n65536"
 METRIC = "tokens/s/GPU causal FAVOR+ r=256 d=64; % tensor-core / HBM roofline"
+DECODE_METRIC = "tokens/s/GPU causal FAVOR+ decode step (one new token per sequence), r=256 d=64; % HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PHASE_NAMES = ["plan", "state", "scan", "output"]
 # source file of each phase's kernel on the tensor-core (tc) and CUDA-core (simt) paths
 KERNEL_SOURCES = {"tc": {"output": "tc.cu", "state": "tc.cu", "scan": "plan.cu", "plan": "plan.cu"},
-                  "simt": {"output": "simt.cu", "state": "simt.cu", "scan": "plan.cu", "plan": "plan.cu"}}
+                  "simt": {"output": "simt.cu", "state": "simt.cu", "scan": "plan.cu", "plan": "plan.cu",
+                           "decode": "decode.cu"}}
 # second measured line: the bidirectional state pass (phi(k)^T [v|1] over every token)
 BIDIR_WORKLOAD = "favor_bidir_b4h8n16384"
+# the decode-step line of the default run
+DECODE_WORKLOAD = "favor_decode_b256h16"
 
 
 def parse_args(argv=None):
@@ -217,12 +221,19 @@ def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None) -> dict:
     if w.map == "favor":
         blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
         om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
+    if w.decode:
+        return cpu_baseline_decode(w, seconds, inputs, om)
     a, b = int(inputs.cu_seqlens[0]), int(inputs.cu_seqlens[1])
     f = oracle.causal if w.causal else oracle.bidir
+    st = carried_state(w, 1) if w.carry else None
 
     def run(h, n):
         sl = slice(a, a + n)
-        f(inputs.q[sl, h:h + 1], inputs.k[sl, h:h + 1], inputs.v[sl, h:h + 1], w.map, omega=om, eps=w.eps)
+        state_in = None
+        if st is not None:
+            state_in = (st[:, h:h + 1, :, :-1].astype(np.float64), st[:, h:h + 1, :, -1].astype(np.float64))
+        f(inputs.q[sl, h:h + 1], inputs.k[sl, h:h + 1], inputs.v[sl, h:h + 1], w.map, omega=om, eps=w.eps,
+          norm=w.norm, state_in=state_in)
 
     n0 = min(2048, b - a)
     t0 = time.perf_counter()
@@ -242,6 +253,32 @@ def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None) -> dict:
                       f"tokens/s = token-heads/s / H"}
 
 
+def carried_state(w: synthetic.Workload, nseq: int) -> np.ndarray:
+    """The carried state a carry or decode workload starts from (seeded)."""
+    return synthetic.random_state(nseq, w.H, w.r, w.dv, seed=w.seed + 1000,
+                                  z_mean=synthetic.mean_feature(w.map, w.r), n_prior=w.n_prior)
+
+
+def cpu_baseline_decode(w: synthetic.Workload, seconds: float, inputs, om) -> dict:
+    """The oracle's decode step on a sample of (sequence, head) pairs, one at a
+    time; tokens/s = (sequence, head) steps per second / H."""
+    import oracle
+    st = carried_state(w, w.nseq)
+    S = st[..., :-1].astype(np.float64); z = st[..., -1].astype(np.float64)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        b, h = n % w.nseq, (n // w.nseq) % w.H
+        oracle.decode_step(inputs.q[b:b + 1, h:h + 1], inputs.k[b:b + 1, h:h + 1], inputs.v[b:b + 1, h:h + 1],
+                           w.map, S[b:b + 1, h:h + 1], z[b:b + 1, h:h + 1], omega=om, eps=w.eps, norm=w.norm)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= w.nseq * w.H:
+            break
+    return {"value": n / w.H / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle decode step on {n} (sequence, head) pairs of the {w.name} workload in "
+                      f"{el:.1f} s, 1 BLAS thread; tokens/s = pair-steps/s / H"}
+
+
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
@@ -258,6 +295,8 @@ def run_ours(args):
     la.load_library()
 
     w = synthetic.workloads()[args.workload]
+    if w.decode:
+        return run_decode(args, la, w, dev, world, rank, local)
     inputs = synthetic.make_qkv(w)
     T, H, dk, dv, r = w.T, w.H, w.dk, w.dv, w.r
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -282,12 +321,18 @@ def run_ours(args):
     call_args = (ptr(dq), ptr(dk_), ptr(dvv), ptr(omega), w.map, tdt, ptr(cu), nseq, T, H, dk, dv, r, w.eps,
                  ptr(out), ptr(ws), ws_bytes, stream.cuda_stream)
 
+    state_in = state_out = None
+    if w.carry:
+        state_in = torch.from_numpy(carried_state(w, nseq)).to(dev)
+        state_out = torch.empty_like(state_in)
+    state_kw = dict(norm=w.norm, state_in=ptr(state_in), state_out=ptr(state_out))
+
     def step(evs=None):
         n = 0
         for ph in range(4):
             if evs is not None:
                 evs[ph].record(stream)
-            n += la.la_forward_phase(w.causal, ph, *call_args)
+            n += la.la_forward_phase(w.causal, ph, *call_args, **state_kw)
         if evs is not None:
             evs[4].record(stream)
         return n
@@ -349,7 +394,7 @@ def run_ours(args):
         byts = alg["bytes"] * token_heads / 2 if dom == "state" else alg_bytes
         achieved = byts / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 else "simt"
+    path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 and w.norm != "sum" else "simt"
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(path, dom, w.name)
     roof["kernel"] = dom
@@ -387,19 +432,179 @@ def run_ours(args):
         "warmup": warmup, "ms_per_step": ms_total_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) q,k scaled by d^-1/4, v)",
         "config": {"workload": w.name, "B": w.nseq, "H": H, "N": w.lengths[0], "d_k": dk, "d_v": dv, "r": r,
-                   "map": w.map, "causal": w.causal, "eps": w.eps, "parallelism": f"replicas x{world}",
+                   "map": w.map, "causal": w.causal, "eps": w.eps, "norm": w.norm, "carried_state": w.carry,
+                   "parallelism": f"replicas x{world}",
                    "l2": "no flush: q, k, v (402 MB) exceed the 126 MB L2",
                    "path": "tcgen05" if path == "tc" else "cuda-core"},
         "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
-    if not args.no_secondary:
+    if not args.no_secondary and w.name == WORKLOAD:
         line["bidir_state_pass"] = bidir_state_pass(la, dev, stream, peaks, K)
+        line["variants"] = forward_variants(la, dev, stream, peaks, K, w, (dq, dk_, dvv), omega)
+        line["decode_step"] = decode_line(la, dev, stream, peaks, max(3, min(K, 20)), DECODE_WORKLOAD)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _phase_timed(la, stream, steps, call_args, **kw):
+    """Mean per-phase ms of `steps` forward calls (after 3 warm-up calls)."""
+    import torch
+    for _ in range(3):
+        for ph in range(4):
+            la.la_forward_phase(call_args[0], ph, *call_args[1:], **kw)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    n = 0
+    for i in range(steps):
+        for ph in range(4):
+            evs[i][ph].record(stream)
+            n += la.la_forward_phase(call_args[0], ph, *call_args[1:], **kw)
+        evs[i][4].record(stream)
+    torch.cuda.synchronize()
+    phase_ms = {PHASE_NAMES[p]: statistics.mean(evs[i][p].elapsed_time(evs[i][p + 1]) for i in range(steps))
+                for p in range(4)}
+    return phase_ms, n // steps
+
+
+def forward_variants(la, dev, stream, peaks, steps, w, dev_qkv, omega) -> dict:
+    """The headline workload's forward with unnormalised output and with a
+    carried state in and out (same q, k, v on the device), and the ELU+1
+    workload with sum normalisation (its own inputs, CUDA-core path): mean
+    per-phase ms over `steps` calls each."""
+    import torch
+    out = {}
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def args_for(wl, qkv, om):
+        o = torch.empty((wl.T, wl.H, wl.dv), dtype=tdt, device=dev)
+        nb = la.la_workspace_bytes(wl.causal, wl.map, tdt, False, wl.nseq, wl.T, wl.H, wl.dk, wl.dv, wl.r)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        a = (wl.causal, ptr(qkv[0]), ptr(qkv[1]), ptr(qkv[2]), ptr(om), wl.map, tdt, None, wl.nseq, wl.T, wl.H,
+             wl.dk, wl.dv, wl.r, wl.eps, ptr(o), ptr(ws), nb, stream.cuda_stream)
+        return a, (o, ws)
+
+    def summary(wl, phase_ms, launches, note):
+        ms = sum(phase_ms.values())
+        return {"workload": wl.name, "norm": wl.norm, "carried_state": wl.carry, "ms": ms,
+                "tokens_per_s": wl.T / (ms * 1e-3), "phase_ms": phase_ms, "launches": launches, "note": note}
+
+    wl = w.with_(name=w.name + "_none", norm="none")
+    a, keep = args_for(wl, dev_qkv, omega)
+    pm, n = _phase_timed(la, stream, steps, a, norm="none")
+    out["none"] = summary(wl, pm, n, "unnormalised output, tensor-core kernels")
+
+    wl = synthetic.workloads()["favor_causal_b1h16n65536_carry"]
+    st_in = torch.from_numpy(carried_state(wl, wl.nseq)).to(dev)
+    st_out = torch.empty_like(st_in)
+    a, keep = args_for(wl, dev_qkv, omega)
+    pm, n = _phase_timed(la, stream, steps, a, state_in=ptr(st_in), state_out=ptr(st_out))
+    out["carry"] = summary(wl, pm, n, "state_in and state_out; same q, k, v as the headline line; "
+                                      "the state pass also sums the last segment")
+
+    wl = synthetic.workloads()["elu_causal_b8h8n4096_sum"]
+    inputs = synthetic.make_qkv(wl)
+    qkv = [torch.from_numpy(np.ascontiguousarray(inputs.storage(n))).view(torch.bfloat16).to(dev)
+           for n in ("q", "k", "v")]
+    a, keep = args_for(wl, qkv, None)
+    pm, n = _phase_timed(la, stream, steps, a, norm="sum")
+    alg = algorithmic(wl)
+    s = summary(wl, pm, n, "sum normalisation, CUDA-core kernels")
+    s["hbm_frac_of_output"] = alg["bytes"] * wl.T * wl.H / (pm["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    out["sum"] = s
+    return out
+
+
+def run_decode(args, la, w, dev, world, rank, local):
+    """Main line for a decode workload: one step = one decode step of every sequence."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    res = decode_line(la, dev, stream, measured_peaks(), args.steps, w.name, warmup=max(args.warmup, 3),
+                      world=world, e2e_steps=args.e2e_steps)
+    line = {
+        "metric": DECODE_METRIC,
+        "value": res["tokens_per_s"] * world, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded q, k, v and carried state)",
+        "config": {"workload": w.name, "B": w.nseq, "H": w.H, "d_k": w.dk, "d_v": w.dv, "r": w.r, "map": w.map,
+                   "norm": w.norm, "eps": w.eps, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: the carried state (272 MB) exceeds the 126 MB L2", "path": "cuda-core"},
+        "roofline": res["roofline"], "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, synthetic.make_qkv(w))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def decode_line(la, dev, stream, peaks, steps, name, warmup=3, world=1, e2e_steps=None) -> dict:
+    """Decode steps of a decode workload, timed with CUDA events on the
+    launching stream.  Algorithmic bytes per (sequence, head): the fp32 state
+    read and written once (2 * 4 * r * (d_v + 1)) plus q, k, v read and out
+    written.  The state updates in place from step to step."""
+    import torch
+    w = synthetic.workloads()[name]
+    inputs = synthetic.make_qkv(w)
+    B, H, dk, dv, r = w.nseq, w.H, w.dk, w.dv, w.r
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {}
+    for n in ("q", "k", "v"):
+        t = torch.from_numpy(np.ascontiguousarray(inputs.storage(n)).reshape(B, H, -1))
+        host[n] = (t.view(torch.bfloat16) if w.dtype == "bf16" else t).pin_memory()
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    omega = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(r, dk)
+        omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), r)
+    state = torch.from_numpy(carried_state(w, B)).to(dev)
+    out = torch.empty((B, H, dv), dtype=tdt, device=dev)
+    for _ in range(warmup):
+        la.la_decode_step(q, k, v, state, w.map, omega=omega, norm=w.norm, eps=w.eps, out=out)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        la.la_decode_step(q, k, v, state, w.map, omega=omega, norm=w.norm, eps=w.eps, out=out)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs), world, dev)
+    esz = 2 if w.dtype == "bf16" else 4
+    byts = B * H * (2 * 4 * r * (dv + 1) + esz * (2 * dk + 2 * dv))
+    gbs = byts / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("simt", "decode", w.name),
+            "kernel": "decode_kernel", "alg_bytes_per_launch": byts,
+            "peak_source": peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")}
+    # end to end: H2D of the new tokens' q, k, v, the step, D2H of out (the state stays resident)
+    out_host = torch.empty((B, H, dv), dtype=tdt).pin_memory()
+    Ke = e2e_steps if e2e_steps is not None else max(3, min(steps, 20))
+    torch.cuda.synchronize()
+    a0 = torch.cuda.Event(enable_timing=True); a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(Ke):
+        q.copy_(host["q"], non_blocking=True); k.copy_(host["k"], non_blocking=True)
+        v.copy_(host["v"], non_blocking=True)
+        la.la_decode_step(q, k, v, state, w.map, omega=omega, norm=w.norm, eps=w.eps, out=out)
+        out_host.copy_(out, non_blocking=True)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world, dev) / Ke
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v"))
+    e2e = {"value": B * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "ms_per_step": e2e_ms}
+    return {"workload": w.name, "ms": ms, "tokens_per_s": B / (ms * 1e-3), "launches": steps,
+            "roofline": roof, "e2e": e2e, "clocks": clocks}
 
 
 def bidir_state_pass(la, dev, stream, peaks, steps: int) -> dict:
@@ -457,14 +662,31 @@ def run_reference(args):
     if w.map == "favor":
         blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
         om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
-    n_sample = 2048
-    sl = slice(0, n_sample)
+    metric = DECODE_METRIC if w.decode else METRIC
+    if w.decode:
+        st = carried_state(w, w.nseq)
+        n_sample = min(w.nseq, 16)
+        S = st[:n_sample, :1, :, :-1].astype(np.float64); z = st[:n_sample, :1, :, -1].astype(np.float64)
 
-    def one():
-        if w.causal:
-            oracle.causal(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps)
-        else:
-            oracle.bidir(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps)
+        def one():
+            oracle.decode_step(inputs.q[:n_sample, :1], inputs.k[:n_sample, :1], inputs.v[:n_sample, :1], w.map,
+                               S, z, omega=om, eps=w.eps, norm=w.norm)
+        sample = (f"each step: fp64 oracle decode step of head 0 of the first {n_sample} sequences of the "
+                  f"{w.name} workload (1 of {w.H} heads); tokens/s = (sequence, head) steps/s / H")
+    else:
+        n_sample = 2048
+        sl = slice(0, n_sample)
+        state_in = None
+        if w.carry:
+            st = carried_state(w, 1)
+            state_in = (st[:, :1, :, :-1].astype(np.float64), st[:, :1, :, -1].astype(np.float64))
+        f = oracle.causal if w.causal else oracle.bidir
+
+        def one():
+            f(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps, norm=w.norm,
+              state_in=state_in)
+        sample = (f"each step: fp64 oracle on the first {n_sample} tokens of head 0 of the "
+                  f"{w.name} workload (1 of {w.H} heads); tokens/s = token-heads/s / H")
 
     for _ in range(args.warmup):
         one()
@@ -473,9 +695,7 @@ def run_reference(args):
         one()
     el = time.perf_counter() - t0
     value = n_sample * args.steps / w.H / el
-    sample = (f"each step: fp64 oracle on the first {n_sample} tokens of head 0 of the "
-              f"{w.name} workload (1 of {w.H} heads); tokens/s = token-heads/s / H")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name},

@@ -81,6 +81,22 @@ typedef enum {
 typedef enum { LA_MAP_IDENTITY = 0, LA_MAP_ELU1 = 1, LA_MAP_FAVOR = 2, LA_MAP_DPFP = 3 } la_map;
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 
+/*
+ * Normalisation of the output (la_forward, la_decode_step):
+ *   LA_NORM_ATTENTION  out = phi(q)^T S / max(phi(q)^T z, eps): a weighted
+ *                      average of the values ("Reassociate a feature-map
+ *                      kernel" ¶1-2; what la_forward_bidir/causal compute).
+ *   LA_NORM_NONE       out = phi(q)^T S: the unnormalised fast-weight output
+ *                      ("The Kernel Zoo" §1.2-1.4, the fast weight programmer).
+ *   LA_NORM_SUM        every query and key feature vector is divided by the
+ *                      sum of its components, phi'(x) = phi(x) /
+ *                      max(sum_f phi(x)_f, eps), and out = phi'(q)^T S' with
+ *                      S' built from phi'(k); there is no attention
+ *                      denominator ("The Kernel Zoo" §7.2-7.4).  Meant for the
+ *                      non-negative maps: LA_MAP_IDENTITY is rejected.
+ */
+typedef enum { LA_NORM_ATTENTION = 0, LA_NORM_NONE = 1, LA_NORM_SUM = 2 } la_norm;
+
 /* Device error codes stored in the workspace error word. */
 #define LA_DEVERR_NONE 0
 #define LA_DEVERR_CU_SEQLENS 1    /* cu_seqlens broke the packing rules: nothing computed */
@@ -136,10 +152,56 @@ LA_API la_status la_forward_causal(const void* q, const void* k, const void* v, 
                             void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * la_forward - the general forward call: either form, a normalisation variant
+ *   and a state carried between calls.
+ *   causal:    1 as la_forward_causal, 0 as la_forward_bidir.
+ *   norm:      la_norm (LA_ERR_INVALID_ARG for LA_NORM_SUM with the identity map).
+ *   state_in:  NULL (every sequence starts from S = 0, z = 0) or fp32
+ *              [nseq, H, r, d_v + 1]: row f of the (sequence, head) block holds
+ *              S[f, 0 .. d_v-1] followed by z[f].  Causal: the state the
+ *              sequence's first token adds to, so a long sequence can be run
+ *              as consecutive calls ("The Kernel Zoo" §9.3: fast weights
+ *              carried from one segment to the next).  Bidirectional: added to
+ *              the whole-sequence sums that every query reads.  Under
+ *              LA_NORM_SUM it holds sums of sum-normalised key features.
+ *   state_out: NULL or the same layout: state_in (or 0) plus the sums over the
+ *              whole sequence, i.e. the state after its last token.  Written
+ *              for every sequence, empty ones included.  May be the same
+ *              array as state_in (the call reads state_in before any of
+ *              state_out is written); must not overlap q, k, v, out or the
+ *              workspace otherwise.
+ *   Other arguments as for la_forward_bidir / la_forward_causal, with
+ *   la_workspace_bytes(causal, ...).  Both state arrays must be 4-byte aligned.
+ *   LA_NORM_SUM runs on the CUDA-core kernels.
+ */
+LA_API la_status la_forward(int causal, int norm, const void* q, const void* k, const void* v,
+                            const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq,
+                            int64_t T, int H, int d_k, int d_v, int r, float eps,
+                            const float* state_in, float* state_out, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * la_decode_step - one new token for each of B independent causal sequences:
+ *   the recurrence's single step S += phi(k) v^T, z += phi(k), then the query
+ *   reads the updated state, out = phi(q)^T S / max(phi(q)^T z, eps) (key i
+ *   visible to query i: "Reassociate a feature-map kernel" ¶4; "The Kernel
+ *   Zoo" §1.3).  norm as for la_forward.
+ *   q, k:  [B, H, d_k]; v, out: [B, H, d_v] (dtype); omega as for la_forward.
+ *   state: fp32 [B, H, r, d_v + 1] in the la_forward state layout, read and
+ *          updated in place (the state_out of a causal la_forward call over
+ *          the prompt continues directly).
+ *   Computed in fp32 on CUDA cores for every dtype; bf16 outputs are rounded
+ *   once.  B = 0 enqueues nothing.  Needs no workspace.
+ */
+LA_API la_status la_decode_step(const void* q, const void* k, const void* v, const float* omega, int map,
+                                int dtype, int norm, int B, int H, int d_k, int d_v, int r, float eps,
+                                float* state, void* out, void* stream);
+
+/*
  * la_forward_phase - one phase of a forward call, for callers that time or
- *   interleave the kernels.  la_forward_bidir / la_forward_causal are exactly
- *   phases LA_PHASE_PLAN .. LA_PHASE_OUTPUT called in order with the same
- *   arguments and workspace:
+ *   interleave the kernels.  la_forward (and so la_forward_bidir /
+ *   la_forward_causal) is exactly phases LA_PHASE_PLAN .. LA_PHASE_OUTPUT
+ *   called in order with the same arguments and workspace:
  *     LA_PHASE_PLAN    split the packed sequences into segments (reads cu_seqlens)
  *     LA_PHASE_STATE   per-segment state sum_j phi(k_j) [v_j | 1]^T
  *     LA_PHASE_SCAN    state entering each segment (causal: exclusive prefix
@@ -154,11 +216,12 @@ LA_API la_status la_forward_causal(const void* q, const void* k, const void* v, 
 #define LA_PHASE_SCAN 2
 #define LA_PHASE_OUTPUT 3
 #define LA_NUM_PHASES 4
-LA_API la_status la_forward_phase(int causal, int phase, const void* q, const void* k, const void* v,
-                           const float* omega, int map, int dtype, const int32_t* cu_seqlens,
-                           int nseq, int64_t T, int H, int d_k, int d_v, int r, float eps,
-                           void* out, void* workspace, size_t workspace_bytes, void* stream,
-                           int* launched);
+LA_API la_status la_forward_phase(int causal, int phase, int norm, const void* q, const void* k,
+                                  const void* v, const float* omega, int map, int dtype,
+                                  const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k,
+                                  int d_v, int r, float eps, const float* state_in, float* state_out,
+                                  void* out, void* workspace, size_t workspace_bytes, void* stream,
+                                  int* launched);
 
 /*
  * la_forward_causal_noalloc - la_forward_causal for callers that cannot
@@ -199,7 +262,9 @@ LA_API la_status la_forward_causal_noalloc(const void* q, const void* k, const v
  * la_workspace_bytes - scratch size for a forward call on the current device.
  *   causal: 1 for la_forward_causal, 0 for la_forward_bidir; `has_cu_seqlens`:
  *   1 when a cu_seqlens array will be passed.  Returns 0 for arguments the
- *   forward call would reject.  The size depends on the device's SM count.
+ *   forward call would reject.  The size depends on the device's SM count and
+ *   covers every kernel path a call with these arguments can take (any norm,
+ *   any operand alignment, with or without state_in / state_out).
  */
 LA_API size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq,
                           int64_t T, int H, int d_k, int d_v, int r);
@@ -236,7 +301,9 @@ LA_API la_status la_orthogonal_features(const double* gauss_blocks, const double
 /*
  * la_selected_path - which kernels a forward call with these arguments runs:
  *   0 = fp32 CUDA-core kernels, 1 = tcgen05 tensor-core kernels.  Assumes
- *   16-byte aligned pointers.  Returns -1 for arguments a call would reject.
+ *   16-byte aligned pointers and LA_NORM_ATTENTION or LA_NORM_NONE
+ *   (LA_NORM_SUM always runs on the CUDA-core kernels).  Returns -1 for
+ *   arguments a call would reject.
  */
 LA_API int la_selected_path(int causal, int map, int dtype, int d_k, int d_v, int r);
 

@@ -12,6 +12,7 @@ _LIB_PATH = os.path.join(_HERE, "lib", "liblinattn.so")
 
 MAP_IDS = {"identity": 0, "elu1": 1, "favor": 2, "dpfp": 3}
 DTYPE_IDS = {torch.float32: 0, torch.bfloat16: 1}
+NORM_IDS = {"attention": 0, "none": 1, "sum": 2}
 
 LA_OK = 0
 _c_i64, _c_int, _c_float, _c_size, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
@@ -45,7 +46,11 @@ def load_library():
         "la_feature_map": ([_vp, _vp, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _vp, _vp], _c_int),
         "la_forward_bidir": (fwd_args, _c_int),
         "la_forward_causal": (fwd_args, _c_int),
-        "la_forward_phase": ([_c_int, _c_int] + fwd_args + [ctypes.POINTER(_c_int)], _c_int),
+        "la_forward_phase": ([_c_int, _c_int, _c_int] + fwd_args[:14] + [_vp, _vp] + fwd_args[14:]
+                             + [ctypes.POINTER(_c_int)], _c_int),
+        "la_forward": ([_c_int, _c_int] + fwd_args[:14] + [_vp, _vp] + fwd_args[14:], _c_int),
+        "la_decode_step": ([_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                            _c_float, _vp, _vp, _vp], _c_int),
         "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
         "la_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_int],
                                _c_size),
@@ -97,6 +102,11 @@ def _map_id(m) -> int:
     if isinstance(m, str):
         return MAP_IDS["dpfp"] if m.startswith("dpfp") else MAP_IDS[m]
     return int(m)
+
+
+def _norm_id(n) -> int:
+    """Normalisation id from a name ("attention", "none", "sum") or an id."""
+    return NORM_IDS[n] if isinstance(n, str) else int(n)
 
 
 def _feature_dim(m, d_k: int, omega) -> int:
@@ -159,15 +169,18 @@ def forward_ptrs(causal: bool, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, 
 
 
 def la_forward_phase(causal: bool, phase: int, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r,
-                     eps, out, workspace, workspace_bytes, stream=None) -> int:
+                     eps, out, workspace, workspace_bytes, stream=None, norm="attention", state_in=None,
+                     state_out=None) -> int:
     """One phase (0 plan, 1 state, 2 scan, 3 output) with integer device
-    pointers; returns the number of kernels it enqueued."""
+    pointers (state_in / state_out too); returns the number of kernels it
+    enqueued."""
     lib = load_library()
     dt = DTYPE_IDS[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     n = _c_int(0)
-    _check("la_forward_phase", lib.la_forward_phase(int(causal), int(phase), q, k, v, omega, _map_id(map), dt,
-                                                    cu_seqlens, nseq, T, H, d_k, d_v, r, eps, out, workspace,
-                                                    workspace_bytes, _stream(stream), ctypes.byref(n)))
+    _check("la_forward_phase", lib.la_forward_phase(int(causal), int(phase), _norm_id(norm), q, k, v, omega,
+                                                    _map_id(map), dt, cu_seqlens, nseq, T, H, d_k, d_v, r, eps,
+                                                    state_in, state_out, out, workspace, workspace_bytes,
+                                                    _stream(stream), ctypes.byref(n)))
     return n.value
 
 
@@ -195,7 +208,8 @@ def la_forward_causal_noalloc(q, k, v, map, omega=None, cu_seqlens=None, nseq=No
     return out
 
 
-def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream):
+def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream, norm="attention",
+             state_in=None, state_out=None):
     _need(q, "q"); _need(k, "k"); _need(v, "v")
     if q.dtype not in DTYPE_IDS or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must share dtype float32 or bfloat16")
@@ -210,6 +224,11 @@ def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace,
         nseq = cu_seqlens.numel() - 1
     elif nseq is None:
         nseq = 1
+    for name, st in (("state_in", state_in), ("state_out", state_out)):
+        if st is not None:
+            _need(st, name, torch.float32)
+            if tuple(st.shape) != (nseq, H, r, d_v + 1):
+                raise ValueError(f"{name} must have shape {(nseq, H, r, d_v + 1)}, got {tuple(st.shape)}")
     if out is None:
         out = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     _need(out, "out", q.dtype)
@@ -218,9 +237,16 @@ def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace,
         raise LinAttnError("la_workspace_bytes", 1)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    forward_ptrs(causal, _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, q.dtype, _ptr(cu_seqlens), nseq, T, H,
-                 d_k, d_v, r, eps, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                 stream)
+    nid = _norm_id(norm)
+    if nid == NORM_IDS["attention"] and state_in is None and state_out is None:
+        forward_ptrs(causal, _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, q.dtype, _ptr(cu_seqlens), nseq, T, H,
+                     d_k, d_v, r, eps, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                     stream)
+    else:
+        _check("la_forward", load_library().la_forward(
+            int(causal), nid, _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype], _ptr(cu_seqlens),
+            nseq, T, H, d_k, d_v, r, eps, _ptr(state_in), _ptr(state_out), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, workspace
 
 
@@ -236,10 +262,48 @@ def la_forward_causal(q, k, v, map, omega=None, cu_seqlens=None, nseq=None, eps=
     return _forward(True, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream)[0]
 
 
+def la_forward(q, k, v, map, omega=None, causal=True, norm="attention", cu_seqlens=None, nseq=None, eps=1e-6,
+               state_in=None, state_out=None, return_state=False, out=None, workspace=None, stream=None):
+    """General forward: norm "attention" | "none" | "sum", optional carried
+    state.  state_in / state_out: fp32 [nseq, H, r, d_v + 1] (row f: S[f, :]
+    then z[f]).  With return_state=True a state_out is allocated when none is
+    given and (out, state_out) is returned."""
+    if return_state and state_out is None:
+        T, H, d_k = q.shape
+        nn = cu_seqlens.numel() - 1 if cu_seqlens is not None else (nseq or 1)
+        r = _feature_dim(map, d_k, omega)
+        state_out = torch.empty((nn, H, r, v.shape[2] + 1), dtype=torch.float32, device=q.device)
+    o = _forward(bool(causal), q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream, norm=norm,
+                 state_in=state_in, state_out=state_out)[0]
+    return (o, state_out) if return_state else o
+
+
+def la_decode_step(q, k, v, state, map, omega=None, norm="attention", eps=1e-6, out=None, stream=None):
+    """One token per sequence: q, k [B, H, d_k], v [B, H, d_v]; state fp32
+    [B, H, r, d_v + 1] is updated in place; returns out [B, H, d_v]."""
+    _need(q, "q"); _need(k, "k"); _need(v, "v"); _need(state, "state", torch.float32)
+    if q.dtype not in DTYPE_IDS or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype float32 or bfloat16")
+    B, H, d_k = q.shape
+    d_v = v.shape[2]
+    r = _feature_dim(map, d_k, omega)
+    if tuple(state.shape) != (B, H, r, d_v + 1):
+        raise ValueError(f"state must have shape {(B, H, r, d_v + 1)}, got {tuple(state.shape)}")
+    if omega is not None:
+        _need(omega, "omega", torch.float32)
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _need(out, "out", q.dtype)
+    _check("la_decode_step", load_library().la_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(omega), _map_id(map), DTYPE_IDS[q.dtype], _norm_id(norm), B, H, d_k, d_v,
+        r, eps, _ptr(state), _ptr(out), _stream(stream)))
+    return out
+
+
 def attention(q, k, v, map="favor", omega=None, causal=True, cu_seqlens=None, nseq=None, eps=1e-6,
-              out=None, workspace=None, stream=None, return_workspace=False):
+              out=None, workspace=None, stream=None, return_workspace=False, norm="attention"):
     """Convenience wrapper: allocates out/workspace with torch, calls the library."""
-    o, ws = _forward(bool(causal), q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream)
+    o, ws = _forward(bool(causal), q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream, norm=norm)
     return (o, ws) if return_workspace else o
 
 

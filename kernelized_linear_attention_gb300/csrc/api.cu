@@ -1,5 +1,6 @@
 // C ABI of liblinattn.so: argument checks, workspace layout, dispatch.
 // The operation each entry point computes is specified in include/linattn.h.
+#include <algorithm>
 #include <cmath>
 #include <vector>
 
@@ -36,8 +37,15 @@ la_status check_dims(int map, int dtype, int nseq, int64_t T, int H, int dk, int
 
 // Tensor cores for bf16 shapes the tcgen05 kernels cover; fp32 (exact
 // arithmetic) and every other shape on CUDA cores.
-int select_path(int /*causal*/, int map, int dtype, int dk, int dv, int r) {
-    return (dtype == LA_BF16 && tc_supported(map, dk, dv, r)) ? kPathTensor : kPathSimt;
+int select_path(int /*causal*/, int map, int dtype, int dk, int dv, int r, int norm = LA_NORM_ATTENTION) {
+    return (dtype == LA_BF16 && norm != LA_NORM_SUM && tc_supported(map, dk, dv, r)) ? kPathTensor : kPathSimt;
+}
+
+// Normalisation variants; sum normalisation needs non-negative features.
+la_status check_norm(int norm, int map) {
+    if (norm < LA_NORM_ATTENTION || norm > LA_NORM_SUM) return LA_ERR_INVALID_ARG;
+    if (norm == LA_NORM_SUM && map == LA_MAP_IDENTITY) return LA_ERR_INVALID_ARG;
+    return LA_OK;
 }
 
 int path_chunk(int path) { return path == kPathTensor ? 128 : simt_chunk(); }
@@ -82,11 +90,14 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const void* k, const void* v,
                   const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
                   int H, int dk, int dv, int r, float eps, void* out, void* workspace,
-                  size_t workspace_bytes, void* stream, int* launched) {
+                  size_t workspace_bytes, void* stream, int* launched, int norm = LA_NORM_ATTENTION,
+                  const float* state_in = nullptr, float* state_out = nullptr) {
     if (launched) *launched = 0;
     const bool has_cu = cu_seqlens != nullptr;
     la_status st = check_dims(map, dtype, nseq, T, H, dk, dv, r, has_cu);
     if (st != LA_OK) return st;
+    if ((st = check_norm(norm, map)) != LA_OK) return st;
+    if ((state_in && !aligned(state_in, 4)) || (state_out && !aligned(state_out, 4))) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
     if (map == LA_MAP_FAVOR && omega == nullptr) return LA_ERR_INVALID_ARG;
     if (workspace == nullptr || !aligned(workspace, kAlign)) return LA_ERR_INVALID_ARG;
@@ -94,7 +105,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     const size_t esz = dtype == LA_F32 ? 4 : 2;
     if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(out, esz)) return LA_ERR_INVALID_ARG;
     if (omega && !aligned(omega, 4)) return LA_ERR_INVALID_ARG;
-    int path = select_path(causal, map, dtype, dk, dv, r);
+    int path = select_path(causal, map, dtype, dk, dv, r, norm);
     // TMA and vector loads need 16-byte aligned operands
     if (path == kPathTensor && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) &&
                                  (omega == nullptr || aligned(omega, 16))))
@@ -111,7 +122,8 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     p.q = q; p.k = k; p.v = v; p.omega = omega; p.out = out;
     p.cu_seqlens = cu_seqlens; p.nseq = nseq; p.T = T;
     p.H = H; p.dk = dk; p.dv = dv; p.r = r; p.dvx = lo.dvx;
-    p.map = map; p.causal = causal; p.eps = eps;
+    p.map = map; p.causal = causal; p.norm = norm; p.eps = eps;
+    p.state_in = state_in; p.state_out = state_out;
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.units = reinterpret_cast<Unit*>(ws + lo.units);
     p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
@@ -120,9 +132,18 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     p.U = lo.U; p.L = lo.L;
 
     // A causal call whose sequences are all single segments starts every unit
-    // from a zero state: the state pass and the scan are skipped.
+    // from its sequence's state_in (or zero): unless the final state is
+    // wanted, the state pass and the scan are skipped and the output kernel
+    // reads state_in in place of the scan's prefix (unit u is sequence u).
+    // A final state needs every segment's sum, the last one included.
     const bool single_segments = !has_cu && lo.U == nseq;
-    const bool need_state = !causal || !single_segments;
+    const bool need_state = !causal || !single_segments || state_out != nullptr;
+    p.keep_last = state_out != nullptr ? 1 : 0;
+    int prefix_is_zero = 0;
+    if (!need_state) {
+        if (state_in) p.prefix = const_cast<float*>(state_in);   // read only by the output kernels
+        else prefix_is_zero = 1;
+    }
     int n = 0;
     cudaError_t e = cudaSuccess;
     for (int ph = phase_lo; ph <= phase_hi && e == cudaSuccess; ++ph) {
@@ -136,12 +157,13 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
                 }
                 break;
             case LA_PHASE_SCAN:
-                if (T > 0 && need_state) { e = launch_scan(p, s); ++n; }
+                // with a final state to write, empty sequences still need the scan
+                if ((T > 0 || state_out) && need_state) { e = launch_scan(p, s); ++n; }
                 break;
             case LA_PHASE_OUTPUT:
                 if (T > 0) {
-                    e = path == kPathTensor ? tc_out(p, need_state ? 0 : 1, s)
-                                            : simt_out(p, dtype, need_state ? 0 : 1, s);
+                    e = path == kPathTensor ? tc_out(p, prefix_is_zero, s)
+                                            : simt_out(p, dtype, prefix_is_zero, s);
                     ++n;
                 }
                 break;
@@ -160,7 +182,7 @@ la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, c
                         int H, int dk, int dv, int r, float eps, void* out, void* workspace,
                         size_t workspace_bytes, void* stream, int* launched) {
     return forward(causal, phase_lo, phase_hi, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, dk, dv, r, eps,
-                   out, workspace, workspace_bytes, stream, launched);
+                   out, workspace, workspace_bytes, stream, launched, LA_NORM_ATTENTION, nullptr, nullptr);
 }
 
 }  // namespace la
@@ -204,13 +226,43 @@ la_status la_forward_causal(const void* q, const void* k, const void* v, const f
                    d_v, r, eps, out, workspace, workspace_bytes, stream, nullptr);
 }
 
-la_status la_forward_phase(int causal, int phase, const void* q, const void* k, const void* v, const float* omega,
-                           int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k,
-                           int d_v, int r, float eps, void* out, void* workspace, size_t workspace_bytes,
-                           void* stream, int* launched) {
+la_status la_forward_phase(int causal, int phase, int norm, const void* q, const void* k, const void* v,
+                           const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
+                           int H, int d_k, int d_v, int r, float eps, const float* state_in, float* state_out,
+                           void* out, void* workspace, size_t workspace_bytes, void* stream, int* launched) {
     if (phase < LA_PHASE_PLAN || phase > LA_PHASE_OUTPUT) return LA_ERR_INVALID_ARG;
     return forward(causal != 0, phase, phase, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r,
-                   eps, out, workspace, workspace_bytes, stream, launched);
+                   eps, out, workspace, workspace_bytes, stream, launched, norm, state_in, state_out);
+}
+
+la_status la_forward(int causal, int norm, const void* q, const void* k, const void* v, const float* omega,
+                     int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k, int d_v,
+                     int r, float eps, const float* state_in, float* state_out, void* out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    return forward(causal != 0, LA_PHASE_PLAN, LA_PHASE_OUTPUT, q, k, v, omega, map, dtype, cu_seqlens, nseq, T,
+                   H, d_k, d_v, r, eps, out, workspace, workspace_bytes, stream, nullptr, norm, state_in,
+                   state_out);
+}
+
+la_status la_decode_step(const void* q, const void* k, const void* v, const float* omega, int map, int dtype,
+                         int norm, int B, int H, int d_k, int d_v, int r, float eps, float* state, void* out,
+                         void* stream) {
+    if (B < 0) return LA_ERR_INVALID_ARG;
+    la_status st = check_dims(map, dtype, 1, B, H, d_k, d_v, r, true);
+    if (st != LA_OK) return st;
+    if ((st = check_norm(norm, map)) != LA_OK) return st;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (map == LA_MAP_FAVOR && omega == nullptr) return LA_ERR_INVALID_ARG;
+    if (B == 0) return LA_OK;
+    if (!q || !k || !v || !out || !state) return LA_ERR_INVALID_ARG;
+    const size_t esz = dtype == LA_F32 ? 4 : 2;
+    if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(out, esz) || !aligned(state, 4) ||
+        (omega && !aligned(omega, 4)))
+        return LA_ERR_INVALID_ARG;
+    if (decode_smem_bytes(d_k, d_v, r) > kSmemLimitBytes) return LA_ERR_UNSUPPORTED;
+    const cudaError_t e = decode_step(q, k, v, omega, map, dtype, norm, B, H, d_k, d_v, r, eps, state, out,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
 size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq, int64_t T, int H,
@@ -220,7 +272,12 @@ size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, in
     if (path_supported(path, map, d_k, d_v, r) != LA_OK) return 0;
     const int nsm = device_sm_count();
     if (nsm <= 0) return 0;
-    return make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm).total;
+    size_t bytes = make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm).total;
+    // sum normalisation and unaligned operands move a tensor-core call to the
+    // CUDA-core kernels: the size covers both
+    if (path == kPathTensor && path_supported(kPathSimt, map, d_k, d_v, r) == LA_OK)
+        bytes = std::max(bytes, make_layout(kPathSimt, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm).total);
+    return bytes;
 }
 
 la_status la_check_cu_seqlens(const int32_t* cu_seqlens, int nseq, int64_t T, void* stream) {
@@ -274,6 +331,6 @@ const char* la_status_string(la_status status) {
     return "unknown status";
 }
 
-int la_version(void) { return 100; }
+int la_version(void) { return 200; }
 
 }  // extern "C"

@@ -59,7 +59,11 @@ struct FwdParams {
     int H, dk, dv, r, dvx;
     int map;       // la_map
     int causal;
+    int norm;      // la_norm
     float eps;
+    const float* state_in;  // [nseq][H][r][dvx] or NULL: state each sequence starts from
+    float* state_out;       // [nseq][H][r][dvx] or NULL: state after each sequence's last token
+    int keep_last;          // causal: the state pass also sums each sequence's last segment
     // workspace regions
     WsHeader* hdr;
     Unit* units;

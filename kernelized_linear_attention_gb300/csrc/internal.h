@@ -38,6 +38,12 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
 cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
                            cudaStream_t s);
 
+// One-token decode step on CUDA cores (decode.cu).
+size_t decode_smem_bytes(int dk, int dv, int r);
+cudaError_t decode_step(const void* q, const void* k, const void* v, const float* omega, int map, int dtype,
+                        int norm, int B, int H, int dk, int dv, int r, float eps, float* state, void* out,
+                        cudaStream_t s);
+
 // Orthogonal random features (orf.cu).
 cudaError_t orf_build(const double* blocks, const double* lengths, int r, int d, float* omega,
                       cudaStream_t s);

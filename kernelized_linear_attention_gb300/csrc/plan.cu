@@ -112,25 +112,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
 constexpr int kScanThreads = 256;
 constexpr int kScanPerThread = 4;
 
-// grid: (ceil(E / (256*4)), nseq, H)
+// grid: (ceil(E / (256*4)), nseq, H).  Each thread owns elements e of one
+// (sequence, head) state and walks the sequence's units in token order, so
+// state_in may alias state_out: it is read before the same thread writes it.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
     const int s = blockIdx.y, h = blockIdx.z;
     const int u0 = p.seq_first[s], u1 = p.seq_first[s + 1];
-    if (u1 <= u0) return;
     const int64_t E = (int64_t)p.r * p.dvx;
     const int64_t e0 = (int64_t)blockIdx.x * kScanThreads * kScanPerThread + threadIdx.x;
+    const int64_t sbase = ((int64_t)s * p.H + h) * E;
     float acc[kScanPerThread];
 #pragma unroll
-    for (int j = 0; j < kScanPerThread; ++j) acc[j] = 0.f;
+    for (int j = 0; j < kScanPerThread; ++j) {
+        const int64_t e = e0 + j * kScanThreads;
+        acc[j] = (p.state_in != nullptr && e < E) ? p.state_in[sbase + e] : 0.f;
+    }
     if (p.causal) {
         for (int u = u0; u < u1; ++u) {
             const int64_t base = ((int64_t)u * p.H + h) * E;
+            const bool add = u + 1 < u1 || p.keep_last;   // the last unit's sum exists only with keep_last
 #pragma unroll
             for (int j = 0; j < kScanPerThread; ++j) {
                 const int64_t e = e0 + j * kScanThreads;
                 if (e < E) {
                     p.prefix[base + e] = acc[j];
-                    acc[j] += p.partial[base + e];   // (the last unit's sum is never stored)
+                    if (add) acc[j] += p.partial[base + e];
                 }
             }
         }
@@ -150,6 +156,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
                 const int64_t e = e0 + j * kScanThreads;
                 if (e < E) p.prefix[base + e] = acc[j];
             }
+        }
+    }
+    if (p.state_out != nullptr) {
+#pragma unroll
+        for (int j = 0; j < kScanPerThread; ++j) {
+            const int64_t e = e0 + j * kScanThreads;
+            if (e < E) p.state_out[sbase + e] = acc[j];
         }
     }
 }

@@ -94,6 +94,20 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
     }
 }
 
+// Sum normalisation phi'(x) = phi(x) / max(sum_f phi(x)_f, eps) of the first
+// nrows rows of phi ([CS][r] in smem), one warp per row ("The Kernel Zoo" §7.2).
+__device__ void sum_normalise_rows(float* phi, int nrows, int r, float eps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int row = warp; row < nrows; row += NW) {
+        float s = 0.f;
+        for (int f = lane; f < r; f += 32) s += phi[row * r + f];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float inv = 1.0f / fmaxf(s, eps);
+        for (int f = lane; f < r; f += 32) phi[row * r + f] *= inv;
+    }
+}
+
 // Places Omega in shared memory as [d][r] when `om_smem` is set, else reads global [r][d].
 __device__ OmegaView stage_omega(float* om_smem, const float* omega, int d, int r) {
     if (om_smem == nullptr) return OmegaView{omega, 1, d};
@@ -183,8 +197,9 @@ __global__ void __launch_bounds__(NT) state_kernel(FwdParams p, int om_in_smem) 
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
-    // causal: no later segment adds the last segment of a sequence to its prefix
-    if (p.causal && u + 1 == p.seq_first[un.seq + 1]) return;
+    // causal: no later segment adds the last segment of a sequence to its
+    // prefix; only a final state needs its sum
+    if (p.causal && !p.keep_last && u + 1 == p.seq_first[un.seq + 1]) return;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const SmemPlan sp = plan_smem(p.map, p.dk, p.dv, p.r, om_in_smem);
     float* sm = reinterpret_cast<float*>(smem_raw);
@@ -208,6 +223,10 @@ __global__ void __launch_bounds__(NT) state_kernel(FwdParams p, int om_in_smem) 
         __syncthreads();
         compute_phi(phk, xk, hs, om, n, p.map, p.dk, r);
         __syncthreads();
+        if (p.norm == LA_NORM_SUM) {
+            sum_normalise_rows(phk, n, r, p.eps);
+            __syncthreads();
+        }
         for (int e = threadIdx.x; e < E; e += NT) {
             const int f = e / dvx, c = e - f * dvx;
             float acc = S[e];
@@ -263,6 +282,11 @@ __global__ void __launch_bounds__(NT) out_kernel(FwdParams p, int om_in_smem, in
         compute_phi(phq, xq, hsq, om, n, p.map, p.dk, r);
         if (p.causal) compute_phi(phk, xk, hsk, om, n, p.map, p.dk, r);
         __syncthreads();
+        if (p.norm == LA_NORM_SUM) {
+            sum_normalise_rows(phq, n, r, p.eps);
+            if (p.causal) sum_normalise_rows(phk, n, r, p.eps);
+            __syncthreads();
+        }
         if (p.causal) {
             // A[i][j] = phi(q_i) . phi(k_j) for j <= i (diagonal included), one warp per entry
             for (int ij = warp; ij < CS * CS; ij += NW) {
@@ -300,8 +324,9 @@ __global__ void __launch_bounds__(NT) out_kernel(FwdParams p, int om_in_smem, in
         }
         for (int e = threadIdx.x; e < n * dv; e += NT) {
             const int i = e / dv, c = e - i * dv;
-            const float den = fmaxf(num[i * dvx + dv], p.eps);   // max(phi(q)^T z, eps)
-            store_elem(O, ((t0 + i) * p.H + h) * (int64_t)dv + c, num[i * dvx + c] / den);
+            float o = num[i * dvx + c];
+            if (p.norm == LA_NORM_ATTENTION) o /= fmaxf(num[i * dvx + dv], p.eps);   // max(phi(q)^T z, eps)
+            store_elem(O, ((t0 + i) * p.H + h) * (int64_t)dv + c, o);
         }
     }
 }

@@ -320,31 +320,6 @@ __device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves, int 
     }
 }
 
-// out row t = O[t][0..63] / max(O[t][64], eps), bf16, to global (when valid).
-__device__ void store_output(uint32_t tbase, float eps, bool valid, __nv_bfloat16* dst_row, int f = threadIdx.x) {
-    const int warp = f >> 5;
-    uint32_t a[32], b[32], c[16];
-    tmem_ld32(tmem_addr(tbase, warp * 32, kColO), a);
-    tmem_ld32(tmem_addr(tbase, warp * 32, kColO + 32), b);
-    tmem_ld16(tmem_addr(tbase, warp * 32, kColO + 64), c);
-    tmem_ld_wait();
-    if (!valid) return;
-    const float inv = 1.0f / fmaxf(__uint_as_float(c[0]), eps);
-    uint4* dst = reinterpret_cast<uint4*>(dst_row);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]) * inv, __uint_as_float(a[8 * q + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(a[8 * q + 2]) * inv, __uint_as_float(a[8 * q + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(a[8 * q + 4]) * inv, __uint_as_float(a[8 * q + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(a[8 * q + 6]) * inv, __uint_as_float(a[8 * q + 7]) * inv));
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        dst[4 + q] = make_uint4(pack_bf16x2(__uint_as_float(b[8 * q]) * inv, __uint_as_float(b[8 * q + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(b[8 * q + 2]) * inv, __uint_as_float(b[8 * q + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(b[8 * q + 4]) * inv, __uint_as_float(b[8 * q + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(b[8 * q + 6]) * inv, __uint_as_float(b[8 * q + 7]) * inv));
-}
-
 // 32 scores of one row (keys key0 .. key0 + 31) as bf16 hi + lo, two keys per word;
 // keys after `row` are zeroed when the block is on the diagonal.  Adds the kept
 // scores to dsum.
@@ -368,10 +343,11 @@ __device__ __forceinline__ void state_row_bf16(unsigned char* tile, int row, con
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, c)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
-// One output row from registers: O[0..63] / max(den, eps) as bf16 to global.
+// One output row from registers as bf16 to global: O[0..63] / max(den, eps)
+// under attention normalisation, O[0..63] itself without it.
 __device__ __forceinline__ void store_output_row(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t den,
-                                                 float eps, __nv_bfloat16* dst_row) {
-    const float inv = 1.0f / fmaxf(__uint_as_float(den), eps);
+                                                 float eps, bool normalise, __nv_bfloat16* dst_row) {
+    const float inv = normalise ? 1.0f / fmaxf(__uint_as_float(den), eps) : 1.0f;
     uint4* dst = reinterpret_cast<uint4*>(dst_row);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -921,7 +897,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             tmem_ld_wait();
             const float den = dsum + __uint_as_float(dz);
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
-            if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+            if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, p.norm == LA_NORM_ATTENTION, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1175,7 +1151,7 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
             tmem_ld_wait();
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O
             if (tr < min(kC, un.end - t0))
-                store_output_row(o0, o1, den, p.eps, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+                store_output_row(o0, o1, den, p.eps, p.norm == LA_NORM_ATTENTION, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1232,8 +1208,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int u = blockIdx.x, head = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
-    // causal: no later segment adds the last segment of a sequence to its prefix
-    if (p.causal && u + 1 == p.seq_first[un.seq + 1]) return;
+    // causal: no later segment adds the last segment of a sequence to its
+    // prefix; only a final state needs its sum
+    if (p.causal && !p.keep_last && u + 1 == p.seq_first[un.seq + 1]) return;
     StateSmem& s = smem_ref<StateSmem>();
     StateBars& B = s.b;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;

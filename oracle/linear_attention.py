@@ -357,23 +357,25 @@ def rescan(q, k, v, kind, omega=None, cu_seqlens=None, eps=1e-6, eps_mode="clamp
 
 
 def causal_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode="clamp",
-                norm="attention"):
+                norm="attention", state0=None):
     """Causal outputs of selected rows of one sequence [start, end) and head.
 
-    Each requested row i gets S_i = sum_{start <= j <= i} phi(k_j) v_j^T and
-    z_i = sum phi(k_j) computed directly from its definition, so single rows of
-    very long sequences can be checked without running the whole recurrence.
+    Each requested row i gets S_i = S_0 + sum_{start <= j <= i} phi(k_j) v_j^T
+    and z_i = z_0 + sum phi(k_j) computed directly from its definition (S_0,
+    z_0 = state0, the carried state, or zero), so single rows of very long
+    sequences can be checked without running the whole recurrence.
     Returns an array [len(rows), dv].
     """
     kk = np.asarray(k[start:end, head], np.float64)
     vv = np.asarray(v[start:end, head], np.float64)
     pk = features(kk, kind, omega, norm, eps)
+    S0, z0 = (0.0, 0.0) if state0 is None else (np.asarray(state0[0], np.float64), np.asarray(state0[1], np.float64))
     outs = []
     for i in rows:
         j = int(i) - start
         assert 0 <= j < end - start
-        S = pk[: j + 1].T @ vv[: j + 1]
-        z = pk[: j + 1].sum(axis=0)
+        S = S0 + pk[: j + 1].T @ vv[: j + 1]
+        z = z0 + pk[: j + 1].sum(axis=0)
         pq = features(np.asarray(q[int(i), head], np.float64), kind, omega, norm, eps)
         outs.append(_out(pq @ S, np.asarray(pq @ z), eps, eps_mode, norm))
     return np.array(outs)

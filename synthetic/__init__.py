@@ -77,6 +77,10 @@ class Workload:
     eps: float = 1e-6
     equal_lengths: bool = True   # True: a B x N batch (cu_seqlens may be omitted)
     seed: int = DATA_SEED_BASE
+    norm: str = "attention"      # "attention" | "none" | "sum"
+    carry: bool = False          # a state is carried in (state_in) and out (state_out)
+    decode: bool = False         # one-token decode steps: lengths = [1] * B against a carried state
+    n_prior: int = 0             # tokens the carried state stands for (carry / decode)
 
     @property
     def T(self) -> int:
@@ -131,7 +135,47 @@ def workloads() -> dict:
         "dpfp2_causal_b8h8n4096", "causal DPFP-2 (r = 256), B=8, H=8, N=4096, d=64, bf16",
         H=8, dk=64, dv=64, r=256, map="dpfp2", causal=True, dtype="bf16",
         lengths=[4096] * 8, qk_scale=1.0, seed=DATA_SEED_BASE + 5)
+    w["favor_causal_b1h16n65536_carry"] = w["favor_causal_b1h16n65536"].with_(
+        name="favor_causal_b1h16n65536_carry",
+        description="causal FAVOR+ r=256, B=1, H=16, N=65536, d=64, bf16, continuing from a carried state "
+                    "(state_in standing for 65536 earlier tokens) and returning the final state",
+        carry=True, n_prior=65536, seed=DATA_SEED_BASE + 6)
+    w["elu_causal_b8h8n4096_sum"] = w["elu_causal_b8h8n4096"].with_(
+        name="elu_causal_b8h8n4096_sum",
+        description="causal ELU+1 with sum normalisation, B=8, H=8, N=4096, d=64, bf16",
+        norm="sum", seed=DATA_SEED_BASE + 7)
+    w["favor_causal_b1h16n65536_none"] = w["favor_causal_b1h16n65536"].with_(
+        name="favor_causal_b1h16n65536_none",
+        description="causal FAVOR+ r=256, unnormalised output, B=1, H=16, N=65536, d=64, bf16",
+        norm="none", seed=DATA_SEED_BASE + 8)
+    w["favor_decode_b256h16"] = Workload(
+        "favor_decode_b256h16", "one-token causal FAVOR+ decode step, r=256, B=256 sequences, H=16, d=64, "
+        "bf16 q/k/v, fp32 state standing for 4096 earlier tokens (272 MB of state)",
+        H=16, dk=64, dv=64, r=256, map="favor", causal=True, dtype="bf16", lengths=[1] * 256, qk_scale=s,
+        decode=True, n_prior=4096, seed=DATA_SEED_BASE + 9)
     return w
+
+
+def random_state(nseq: int, H: int, r: int, dv: int, seed: int, z_mean: float, n_prior: int) -> np.ndarray:
+    """A carried state [nseq, H, r, dv + 1] fp32 (row f: S[f, 0..dv-1], then z[f])
+    with the magnitudes of sums over n_prior earlier tokens: z[f] = z_mean *
+    n_prior * U(0.5, 1.5) (a sum of positive features whose mean is z_mean) and
+    S[f, c] = z[f] * N(0, 1) / sqrt(n_prior) (feature-weighted sums of N(0, 1)
+    values).  Random numbers only: no attention arithmetic."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    st = np.empty((nseq, H, r, dv + 1), np.float32)
+    z = (z_mean * n_prior * rng.uniform(0.5, 1.5, size=(nseq, H, r))).astype(np.float32)
+    st[..., dv] = z
+    st[..., :dv] = z[..., None] * rng.standard_normal((nseq, H, r, dv), dtype=np.float32) / np.float32(
+        np.sqrt(max(n_prior, 1)))
+    return st
+
+
+def mean_feature(kind: str, r: int) -> float:
+    """Typical mean of one feature for q, k ~ N(0, 1)-scaled inputs: 1/sqrt(r)
+    for FAVOR+ (its features are unbiased for exp(x^T y) with E = 1 per
+    pair, spread over r features), 1 for the element-wise maps."""
+    return 1.0 / np.sqrt(r) if kind == "favor" else 1.0
 
 
 @dataclass

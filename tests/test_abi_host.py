@@ -126,3 +126,62 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 1, 8)
     with pytest.raises(ValueError):
         la.la_forward_causal(x, x, x, "elu1")
+
+
+def _fwd_general(lib, **kw):
+    a = dict(causal=1, norm=0, q=1 << 20, k=1 << 20, v=1 << 20, omega=1 << 20, map=2, dtype=1, cu=None, nseq=1,
+             T=128, H=2, dk=64, dv=64, r=256, eps=1e-6, state_in=None, state_out=None, out=1 << 21, ws=1 << 22,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.la_forward(a["causal"], a["norm"], a["q"], a["k"], a["v"], a["omega"], a["map"], a["dtype"], a["cu"],
+                          a["nseq"], a["T"], a["H"], a["dk"], a["dv"], a["r"], a["eps"], a["state_in"],
+                          a["state_out"], a["out"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("bad,code", [
+    (dict(norm=3), 1), (dict(norm=-1), 1),
+    (dict(norm=2, map=0, r=64), 1),                     # sum normalisation needs non-negative features
+    (dict(state_in=(1 << 23) + 2), 1), (dict(state_out=(1 << 23) + 1), 1),   # fp32 state alignment
+    (dict(map=1, r=256), 1), (dict(omega=None), 1), (dict(eps=-1.0), 1), (dict(ws=None), 1),
+    (dict(dv=512), 2),
+])
+def test_general_forward_rejects_bad_arguments_on_host(lib, causal, bad, code):
+    assert _fwd_general(lib, causal=causal, **bad) == code
+
+
+def _decode(lib, **kw):
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, omega=1 << 20, map=2, dtype=1, norm=0, B=4, H=2, dk=64, dv=64,
+             r=256, eps=1e-6, state=1 << 22, out=1 << 21, stream=None)
+    a.update(kw)
+    return lib.la_decode_step(a["q"], a["k"], a["v"], a["omega"], a["map"], a["dtype"], a["norm"], a["B"], a["H"],
+                              a["dk"], a["dv"], a["r"], a["eps"], a["state"], a["out"], a["stream"])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(B=-1), 1), (dict(H=0), 1), (dict(map=7), 1), (dict(dtype=3), 1), (dict(norm=4), 1),
+    (dict(norm=2, map=0, r=64), 1), (dict(omega=None), 1), (dict(map=1, r=128), 1),
+    (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
+    (dict(state=None), 1), (dict(out=None), 1), (dict(q=None), 1),
+    (dict(state=(1 << 22) + 2), 1), (dict(q=(1 << 20) + 1), 1),
+    (dict(dk=300, r=300, map=1), 2), (dict(r=1024), 2),
+    (dict(B=0), 0),                                     # nothing to do: returns before any launch
+    (dict(B=0, state=None, out=None), 0),
+])
+def test_decode_step_rejects_bad_arguments_on_host(lib, bad, code):
+    assert _decode(lib, **bad) == code
+
+
+def test_binding_checks_state_shapes_and_devices():
+    torch = pytest.importorskip("torch")
+    import kernelized_linear_attention_gb300 as la
+    x = torch.zeros(2, 1, 8)
+    st = torch.zeros(2, 1, 8, 9)
+    with pytest.raises(ValueError):
+        la.la_decode_step(x, x, x, st, "elu1")
+    with pytest.raises(ValueError):
+        la.la_forward(x, x, x, "elu1", norm="sum", state_in=st)
+    from kernelized_linear_attention_gb300._binding import _norm_id
+    assert [_norm_id(n) for n in ("attention", "none", "sum")] == [0, 1, 2]
+    with pytest.raises(KeyError):
+        _norm_id("softmax")

@@ -528,3 +528,15 @@ def test_decode_steps_equal_the_causal_recurrence(norm):
         assert np.allclose(steps.reshape(B * n, H, dv), ref, rtol=1e-12, atol=1e-13)
         Sf, zf = _state_pair(finals, B, H)
         assert np.allclose(S, Sf, rtol=1e-12, atol=1e-14) and np.allclose(z, zf, rtol=1e-12, atol=1e-14)
+
+
+def test_row_sampler_with_carried_state_matches_recurrence():
+    rng = np.random.default_rng(6)
+    T, H, d = 30, 2, 5
+    q, k, v = (rng.standard_normal((T, H, d)) * 0.5 for _ in range(3))
+    om = rng.standard_normal((8, d))
+    S0 = rng.standard_normal((1, H, 8, d)); z0 = rng.uniform(1, 2, size=(1, H, 8))
+    full = oracle.causal(q, k, v, "favor", omega=om, state_in=(S0, z0))
+    rows = [0, 7, 29]
+    got = oracle.causal_rows(q, k, v, "favor", om, 0, T, 1, rows, state0=(S0[0, 1], z0[0, 1]))
+    assert np.allclose(got, full[rows, 1], rtol=1e-12, atol=1e-14)
