@@ -126,33 +126,16 @@ __device__ void decode_phi(float* phq, float* phk, const float* xq, const float*
     }
 }
 
-// NJ = ceil((d_v + 1) / 32) column groups per lane (one instantiation each).
-template <typename TIn, int NJ>
-__global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodeParams p) {
-    constexpr int kRows = kInFlight / NJ < 8 ? kInFlight / NJ : 8;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const DecSmem sp = plan_dec_smem(p.dk, p.dv, p.r);
-    float* sm = reinterpret_cast<float*>(smem_raw);
-    float* xq = sm + sp.xq / 4;
-    float* xk = sm + sp.xk / 4;
-    float* vx = sm + sp.vx / 4;
-    float* phq = sm + sp.phq / 4;
-    float* phk = sm + sp.phk / 4;
-    float* red = sm + sp.red / 4;
-    float* misc = sm + sp.misc / 4;
-    const int b = blockIdx.x, h = blockIdx.y;
+// The new token's side of a step (every thread of the block): q, k and
+// [v | 1] into shared memory, then phi(q) and phi(k) (sum-normalised under
+// LA_NORM_SUM, "The Kernel Zoo" §7.2).  Ends with the block synchronised.
+template <typename TIn>
+__device__ void decode_prologue(const DecodeParams& p, int64_t bh, float* xq, float* xk, float* vx, float* phq,
+                                float* phk, float* misc) {
     const int dk = p.dk, dv = p.dv, dvx = dv + 1, r = p.r;
-    const int64_t bh = (int64_t)b * p.H + h;
     const TIn* Q = static_cast<const TIn*>(p.q) + bh * dk;
     const TIn* K = static_cast<const TIn*>(p.k) + bh * dk;
     const TIn* V = static_cast<const TIn*>(p.v) + bh * dv;
-    float* St = p.state + bh * (int64_t)r * dvx;
-    {
-        // pull this block's state toward L2 while the features are computed
-        const int64_t E = (int64_t)r * dvx;
-        for (int64_t e = (int64_t)threadIdx.x * 32; e < E; e += kDecThreads * 32)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(St + e));
-    }
     for (int c = threadIdx.x; c < dk; c += kDecThreads) {
         xq[c] = load_elem(Q, c);
         xk[c] = load_elem(K, c);
@@ -173,7 +156,6 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodePara
     decode_phi(phq, phk, xq, xk, p.omega, hq, hk, p.map, dk, r);
     __syncthreads();
     if (p.norm == LA_NORM_SUM) {
-        // phi' = phi / max(sum_f phi_f, eps) ("The Kernel Zoo" §7.2)
         float sq = 0.f, sk = 0.f;
         for (int f = threadIdx.x; f < r; f += kDecThreads) { sq += phq[f]; sk += phk[f]; }
         const float iq = 1.0f / fmaxf(block_sum(sq, misc), p.eps);
@@ -181,6 +163,61 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodePara
         for (int f = threadIdx.x; f < r; f += kDecThreads) { phq[f] *= iq; phk[f] *= ik; }
         __syncthreads();
     }
+}
+
+// Per-warp column sums acc -> out = num / max(den, eps) (attention
+// normalisation; column d_v of the numerator is the denominator phi(q)^T z)
+// or num.
+template <typename TIn, int NJ>
+__device__ void decode_epilogue(const DecodeParams& p, int64_t bh, const float (&acc)[NJ], float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int dv = p.dv, dvx = dv + 1;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int c = lane + 32 * j;
+        if (c < dvx) red[warp * dvx + c] = acc[j];
+    }
+    __syncthreads();
+    float den = 0.f;
+    if (p.norm == LA_NORM_ATTENTION) {
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) den += red[w * dvx + dv];
+        den = fmaxf(den, p.eps);
+    }
+    TIn* O = static_cast<TIn*>(p.out) + bh * dv;
+    for (int c = threadIdx.x; c < dv; c += kDecThreads) {
+        float num = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) num += red[w * dvx + c];
+        store_elem(O, c, p.norm == LA_NORM_ATTENTION ? num / den : num);
+    }
+}
+
+// NJ = ceil((d_v + 1) / 32) column groups per lane (one instantiation each).
+template <typename TIn, int NJ>
+__global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodeParams p) {
+    constexpr int kRows = kInFlight / NJ < 8 ? kInFlight / NJ : 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const DecSmem sp = plan_dec_smem(p.dk, p.dv, p.r);
+    float* sm = reinterpret_cast<float*>(smem_raw);
+    float* xq = sm + sp.xq / 4;
+    float* xk = sm + sp.xk / 4;
+    float* vx = sm + sp.vx / 4;
+    float* phq = sm + sp.phq / 4;
+    float* phk = sm + sp.phk / 4;
+    float* red = sm + sp.red / 4;
+    float* misc = sm + sp.misc / 4;
+    const int b = blockIdx.x, h = blockIdx.y;
+    const int dk = p.dk, dv = p.dv, dvx = dv + 1, r = p.r;
+    const int64_t bh = (int64_t)b * p.H + h;
+    float* St = p.state + bh * (int64_t)r * dvx;
+    {
+        // pull this block's state toward L2 while the features are computed
+        const int64_t E = (int64_t)r * dvx;
+        for (int64_t e = (int64_t)threadIdx.x * 32; e < E; e += kDecThreads * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(St + e));
+    }
+    decode_prologue<TIn>(p, bh, xq, xk, vx, phq, phk, misc);
 
     // state update and readout: warp w owns rows f = w, w + 8, ...; lane owns
     // columns lane + 32 j.  A batch of kRows rows is loaded into registers
@@ -225,47 +262,28 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodePara
             }
         }
     }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int c = lane + 32 * j;
-        if (c < dvx) red[warp * dvx + c] = acc[j];
-    }
-    __syncthreads();
-    // column dv of the numerator is the denominator phi(q)^T z
-    float den = 0.f;
-    if (p.norm == LA_NORM_ATTENTION) {
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) den += red[w * dvx + dv];
-        den = fmaxf(den, p.eps);
-    }
-    TIn* O = static_cast<TIn*>(p.out) + bh * dv;
-    for (int c = threadIdx.x; c < dv; c += kDecThreads) {
-        float num = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) num += red[w * dvx + c];
-        store_elem(O, c, p.norm == LA_NORM_ATTENTION ? num / den : num);
-    }
+    decode_epilogue<TIn, NJ>(p, bh, acc, red);
 }
 
 template <typename TIn, int NJ>
-cudaError_t launch_one(dim3 grid, size_t bytes, cudaStream_t s, const DecodeParams& p) {
-    decode_kernel<TIn, NJ><<<grid, kDecThreads, bytes, s>>>(p);
+cudaError_t launch_one(dim3 grid, cudaStream_t s, const DecodeParams& p) {
+    decode_kernel<TIn, NJ><<<grid, kDecThreads, plan_dec_smem(p.dk, p.dv, p.r).total, s>>>(p);
     return cudaGetLastError();
 }
 
 template <typename TIn>
-cudaError_t launch_nj(int nj, dim3 grid, size_t bytes, cudaStream_t s, const DecodeParams& p) {
+cudaError_t launch_nj(int nj, dim3 grid, cudaStream_t s, const DecodeParams& p) {
     static_assert(kMaxColsPerLane == 9, "one case per column-group count");
     switch (nj) {
-        case 1: return launch_one<TIn, 1>(grid, bytes, s, p);
-        case 2: return launch_one<TIn, 2>(grid, bytes, s, p);
-        case 3: return launch_one<TIn, 3>(grid, bytes, s, p);
-        case 4: return launch_one<TIn, 4>(grid, bytes, s, p);
-        case 5: return launch_one<TIn, 5>(grid, bytes, s, p);
-        case 6: return launch_one<TIn, 6>(grid, bytes, s, p);
-        case 7: return launch_one<TIn, 7>(grid, bytes, s, p);
-        case 8: return launch_one<TIn, 8>(grid, bytes, s, p);
-        default: return launch_one<TIn, 9>(grid, bytes, s, p);
+        case 1: return launch_one<TIn, 1>(grid, s, p);
+        case 2: return launch_one<TIn, 2>(grid, s, p);
+        case 3: return launch_one<TIn, 3>(grid, s, p);
+        case 4: return launch_one<TIn, 4>(grid, s, p);
+        case 5: return launch_one<TIn, 5>(grid, s, p);
+        case 6: return launch_one<TIn, 6>(grid, s, p);
+        case 7: return launch_one<TIn, 7>(grid, s, p);
+        case 8: return launch_one<TIn, 8>(grid, s, p);
+        default: return launch_one<TIn, 9>(grid, s, p);
     }
 }
 
@@ -277,10 +295,9 @@ cudaError_t decode_step(const void* q, const void* k, const void* v, const float
                         int norm, int B, int H, int dk, int dv, int r, float eps, float* state, void* out,
                         cudaStream_t s) {
     const DecodeParams p{q, k, v, omega, state, out, map, norm, H, dk, dv, r, eps};
-    const size_t bytes = plan_dec_smem(dk, dv, r).total;
     const dim3 grid((unsigned)B, (unsigned)H);
     const int nj = (dv + 1 + 31) / 32;
-    return dtype == LA_F32 ? launch_nj<float>(nj, grid, bytes, s, p) : launch_nj<__nv_bfloat16>(nj, grid, bytes, s, p);
+    return dtype == LA_F32 ? launch_nj<float>(nj, grid, s, p) : launch_nj<__nv_bfloat16>(nj, grid, s, p);
 }
 
 }  // namespace la

@@ -345,3 +345,27 @@ def test_full_size_carry_workload_sampled(la):
         M_end = np.abs(S0) + pk.T @ np.abs(vv)
         _assert_state(st_out[0, h], np.concatenate([S_end, z_end[:, None]], axis=-1),
                       np.concatenate([M_end, z_end[:, None]], axis=-1), True, f"final state head {h}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_step_unaligned_state_and_odd_r(la, dtype):
+    """A state that is only 4-byte aligned, or r not a multiple of 4, cannot be
+    moved by 16-byte bulk copies: the step then runs the register-staged
+    kernel, which must give the same results."""
+    B, H, dk, dv = 3, 2, 16, 20
+    for r, offset in ((32, 1), (30, 0), (30, 3)):
+        om = omega_for(r, dk)
+        inp = synthetic.random_inputs([1] * B, H=H, dk=dk, dv=dv, dtype=dtype, seed=36, qk_scale=dk ** -0.25)
+        st = synthetic.random_state(B, H, r, dv, seed=37, z_mean=r ** -0.5, n_prior=80)
+        store = torch.zeros(st.size + 4, dtype=torch.float32, device="cuda")
+        st_t = store[offset:offset + st.size].view(st.shape)
+        st_t.copy_(torch.from_numpy(st))
+        q, k, v = to_torch(inp)
+        out = la.la_decode_step(q, k, v, st_t, "favor", omega=torch.from_numpy(om).cuda())
+        torch.cuda.synchronize()
+        S, z = _pair(st)
+        ref, S2, z2 = oracle.decode_step(inp.q, inp.k, inp.v, "favor", S, z, omega=om)
+        assert_close(from_torch(out), ref, dtype, f"decode r={r} offset={offset}")
+        _assert_state(st_t.cpu().numpy(), np.concatenate([S2, z2[..., None]], axis=-1), None, False,
+                      f"decode state r={r} offset={offset}")
+        assert torch.count_nonzero(store[:offset]) == 0 and torch.count_nonzero(store[offset + st.size:]) == 0
