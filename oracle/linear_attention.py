@@ -36,7 +36,10 @@ the source pages, one sequence and one head at a time:
 * a state carried in from an earlier segment of each sequence and out to the
   next ("The Kernel Zoo" §9.3, fast weights carried across training segments),
   and the one-token decode step of the recurrence ("Reassociate a feature-map
-  kernel", ¶4).
+  kernel", ¶4);
+* the backward pass: gradients of sum(dout * out) with respect to q, k and v,
+  by the chain rule on the quadratic form ("Reassociate a feature-map kernel",
+  ¶5: errors in outputs and gradients).
 
 Every function here is pinned by tests against values the pages print,
 closed forms or brute force (see tests/test_oracle_pins.py).
@@ -389,6 +392,106 @@ def bidir_rows(q, k, v, kind, omega, start, end, head, rows, eps=1e-6, eps_mode=
     z = pk.sum(axis=0)
     pq = features(np.asarray(q[np.asarray(rows, int), head], np.float64), kind, omega, norm, eps)
     return _out(pq @ S, pq @ z, eps, eps_mode, norm)
+
+
+def feature_map_vjp(x, kind: str, omega, dphi) -> np.ndarray:
+    """dL/dx given dL/dphi for phi = feature_map(x) (the chain rule through each map).
+
+    identity: dx = dphi.  elu1: phi' = 1 for x > 0, exp(x) otherwise.
+    favor: d phi_f / dx = phi_f (omega_f - x), so dx = Omega^T (dphi * phi)
+           - x sum_f dphi_f phi_f.
+    dpfp<nu>: phi_f = x~_a x~_b with b = (a + s) mod 2d gives dx~_a += dphi_f
+           x~_b and dx~_b += dphi_f x~_a; x~ = relu([x, -x]) passes dx~_i for
+           x_i > 0 and -dx~_{i+d} for x_i < 0.
+    """
+    x = np.asarray(x, np.float64)
+    dphi = np.asarray(dphi, np.float64)
+    nu = dpfp_nu(kind)
+    if kind == "identity":
+        return dphi.copy()
+    if kind == "elu1":
+        return dphi * np.where(x > 0, 1.0, np.exp(np.minimum(x, 0.0)))
+    if kind == "favor":
+        om = np.asarray(omega, np.float64)
+        u = dphi * feature_map(x, "favor", om)
+        return u @ om - x * u.sum(axis=-1, keepdims=True)
+    if nu is not None:
+        d = x.shape[-1]
+        xt = np.maximum(np.concatenate([x, -x], axis=-1), 0.0)
+        dxt = np.zeros_like(xt)
+        for s_ in range(1, nu + 1):
+            g = dphi[..., (s_ - 1) * 2 * d:s_ * 2 * d]
+            partner = np.roll(xt, -s_, axis=-1)           # x~_{(i+s) mod 2d}
+            dxt += g * partner                              # d/dx~_a of x~_a x~_b
+            dxt += np.roll(g * xt, s_, axis=-1)             # d/dx~_b, moved back to index b
+        return dxt[..., :d] * (x > 0) - dxt[..., d:] * (x < 0)
+    raise ValueError(kind)
+
+
+def features_vjp(x, kind: str, omega, norm: str, eps: float, dfeat) -> np.ndarray:
+    """dL/dx given dL/dphi' for the features attention uses (sum-normalised
+    under norm "sum": phi' = phi / sigma, sigma = max(sum_f phi_f, eps), so
+    dphi = (dphi' - (dphi' . phi') 1) / sigma when the sum exceeds eps and
+    dphi' / eps when it was clamped)."""
+    dfeat = np.asarray(dfeat, np.float64)
+    if norm == "sum":
+        phi = feature_map(x, kind, omega)
+        tot = phi.sum(axis=-1, keepdims=True)
+        sig = np.maximum(tot, eps)
+        p = phi / sig
+        dot = np.where(tot > eps, (dfeat * p).sum(axis=-1, keepdims=True), 0.0)
+        dphi = (dfeat - dot) / sig
+    else:
+        dphi = dfeat
+    return feature_map_vjp(x, kind, omega, dphi)
+
+
+def backward(q, k, v, dout, kind, causal_form, omega=None, cu_seqlens=None, eps=1e-6, norm="attention"):
+    """Gradients (dq, dk, dv) of L = sum(dout * out) for the forward of the
+    same arguments ("Reassociate a feature-map kernel" ¶5 asks for errors in
+    outputs and gradients), from the quadratic form of one sequence and head:
+    W = Phi_Q Phi_K^T (lower triangle, diagonal included, when causal),
+    num = W V, den = W 1, out = num / max(den, eps).  By the chain rule
+    dnum = dout / max(den, eps), dden = -(dout . out) / den where den > eps
+    (0 where the clamp holds), dW = dnum V^T + dden 1^T (masked like W),
+    dPhi_Q = dW Phi_K, dPhi_K = dW^T Phi_Q, dV = W^T dnum; then through the
+    features (features_vjp).  norm "none" and "sum" have dnum = dout and no
+    denominator term.  Omega is a constant (sampled once and frozen).
+    """
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    T, H, dk_ = q.shape
+    cu = _bounds(cu_seqlens, T)
+    dq = np.zeros_like(q); dk = np.zeros_like(k); dv = np.zeros_like(v)
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            continue
+        for h in range(H):
+            pq = features(q[a:b, h], kind, omega, norm, eps)
+            pk = features(k[a:b, h], kind, omega, norm, eps)
+            W = pq @ pk.T
+            if causal_form:
+                W = np.tril(W)
+            vv = v[a:b, h]
+            g = dout[a:b, h]
+            num = W @ vv
+            den = W.sum(axis=1)
+            if norm == "attention":
+                dc = np.maximum(den, eps)
+                out = num / dc[:, None]
+                dnum = g / dc[:, None]
+                dden = np.where(den > eps, -(g * out).sum(axis=1) / np.where(den > eps, den, 1.0), 0.0)
+            else:
+                dnum = g
+                dden = np.zeros(b - a)
+            dW = dnum @ vv.T + dden[:, None]
+            if causal_form:
+                dW = np.tril(dW)
+            dq[a:b, h] = features_vjp(q[a:b, h], kind, omega, norm, eps, dW @ pk)
+            dk[a:b, h] = features_vjp(k[a:b, h], kind, omega, norm, eps, dW.T @ pq)
+            dv[a:b, h] = W.T @ dnum
+    return dq, dk, dv
 
 
 def forward(q, k, v, kind, causal_form, omega=None, cu_seqlens=None, eps=1e-6, norm="attention",

@@ -540,3 +540,89 @@ def test_row_sampler_with_carried_state_matches_recurrence():
     rows = [0, 7, 29]
     got = oracle.causal_rows(q, k, v, "favor", om, 0, T, 1, rows, state0=(S0[0, 1], z0[0, 1]))
     assert np.allclose(got, full[rows, 1], rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# Backward pass
+# ----------------------------------------------------------------------------
+def _loss(q, k, v, dout, kind, causal_form, om, cu, norm):
+    return float(np.sum(dout * oracle.forward(q, k, v, kind, causal_form, omega=om, cu_seqlens=cu, norm=norm)))
+
+
+def _finite_difference_grads(q, k, v, dout, kind, causal_form, om, cu, norm, h=1e-6):
+    grads = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(args[which])
+        it = np.nditer(args[which], flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            base = args[which][i]
+            args[which][i] = base + h
+            lp = _loss(*args, dout, kind, causal_form, om, cu, norm)
+            args[which][i] = base - h
+            lm = _loss(*args, dout, kind, causal_form, om, cu, norm)
+            args[which][i] = base
+            g[i] = (lp - lm) / (2 * h)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("kind", ["identity", "elu1", "favor", "dpfp1"])
+@pytest.mark.parametrize("causal_form", [True, False])
+@pytest.mark.parametrize("norm", ["attention", "none", "sum"])
+def test_backward_matches_finite_differences(kind, causal_form, norm):
+    """Central differences of sum(dout * out), element by element, on tiny
+    packed inputs (two sequences, one of them a single token)."""
+    if kind == "identity" and norm == "sum":
+        pytest.skip("sum normalisation needs non-negative features")
+    rng = np.random.default_rng(41)
+    lengths = [4, 1]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, d, dv = cu[-1], 1, 3, 2
+    q, k = (rng.standard_normal((T, H, d)) * 0.7 for _ in range(2))
+    if kind == "identity":   # keep the identity-map denominators well away from the eps clamp
+        q, k = np.abs(q) + 0.2, np.abs(k) + 0.2
+    v = rng.standard_normal((T, H, dv))
+    dout = rng.standard_normal((T, H, dv))
+    om = rng.standard_normal((5, d))
+    got = oracle.backward(q, k, v, dout, kind, causal_form, omega=om, cu_seqlens=cu, norm=norm)
+    want = _finite_difference_grads(q, k, v, dout, kind, causal_form, om, cu, norm)
+    for g, w, name in zip(got, want, ("dq", "dk", "dv")):
+        scale = max(1.0, np.abs(w).max())
+        assert np.allclose(g, w, rtol=0, atol=2e-7 * scale), f"{name}: {np.abs(g - w).max():.2e}"
+
+
+def test_backward_value_gradient_sums_to_upstream_gradient():
+    """Attention-normalised outputs are convex combinations of the values
+    (weights w_ij / den_i summing to 1 over j), so sum_j dL/dv_j equals
+    sum_i dL/dout_i within every sequence and head."""
+    rng = np.random.default_rng(42)
+    lengths = [6, 3]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, d = cu[-1], 2, 4
+    q, k = (rng.standard_normal((T, H, d)) * 0.5 for _ in range(2))
+    v, dout = (rng.standard_normal((T, H, 3)) for _ in range(2))
+    om = rng.standard_normal((8, d))
+    for causal_form in (True, False):
+        _, _, dv = oracle.backward(q, k, v, dout, "favor", causal_form, omega=om, cu_seqlens=cu)
+        for s in range(2):
+            a, b = cu[s], cu[s + 1]
+            assert np.allclose(dv[a:b].sum(axis=0), dout[a:b].sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_backward_of_packed_batch_equals_each_sequence_alone():
+    rng = np.random.default_rng(43)
+    lengths = [5, 0, 4]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T, H, d = cu[-1], 2, 3
+    q, k, v, dout = (rng.standard_normal((T, H, d)) * 0.6 for _ in range(4))
+    om = rng.standard_normal((6, d))
+    packed = oracle.backward(q, k, v, dout, "favor", True, omega=om, cu_seqlens=cu)
+    for s in range(3):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            continue
+        alone = oracle.backward(q[a:b], k[a:b], v[a:b], dout[a:b], "favor", True, omega=om)
+        for x, y in zip(packed, alone):
+            assert np.array_equal(x[a:b], y)
