@@ -45,8 +45,11 @@ KERNEL_SOURCES = {"tc": {"output": "tc.cu", "state": "tc.cu", "scan": "plan.cu",
                            "decode": "decode.cu"}}
 # second measured line: the bidirectional state pass (phi(k)^T [v|1] over every token)
 BIDIR_WORKLOAD = "favor_bidir_b4h8n16384"
-# the decode-step line of the default run
+# the decode-step and backward lines of the default run
 DECODE_WORKLOAD = "favor_decode_b256h16"
+BACKWARD_WORKLOAD = "favor_causal_b4h8n4096_bwd"
+# fp32 FMA peak of the CUDA-core kernels: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def parse_args(argv=None):
@@ -442,6 +445,7 @@ def run_ours(args):
         line["bidir_state_pass"] = bidir_state_pass(la, dev, stream, peaks, K)
         line["variants"] = forward_variants(la, dev, stream, peaks, K, w, (dq, dk_, dvv), omega)
         line["decode_step"] = decode_line(la, dev, stream, peaks, max(3, min(K, 20)), DECODE_WORKLOAD)
+        line["backward"] = backward_line(la, dev, stream, max(3, min(K, 10)), BACKWARD_WORKLOAD)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
     if rank == 0:
@@ -605,6 +609,60 @@ def decode_line(la, dev, stream, peaks, steps, name, warmup=3, world=1, e2e_step
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "ms_per_step": e2e_ms}
     return {"workload": w.name, "ms": ms, "tokens_per_s": B / (ms * 1e-3), "launches": steps,
             "roofline": roof, "e2e": e2e, "clocks": clocks}
+
+
+def backward_flops(w: synthetic.Workload) -> int:
+    """Algorithmic FLOPs of the backward per token-head: the features of q and
+    k (FAVOR+: 2 * 2 d r) and their chain rule (2 * 2 d r), the output
+    recomputed (readout and state, 2 * 2 r (d_v + 1)), dphi(q) = S g, the
+    reverse sum R, dphi(k) = R [v|1] (3 * 2 r (d_v + 1)) and dv = R^T phi(k)
+    (2 r d_v)."""
+    dvx = w.dv + 1
+    proj = 8 * w.dk * w.r if w.map == "favor" else 0
+    return proj + 10 * w.r * dvx + 2 * w.r * w.dv - 2 * w.r
+
+
+def backward_line(la, dev, stream, steps, name, warmup=3, world=1) -> dict:
+    """la_backward on a backward workload, timed with CUDA events on the
+    launching stream; inputs (q, k, v, dout: 134 MB) and the 268 MB of fp32
+    workspace rows exceed L2."""
+    import torch
+    w = synthetic.workloads()[name]
+    inputs = synthetic.make_qkv(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(tdt).to(dev)  # noqa: E731
+    q, k, v = (to(inputs.storage(n)) for n in ("q", "k", "v"))
+    rng = np.random.Generator(np.random.PCG64(w.seed + 1))
+    dout_np = synthetic.quantise(rng.standard_normal(inputs.v.shape).astype(np.float32), w.dtype)
+    dout = to(dout_np if w.dtype == "f32" else synthetic.bf16_bits(dout_np).view(np.int16))
+    omega = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), w.r)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = la.la_backward_workspace_bytes(w.causal, w.map, tdt, False, w.nseq, w.T, w.H, w.dk, w.dv, w.r)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    call = lambda: la.la_backward(q, k, v, dout, w.map, omega=omega, causal=w.causal, norm=w.norm,  # noqa: E731
+                                  nseq=w.nseq, eps=w.eps, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    if la.la_workspace_error(ws) != 0:
+        raise RuntimeError("device error in the backward warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    flops = backward_flops(w) * w.T * w.H
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "ms": ms, "tokens_per_s": w.T / (ms * 1e-3), "launches_per_call": 6,
+            "path": "cuda-core fp32",
+            "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                         "frac": tf / FP32_ALU_TFLOPS, "alg_flops_per_call": flops,
+                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz"}}
 
 
 def bidir_state_pass(la, dev, stream, peaks, steps: int) -> dict:

@@ -198,6 +198,35 @@ LA_API la_status la_decode_step(const void* q, const void* k, const void* v, con
                                 float* state, void* out, void* stream);
 
 /*
+ * la_backward - gradients of L = sum(dout * out) with respect to q, k and v,
+ *   where out is what la_forward(causal, norm, ...) returns for the same
+ *   arguments without a carried state ("Reassociate a feature-map kernel" ¶5
+ *   asks for errors in gradients as well as outputs).  With g_i the gradient
+ *   with respect to num_i | den_i (dout_i / max(den_i, eps) and
+ *   -(dout_i . out_i) / den_i, 0 where the clamp holds; dout_i and 0 without
+ *   attention normalisation): dphi(q_i) = S_i g_i, dphi(k_j) = R_j [v_j | 1],
+ *   dv_j = R_j^T phi(k_j) restricted to the first d_v entries, with S_i the
+ *   forward state and R_j = sum_{i >= j} phi(q_i) g_i^T (every i for the
+ *   bidirectional form), then the chain rule through the feature map (and the
+ *   sum normalisation).  Omega is treated as a constant.
+ *   dout: [T, H, d_v]; dq, dk: [T, H, d_k]; dv: [T, H, d_v], all of `dtype`,
+ *   written for every row; must not overlap the inputs or each other.
+ *   workspace: at least la_backward_workspace_bytes(...) bytes, 256-byte
+ *   aligned.  Computed in fp32 on CUDA cores for every dtype (bf16 gradients
+ *   are rounded once); the output is recomputed, not read.  Other arguments
+ *   and errors as for la_forward.
+ */
+LA_API la_status la_backward(int causal, int norm, const void* q, const void* k, const void* v,
+                             const float* omega, int map, int dtype, const int32_t* cu_seqlens,
+                             int nseq, int64_t T, int H, int d_k, int d_v, int r, float eps,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* la_backward_workspace_bytes - scratch size for la_backward (0 for arguments it rejects). */
+LA_API size_t la_backward_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq,
+                                          int64_t T, int H, int d_k, int d_v, int r);
+
+/*
  * la_forward_phase - one phase of a forward call, for callers that time or
  *   interleave the kernels.  la_forward (and so la_forward_bidir /
  *   la_forward_causal) is exactly phases LA_PHASE_PLAN .. LA_PHASE_OUTPUT

@@ -49,6 +49,9 @@ def load_library():
         "la_forward_phase": ([_c_int, _c_int, _c_int] + fwd_args[:14] + [_vp, _vp] + fwd_args[14:]
                              + [ctypes.POINTER(_c_int)], _c_int),
         "la_forward": ([_c_int, _c_int] + fwd_args[:14] + [_vp, _vp] + fwd_args[14:], _c_int),
+        "la_backward": ([_c_int, _c_int] + fwd_args[:14] + [_vp, _vp, _vp, _vp] + fwd_args[15:], _c_int),
+        "la_backward_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int,
+                                         _c_int], _c_size),
         "la_decode_step": ([_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_float, _vp, _vp, _vp], _c_int),
         "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
@@ -298,6 +301,48 @@ def la_decode_step(q, k, v, state, map, omega=None, norm="attention", eps=1e-6, 
         _ptr(q), _ptr(k), _ptr(v), _ptr(omega), _map_id(map), DTYPE_IDS[q.dtype], _norm_id(norm), B, H, d_k, d_v,
         r, eps, _ptr(state), _ptr(out), _stream(stream)))
     return out
+
+
+def la_backward_workspace_bytes(causal: bool, map, dtype, has_cu_seqlens: bool, nseq: int, T: int, H: int,
+                                d_k: int, d_v: int, r: int) -> int:
+    dt = DTYPE_IDS[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return load_library().la_backward_workspace_bytes(int(causal), _map_id(map), dt, int(has_cu_seqlens), nseq, T,
+                                                      H, d_k, d_v, r)
+
+
+def la_backward(q, k, v, dout, map, omega=None, causal=True, norm="attention", cu_seqlens=None, nseq=None,
+                eps=1e-6, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) for the forward with the same
+    arguments; allocates what is not given."""
+    _need(q, "q"); _need(k, "k"); _need(v, "v"); _need(dout, "dout")
+    if q.dtype not in DTYPE_IDS or any(t.dtype != q.dtype for t in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share dtype float32 or bfloat16")
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    m = _map_id(map)
+    r = _feature_dim(map, d_k, omega)
+    if omega is not None:
+        _need(omega, "omega", torch.float32)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        nseq = cu_seqlens.numel() - 1
+    elif nseq is None:
+        nseq = 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, name, q.dtype)
+    need = la_backward_workspace_bytes(causal, m, q.dtype, cu_seqlens is not None, nseq, T, H, d_k, d_v, r)
+    if need == 0:
+        raise LinAttnError("la_backward_workspace_bytes", 1)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("la_backward", load_library().la_backward(
+        int(causal), _norm_id(norm), _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype],
+        _ptr(cu_seqlens), nseq, T, H, d_k, d_v, r, eps, _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
 
 
 def attention(q, k, v, map="favor", omega=None, causal=True, cu_seqlens=None, nseq=None, eps=1e-6,

@@ -58,7 +58,7 @@ la_status path_supported(int path, int map, int dk, int dv, int r) {
 // Segment length and unit bound.  Equal-length batches split every sequence
 // into the same number of segments so that units * heads fills the SMs;
 // packed batches (lengths only known on the device) use one length for all.
-Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm) {
+Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm, bool bwd = false) {
     Layout lo{};
     const int64_t C = path_chunk(path);
     int64_t L, U;
@@ -81,6 +81,10 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     const size_t state_bytes = sizeof(float) * (size_t)U * H * r * lo.dvx;
     lo.partial = o;   o = align_up(o + state_bytes, kAlign);
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
+    if (bwd) {
+        lo.suffix = o; o = align_up(o + state_bytes, kAlign);
+        lo.g = o;      o = align_up(o + sizeof(float) * (size_t)T * H * lo.dvx, kAlign);
+    }
     lo.total = o;
     return lo;
 }
@@ -175,6 +179,77 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
+// The backward pass (always the fp32 CUDA-core kernels): plan, forward state
+// pass and scan (the state entering every segment), bwd_q (g, dq, per-segment
+// sums of phi(q) g^T), reverse scan (those sums over the later segments),
+// bwd_kv (dk, dv).
+la_status backward(int causal, int norm, const void* q, const void* k, const void* v, const float* omega, int map,
+                   int dtype, const int32_t* cu_seqlens, int nseq, int64_t T, int H, int dk, int dv, int r,
+                   float eps, const void* dout, void* dq, void* dkk, void* dvv, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    const bool has_cu = cu_seqlens != nullptr;
+    la_status st = check_dims(map, dtype, nseq, T, H, dk, dv, r, has_cu);
+    if (st != LA_OK) return st;
+    if ((st = check_norm(norm, map)) != LA_OK) return st;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (map == LA_MAP_FAVOR && omega == nullptr) return LA_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned(workspace, kAlign)) return LA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !dout || !dq || !dkk || !dvv)) return LA_ERR_INVALID_ARG;
+    const size_t esz = dtype == LA_F32 ? 4 : 2;
+    for (const void* ptr : {q, k, v, dout, static_cast<const void*>(dq), static_cast<const void*>(dkk),
+                            static_cast<const void*>(dvv)})
+        if (!aligned(ptr, esz)) return LA_ERR_INVALID_ARG;
+    if (omega && !aligned(omega, 4)) return LA_ERR_INVALID_ARG;
+    if (bwd_smem_bytes(dk, dv, r) > kSmemLimitBytes || path_supported(kPathSimt, map, dk, dv, r) != LA_OK)
+        return LA_ERR_UNSUPPORTED;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return LA_ERR_CUDA;
+    const Layout lo = make_layout(kPathSimt, has_cu, nseq, T, H, dv, r, nsm, true);
+    if (workspace_bytes < lo.total) return LA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.omega = omega; p.out = nullptr;
+    p.cu_seqlens = cu_seqlens; p.nseq = nseq; p.T = T;
+    p.H = H; p.dk = dk; p.dv = dv; p.r = r; p.dvx = lo.dvx;
+    p.map = map; p.causal = causal; p.norm = norm; p.eps = eps;
+    p.dout = dout; p.dq_out = dq; p.dk_out = dkk; p.dv_out = dvv;
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.units = reinterpret_cast<Unit*>(ws + lo.units);
+    p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
+    p.partial = reinterpret_cast<float*>(ws + lo.partial);
+    p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
+    p.suffix = reinterpret_cast<float*>(ws + lo.suffix);
+    p.g = reinterpret_cast<float*>(ws + lo.g);
+    p.U = lo.U; p.L = lo.L;
+    cudaError_t e = launch_plan(p, s);
+    if (e != cudaSuccess || T == 0) return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    const bool single_segments = !has_cu && lo.U == nseq;
+    const bool need_state = !causal || !single_segments;
+    if (need_state) {
+        if ((e = simt_state(p, dtype, s)) != cudaSuccess) return LA_ERR_CUDA;
+        if ((e = launch_scan(p, s)) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    if ((e = bwd_q(p, dtype, need_state ? 0 : 1, s)) != cudaSuccess) return LA_ERR_CUDA;
+    FwdParams pr = p;           // suffix sums: scan of the bwd_q partials, written to the suffix buffer
+    pr.prefix = p.suffix;
+    pr.reverse = 1;
+    pr.keep_last = 1;
+    if ((e = launch_scan(pr, s)) != cudaSuccess) return LA_ERR_CUDA;
+    if ((e = bwd_kv(p, dtype, s)) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+size_t backward_workspace_bytes(int causal, int map, int dtype, int has_cu, int nseq, int64_t T, int H, int dk,
+                                int dv, int r) {
+    (void)causal;
+    if (check_dims(map, dtype, nseq, T, H, dk, dv, r, has_cu != 0) != LA_OK) return 0;
+    if (bwd_smem_bytes(dk, dv, r) > kSmemLimitBytes) return 0;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return 0;
+    return make_layout(kPathSimt, has_cu != 0, nseq, T, H, dv, r, nsm, true).total;
+}
+
 }  // namespace
 
 la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, const void* k, const void* v,
@@ -263,6 +338,19 @@ la_status la_decode_step(const void* q, const void* k, const void* v, const floa
     const cudaError_t e = decode_step(q, k, v, omega, map, dtype, norm, B, H, d_k, d_v, r, eps, state, out,
                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+la_status la_backward(int causal, int norm, const void* q, const void* k, const void* v, const float* omega, int map,
+                      int dtype, const int32_t* cu_seqlens, int nseq, int64_t T, int H, int d_k, int d_v, int r,
+                      float eps, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return backward(causal != 0, norm, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r, eps, dout,
+                    dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+size_t la_backward_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq, int64_t T, int H,
+                                   int d_k, int d_v, int r) {
+    return backward_workspace_bytes(causal, map, dtype, has_cu_seqlens, nseq, T, H, d_k, d_v, r);
 }
 
 size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, int nseq, int64_t T, int H,

@@ -1,0 +1,438 @@
+// Backward pass of kernelized attention on CUDA cores (fp32 for every dtype):
+// gradients of L = sum(dout * out) with respect to q, k and v.
+//
+// With [v | 1] as the values (so num | den is one product) and g_i the
+// gradient of L with respect to num_i | den_i,
+//
+//     g_i = [dout_i / max(den_i, eps) | -(dout_i . out_i) / den_i]   (attention
+//           normalisation; the last entry is 0 where the clamp holds)
+//     g_i = [dout_i | 0]                                              (none, sum)
+//
+// the chain rule through num_i = sum_{j<=i} (phi(q_i) . phi(k_j)) [v_j | 1]
+// gives, with S_i = sum_{j<=i} phi(k_j) [v_j | 1]^T (the forward state) and
+// R_j = sum_{i>=j} phi(q_i) g_i^T (the same sum run backwards in time):
+//
+//     dphi(q_i) = S_i g_i,   dphi(k_j) = R_j [v_j | 1],   dv_j = (R_j^T phi(k_j))[:d_v]
+//
+// (j over the whole sequence, and S, R the whole-sequence sums, for the
+// bidirectional form), then dq, dk through the feature map.  Omega is a
+// constant.  The causal form runs as a chunked scan in both directions: the
+// forward state pass and scan give S at every segment start; bwd_q_kernel
+// walks each segment forwards, recomputing num | den to form g (kept in the
+// workspace), writing dq and summing phi(q) g^T of the segment; a reverse scan
+// gives R at every segment end; bwd_kv_kernel walks each segment backwards and
+// writes dk and dv.  ("Reassociate a feature-map kernel" ¶5 asks for errors
+// in gradients as well as outputs; the recurrence is that of "The Kernel Zoo"
+// §1.3.)
+#include "simt_common.cuh"
+
+namespace la {
+
+namespace {
+
+struct BwdSmem {
+    size_t st, racc, xq, xk, phq, phk, dph, vx, gg, num, go, a, gm, hsq, hsk, sgq, sgk, su, total;
+};
+
+__host__ __device__ inline size_t bfl(size_t n) { return (n * sizeof(float) + 15) / 16 * 16; }
+
+// `racc`: bwd_q_kernel's running sum of phi(q) g^T (bwd_kv_kernel needs none).
+__host__ __device__ inline BwdSmem plan_bwd_smem(int dk, int dv, int r, bool racc) {
+    BwdSmem s{};
+    size_t o = 0;
+    const int dvx = dv + 1;
+    s.st = o;   o += bfl((size_t)r * dvx);
+    s.racc = o; o += racc ? bfl((size_t)r * dvx) : 0;
+    s.xq = o;   o += bfl((size_t)CS * dk);
+    s.xk = o;   o += bfl((size_t)CS * dk);
+    s.phq = o;  o += bfl((size_t)CS * r);
+    s.phk = o;  o += bfl((size_t)CS * r);
+    s.dph = o;  o += bfl((size_t)CS * r);
+    s.vx = o;   o += bfl((size_t)CS * dvx);
+    s.gg = o;   o += bfl((size_t)CS * dvx);
+    s.num = o;  o += bfl((size_t)CS * dvx);
+    s.go = o;   o += bfl((size_t)CS * dv);
+    s.a = o;    o += bfl((size_t)CS * CS);
+    s.gm = o;   o += bfl((size_t)CS * CS);
+    s.hsq = o;  o += bfl(CS);
+    s.hsk = o;  o += bfl(CS);
+    s.sgq = o;  o += bfl(CS);
+    s.sgk = o;  o += bfl(CS);
+    s.su = o;   o += bfl(CS);
+    s.total = o;
+    return s;
+}
+
+// Sum normalisation of the first nrows rows that keeps each row's raw sum
+// (the backward pass needs it): phi' = phi / max(sum, eps).
+__device__ void sum_normalise_keep(float* phi, float* raw_sum, int nrows, int r, float eps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int row = warp; row < nrows; row += NW) {
+        float s = 0.f;
+        for (int f = lane; f < r; f += 32) s += phi[row * r + f];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) raw_sum[row] = s;
+        const float inv = 1.0f / fmaxf(s, eps);
+        for (int f = lane; f < r; f += 32) phi[row * r + f] *= inv;
+    }
+}
+
+// dx of nrows rows from dph = dL/dphi' (overwritten): first through the sum
+// normalisation (norm LA_NORM_SUM: dphi = (dphi' - (dphi' . phi') 1) / sigma,
+// or dphi' / eps where the sum was clamped; phi is turned back into the raw
+// features), then through the map:
+//   identity  dx = dphi;  ELU+1  dx = dphi * (x > 0 ? 1 : exp(x));
+//   FAVOR+    u = dphi * phi, dx = Omega^T u - x sum_f u_f;
+//   DPFP-nu   phi_f = x~_a x~_b (b = (a + s) mod 2d) sends dphi_f x~_b to x~_a
+//             and dphi_f x~_a to x~_b; x~ = relu([x, -x]).
+// Writes dx rows row0.. of head h to global (dtype of TOut).
+template <typename TOut>
+__device__ void features_vjp_rows(float* dph, float* phi, const float* x, const float* raw_sum, float* su,
+                                  int nrows, const FwdParams& p, const OmegaView om, TOut* dst, int64_t row0,
+                                  int h) {
+    const int r = p.r, d = p.dk;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (p.norm == LA_NORM_SUM) {
+        for (int row = warp; row < nrows; row += NW) {
+            float dot = 0.f;
+            for (int f = lane; f < r; f += 32) dot = fmaf(dph[row * r + f], phi[row * r + f], dot);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float raw = raw_sum[row];
+            const float sig = fmaxf(raw, p.eps);
+            const float sub = raw > p.eps ? dot : 0.f;
+            for (int f = lane; f < r; f += 32) {
+                dph[row * r + f] = (dph[row * r + f] - sub) / sig;
+                phi[row * r + f] *= sig;
+            }
+        }
+        __syncthreads();
+    }
+    if (p.map == LA_MAP_FAVOR) {
+        for (int row = warp; row < nrows; row += NW) {
+            float s = 0.f;
+            for (int f = lane; f < r; f += 32) {
+                const float u = dph[row * r + f] * phi[row * r + f];
+                dph[row * r + f] = u;
+                s += u;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) su[row] = s;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+            const int row = e / d, c = e - row * d;
+            float acc = 0.f;
+            for (int f = 0; f < r; ++f) acc = fmaf(dph[row * r + f], om(c, f), acc);
+            store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, acc - x[row * d + c] * su[row]);
+        }
+    } else if (p.map == LA_MAP_DPFP) {
+        const int d2 = 2 * d, nu = r / d2;
+        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+            const int row = e / d, c = e - row * d;
+            const float* xr = x + row * d;
+            const float* g = dph + row * r;
+            auto xt = [&](int i) { return i < d ? fmaxf(xr[i], 0.f) : fmaxf(-xr[i - d], 0.f); };
+            float dp = 0.f, dn = 0.f;   // dL/dx~_c and dL/dx~_{c+d}
+            for (int s = 1; s <= nu; ++s) {
+                const float* gs = g + (s - 1) * d2;
+                int i = c;
+                dp = fmaf(gs[i], xt((i + s) % d2), dp);
+                dp = fmaf(gs[(i - s + d2) % d2], xt((i - s + d2) % d2), dp);
+                i = c + d;
+                dn = fmaf(gs[i], xt((i + s) % d2), dn);
+                dn = fmaf(gs[(i - s + d2) % d2], xt((i - s + d2) % d2), dn);
+            }
+            const float xv = xr[c];
+            store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, (xv > 0.f ? dp : 0.f) - (xv < 0.f ? dn : 0.f));
+        }
+    } else {
+        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+            const int row = e / d, c = e - row * d;   // r == d
+            const float xv = x[row * d + c], gv = dph[row * r + c];
+            const float dxv = (p.map == LA_MAP_ELU1) ? gv * (xv > 0.f ? 1.f : expf(xv)) : gv;
+            store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, dxv);
+        }
+    }
+}
+
+struct BwdView {
+    float *st, *racc, *xq, *xk, *phq, *phk, *dph, *vx, *gg, *num, *go, *a, *gm, *hsq, *hsk, *sgq, *sgk, *su;
+};
+
+__device__ BwdView bwd_view(unsigned char* raw, const BwdSmem& sp) {
+    float* sm = reinterpret_cast<float*>(raw);
+    return BwdView{sm + sp.st / 4, sm + sp.racc / 4, sm + sp.xq / 4, sm + sp.xk / 4, sm + sp.phq / 4,
+                   sm + sp.phk / 4, sm + sp.dph / 4, sm + sp.vx / 4, sm + sp.gg / 4, sm + sp.num / 4,
+                   sm + sp.go / 4, sm + sp.a / 4, sm + sp.gm / 4, sm + sp.hsq / 4, sm + sp.hsk / 4,
+                   sm + sp.sgq / 4, sm + sp.sgk / 4, sm + sp.su / 4};
+}
+
+// A[i][j] = phi(q_i) . phi(k_j) for j <= i < n (diagonal included), else 0; one warp per entry.
+__device__ void causal_scores(float* A, const float* phq, const float* phk, int n, int r) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int ij = warp; ij < CS * CS; ij += NW) {
+        const int i = ij / CS, j = ij - i * CS;
+        float acc = 0.f;
+        if (j <= i && i < n) {
+            for (int f = lane; f < r; f += 32) acc = fmaf(phq[i * r + f], phk[j * r + f], acc);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        }
+        if (lane == 0) A[ij] = acc;
+    }
+}
+
+// Gm[i][j] = g_i . [v_j | 1] for j <= i < n, else 0.
+__device__ void causal_gv(float* Gm, const float* gg, const float* vx, int n, int dvx) {
+    for (int ij = threadIdx.x; ij < CS * CS; ij += NT) {
+        const int i = ij / CS, j = ij - i * CS;
+        float acc = 0.f;
+        if (j <= i && i < n)
+            for (int c = 0; c < dvx; ++c) acc = fmaf(gg[i * dvx + c], vx[j * dvx + c], acc);
+        Gm[ij] = acc;
+    }
+}
+
+// Forward walk of one segment: g of every row, dq, and the segment's sum of
+// phi(q_i) g_i^T (into p.partial).
+template <typename TIn>
+__global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_zero) {
+    const int u = blockIdx.x, h = blockIdx.y;
+    if (u >= p.hdr->n_units) return;
+    const Unit un = p.units[u];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const BwdView w = bwd_view(smem_raw, plan_bwd_smem(p.dk, p.dv, p.r, true));
+    const OmegaView om = (p.map == LA_MAP_FAVOR) ? stage_omega(nullptr, p.omega, p.dk, p.r) : OmegaView{nullptr, 0, 0};
+    const int r = p.r, dv = p.dv, dvx = p.dvx, dk = p.dk;
+    const int E = r * dvx;
+    const bool attn = p.norm == LA_NORM_ATTENTION;
+    const float* src = p.prefix + ((int64_t)u * p.H + h) * E;
+    for (int e = threadIdx.x; e < E; e += NT) {
+        w.st[e] = prefix_is_zero ? 0.f : src[e];
+        w.racc[e] = 0.f;
+    }
+    const TIn* Q = static_cast<const TIn*>(p.q);
+    const TIn* K = static_cast<const TIn*>(p.k);
+    const TIn* V = static_cast<const TIn*>(p.v);
+    const TIn* DO = static_cast<const TIn*>(p.dout);
+    TIn* DQ = static_cast<TIn*>(p.dq_out);
+    for (int64_t t0 = un.start; t0 < un.end; t0 += CS) {
+        const int n = (int)min64(CS, un.end - t0);
+        __syncthreads();
+        load_rows(w.xq, Q, t0, n, p.H, h, dk);
+        load_rows(w.go, DO, t0, n, p.H, h, dv);
+        if (p.causal) {
+            load_rows(w.xk, K, t0, n, p.H, h, dk);
+            load_vx(w.vx, V, t0, n, p.H, h, dv);
+        }
+        __syncthreads();
+        compute_phi(w.phq, w.xq, w.hsq, om, n, p.map, dk, r);
+        if (p.causal) compute_phi(w.phk, w.xk, w.hsk, om, n, p.map, dk, r);
+        __syncthreads();
+        if (p.norm == LA_NORM_SUM) {
+            sum_normalise_keep(w.phq, w.sgq, n, r, p.eps);
+            if (p.causal) sum_normalise_keep(w.phk, w.sgk, n, r, p.eps);
+            __syncthreads();
+        }
+        if (p.causal) {
+            causal_scores(w.a, w.phq, w.phk, n, r);
+            __syncthreads();
+        }
+        // num | den of each row: phi(q_i) S (+ in-chunk terms)
+        for (int e = threadIdx.x; e < n * dvx; e += NT) {
+            const int i = e / dvx, c = e - i * dvx;
+            float acc = 0.f;
+            for (int f = 0; f < r; ++f) acc = fmaf(w.phq[i * r + f], w.st[f * dvx + c], acc);
+            if (p.causal) {
+#pragma unroll
+                for (int j = 0; j < CS; ++j) acc = fmaf(w.a[i * CS + j], w.vx[j * dvx + c], acc);
+            }
+            w.num[e] = acc;
+        }
+        __syncthreads();
+        // g_i = dL/d(num_i | den_i)
+        for (int e = threadIdx.x; e < CS * dvx; e += NT) {
+            const int i = e / dvx, c = e - i * dvx;
+            float gv = 0.f;
+            if (i < n) {
+                if (!attn) {
+                    gv = c < dv ? w.go[i * dv + c] : 0.f;
+                } else {
+                    const float den = w.num[i * dvx + dv];
+                    const float dc = fmaxf(den, p.eps);
+                    if (c < dv) {
+                        gv = w.go[i * dv + c] / dc;
+                    } else if (den > p.eps) {
+                        float dot = 0.f;   // dout_i . out_i
+                        for (int c2 = 0; c2 < dv; ++c2) dot = fmaf(w.go[i * dv + c2], w.num[i * dvx + c2] / dc, dot);
+                        gv = -dot / den;
+                    }
+                }
+                p.g[((t0 + i) * p.H + h) * (int64_t)dvx + c] = gv;
+            }
+            w.gg[e] = gv;
+        }
+        __syncthreads();
+        if (p.causal) {
+            causal_gv(w.gm, w.gg, w.vx, n, dvx);
+            __syncthreads();
+        }
+        // dphi(q_i) = S g_i (+ sum_{j<=i} (g_i . [v_j|1]) phi(k_j))
+        for (int e = threadIdx.x; e < n * r; e += NT) {
+            const int i = e / r, f = e - i * r;
+            float acc = 0.f;
+            for (int c = 0; c < dvx; ++c) acc = fmaf(w.st[f * dvx + c], w.gg[i * dvx + c], acc);
+            if (p.causal) {
+#pragma unroll
+                for (int j = 0; j < CS; ++j) acc = fmaf(w.gm[i * CS + j], w.phk[j * r + f], acc);
+            }
+            w.dph[e] = acc;
+        }
+        __syncthreads();   // the state is read above and updated below
+        // the segment's sum of phi(q_i) g_i^T, and (causal) the state after the chunk
+        for (int e = threadIdx.x; e < E; e += NT) {
+            const int f = e / dvx, c = e - f * dvx;
+            float ra = w.racc[e];
+#pragma unroll
+            for (int i = 0; i < CS; ++i) ra = fmaf(w.phq[i * r + f], w.gg[i * dvx + c], ra);
+            w.racc[e] = ra;
+            if (p.causal) {
+                float sa = w.st[e];
+#pragma unroll
+                for (int i = 0; i < CS; ++i) sa = fmaf(w.phk[i * r + f], w.vx[i * dvx + c], sa);
+                w.st[e] = sa;
+            }
+        }
+        __syncthreads();
+        features_vjp_rows(w.dph, w.phq, w.xq, w.sgq, w.su, n, p, om, DQ, t0, h);
+    }
+    __syncthreads();
+    float* dst = p.partial + ((int64_t)u * p.H + h) * E;
+    for (int e = threadIdx.x; e < E; e += NT) dst[e] = w.racc[e];
+}
+
+// Backward walk of one segment: R starts as the sum of phi(q) g^T over the
+// later segments (the whole sequence for the bidirectional form); writes dk
+// and dv.
+template <typename TIn>
+__global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
+    const int u = blockIdx.x, h = blockIdx.y;
+    if (u >= p.hdr->n_units) return;
+    const Unit un = p.units[u];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const BwdView w = bwd_view(smem_raw, plan_bwd_smem(p.dk, p.dv, p.r, false));
+    const OmegaView om = (p.map == LA_MAP_FAVOR) ? stage_omega(nullptr, p.omega, p.dk, p.r) : OmegaView{nullptr, 0, 0};
+    const int r = p.r, dv = p.dv, dvx = p.dvx, dk = p.dk;
+    const int E = r * dvx;
+    float* R = w.st;
+    const float* src = p.suffix + ((int64_t)u * p.H + h) * E;
+    for (int e = threadIdx.x; e < E; e += NT) R[e] = src[e];
+    const TIn* Q = static_cast<const TIn*>(p.q);
+    const TIn* K = static_cast<const TIn*>(p.k);
+    const TIn* V = static_cast<const TIn*>(p.v);
+    TIn* DK = static_cast<TIn*>(p.dk_out);
+    TIn* DV = static_cast<TIn*>(p.dv_out);
+    const int nch = (int)ceil_div(un.end - un.start, CS);
+    for (int m = nch - 1; m >= 0; --m) {
+        const int64_t t0 = un.start + (int64_t)m * CS;
+        const int n = (int)min64(CS, un.end - t0);
+        __syncthreads();
+        load_rows(w.xk, K, t0, n, p.H, h, dk);
+        load_vx(w.vx, V, t0, n, p.H, h, dv);
+        if (p.causal) load_rows(w.xq, Q, t0, n, p.H, h, dk);
+        for (int e = threadIdx.x; e < CS * dvx; e += NT) {
+            const int i = e / dvx;
+            w.gg[e] = i < n ? p.g[((t0 + i) * p.H + h) * (int64_t)dvx + (e - i * dvx)] : 0.f;
+        }
+        __syncthreads();
+        compute_phi(w.phk, w.xk, w.hsk, om, n, p.map, dk, r);
+        if (p.causal) compute_phi(w.phq, w.xq, w.hsq, om, n, p.map, dk, r);
+        __syncthreads();
+        if (p.norm == LA_NORM_SUM) {
+            sum_normalise_keep(w.phk, w.sgk, n, r, p.eps);
+            if (p.causal) sum_normalise_keep(w.phq, w.sgq, n, r, p.eps);
+            __syncthreads();
+        }
+        if (p.causal) {
+            causal_scores(w.a, w.phq, w.phk, n, r);   // A[i][j], j <= i
+            causal_gv(w.gm, w.gg, w.vx, n, dvx);      // Gm[i][j] = g_i . [v_j | 1], j <= i
+            __syncthreads();
+        }
+        // dphi(k_j) = R [v_j | 1] (+ sum_{i>=j} (g_i . [v_j|1]) phi(q_i))
+        for (int e = threadIdx.x; e < n * r; e += NT) {
+            const int j = e / r, f = e - j * r;
+            float acc = 0.f;
+            for (int c = 0; c < dvx; ++c) acc = fmaf(R[f * dvx + c], w.vx[j * dvx + c], acc);
+            if (p.causal) {
+#pragma unroll
+                for (int i = 0; i < CS; ++i) acc = fmaf(w.gm[i * CS + j], w.phq[i * r + f], acc);
+            }
+            w.dph[e] = acc;
+        }
+        // dv_j = R^T phi(k_j) (+ sum_{i>=j} (phi(q_i) . phi(k_j)) g_i), first d_v entries
+        for (int e = threadIdx.x; e < n * dv; e += NT) {
+            const int j = e / dv, c = e - j * dv;
+            float acc = 0.f;
+            for (int f = 0; f < r; ++f) acc = fmaf(R[f * dvx + c], w.phk[j * r + f], acc);
+            if (p.causal) {
+#pragma unroll
+                for (int i = 0; i < CS; ++i) acc = fmaf(w.a[i * CS + j], w.gg[i * dvx + c], acc);
+            }
+            store_elem(DV, ((t0 + j) * p.H + h) * (int64_t)dv + c, acc);
+        }
+        __syncthreads();   // R is read above and updated below
+        if (p.causal) {
+            for (int e = threadIdx.x; e < E; e += NT) {
+                const int f = e / dvx, c = e - f * dvx;
+                float ra = R[e];
+#pragma unroll
+                for (int i = 0; i < CS; ++i) ra = fmaf(w.phq[i * r + f], w.gg[i * dvx + c], ra);
+                R[e] = ra;
+            }
+        }
+        __syncthreads();
+        features_vjp_rows(w.dph, w.phk, w.xk, w.sgk, w.su, n, p, om, DK, t0, h);
+    }
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int dk, int dv, int r) { return plan_bwd_smem(dk, dv, r, true).total; }
+
+template <typename Kern>
+static cudaError_t bwd_set_smem(Kern k, size_t bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t bwd_q(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_t s) {
+    const size_t bytes = plan_bwd_smem(p.dk, p.dv, p.r, true).total;
+    const dim3 grid((unsigned)p.U, (unsigned)p.H);
+    cudaError_t e;
+    if (dtype == LA_F32) {
+        if ((e = bwd_set_smem(bwd_q_kernel<float>, bytes)) != cudaSuccess) return e;
+        bwd_q_kernel<float><<<grid, NT, bytes, s>>>(p, prefix_is_zero);
+    } else {
+        if ((e = bwd_set_smem(bwd_q_kernel<__nv_bfloat16>, bytes)) != cudaSuccess) return e;
+        bwd_q_kernel<__nv_bfloat16><<<grid, NT, bytes, s>>>(p, prefix_is_zero);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t bwd_kv(const FwdParams& p, int dtype, cudaStream_t s) {
+    const size_t bytes = plan_bwd_smem(p.dk, p.dv, p.r, false).total;
+    const dim3 grid((unsigned)p.U, (unsigned)p.H);
+    cudaError_t e;
+    if (dtype == LA_F32) {
+        if ((e = bwd_set_smem(bwd_kv_kernel<float>, bytes)) != cudaSuccess) return e;
+        bwd_kv_kernel<float><<<grid, NT, bytes, s>>>(p);
+    } else {
+        if ((e = bwd_set_smem(bwd_kv_kernel<__nv_bfloat16>, bytes)) != cudaSuccess) return e;
+        bwd_kv_kernel<__nv_bfloat16><<<grid, NT, bytes, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace la

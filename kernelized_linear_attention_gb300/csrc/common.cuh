@@ -34,6 +34,8 @@ struct Layout {
     size_t seq_first;  // int[nseq + 1]: first unit of each sequence (+ total)
     size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
+    size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
+    size_t g;          // backward: float[T][H][dvx], d num | d den of every row
     size_t total;      // bytes
     int U;             // upper bound on units
     int L;             // segment length in tokens
@@ -64,6 +66,14 @@ struct FwdParams {
     const float* state_in;  // [nseq][H][r][dvx] or NULL: state each sequence starts from
     float* state_out;       // [nseq][H][r][dvx] or NULL: state after each sequence's last token
     int keep_last;          // causal: the state pass also sums each sequence's last segment
+    // backward pass only
+    const void* dout;       // [T][H][dv] upstream gradient
+    void* dq_out;           // [T][H][dk] gradients written
+    void* dk_out;           // [T][H][dk]
+    void* dv_out;           // [T][H][dv]
+    float* g;               // [T][H][dvx] workspace: d num | d den of every row
+    float* suffix;          // [U][H][r][dvx] workspace: sum of phi(q_i) g_i^T over later units
+    int reverse;            // scan: suffix (later units) instead of prefix
     // workspace regions
     WsHeader* hdr;
     Unit* units;

@@ -38,6 +38,12 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
 cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
                            cudaStream_t s);
 
+// Backward pass on CUDA cores (bwd.cu): bwd_q writes g, dq and each unit's
+// sum of phi(q) g^T (p.partial); bwd_kv writes dk, dv from p.suffix.
+size_t bwd_smem_bytes(int dk, int dv, int r);
+cudaError_t bwd_q(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_t s);
+cudaError_t bwd_kv(const FwdParams& p, int dtype, cudaStream_t s);
+
 // One-token decode step on CUDA cores (decode.cu).
 size_t decode_smem_bytes(int dk, int dv, int r);
 cudaError_t decode_step(const void* q, const void* k, const void* v, const float* omega, int map, int dtype,

@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
 constexpr int kScanThreads = 256;
 constexpr int kScanPerThread = 4;
 
-// grid: (ceil(E / (256*4)), nseq, H).  Each thread owns elements e of one
+// grid: (ceil(E / (256*4)), nseq, H).  The result goes to p.prefix (the
+// backward pass points it at its suffix buffer and sets p.reverse).  Each
+// thread owns elements e of one
 // (sequence, head) state and walks the sequence's units in token order, so
 // state_in may alias state_out: it is read before the same thread writes it.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
@@ -127,7 +129,20 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
         const int64_t e = e0 + j * kScanThreads;
         acc[j] = (p.state_in != nullptr && e < E) ? p.state_in[sbase + e] : 0.f;
     }
-    if (p.causal) {
+    if (p.causal && p.reverse) {
+        // suffix: the sums of the units after u, walking the sequence backwards
+        for (int u = u1 - 1; u >= u0; --u) {
+            const int64_t base = ((int64_t)u * p.H + h) * E;
+#pragma unroll
+            for (int j = 0; j < kScanPerThread; ++j) {
+                const int64_t e = e0 + j * kScanThreads;
+                if (e < E) {
+                    p.prefix[base + e] = acc[j];
+                    acc[j] += p.partial[base + e];
+                }
+            }
+        }
+    } else if (p.causal) {
         for (int u = u0; u < u1; ++u) {
             const int64_t base = ((int64_t)u * p.H + h) * E;
             const bool add = u + 1 < u1 || p.keep_last;   // the last unit's sum exists only with keep_last

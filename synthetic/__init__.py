@@ -81,6 +81,7 @@ class Workload:
     carry: bool = False          # a state is carried in (state_in) and out (state_out)
     decode: bool = False         # one-token decode steps: lengths = [1] * B against a carried state
     n_prior: int = 0             # tokens the carried state stands for (carry / decode)
+    backward: bool = False       # the gradients of sum(dout * out) rather than the forward
 
     @property
     def T(self) -> int:
@@ -153,6 +154,10 @@ def workloads() -> dict:
         "bf16 q/k/v, fp32 state standing for 4096 earlier tokens (272 MB of state)",
         H=16, dk=64, dv=64, r=256, map="favor", causal=True, dtype="bf16", lengths=[1] * 256, qk_scale=s,
         decode=True, n_prior=4096, seed=DATA_SEED_BASE + 9)
+    w["favor_causal_b4h8n4096_bwd"] = Workload(
+        "favor_causal_b4h8n4096_bwd", "backward (dq, dk, dv) of causal FAVOR+ r=256, B=4, H=8, N=4096, d=64, bf16, "
+        "dout ~ N(0, 1)", H=8, dk=64, dv=64, r=256, map="favor", causal=True, dtype="bf16",
+        lengths=[4096] * 4, qk_scale=s, backward=True, seed=DATA_SEED_BASE + 10)
     return w
 
 

@@ -185,3 +185,30 @@ def test_binding_checks_state_shapes_and_devices():
     assert [_norm_id(n) for n in ("attention", "none", "sum")] == [0, 1, 2]
     with pytest.raises(KeyError):
         _norm_id("softmax")
+
+
+def _bwd(lib, **kw):
+    a = dict(causal=1, norm=0, q=1 << 20, k=1 << 20, v=1 << 20, omega=1 << 20, map=2, dtype=1, cu=None, nseq=1,
+             T=128, H=2, dk=64, dv=64, r=256, eps=1e-6, dout=1 << 21, dq=1 << 22, dk_=1 << 23, dv_=1 << 24,
+             ws=1 << 25, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.la_backward(a["causal"], a["norm"], a["q"], a["k"], a["v"], a["omega"], a["map"], a["dtype"], a["cu"],
+                           a["nseq"], a["T"], a["H"], a["dk"], a["dv"], a["r"], a["eps"], a["dout"], a["dq"],
+                           a["dk_"], a["dv_"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(norm=3), 1), (dict(norm=2, map=0, r=64), 1), (dict(map=7), 1), (dict(dtype=4), 1),
+    (dict(omega=None), 1), (dict(map=1, r=128), 1), (dict(eps=-1.0), 1), (dict(ws=None), 1),
+    (dict(ws=(1 << 25) + 8), 1), (dict(dout=None), 1), (dict(dq=None), 1), (dict(dv_=None), 1),
+    (dict(dk_=(1 << 23) + 1), 1), (dict(T=130, nseq=4), 1),
+    (dict(r=512, dv=256), 2),                           # state does not fit the CUDA-core kernels' shared memory
+])
+def test_backward_rejects_bad_arguments_on_host(lib, bad, code):
+    assert _bwd(lib, **bad) == code
+
+
+def test_backward_workspace_query_rejects_bad_shapes(lib):
+    import kernelized_linear_attention_gb300 as la
+    assert la.la_backward_workspace_bytes(True, "elu1", 1, False, 3, 100, 2, 64, 64, 64) == 0
+    assert la.la_backward_workspace_bytes(True, "favor", 1, False, 1, 128, 2, 64, 256, 512) == 0
