@@ -282,6 +282,37 @@ def cpu_baseline_decode(w: synthetic.Workload, seconds: float, inputs, om) -> di
                       f"{el:.1f} s, 1 BLAS thread; tokens/s = pair-steps/s / H"}
 
 
+def cpu_baseline_backward(w: synthetic.Workload, seconds: float) -> dict:
+    """The oracle's backward (quadratic form) on the first n tokens of one
+    head of sequence 0, n grown until the sample takes about `seconds`;
+    tokens/s = token-heads/s / H."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_limits
+        limiter = threadpool_limits(limits=1)  # noqa: F841  (held for the duration of the sample)
+    except Exception:
+        limiter = None  # noqa: F841
+    inputs = synthetic.make_qkv(w)
+    om = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 1))
+    dout = rng.standard_normal(inputs.v.shape).astype(np.float32)
+    n, el = 256, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.backward(inputs.q[:n, :1], inputs.k[:n, :1], inputs.v[:n, :1], dout[:n, :1], w.map, w.causal,
+                        omega=om, eps=w.eps, norm=w.norm)
+        el = time.perf_counter() - t0
+        if el >= seconds / 3 or n >= w.lengths[0]:
+            break
+        n = min(w.lengths[0], n * 2)
+    return {"value": n / w.H / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle backward (quadratic form) on tokens 0..{n - 1} of head 0 of sequence 0 of "
+                      f"{w.name} in {el:.2f} s, 1 BLAS thread; tokens/s = token-heads/s / H"}
+
+
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
@@ -448,6 +479,14 @@ def run_ours(args):
         line["backward"] = backward_line(la, dev, stream, max(3, min(K, 10)), BACKWARD_WORKLOAD)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
+        if "variants" in line:
+            # the oracle beside each further row, on a bounded sample of its workload
+            secs = max(2.0, args.cpu_seconds / 4)
+            for key, wname in (("none", "favor_causal_b1h16n65536_none"), ("carry", "favor_causal_b1h16n65536_carry"),
+                               ("sum", "elu_causal_b8h8n4096_sum")):
+                line["variants"][key]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[wname], secs)
+            line["decode_step"]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[DECODE_WORKLOAD], secs)
+            line["backward"]["cpu_baseline"] = cpu_baseline_backward(synthetic.workloads()[BACKWARD_WORKLOAD], secs)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
