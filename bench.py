@@ -331,6 +331,8 @@ def run_ours(args):
     w = synthetic.workloads()[args.workload]
     if w.decode:
         return run_decode(args, la, w, dev, world, rank, local)
+    if w.backward:
+        return run_backward(args, la, w, dev, world, rank)
     inputs = synthetic.make_qkv(w)
     T, H, dk, dv, r = w.T, w.H, w.dk, w.dv, w.r
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -562,6 +564,31 @@ def forward_variants(la, dev, stream, peaks, steps, w, dev_qkv, omega) -> dict:
     return out
 
 
+def run_backward(args, la, w, dev, world, rank):
+    """Main line for a backward workload: one step = one la_backward call."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    res = backward_line(la, dev, stream, args.steps, w.name, warmup=max(args.warmup, 3), world=world)
+    clocks = sampler.stop()
+    line = {
+        "metric": "tokens/s/GPU backward (dq, dk, dv) of causal FAVOR+ r=256 d=64; % fp32 ALU roofline",
+        "value": res["tokens_per_s"] * world, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded q, k, v, dout)",
+        "config": {"workload": w.name, "B": w.nseq, "H": w.H, "N": w.lengths[0], "d_k": w.dk, "d_v": w.dv,
+                   "r": w.r, "map": w.map, "causal": w.causal, "norm": w.norm, "eps": w.eps,
+                   "parallelism": f"replicas x{world}", "l2": "no flush: inputs and fp32 workspace rows exceed L2",
+                   "path": res["path"]},
+        "roofline": res["roofline"], "gpu_launches": res["launches_per_call"] * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_backward(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_decode(args, la, w, dev, world, rank, local):
     """Main line for a decode workload: one step = one decode step of every sequence."""
     import torch
@@ -697,7 +724,8 @@ def backward_line(la, dev, stream, steps, name, warmup=3, world=1) -> dict:
     ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     flops = backward_flops(w) * w.T * w.H
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": w.name, "ms": ms, "tokens_per_s": w.T / (ms * 1e-3), "launches_per_call": 6,
+    return {"workload": w.name, "ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
+            "launches_per_call": 7 if w.map == "favor" else 6,
             "path": "cuda-core fp32",
             "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
                          "frac": tf / FP32_ALU_TFLOPS, "alg_flops_per_call": flops,

@@ -84,6 +84,7 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     if (bwd) {
         lo.suffix = o; o = align_up(o + state_bytes, kAlign);
         lo.g = o;      o = align_up(o + sizeof(float) * (size_t)T * H * lo.dvx, kAlign);
+        lo.omega_t = o; o = align_up(o + sizeof(float) * (size_t)r * LA_MAX_DK, kAlign);
     }
     lo.total = o;
     return lo;
@@ -221,8 +222,10 @@ la_status backward(int causal, int norm, const void* q, const void* k, const voi
     p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
     p.suffix = reinterpret_cast<float*>(ws + lo.suffix);
     p.g = reinterpret_cast<float*>(ws + lo.g);
+    p.omega_t = reinterpret_cast<float*>(ws + lo.omega_t);
     p.U = lo.U; p.L = lo.L;
     cudaError_t e = launch_plan(p, s);
+    if (e == cudaSuccess && T > 0 && map == LA_MAP_FAVOR) e = bwd_transpose_omega(p, s);
     if (e != cudaSuccess || T == 0) return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
     const bool single_segments = !has_cu && lo.U == nseq;
     const bool need_state = !causal || !single_segments;

@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
     const Unit un = p.units[u];
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const BwdView w = bwd_view(smem_raw, plan_bwd_smem(p.dk, p.dv, p.r, true));
+    // features read Omega transposed ([dk][r]: lanes over features, coalesced), the chain
+    // rule reads it as given ([r][dk]: lanes over input columns, coalesced)
+    const OmegaView om_phi{p.omega_t, p.r, 1};
     const OmegaView om = (p.map == LA_MAP_FAVOR) ? stage_omega(nullptr, p.omega, p.dk, p.r) : OmegaView{nullptr, 0, 0};
     const int r = p.r, dv = p.dv, dvx = p.dvx, dk = p.dk;
     const int E = r * dvx;
@@ -229,8 +232,8 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
             load_vx(w.vx, V, t0, n, p.H, h, dv);
         }
         __syncthreads();
-        compute_phi(w.phq, w.xq, w.hsq, om, n, p.map, dk, r);
-        if (p.causal) compute_phi(w.phk, w.xk, w.hsk, om, n, p.map, dk, r);
+        compute_phi(w.phq, w.xq, w.hsq, om_phi, n, p.map, dk, r);
+        if (p.causal) compute_phi(w.phk, w.xk, w.hsk, om_phi, n, p.map, dk, r);
         __syncthreads();
         if (p.norm == LA_NORM_SUM) {
             sum_normalise_keep(w.phq, w.sgq, n, r, p.eps);
@@ -324,6 +327,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
     const Unit un = p.units[u];
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const BwdView w = bwd_view(smem_raw, plan_bwd_smem(p.dk, p.dv, p.r, false));
+    const OmegaView om_phi{p.omega_t, p.r, 1};
     const OmegaView om = (p.map == LA_MAP_FAVOR) ? stage_omega(nullptr, p.omega, p.dk, p.r) : OmegaView{nullptr, 0, 0};
     const int r = p.r, dv = p.dv, dvx = p.dvx, dk = p.dk;
     const int E = r * dvx;
@@ -348,8 +352,8 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
             w.gg[e] = i < n ? p.g[((t0 + i) * p.H + h) * (int64_t)dvx + (e - i * dvx)] : 0.f;
         }
         __syncthreads();
-        compute_phi(w.phk, w.xk, w.hsk, om, n, p.map, dk, r);
-        if (p.causal) compute_phi(w.phq, w.xq, w.hsq, om, n, p.map, dk, r);
+        compute_phi(w.phk, w.xk, w.hsk, om_phi, n, p.map, dk, r);
+        if (p.causal) compute_phi(w.phq, w.xq, w.hsq, om_phi, n, p.map, dk, r);
         __syncthreads();
         if (p.norm == LA_NORM_SUM) {
             sum_normalise_keep(w.phk, w.sgk, n, r, p.eps);
@@ -398,7 +402,21 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
     }
 }
 
+__global__ void transpose_omega_kernel(const float* omega, float* omega_t, int r, int d) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;   // index into omega_t [d][r]
+    if (i < r * d) {
+        const int c = i / r, f = i - c * r;
+        omega_t[i] = omega[(int64_t)f * d + c];
+    }
+}
+
 }  // namespace
+
+cudaError_t bwd_transpose_omega(const FwdParams& p, cudaStream_t s) {
+    const int n = p.r * p.dk;
+    transpose_omega_kernel<<<(n + 255) / 256, 256, 0, s>>>(p.omega, p.omega_t, p.r, p.dk);
+    return cudaGetLastError();
+}
 
 size_t bwd_smem_bytes(int dk, int dv, int r) { return plan_bwd_smem(dk, dv, r, true).total; }
 

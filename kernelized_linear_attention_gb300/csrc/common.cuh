@@ -36,6 +36,7 @@ struct Layout {
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
     size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
     size_t g;          // backward: float[T][H][dvx], d num | d den of every row
+    size_t omega_t;    // backward: float[dk][r], Omega transposed
     size_t total;      // bytes
     int U;             // upper bound on units
     int L;             // segment length in tokens
@@ -74,6 +75,7 @@ struct FwdParams {
     float* g;               // [T][H][dvx] workspace: d num | d den of every row
     float* suffix;          // [U][H][r][dvx] workspace: sum of phi(q_i) g_i^T over later units
     int reverse;            // scan: suffix (later units) instead of prefix
+    float* omega_t;         // [dk][r] workspace: Omega transposed (coalesced feature loads)
     // workspace regions
     WsHeader* hdr;
     Unit* units;

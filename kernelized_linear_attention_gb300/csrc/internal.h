@@ -43,6 +43,7 @@ cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, 
 size_t bwd_smem_bytes(int dk, int dv, int r);
 cudaError_t bwd_q(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_t s);
 cudaError_t bwd_kv(const FwdParams& p, int dtype, cudaStream_t s);
+cudaError_t bwd_transpose_omega(const FwdParams& p, cudaStream_t s);   // p.omega [r][dk] -> p.omega_t [dk][r]
 
 // One-token decode step on CUDA cores (decode.cu).
 size_t decode_smem_bytes(int dk, int dv, int r);
