@@ -479,6 +479,7 @@ def run_ours(args):
         line["variants"] = forward_variants(la, dev, stream, peaks, K, w, (dq, dk_, dvv), omega)
         line["decode_step"] = decode_line(la, dev, stream, peaks, max(3, min(K, 20)), DECODE_WORKLOAD)
         line["backward"] = backward_line(la, dev, stream, max(3, min(K, 10)), BACKWARD_WORKLOAD)
+        line["fp32_n1024"] = small_config_line(la, dev, stream, max(5, min(K, 20)))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
         if "variants" in line:
@@ -675,6 +676,34 @@ def decode_line(la, dev, stream, peaks, steps, name, warmup=3, world=1, e2e_step
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "ms_per_step": e2e_ms}
     return {"workload": w.name, "ms": ms, "tokens_per_s": B / (ms * 1e-3), "launches": steps,
             "roofline": roof, "e2e": e2e, "clocks": clocks}
+
+
+def small_config_line(la, dev, stream, steps) -> dict:
+    """Latency of the fp32 single-head N=1024 case (a parity configuration,
+    reported as time only): whole forwards on the fp32 CUDA-core kernels, for
+    both maps and both forms, CUDA events on the launching stream."""
+    import torch
+    w = synthetic.workloads()["fp32_n1024"]
+    inputs = synthetic.make_qkv(w)
+    q, k, v = (torch.from_numpy(np.ascontiguousarray(inputs.storage(n))).to(dev) for n in ("q", "k", "v"))
+    blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+    omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), w.r)
+    res = {"workload": w.name, "path": "cuda-core fp32", "unit": "ms per forward"}
+    for kind in ("favor", "elu1"):
+        for causal in (True, False):
+            om = omega if kind == "favor" else None
+            out, ws = la.attention(q, k, v, kind, om, causal=causal, return_workspace=True, stream=stream)
+            for _ in range(3):
+                la.attention(q, k, v, kind, om, causal=causal, out=out, workspace=ws, stream=stream)
+            e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(steps):
+                la.attention(q, k, v, kind, om, causal=causal, out=out, workspace=ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[f"{kind}_{'causal' if causal else 'bidir'}_ms"] = e0.elapsed_time(e1) / steps
+    return res
 
 
 def backward_flops(w: synthetic.Workload) -> int:
