@@ -30,6 +30,10 @@ namespace la {
 
 namespace {
 
+// 16 warps per block: one block per SM fits (its states fill the shared
+// memory), so the block itself supplies the warps that hide latency.
+constexpr int kBwdThreads = 512;
+
 struct BwdSmem {
     size_t st, racc, xq, xk, phq, phk, dph, vx, gg, num, go, a, gm, hsq, hsk, sgq, sgk, su, total;
 };
@@ -67,7 +71,7 @@ __host__ __device__ inline BwdSmem plan_bwd_smem(int dk, int dv, int r, bool rac
 // (the backward pass needs it): phi' = phi / max(sum, eps).
 __device__ void sum_normalise_keep(float* phi, float* raw_sum, int nrows, int r, float eps) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int row = warp; row < nrows; row += NW) {
+    for (int row = warp; row < nrows; row += (blockDim.x >> 5)) {
         float s = 0.f;
         for (int f = lane; f < r; f += 32) s += phi[row * r + f];
 #pragma unroll
@@ -94,7 +98,7 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
     const int r = p.r, d = p.dk;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (p.norm == LA_NORM_SUM) {
-        for (int row = warp; row < nrows; row += NW) {
+        for (int row = warp; row < nrows; row += (blockDim.x >> 5)) {
             float dot = 0.f;
             for (int f = lane; f < r; f += 32) dot = fmaf(dph[row * r + f], phi[row * r + f], dot);
 #pragma unroll
@@ -110,7 +114,7 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
         __syncthreads();
     }
     if (p.map == LA_MAP_FAVOR) {
-        for (int row = warp; row < nrows; row += NW) {
+        for (int row = warp; row < nrows; row += (blockDim.x >> 5)) {
             float s = 0.f;
             for (int f = lane; f < r; f += 32) {
                 const float u = dph[row * r + f] * phi[row * r + f];
@@ -122,7 +126,7 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
             if (lane == 0) su[row] = s;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+        for (int e = threadIdx.x; e < nrows * d; e += blockDim.x) {
             const int row = e / d, c = e - row * d;
             float acc = 0.f;
             for (int f = 0; f < r; ++f) acc = fmaf(dph[row * r + f], om(c, f), acc);
@@ -130,7 +134,7 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
         }
     } else if (p.map == LA_MAP_DPFP) {
         const int d2 = 2 * d, nu = r / d2;
-        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+        for (int e = threadIdx.x; e < nrows * d; e += blockDim.x) {
             const int row = e / d, c = e - row * d;
             const float* xr = x + row * d;
             const float* g = dph + row * r;
@@ -149,7 +153,7 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
             store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, (xv > 0.f ? dp : 0.f) - (xv < 0.f ? dn : 0.f));
         }
     } else {
-        for (int e = threadIdx.x; e < nrows * d; e += NT) {
+        for (int e = threadIdx.x; e < nrows * d; e += blockDim.x) {
             const int row = e / d, c = e - row * d;   // r == d
             const float xv = x[row * d + c], gv = dph[row * r + c];
             const float dxv = (p.map == LA_MAP_ELU1) ? gv * (xv > 0.f ? 1.f : expf(xv)) : gv;
@@ -173,7 +177,7 @@ __device__ BwdView bwd_view(unsigned char* raw, const BwdSmem& sp) {
 // A[i][j] = phi(q_i) . phi(k_j) for j <= i < n (diagonal included), else 0; one warp per entry.
 __device__ void causal_scores(float* A, const float* phq, const float* phk, int n, int r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int ij = warp; ij < CS * CS; ij += NW) {
+    for (int ij = warp; ij < CS * CS; ij += (blockDim.x >> 5)) {
         const int i = ij / CS, j = ij - i * CS;
         float acc = 0.f;
         if (j <= i && i < n) {
@@ -187,7 +191,7 @@ __device__ void causal_scores(float* A, const float* phq, const float* phk, int 
 
 // Gm[i][j] = g_i . [v_j | 1] for j <= i < n, else 0.
 __device__ void causal_gv(float* Gm, const float* gg, const float* vx, int n, int dvx) {
-    for (int ij = threadIdx.x; ij < CS * CS; ij += NT) {
+    for (int ij = threadIdx.x; ij < CS * CS; ij += blockDim.x) {
         const int i = ij / CS, j = ij - i * CS;
         float acc = 0.f;
         if (j <= i && i < n)
@@ -199,7 +203,7 @@ __device__ void causal_gv(float* Gm, const float* gg, const float* vx, int n, in
 // Forward walk of one segment: g of every row, dq, and the segment's sum of
 // phi(q_i) g_i^T (into p.partial).
 template <typename TIn>
-__global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_zero) {
+__global__ void __launch_bounds__(kBwdThreads) bwd_q_kernel(FwdParams p, int prefix_is_zero) {
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
     const int E = r * dvx;
     const bool attn = p.norm == LA_NORM_ATTENTION;
     const float* src = p.prefix + ((int64_t)u * p.H + h) * E;
-    for (int e = threadIdx.x; e < E; e += NT) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
         w.st[e] = prefix_is_zero ? 0.f : src[e];
         w.racc[e] = 0.f;
     }
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
             __syncthreads();
         }
         // num | den of each row: phi(q_i) S (+ in-chunk terms)
-        for (int e = threadIdx.x; e < n * dvx; e += NT) {
+        for (int e = threadIdx.x; e < n * dvx; e += blockDim.x) {
             const int i = e / dvx, c = e - i * dvx;
             float acc = 0.f;
             for (int f = 0; f < r; ++f) acc = fmaf(w.phq[i * r + f], w.st[f * dvx + c], acc);
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
         }
         __syncthreads();
         // g_i = dL/d(num_i | den_i)
-        for (int e = threadIdx.x; e < CS * dvx; e += NT) {
+        for (int e = threadIdx.x; e < CS * dvx; e += blockDim.x) {
             const int i = e / dvx, c = e - i * dvx;
             float gv = 0.f;
             if (i < n) {
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
             __syncthreads();
         }
         // dphi(q_i) = S g_i (+ sum_{j<=i} (g_i . [v_j|1]) phi(k_j))
-        for (int e = threadIdx.x; e < n * r; e += NT) {
+        for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
             const int i = e / r, f = e - i * r;
             float acc = 0.f;
             for (int c = 0; c < dvx; ++c) acc = fmaf(w.st[f * dvx + c], w.gg[i * dvx + c], acc);
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
         }
         __syncthreads();   // the state is read above and updated below
         // the segment's sum of phi(q_i) g_i^T, and (causal) the state after the chunk
-        for (int e = threadIdx.x; e < E; e += NT) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
             const int f = e / dvx, c = e - f * dvx;
             float ra = w.racc[e];
 #pragma unroll
@@ -314,14 +318,14 @@ __global__ void __launch_bounds__(NT) bwd_q_kernel(FwdParams p, int prefix_is_ze
     }
     __syncthreads();
     float* dst = p.partial + ((int64_t)u * p.H + h) * E;
-    for (int e = threadIdx.x; e < E; e += NT) dst[e] = w.racc[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) dst[e] = w.racc[e];
 }
 
 // Backward walk of one segment: R starts as the sum of phi(q) g^T over the
 // later segments (the whole sequence for the bidirectional form); writes dk
 // and dv.
 template <typename TIn>
-__global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads) bwd_kv_kernel(FwdParams p) {
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
     const int E = r * dvx;
     float* R = w.st;
     const float* src = p.suffix + ((int64_t)u * p.H + h) * E;
-    for (int e = threadIdx.x; e < E; e += NT) R[e] = src[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) R[e] = src[e];
     const TIn* Q = static_cast<const TIn*>(p.q);
     const TIn* K = static_cast<const TIn*>(p.k);
     const TIn* V = static_cast<const TIn*>(p.v);
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
         load_rows(w.xk, K, t0, n, p.H, h, dk);
         load_vx(w.vx, V, t0, n, p.H, h, dv);
         if (p.causal) load_rows(w.xq, Q, t0, n, p.H, h, dk);
-        for (int e = threadIdx.x; e < CS * dvx; e += NT) {
+        for (int e = threadIdx.x; e < CS * dvx; e += blockDim.x) {
             const int i = e / dvx;
             w.gg[e] = i < n ? p.g[((t0 + i) * p.H + h) * (int64_t)dvx + (e - i * dvx)] : 0.f;
         }
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
             __syncthreads();
         }
         // dphi(k_j) = R [v_j | 1] (+ sum_{i>=j} (g_i . [v_j|1]) phi(q_i))
-        for (int e = threadIdx.x; e < n * r; e += NT) {
+        for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
             const int j = e / r, f = e - j * r;
             float acc = 0.f;
             for (int c = 0; c < dvx; ++c) acc = fmaf(R[f * dvx + c], w.vx[j * dvx + c], acc);
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
             w.dph[e] = acc;
         }
         // dv_j = R^T phi(k_j) (+ sum_{i>=j} (phi(q_i) . phi(k_j)) g_i), first d_v entries
-        for (int e = threadIdx.x; e < n * dv; e += NT) {
+        for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
             const int j = e / dv, c = e - j * dv;
             float acc = 0.f;
             for (int f = 0; f < r; ++f) acc = fmaf(R[f * dvx + c], w.phk[j * r + f], acc);
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(NT) bwd_kv_kernel(FwdParams p) {
         }
         __syncthreads();   // R is read above and updated below
         if (p.causal) {
-            for (int e = threadIdx.x; e < E; e += NT) {
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
                 const int f = e / dvx, c = e - f * dvx;
                 float ra = R[e];
 #pragma unroll
@@ -431,10 +435,10 @@ cudaError_t bwd_q(const FwdParams& p, int dtype, int prefix_is_zero, cudaStream_
     cudaError_t e;
     if (dtype == LA_F32) {
         if ((e = bwd_set_smem(bwd_q_kernel<float>, bytes)) != cudaSuccess) return e;
-        bwd_q_kernel<float><<<grid, NT, bytes, s>>>(p, prefix_is_zero);
+        bwd_q_kernel<float><<<grid, kBwdThreads, bytes, s>>>(p, prefix_is_zero);
     } else {
         if ((e = bwd_set_smem(bwd_q_kernel<__nv_bfloat16>, bytes)) != cudaSuccess) return e;
-        bwd_q_kernel<__nv_bfloat16><<<grid, NT, bytes, s>>>(p, prefix_is_zero);
+        bwd_q_kernel<__nv_bfloat16><<<grid, kBwdThreads, bytes, s>>>(p, prefix_is_zero);
     }
     return cudaGetLastError();
 }
@@ -445,10 +449,10 @@ cudaError_t bwd_kv(const FwdParams& p, int dtype, cudaStream_t s) {
     cudaError_t e;
     if (dtype == LA_F32) {
         if ((e = bwd_set_smem(bwd_kv_kernel<float>, bytes)) != cudaSuccess) return e;
-        bwd_kv_kernel<float><<<grid, NT, bytes, s>>>(p);
+        bwd_kv_kernel<float><<<grid, kBwdThreads, bytes, s>>>(p);
     } else {
         if ((e = bwd_set_smem(bwd_kv_kernel<__nv_bfloat16>, bytes)) != cudaSuccess) return e;
-        bwd_kv_kernel<__nv_bfloat16><<<grid, NT, bytes, s>>>(p);
+        bwd_kv_kernel<__nv_bfloat16><<<grid, kBwdThreads, bytes, s>>>(p);
     }
     return cudaGetLastError();
 }

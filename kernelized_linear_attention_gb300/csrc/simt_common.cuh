@@ -1,5 +1,5 @@
 // Building blocks of the fp32 CUDA-core kernels (forward and backward): work
-// in chunks of CS tokens with NT threads, rows staged in shared memory as
+// in chunks of CS tokens, rows staged in shared memory as
 // fp32.  Internal to liblinattn.so; everything has internal linkage.
 #pragma once
 
@@ -9,7 +9,7 @@ namespace la {
 namespace {
 
 constexpr int CS = 16;    // tokens per chunk
-constexpr int NT = 256;   // threads per block
+constexpr int NT = 256;   // threads per block of the forward kernels (the helpers below use blockDim.x)
 constexpr int NW = NT / 32;
 
 struct OmegaView {
@@ -20,7 +20,7 @@ struct OmegaView {
 
 template <typename TIn>
 __device__ void load_rows(float* dst, const TIn* src, int64_t row0, int nrows, int H, int h, int d) {
-    for (int i = threadIdx.x; i < CS * d; i += NT) {
+    for (int i = threadIdx.x; i < CS * d; i += blockDim.x) {
         const int rr = i / d, c = i - rr * d;
         dst[i] = (rr < nrows) ? load_elem(src, ((row0 + rr) * H + h) * (int64_t)d + c) : 0.f;
     }
@@ -30,7 +30,7 @@ __device__ void load_rows(float* dst, const TIn* src, int64_t row0, int nrows, i
 template <typename TIn>
 __device__ void load_vx(float* dst, const TIn* v, int64_t row0, int nrows, int H, int h, int dv) {
     const int dvx = dv + 1;
-    for (int i = threadIdx.x; i < CS * dvx; i += NT) {
+    for (int i = threadIdx.x; i < CS * dvx; i += blockDim.x) {
         const int rr = i / dvx, c = i - rr * dvx;
         float x = 0.f;
         if (rr < nrows) x = (c < dv) ? load_elem(v, ((row0 + rr) * H + h) * (int64_t)dv + c) : 1.f;
@@ -43,7 +43,7 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
                             int nrows, int map, int d, int r) {
     if (map == LA_MAP_FAVOR) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        for (int row = warp; row < CS; row += NW) {
+        for (int row = warp; row < CS; row += (blockDim.x >> 5)) {
             float s = 0.f;
             for (int c = lane; c < d; c += 32) s = fmaf(x[row * d + c], x[row * d + c], s);
 #pragma unroll
@@ -52,7 +52,7 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
         }
         __syncthreads();
         const float inv_sqrt_r = rsqrtf((float)r);
-        for (int i = threadIdx.x; i < CS * r; i += NT) {
+        for (int i = threadIdx.x; i < CS * r; i += blockDim.x) {
             const int row = i / r, f = i - row * r;
             float val = 0.f;
             if (row < nrows) {
@@ -65,7 +65,7 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
     } else if (map == LA_MAP_DPFP) {
         // x~ = relu([x, -x]); feature (s-1) 2d + i = x~_i x~_{(i+s) mod 2d}, s = 1..r / 2d
         const int d2 = 2 * d;
-        for (int i = threadIdx.x; i < CS * r; i += NT) {
+        for (int i = threadIdx.x; i < CS * r; i += blockDim.x) {
             const int row = i / r, f = i - row * r;
             float val = 0.f;
             if (row < nrows) {
@@ -78,7 +78,7 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
             phi[i] = val;
         }
     } else {
-        for (int i = threadIdx.x; i < CS * r; i += NT) {
+        for (int i = threadIdx.x; i < CS * r; i += blockDim.x) {
             const int row = i / r;
             const float xv = x[i];   // r == d
             float val = 0.f;
@@ -92,7 +92,7 @@ __device__ void compute_phi(float* phi, const float* x, float* half_sq, const Om
 // nrows rows of phi ([CS][r] in smem), one warp per row ("The Kernel Zoo" §7.2).
 __device__ void sum_normalise_rows(float* phi, int nrows, int r, float eps) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int row = warp; row < nrows; row += NW) {
+    for (int row = warp; row < nrows; row += (blockDim.x >> 5)) {
         float s = 0.f;
         for (int f = lane; f < r; f += 32) s += phi[row * r + f];
 #pragma unroll
@@ -105,7 +105,7 @@ __device__ void sum_normalise_rows(float* phi, int nrows, int r, float eps) {
 // Places Omega in shared memory as [d][r] when `om_smem` is set, else reads global [r][d].
 __device__ OmegaView stage_omega(float* om_smem, const float* omega, int d, int r) {
     if (om_smem == nullptr) return OmegaView{omega, 1, d};
-    for (int j = threadIdx.x; j < d * r; j += NT) {
+    for (int j = threadIdx.x; j < d * r; j += blockDim.x) {
         const int c = j / r, f = j - c * r;
         om_smem[j] = omega[f * d + c];
     }
