@@ -236,10 +236,9 @@ def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace,
         out = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     _need(out, "out", q.dtype)
     need = la_workspace_bytes(causal, m, q.dtype, cu_seqlens is not None, nseq, T, H, d_k, d_v, r)
-    if need == 0:
-        raise LinAttnError("la_workspace_bytes", 1)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        # a size of 0 means the call will be rejected: let the library say why
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     nid = _norm_id(norm)
     if nid == NORM_IDS["attention"] and state_in is None and state_out is None:
         forward_ptrs(causal, _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, q.dtype, _ptr(cu_seqlens), nseq, T, H,
@@ -334,10 +333,8 @@ def la_backward(q, k, v, dout, map, omega=None, causal=True, norm="attention", c
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _need(t, name, q.dtype)
     need = la_backward_workspace_bytes(causal, m, q.dtype, cu_seqlens is not None, nseq, T, H, d_k, d_v, r)
-    if need == 0:
-        raise LinAttnError("la_backward_workspace_bytes", 1)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("la_backward", load_library().la_backward(
         int(causal), _norm_id(norm), _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype],
         _ptr(cu_seqlens), nseq, T, H, d_k, d_v, r, eps, _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),

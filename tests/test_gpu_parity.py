@@ -278,3 +278,30 @@ def test_full_size_workload_sampled_rows(la, name):
             e = abs_err_over_rms(got[rows, h], ref)
             worst = max(worst, e)
     assert worst <= BF16_RMS_TOL, worst
+
+
+# ----------------------------------------------------------------------------
+# Largest shapes
+# ----------------------------------------------------------------------------
+def test_largest_head_sizes_that_fit_fp32(la):
+    """d_k = d_v = 256 (the limits) with r = 128 fits the CUDA-core kernels'
+    shared memory: parity at those sizes, both forms, a ragged tail."""
+    inp = synthetic.random_inputs([37, 129], H=1, dk=256, dv=256, dtype="f32", seed=61, qk_scale=256 ** -0.25)
+    om = omega_for(128, 256)
+    for causal in (True, False):
+        assert_close(_run(la, inp, "favor", causal, om), _oracle(inp, "favor", causal, om), "f32",
+                     f"d=256 r=128 causal={causal}")
+
+
+def test_shapes_beyond_shared_memory_are_rejected_not_run(la):
+    """ELU+1 with d_k = d_v = 256 needs a 256 x 257 fp32 state per block (263
+    KB), more than an SM's shared memory: the call returns LA_ERR_UNSUPPORTED
+    before launching anything and leaves out untouched."""
+    z = torch.zeros((16, 1, 256), dtype=torch.float32, device="cuda")
+    out = torch.full_like(z, 7.0)
+    with pytest.raises(la.LinAttnError) as e:
+        la.la_forward_causal(z, z, z, "elu1", out=out, workspace=torch.empty(1 << 20, dtype=torch.uint8,
+                                                                               device="cuda"))
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
