@@ -37,9 +37,14 @@ la_status check_dims(int map, int dtype, int nseq, int64_t T, int H, int dk, int
 
 // Tensor cores for bf16 shapes the tcgen05 kernels cover; fp32 (exact
 // arithmetic) and every other shape on CUDA cores.
-int select_path(int /*causal*/, int map, int dtype, int dk, int dv, int r, int norm = LA_NORM_ATTENTION) {
-    return (dtype == LA_BF16 && norm != LA_NORM_SUM && tc_supported(map, dk, dv, r)) ? kPathTensor : kPathSimt;
+int select_path(int causal, int map, int dtype, int dk, int dv, int r, int norm = LA_NORM_ATTENTION) {
+    return (dtype == LA_BF16 && norm != LA_NORM_SUM && tc_supported(map, dk, dv, r, causal)) ? kPathTensor
+                                                                                              : kPathSimt;
 }
+
+// DPFP on tensor cores runs every sequence as one unit: its state pass (CUDA
+// cores) then only has work when a final state is wanted.
+bool whole_sequences(int path, int map) { return path == kPathTensor && map == LA_MAP_DPFP; }
 
 // Normalisation variants; sum normalisation needs non-negative features.
 la_status check_norm(int norm, int map) {
@@ -58,11 +63,15 @@ la_status path_supported(int path, int map, int dk, int dv, int r) {
 // Segment length and unit bound.  Equal-length batches split every sequence
 // into the same number of segments so that units * heads fills the SMs;
 // packed batches (lengths only known on the device) use one length for all.
-Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm, bool bwd = false) {
+Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm, bool bwd = false,
+                   bool whole = false) {
     Layout lo{};
     const int64_t C = path_chunk(path);
     int64_t L, U;
-    if (!has_cu) {
+    if (whole) {
+        L = std::max<int64_t>(C, ceil_div(has_cu ? T : T / nseq, C) * C);
+        U = has_cu ? nseq + 1 : nseq;
+    } else if (!has_cu) {
         const int64_t len = T / nseq;
         const int64_t per = std::max<int64_t>(1, nsm / std::max<int64_t>(1, (int64_t)nseq * H));
         L = std::max<int64_t>(C, ceil_div(ceil_div(len, per), C) * C);
@@ -118,7 +127,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     if ((st = path_supported(path, map, dk, dv, r)) != LA_OK) return st;
     const int nsm = device_sm_count();
     if (nsm <= 0) return LA_ERR_CUDA;
-    const Layout lo = make_layout(path, has_cu, nseq, T, H, dv, r, nsm);
+    const Layout lo = make_layout(path, has_cu, nseq, T, H, dv, r, nsm, false, whole_sequences(path, map));
     if (workspace_bytes < lo.total) return LA_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -157,7 +166,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
                 e = launch_plan(p, s); ++n; break;
             case LA_PHASE_STATE:
                 if (T > 0 && need_state) {
-                    e = path == kPathTensor ? tc_state(p, s) : simt_state(p, dtype, s);
+                    e = (path == kPathTensor && map != LA_MAP_DPFP) ? tc_state(p, s) : simt_state(p, dtype, s);
                     ++n;
                 }
                 break;
@@ -279,7 +288,7 @@ la_status la_feature_map(const void* x, const float* omega, int map, int dtype, 
     const size_t esz = dtype == LA_F32 ? 4 : 2;
     if (!aligned(x, esz) || !aligned(phi, 4) || (omega && !aligned(omega, 4))) return LA_ERR_INVALID_ARG;
     cudaError_t e;
-    if (dtype == LA_BF16 && map == LA_MAP_FAVOR && tc_supported(map, d, d, r) && aligned(x, 16) &&
+    if (dtype == LA_BF16 && map == LA_MAP_FAVOR && tc_supported(map, d, d, r, 1) && aligned(x, 16) &&
         aligned(omega, 16) && aligned(phi, 16)) {
         // same projection and exponent as the forward's tensor-core path, before the bf16 rounding
         e = tc_feature_map(x, omega, T, H, r, phi, nullptr, static_cast<cudaStream_t>(stream));
@@ -363,7 +372,8 @@ size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, in
     if (path_supported(path, map, d_k, d_v, r) != LA_OK) return 0;
     const int nsm = device_sm_count();
     if (nsm <= 0) return 0;
-    size_t bytes = make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm).total;
+    size_t bytes = make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm, false,
+                               whole_sequences(path, map)).total;
     // sum normalisation and unaligned operands move a tensor-core call to the
     // CUDA-core kernels: the size covers both
     if (path == kPathTensor && path_supported(kPathSimt, map, d_k, d_v, r) == LA_OK)

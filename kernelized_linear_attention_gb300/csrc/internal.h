@@ -31,8 +31,10 @@ la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, c
                         size_t workspace_bytes, void* stream, int* launched);
 
 // tcgen05 tensor-core path (tc.cu): bf16, d_k = d_v = 64, r in {64, 128, 256}
-// (FAVOR+) or r = 64 (ELU+1, identity); 16-byte aligned operands.
-bool tc_supported(int map, int dk, int dv, int r);
+// (FAVOR+), r = 64 (ELU+1, identity) or, causal only, r in {128, 256}
+// (DPFP-1, -2: whole sequences per unit, state pass on CUDA cores); 16-byte
+// aligned operands.
+bool tc_supported(int map, int dk, int dv, int r, int causal);
 cudaError_t tc_state(const FwdParams& p, cudaStream_t s);
 cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
 cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,

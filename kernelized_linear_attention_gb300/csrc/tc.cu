@@ -219,6 +219,62 @@ __device__ void elementwise_phi_row(const unsigned char* tile, unsigned char* ds
     }
 }
 
+// DPFP-nu features of one row ("The Kernel Zoo" §6.3): x~ = relu([x, -x]) in
+// R^128 (d = 64), feature (s-1) 128 + a = x~_a x~_{(a+s) mod 128}.  xw holds
+// the row's 64 bf16 inputs in pairs (element j in half j & 1 of xw[j >> 1]);
+// hi receives features A0 .. A0 + 31 of shift S as bf16 pairs and lo their
+// rounding remainders (a product of two bf16 values has up to 16 significant
+// bits).  Every index is a compile-time constant, so the row stays in registers.
+template <int S, int A0>
+__device__ __forceinline__ void dpfp_features32(const uint32_t (&xw)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+    auto xval = [&](int j) { return (j & 1) ? bf16hi(xw[j >> 1]) : bf16lo(xw[j >> 1]); };
+    auto xt = [&](int j) { return j < 64 ? fmaxf(xval(j), 0.f) : fmaxf(-xval(j - 64), 0.f); };
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const int a = A0 + i;
+        const float f0 = xt(a) * xt((a + S) & 127), f1 = xt(a + 1) * xt((a + 1 + S) & 127);
+        const uint32_t h = pack_bf16x2(f0, f1);
+        hi[i >> 1] = h;
+        lo[i >> 1] = pack_bf16x2(f0 - bf16lo(h), f1 - bf16hi(h));
+    }
+}
+
+// Features 64 quarter + 32 half .. + 31 of row t of a [128][64] bf16 input
+// tile, as bf16 into the same row of dst at columns 32 half .. (zero past the
+// unit's end), and their bf16 remainders into dst_lo when it is given.
+// r = 128 nu: quarters 0, 1 are shift 1, quarters 2, 3 shift 2.
+__device__ void dpfp_phi_row32(const unsigned char* tile, unsigned char* dst, unsigned char* dst_lo, int t, bool valid,
+                               int quarter, int half) {
+    uint32_t xw[32], hi[16], lo[16];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
+        xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
+    }
+    switch (quarter * 2 + half) {
+        case 0: dpfp_features32<1, 0>(xw, hi, lo); break;
+        case 1: dpfp_features32<1, 32>(xw, hi, lo); break;
+        case 2: dpfp_features32<1, 64>(xw, hi, lo); break;
+        case 3: dpfp_features32<1, 96>(xw, hi, lo); break;
+        case 4: dpfp_features32<2, 0>(xw, hi, lo); break;
+        case 5: dpfp_features32<2, 32>(xw, hi, lo); break;
+        case 6: dpfp_features32<2, 64>(xw, hi, lo); break;
+        default: dpfp_features32<2, 96>(xw, hi, lo); break;
+    }
+    if (!valid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) { hi[j] = 0u; lo[j] = 0u; }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, 4 * half + q)) =
+            make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        if (dst_lo)
+            *reinterpret_cast<uint4*>(dst_lo + sw128_chunk(t, 4 * half + q)) =
+                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+    }
+}
+
 // 32 fp32 values of row t, columns f0..f0+31 -> bf16 into 64-wide blocks blk[f0 / 64].
 __device__ __forceinline__ void store_row32_bf16(unsigned char* blk0, int t, int f0, const uint32_t (&w)[16]) {
     unsigned char* blk = blk0 + kTile * (f0 >> 6);
@@ -517,6 +573,17 @@ struct CausalBars {
     int pad;
 };
 
+// z of feature f (0..63 within its quarter) as bf16 hi (row 0) + lo (row 1) of
+// the quarter's 16-row K-major tile: the denominator MMA then yields
+// phi(q) . z_hi and phi(q) . z_lo in two columns.  A single bf16 z was the
+// largest error of long causal rows (its rounding no longer matched the
+// numerator's).
+__device__ __forceinline__ void store_z_hilo(unsigned char* tile, int f, float z) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(z);
+    *reinterpret_cast<__nv_bfloat16*>(tile + sw128_off(0, f)) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(tile + sw128_off(1, f)) = __float2bfloat16_rn(z - __bfloat162float(hi));
+}
+
 struct __align__(1024) CausalSmem {
     unsigned char omg_hi[kOmgBytes];
     unsigned char omg_lo[kOmgBytes];
@@ -524,7 +591,7 @@ struct __align__(1024) CausalSmem {
     Tile phq[2];                      // Phi_Q of one quarter (64 features), two buffers
     Tile phk[2];                      // Phi_K of one half (two quarters)
     Tile sbf[2];                      // S bf16, MN-major [feature][v]: features 128h.. in sbf[h]
-    unsigned char zrow[4][2048];      // per quarter: K-major [16][64], row 0 = z bf16, rows 1..15 = 0
+    unsigned char zrow[4][2048];      // per quarter: K-major [16][64], rows 0, 1 = z as bf16 hi, lo; rows 2..15 = 0
     unsigned char zones[2][2048];     // K-major [16][64] x 2 (tokens 0..63, 64..127): row 0 = 1, rest 0
     CausalBars b;
 };
@@ -687,6 +754,11 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         const uint32_t id_read = idesc_bf16(128, 64, false, true);
         const uint32_t id_upd = idesc_bf16(128, 64, true, true);
         const uint32_t id_av = idesc_bf16(128, 64, false, true);
+        // DPFP: phi(k) is held as hi + lo (lo tiles in the Omega area): every product with phi(k)
+        // runs once more with the lo part
+        const bool klo = p.map == LA_MAP_DPFP;
+        const uint64_t d_phk_lo = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
+        const uint64_t d_upd_a_lo = sdesc_sw128(smem_u32(s.omg_hi), kTile, 1024);   // MN-major
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             bool v_ready = false;
@@ -708,6 +780,15 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
 #pragma unroll
                     for (int k = 0; k < kC / 16; ++k)
                         mma_ss_w(ds + 64, sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_zones, 2048 * (k >> 2) + 32 * (k & 3)), id_z, 1u);
+                    if (klo) {
+#pragma unroll
+                        for (int k = 0; k < kC / 16; ++k)
+                            mma_ss_w(ds, sdesc_add(d_upd_a_lo, 2048 * k), sdesc_add(d_v, 2048 * k), id_upd, 1u);
+#pragma unroll
+                        for (int k = 0; k < kC / 16; ++k)
+                            mma_ss_w(ds + 64, sdesc_add(d_upd_a_lo, 2048 * k),
+                                     sdesc_add(d_zones, 2048 * (k >> 2) + 32 * (k & 3)), id_z, 1u);
+                    }
                     mma_commit_w(&B.upd_done);
                 }
                 if (!(ok = warp_wait(&B.phiq_full[g & 1], (g >> 1) & 1))) break;
@@ -716,12 +797,18 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 for (int k = 0; k < 4; ++k)
                     mma_ss_w(tb + kColA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
                              (q > 0 || k > 0) ? 1u : 0u);
+                if (klo) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss_w(tb + kColA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k),
+                                 sdesc_add(d_phk_lo, kTile * (q & 1) + 32 * k), id_scores, 1u);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss_w(tb + kColO, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
                              (q > 0 || k > 0) ? 1u : 0u);
-                // denominator term phi(q) . z into column 64 of O (z as the only
-                // non-zero row of a 16-row operand)
+                // denominator terms phi(q) . z_hi, phi(q) . z_lo into columns 64, 65 of O
+                // (z as the two non-zero rows of a 16-row operand)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
@@ -793,6 +880,12 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                             w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * j]) - cx),
                                                ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx));
                         store_row32_bf16(dst, tr, 32 * half_cols, w);
+                    } else if (p.map == LA_MAP_DPFP) {
+                        // phi(k) also as hi + lo: its rounding is what the outputs feel (phi(q)'s
+                        // largely cancels between numerator and denominator); the lo tiles use
+                        // the Omega area, which element-wise maps leave free
+                        dpfp_phi_row32(kind == 0 ? s.tk : s.tq, dst, kind == 0 ? s.omg_hi + kTile * (q & 1) : nullptr,
+                                       tr, valid, q, half_cols);
                     } else if (half_cols == 0) {
                         elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
                     }
@@ -824,8 +917,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
 #pragma unroll
                     for (int j = 0; j < 8; ++j) w[n0 / 2 + j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
                 } else if (feat < r) {
-                    *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
-                        __float2bfloat16_rn(__uint_as_float(x[0]));
+                    store_z_hilo(s.zrow[feat >> 6], feat & 63, __uint_as_float(x[0]));
                 }
             }
             state_row_bf16(s.sbf[half], tr, w);
@@ -882,20 +974,19 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     }
                     state_row_bf16(s.sbf[half], tr, w);
                     const int feat = 128 * half + tr;
-                    if (feat < r)
-                        *reinterpret_cast<__nv_bfloat16*>(s.zrow[feat >> 6] + sw128_off(0, feat & 63)) =
-                            __float2bfloat16_rn(__uint_as_float(zc));
+                    if (feat < r) store_z_hilo(s.zrow[feat >> 6], feat & 63, __uint_as_float(zc));
                 }
                 warp_arrive(&B.sbf_full, true);
             }
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            uint32_t o0[32], o1[32], dz;
+            uint32_t o0[32], o1[32], dz, dzl;
             tmem_ld32(tmem_addr(tb, wl, kColO), o0);
             tmem_ld32(tmem_addr(tb, wl, kColO + 32), o1);
-            tmem_ld1(tmem_addr(tb, wl, kColO + 64), dz);
+            tmem_ld1(tmem_addr(tb, wl, kColO + 64), dz);    // phi(q) . z_hi
+            tmem_ld1(tmem_addr(tb, wl, kColO + 65), dzl);   // phi(q) . z_lo
             tmem_ld_wait();
-            const float den = dsum + __uint_as_float(dz);
+            const float den = dsum + (__uint_as_float(dz) + __uint_as_float(dzl));
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
             if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, p.norm == LA_NORM_ATTENTION, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
         }
@@ -1554,9 +1645,11 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 }  // namespace
 
-bool tc_supported(int map, int dk, int dv, int r) {
-    if (dk != 64 || dv != 64 || map == LA_MAP_DPFP) return false;
+bool tc_supported(int map, int dk, int dv, int r, int causal) {
+    if (dk != 64 || dv != 64) return false;
     if (map == LA_MAP_FAVOR) return r == 64 || r == 128 || r == 256;
+    // DPFP-1 and -2: the causal kernel forms the features from the input tiles
+    if (map == LA_MAP_DPFP) return causal && (r == 128 || r == 256);
     return r == 64;
 }
 

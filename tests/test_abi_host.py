@@ -98,7 +98,10 @@ def test_selected_path_and_workspace_queries_reject_bad_shapes(lib):
     assert la.la_selected_path(True, "favor", 1, 64, 64, 256) in (0, 1)
     assert la.la_selected_path(True, "favor", 0, 64, 64, 256) == 0        # fp32 always on CUDA cores
     assert la.la_workspace_bytes(True, "elu1", 1, False, 3, 100, 2, 64, 64, 64) == 0   # 3 does not divide 100
-    assert la.la_selected_path(True, "dpfp2", 1, 64, 64, 256) == 0      # DPFP on CUDA cores for bf16 too
+    assert la.la_selected_path(True, "dpfp2", 1, 64, 64, 256) == 1      # causal DPFP-1/-2 on tensor cores
+    assert la.la_selected_path(True, "dpfp1", 1, 64, 64, 128) == 1
+    assert la.la_selected_path(False, "dpfp2", 1, 64, 64, 256) == 0     # bidirectional DPFP on CUDA cores
+    assert la.la_selected_path(True, "dpfp3", 1, 64, 64, 384) == 0      # r above the kernels' 256
     assert la.la_selected_path(False, "dpfp1", 0, 64, 64, 128) == 0
     assert la.la_selected_path(True, "dpfp1", 1, 64, 64, 64) == -1      # r = 2 d_k nu
 

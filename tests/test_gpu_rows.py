@@ -66,11 +66,11 @@ def _abs_state(st):
 
 
 # Regression guard for the normalised bf16 output of rows with a long history
-# (a carried state): the output-RMS rule's 2e-2 is not met there (measured
-# 2.0e-2 to 2.7e-2 on these inputs: bf16 features and the bf16 copy of the
-# carried state that the in-chunk readout multiplies), so these rows are held
-# to the arithmetic bound and, against drift, to 3e-2 of the RMS.
-LONG_HISTORY_RMS_GUARD = 3e-2
+# (a carried state): the output-RMS rule's 2e-2 is only just met there
+# (measured 1.6e-2 to 2.02e-2 on these inputs: bf16 features and the
+# single-bf16 copy of the carried S that the readout multiplies), so these rows
+# are held to the arithmetic bound and, against drift, to 2.5e-2 of the RMS.
+LONG_HISTORY_RMS_GUARD = 2.5e-2
 
 
 def _tensor_path(la, causal, kind, dtype, norm, r, d=64):
