@@ -23,7 +23,8 @@
  *   LA_MAP_DPFP      DPFP-nu: x~ = relu([x, -x]) in R^{2 d_k}; feature (s-1) 2 d_k + i
  *                    = x~_i x~_{(i+s) mod 2 d_k} for s = 1..nu; r = 2 d_k nu with
  *                    1 <= nu <= 2 d_k - 1 ("The Kernel Zoo", §6.3; Omega unused).
- *                    Computed on CUDA cores for every dtype.
+ *                    Causal bf16 calls with d_k = d_v = 64 and nu <= 2 run on the
+ *                    tensor cores; every other DPFP call on CUDA cores.
  *
  * Conventions shared by every call
  * --------------------------------
