@@ -430,7 +430,8 @@ def run_ours(args):
         byts = alg["bytes"] * token_heads / 2 if dom == "state" else alg_bytes
         achieved = byts / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 and w.norm != "sum" else "simt"
+    path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 and not (w.norm == "sum" and w.carry) \
+        else "simt"
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(path, dom, w.name)
     roof["kernel"] = dom
@@ -593,7 +594,8 @@ def forward_variants(la, dev, stream, peaks, steps, w, dev_qkv, omega) -> dict:
     a, keep = args_for(wl, qkv, None)
     pm, n = _phase_timed(la, stream, steps, a, norm="sum")
     alg = algorithmic(wl)
-    s = summary(wl, pm, n, "sum normalisation, CUDA-core kernels")
+    s = summary(wl, pm, n, "sum normalisation on tensor cores: feature sums, values / sigma_k, unnormalised "
+                           "kernels, output / sigma_q")
     s["hbm_frac_of_output"] = alg["bytes"] * wl.T * wl.H / (pm["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
     out["sum"] = s
     return out

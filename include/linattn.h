@@ -173,7 +173,11 @@ LA_API la_status la_forward_causal(const void* q, const void* k, const void* v, 
  *              workspace otherwise.
  *   Other arguments as for la_forward_bidir / la_forward_causal, with
  *   la_workspace_bytes(causal, ...).  Both state arrays must be 4-byte aligned.
- *   LA_NORM_SUM runs on the CUDA-core kernels.
+ *   LA_NORM_SUM on the tensor-core path (shapes la_selected_path reports as 1,
+ *   no carried state): the plan phase computes the feature sums of every q and
+ *   k row and writes v / max(sigma_k, eps) into `out`, the kernels form the
+ *   unnormalised output of those values, and the output phase divides it by
+ *   max(sigma_q, eps).  With a carried state it runs on the CUDA-core kernels.
  */
 LA_API la_status la_forward(int causal, int norm, const void* q, const void* k, const void* v,
                             const float* omega, int map, int dtype, const int32_t* cu_seqlens, int nseq,
@@ -331,9 +335,8 @@ LA_API la_status la_orthogonal_features(const double* gauss_blocks, const double
 /*
  * la_selected_path - which kernels a forward call with these arguments runs:
  *   0 = fp32 CUDA-core kernels, 1 = tcgen05 tensor-core kernels.  Assumes
- *   16-byte aligned pointers and LA_NORM_ATTENTION or LA_NORM_NONE
- *   (LA_NORM_SUM always runs on the CUDA-core kernels).  Returns -1 for
- *   arguments a call would reject.
+ *   16-byte aligned pointers and no carried state under LA_NORM_SUM.
+ *   Returns -1 for arguments a call would reject.
  */
 LA_API int la_selected_path(int causal, int map, int dtype, int d_k, int d_v, int r);
 

@@ -90,6 +90,8 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     const size_t state_bytes = sizeof(float) * (size_t)U * H * r * lo.dvx;
     lo.partial = o;   o = align_up(o + state_bytes, kAlign);
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
+    lo.sig_q = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
+    lo.sig_k = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     if (bwd) {
         lo.suffix = o; o = align_up(o + state_bytes, kAlign);
         lo.g = o;      o = align_up(o + sizeof(float) * (size_t)T * H * lo.dvx, kAlign);
@@ -119,7 +121,10 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     const size_t esz = dtype == LA_F32 ? 4 : 2;
     if (!aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) || !aligned(out, esz)) return LA_ERR_INVALID_ARG;
     if (omega && !aligned(omega, 4)) return LA_ERR_INVALID_ARG;
-    int path = select_path(causal, map, dtype, dk, dv, r, norm);
+    int path = select_path(causal, map, dtype, dk, dv, r);
+    // sum normalisation with a carried state stays on the CUDA-core kernels (their states hold
+    // the sum-normalised z; the tensor-core route below scales only the values)
+    if (norm == LA_NORM_SUM && (state_in || state_out)) path = kPathSimt;
     // TMA and vector loads need 16-byte aligned operands
     if (path == kPathTensor && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) &&
                                  (omega == nullptr || aligned(omega, 16))))
@@ -138,11 +143,22 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     p.H = H; p.dk = dk; p.dv = dv; p.r = r; p.dvx = lo.dvx;
     p.map = map; p.causal = causal; p.norm = norm; p.eps = eps;
     p.state_in = state_in; p.state_out = state_out;
+    // Sum normalisation on tensor cores: the kernels compute the unnormalised output for the
+    // values v / sigma_k, which the plan phase writes into `out`; the output phase divides by
+    // sigma_q (norm.cu).
+    const bool tc_sum = path == kPathTensor && norm == LA_NORM_SUM;
+    if (tc_sum) {
+        p.v = out;
+        p.norm = LA_NORM_NONE;
+    }
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.units = reinterpret_cast<Unit*>(ws + lo.units);
     p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
     p.partial = reinterpret_cast<float*>(ws + lo.partial);
     p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
+    p.sig_q = reinterpret_cast<float*>(ws + lo.sig_q);
+    p.sig_k = reinterpret_cast<float*>(ws + lo.sig_k);
+    if (tc_sum) p.div_rows = p.sig_q;   // the output kernels divide by max(sigma_q, eps)
     p.U = lo.U; p.L = lo.L;
 
     // A causal call whose sequences are all single segments starts every unit
@@ -163,7 +179,19 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     for (int ph = phase_lo; ph <= phase_hi && e == cudaSuccess; ++ph) {
         switch (ph) {
             case LA_PHASE_PLAN:
-                e = launch_plan(p, s); ++n; break;
+                e = launch_plan(p, s); ++n;
+                if (e == cudaSuccess && tc_sum && T > 0) {
+                    if (map == LA_MAP_FAVOR) {
+                        e = tc_feature_sums(q, omega, T, H, r, p.sig_q, &p.hdr->error, s);
+                        if (e == cudaSuccess) e = tc_feature_sums(k, omega, T, H, r, p.sig_k, &p.hdr->error, s);
+                        if (e == cudaSuccess) e = sum_scale_values(v, p.sig_k, eps, T, H, dv, out, s);
+                        n += 3;
+                    } else {
+                        e = sum_prologue_elementwise(q, k, v, map, T, H, r, eps, p.sig_q, out, s);
+                        ++n;
+                    }
+                }
+                break;
             case LA_PHASE_STATE:
                 if (T > 0 && need_state) {
                     e = (path == kPathTensor && map != LA_MAP_DPFP) ? tc_state(p, s) : simt_state(p, dtype, s);

@@ -34,6 +34,8 @@ struct Layout {
     size_t seq_first;  // int[nseq + 1]: first unit of each sequence (+ total)
     size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
+    size_t sig_q;      // float[T][H]: sum_f phi_f(q) (sum normalisation on the tensor-core path)
+    size_t sig_k;      // float[T][H]: sum_f phi_f(k)
     size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
     size_t g;          // backward: float[T][H][dvx], d num | d den of every row
     size_t omega_t;    // backward: float[dk][r], Omega transposed
@@ -76,6 +78,9 @@ struct FwdParams {
     float* suffix;          // [U][H][r][dvx] workspace: sum of phi(q_i) g_i^T over later units
     int reverse;            // scan: suffix (later units) instead of prefix
     float* omega_t;         // [dk][r] workspace: Omega transposed (coalesced feature loads)
+    float* sig_q;           // [T][H] workspace: feature sums of q and k (sum normalisation)
+    float* sig_k;
+    const float* div_rows;  // [T][H] or NULL: tensor-core outputs are divided by max(div_rows, eps)
     // workspace regions
     WsHeader* hdr;
     Unit* units;

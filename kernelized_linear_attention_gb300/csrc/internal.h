@@ -39,6 +39,17 @@ cudaError_t tc_state(const FwdParams& p, cudaStream_t s);
 cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
 cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
                            cudaStream_t s);
+// sums[t][h] = sum_f phi_f(x_th) for the FAVOR+ map (same projection and exponent as tc_feature_map)
+cudaError_t tc_feature_sums(const void* x, const float* omega, int64_t T, int H, int r, float* sums, int* err,
+                            cudaStream_t s);
+
+// Sum normalisation on the tensor-core path (norm.cu): out = phi(q)^T S' / max(sigma_q, eps) with
+// S' built from v / max(sigma_k, eps), sigma = sum_f phi_f; the output kernels divide (p.div_rows).
+cudaError_t sum_scale_values(const void* v, const float* sigma_k, float eps, int64_t T, int H, int dv, void* dst,
+                             cudaStream_t s);
+// element-wise maps, d_k = d_v = 64: sigma_q into sig_q and v / max(sigma_k, eps) into dst in one pass
+cudaError_t sum_prologue_elementwise(const void* q, const void* k, const void* v, int map, int64_t T, int H, int r,
+                                     float eps, float* sig_q, void* dst, cudaStream_t s);
 
 // Backward pass on CUDA cores (bwd.cu): bwd_q writes g, dq and each unit's
 // sum of phi(q) g^T (p.partial); bwd_kv writes dk, dv from p.suffix.

@@ -324,6 +324,20 @@ __device__ void projection_to_global(uint32_t tbase, int nf, float c, bool valid
     }
 }
 
+// Sum over features nf of phi = 2^(P - c) of this thread's row (TMEM lane), in fp32.
+__device__ float projection_rowsum(uint32_t tbase, int nf, float c) {
+    const int warp = threadIdx.x >> 5;
+    float acc = 0.f;
+    for (int f0 = 0; f0 < nf; f0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tbase, warp * 32, kColP + f0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc += ex2_approx(__uint_as_float(v[j]) - c);
+    }
+    return acc;
+}
+
 // The fp32 state a unit starts from ([r][65] in global; zero if `zero`):
 // into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
 // rounding remainder into lo when lo != nullptr).
@@ -988,7 +1002,11 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             tmem_ld_wait();
             const float den = dsum + (__uint_as_float(dz) + __uint_as_float(dzl));
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
-            if (valid) store_output_row(o0, o1, __float_as_uint(den), p.eps, p.norm == LA_NORM_ATTENTION, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+            const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
+            // sum normalisation divides by sigma_q of the row instead of the attention denominator
+            const float dv_ = p.div_rows ? (valid ? p.div_rows[orow] : 1.f) : den;
+            if (valid) store_output_row(o0, o1, __float_as_uint(dv_), p.eps, p.norm == LA_NORM_ATTENTION || p.div_rows,
+                                        out + orow * 64);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1241,8 +1259,11 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
             tmem_ld1(tmem_addr(tb, wl, kColBO + 64), den);
             tmem_ld_wait();
             warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O
-            if (tr < min(kC, un.end - t0))
-                store_output_row(o0, o1, den, p.eps, p.norm == LA_NORM_ATTENTION, out + ((int64_t)(t0 + tr) * p.H + head) * 64);
+            if (tr < min(kC, un.end - t0)) {
+                const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
+                const uint32_t dv_ = p.div_rows ? __float_as_uint(p.div_rows[orow]) : den;
+                store_output_row(o0, o1, dv_, p.eps, p.norm == LA_NORM_ATTENTION || p.div_rows, out + orow * 64);
+            }
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1569,7 +1590,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fmap_kernel(const __grid_constant__ CUtensorMap map_x, const float* omega, int T, int H, int r, float* phi,
-               int* err) {
+               float* sums, int* err) {
     FmapSmem& s = smem_ref<FmapSmem>();
     const int t = threadIdx.x, head = blockIdx.y;
     const int t0 = blockIdx.x * kC;
@@ -1589,6 +1610,7 @@ tc_fmap_kernel(const __grid_constant__ CUtensorMap map_x, const float* omega, in
     if (ok) {
         const float c = favor_offset(s.tq, t, r);
         const bool valid = t0 + t < T;
+        float rowsum = 0.f;
         for (int half = 0; half < nhalves; ++half) {
             if (t == 0) {
                 mma_projection(tb + kColP, s.tq, s.omg_hi, s.omg_lo, 128 * half, fh);
@@ -1596,11 +1618,13 @@ tc_fmap_kernel(const __grid_constant__ CUtensorMap map_x, const float* omega, in
             }
             if (!(ok = mp.wait(&s.b.mma))) break;
             tc_fence_after();
-            projection_to_global(tb, fh, c, valid, phi + ((int64_t)(t0 + t) * H + head) * r + 128 * half);
+            if (phi) projection_to_global(tb, fh, c, valid, phi + ((int64_t)(t0 + t) * H + head) * r + 128 * half);
+            else rowsum += projection_rowsum(tb, fh, c);
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
         }
+        if (ok && !phi && valid) sums[(int64_t)(t0 + t) * H + head] = rowsum;   // sum_f phi_f of the row
     }
     if (!ok) drain_after_timeout(s.b, err);
     teardown(s.b);
@@ -1695,16 +1719,26 @@ cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
-                           cudaStream_t s) {
+static cudaError_t launch_fmap(const void* x, const float* omega, int64_t T, int H, int r, float* phi, float* sums,
+                               int* err, cudaStream_t s) {
     CUtensorMap mx;
     if (!make_row_map(&mx, x, T, H)) return cudaErrorInvalidValue;
     const size_t bytes = smem_bytes<FmapSmem>();
     cudaError_t e = set_smem(tc_fmap_kernel, bytes);
     if (e != cudaSuccess) return e;
     tc_fmap_kernel<<<dim3((unsigned)ceil_div(T, kC), (unsigned)H), kThreads, bytes, s>>>(mx, omega, (int)T, H, r,
-                                                                                        phi, err);
+                                                                                        phi, sums, err);
     return cudaGetLastError();
+}
+
+cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,
+                           cudaStream_t s) {
+    return launch_fmap(x, omega, T, H, r, phi, nullptr, err, s);
+}
+
+cudaError_t tc_feature_sums(const void* x, const float* omega, int64_t T, int H, int r, float* sums, int* err,
+                            cudaStream_t s) {
+    return launch_fmap(x, omega, T, H, r, nullptr, sums, err, s);
 }
 
 }  // namespace la

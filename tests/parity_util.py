@@ -80,10 +80,12 @@ def _bound_ratio(got, ref, scale, stored_bf16):
     return float(np.max(excess / np.where(scale > 0, scale, 1.0))) / BF16_U if ref.size else 0.0
 
 
-def assert_within_rounding_bound(got, ref, M, what=""):
-    """Unnormalised bf16-path output: |got - ref| <= 3.25u M + u |ref|."""
+def assert_within_rounding_bound(got, ref, M, what="", units=3.25):
+    """Unnormalised bf16-path output: |got - ref| <= 3.25u M + u |ref|.  Under sum
+    normalisation on tensor cores the values enter as bf16(v / sigma_k), one
+    rounding more: units = 4.25, M the sum-normalised output for |v|."""
     k = _bound_ratio(got, ref, M, True)
-    assert k <= 3.25, f"{what}: error {k:.2f} u M > 3.25 u M"
+    assert k <= units, f"{what}: error {k:.2f} u M > {units} u M"
     return k
 
 

@@ -73,9 +73,11 @@ def _abs_state(st):
 LONG_HISTORY_RMS_GUARD = 2.5e-2
 
 
-def _tensor_path(la, causal, kind, dtype, norm, r, d=64):
+def _tensor_path(la, causal, kind, dtype, norm, r, d=64, carried=False):
+    """Whether the call runs the tensor-core kernels (sum normalisation with a
+    carried state stays on CUDA cores)."""
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    return norm != "sum" and la.la_selected_path(causal, kind, tdt, d, d, r) == 1
+    return not (norm == "sum" and carried) and la.la_selected_path(causal, kind, tdt, d, d, r) == 1
 
 
 # ----------------------------------------------------------------------------
@@ -96,10 +98,13 @@ def test_norm_variants_ragged_packed(la, dtype, kind, causal, norm):
     out = la.la_forward(q, k, v, kind, omega=om_t, causal=causal, norm=norm, cu_seqlens=cu)
     torch.cuda.synchronize()
     ref = oracle.forward(inp.q, inp.k, inp.v, kind, causal, omega=om, cu_seqlens=inp.cu_seqlens, norm=norm)
-    if norm == "none" and dtype == "bf16":
+    tensor = _tensor_path(la, causal, kind, dtype, norm, 256 if kind == "favor" else (128 if kind == "dpfp1" else 64))
+    if tensor:
+        # unnormalised and sum-normalised rows grow with position: the arithmetic bound, not one RMS
         M = oracle.forward(inp.q, inp.k, np.abs(inp.v), kind, causal, omega=om, cu_seqlens=inp.cu_seqlens,
-                           norm="none")
-        assert_within_rounding_bound(from_torch(out), ref, M, f"{kind} causal={causal} norm=none")
+                           norm=norm)
+        assert_within_rounding_bound(from_torch(out), ref, M, f"{kind} causal={causal} norm={norm}",
+                                     units=4.25 if norm == "sum" else 3.25)
     else:
         assert_close(from_torch(out), ref, dtype, f"{kind} causal={causal} norm={norm}")
 
