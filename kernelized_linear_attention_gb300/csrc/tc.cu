@@ -770,7 +770,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         const uint32_t id_av = idesc_bf16(128, 64, false, true);
         // DPFP: phi(k) is held as hi + lo (lo tiles in the Omega area): every product with phi(k)
         // runs once more with the lo part
-        const bool klo = p.map == LA_MAP_DPFP;
+        const bool klo = !favor && p.map == LA_MAP_DPFP;   // compile-time false for FAVOR+
         const uint64_t d_phk_lo = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
         const uint64_t d_upd_a_lo = sdesc_sw128(smem_u32(s.omg_hi), kTile, 1024);   // MN-major
         bool ok = true;
