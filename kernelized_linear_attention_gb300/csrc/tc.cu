@@ -96,10 +96,9 @@ struct StateBars {
     uint64_t k_full[kStateStages], k_empty[kStateStages];   // TMA -> NE / PE;  (projection commit + NE) / 8 PE warps -> TMA
     uint64_t v_full[kStateStages], v_empty[kStateStages];   // TMA -> update issuer;  its commit -> TMA
     uint64_t cx_full[kStateStages];   // NE -> projection issuer: exponent offsets of the stage's tokens staged
-    uint64_t p_full[2];      // MMA commit -> PE: phi exponent of a feature half in fp32 buffer b
-    uint64_t p_empty[2];     // PE (8 warps) -> MMA: buffer b read out
-    uint64_t a_full[2];      // PE (8 warps) -> MMA: phi(k)^T of a half in bf16 buffer a
-    uint64_t a_empty[2];     // MMA commit -> PE: the update has read buffer a
+    uint64_t p_full[2];      // projection commit -> PE: phi exponent of a feature half in buffer b
+    uint64_t a_full[2];      // PE (8 warps) -> update issuer: phi(k)^T of that half in buffer b (bf16)
+    uint64_t a_empty[2];     // update commit -> projection issuer: buffer b read
     uint64_t drain[2];
     uint32_t tmem_base;
     int pad;
@@ -110,8 +109,8 @@ struct __align__(1024) StateSmem {
     unsigned char omg_lo[kOmgBytes];
     Tile tk[kStateStages], tv[kStateStages];
     Tile bias;                    // K-major [token][64]: columns 16 st, 16 st + 1 = -offset (hi, lo) of stage st
-    Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1
-    float zsum[256];              // normaliser column: second warpgroup's share
+    Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1; rows 0..15 also
+                                  // serve as the ones atom of the update's [V|1] (columns 64, 65)
     StateBars b;
 };
 
@@ -158,18 +157,6 @@ __device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* o
         *reinterpret_cast<uint4*>(hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
     }
-}
-
-__device__ void fill_ones(unsigned char* blk) {
-    for (int i = threadIdx.x; i < kC * 8; i += blockDim.x) {
-        const int row = i >> 3, c = i & 7;
-        *reinterpret_cast<uint4*>(blk + sw128_chunk(row, c)) = make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
-    }
-}
-
-__device__ __forceinline__ void zero_row(unsigned char* blk, int t) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(blk + sw128_chunk(t, c)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // |x_t|^2 of row t of a staged [128][64] bf16 tile.
@@ -285,25 +272,6 @@ __device__ __forceinline__ void store_row32_bf16(unsigned char* blk0, int t, int
             make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
-// Projection epilogue: P (TMEM columns col.., lane = token) -> phi = 2^(p - c)
-// -> bf16 K-major blocks starting at dst (nf features, a multiple of 32).
-__device__ void projection_epilogue(uint32_t tbase, uint32_t col, int nf, float c, bool valid, unsigned char* dst) {
-    const int warp = threadIdx.x >> 5, t = threadIdx.x;
-    for (int f0 = 0; f0 < nf; f0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(tbase, warp * 32, col + f0), v);
-        tmem_ld_wait();
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float a = valid ? ex2_approx(__uint_as_float(v[2 * j]) - c) : 0.f;
-            const float b = valid ? ex2_approx(__uint_as_float(v[2 * j + 1]) - c) : 0.f;
-            w[j] = pack_bf16x2(a, b);
-        }
-        store_row32_bf16(dst, t, f0, w);
-    }
-}
-
 // fp32 projection epilogue for la_feature_map: phi = 2^(p - c) to global fp32.
 __device__ void projection_to_global(uint32_t tbase, int nf, float c, bool valid, float* dst) {
     const int warp = threadIdx.x >> 5;
@@ -367,27 +335,6 @@ __device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[k
         }
     }
     if (to_tmem) tmem_st_wait();
-}
-
-// Writes the fp32 state held in TMEM (features < r, 65 columns) to global [r][65].
-// Zeros instead when `zero` (a unit without tokens); thread f = TMEM lane f.
-__device__ void store_state(uint32_t tbase, float* dst, int r, int nhalves, int f = threadIdx.x, bool zero = false) {
-    const int warp = f >> 5;
-    for (int half = 0; half < nhalves; ++half) {
-        const int feat = 128 * half + f;
-        for (int n0 = 0; n0 < kNX; n0 += 16) {
-            uint32_t w[16] = {};
-            if (!zero) {
-                tmem_ld16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
-                tmem_ld_wait();
-            }
-            if (feat < r) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (n0 + j < 65) dst[(int64_t)feat * 65 + n0 + j] = __uint_as_float(w[j]);
-            }
-        }
-    }
 }
 
 // 32 scores of one row (keys key0 .. key0 + 31) as bf16 hi + lo, two keys per word;
@@ -464,29 +411,6 @@ __device__ __forceinline__ void mma_projection(uint32_t d, const unsigned char* 
     mma_kk(d, x, 0, omg_lo + 128u * f0, 0, 4, idesc, true);
 }
 
-// [S|z] (+)= Phi_K^T [V|1]: A MN-major (features contiguous, blocks phk0, phk0 + kTile),
-// B MN-major (tv | ones at tv + lbo).
-__device__ __forceinline__ void mma_state_update(uint32_t d, const unsigned char* phk0, const unsigned char* tv,
-                                                 const unsigned char* ones) {
-    const uint32_t idesc = idesc_bf16(128, kNX, true, true);
-    const uint32_t lbo_b = smem_u32(ones) - smem_u32(tv);
-    for (int k = 0; k < kC / 16; ++k)
-        mma_ss(d, sdesc_sw128(smem_u32(phk0) + 2048u * k, kTile, 1024),
-               sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
-}
-
-// O += tril(A) [V|1] with the masked scores as two bf16 parts in tensor memory
-// (a_hi, a_lo: 64 columns each, two keys per column), B MN-major.
-__device__ __forceinline__ void mma_in_chunk(uint32_t d, uint32_t a_hi, uint32_t a_lo, const unsigned char* tv,
-                                             const unsigned char* ones) {
-    const uint32_t idesc = idesc_bf16(128, kNX, false, true);
-    const uint32_t lbo_b = smem_u32(ones) - smem_u32(tv);
-    for (int k = 0; k < kC / 16; ++k)
-        mma_ts(d, a_hi + 8u * k, sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
-    for (int k = 0; k < kC / 16; ++k)
-        mma_ts(d, a_lo + 8u * k, sdesc_sw128(smem_u32(tv) + 2048u * k, lbo_b, 1024), idesc, 1u);
-}
-
 __device__ void setup_bars(Bars& b) {
     if (threadIdx.x == 0) {
         mbar_init(&b.load, 1);
@@ -526,20 +450,6 @@ struct Phase {
         const bool ok = wait_all(bar, bit);
         bit ^= 1u;
         return ok;
-    }
-};
-
-// Completion counter of the MMA groups committed to one barrier, one commit at
-// a time outstanding at most two phases apart: wait_for(n) returns once n
-// commits have completed (all threads call it with the same n).
-struct Commits {
-    uint32_t issued = 0, done = 0;
-    __device__ __forceinline__ bool wait_for(uint64_t* bar, uint32_t n) {
-        while (done < n) {
-            if (!wait_all(bar, done & 1u)) return false;
-            ++done;
-        }
-        return true;
     }
 };
 
@@ -1284,30 +1194,36 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // The projection is computed transposed, P^T = Omega' K^T (TMEM lanes = features,
 // columns = tokens); one more K step adds each token's exponent offset -(log2(e)
 // |k|^2 / 2 + log2(sqrt r)) as bf16 hi + lo, so that phi = 2^P^T element-wise.
-// The PE warps turn it into phi(k)^T, write it to tensor memory
-// as bf16 and keep the normaliser z = sum_t phi(k_t) in registers (from the same
-// bf16 values); S += phi(k)^T V takes its A operand from tensor memory.  Neither
-// phi(k) nor the update's A operand passes through shared memory.
-// TMEM: S [0, 128) (64 columns per 128-feature half), two fp32 projection buffers
-// [128, 384), two bf16 phi(k)^T buffers [384, 512).
+// The PE warps turn it into phi(k)^T as bf16 and write it back into the same
+// buffer (the first 32 of each warpgroup's 64 columns); [S|z] += phi(k)^T [V|1]
+// takes its A operand from there and its B operand from V with a ones tile as the
+// second 64-column atom, so z = sum_t phi(k_t) (column 64) comes from the same bf16
+// values as S.  Neither phi(k) nor the update's A operand passes through shared memory.
+// TMEM: [S|z] [0, 160) (80 columns per 128-feature half), two fp32 projection
+// buffers [160, 416).
 // Roles (416 threads):
 //   warp 0 lane 0     TMA: k and v tiles of each chunk into four stages (and L2 prefetch)
 //   warp 1            projection MMAs (one elected lane; warp 1 owns the TMEM
-//                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the PE
-//                     has read that buffer out
-//   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T.
-//                     The two issuers touch disjoint tensor memory and never wait
-//                     on each other
+//                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the
+//                     update has read that buffer's previous phi(k)^T
+//   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T
 //   warps 3, 12 (NE)  the exponent offset of every token of a stage (FAVOR+), into
 //                     the bias operand of the projection (64 tokens each, on two
 //                     different SM sub-partitions)
 //   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
 //                     every half (lane = feature)
-// The state accumulates in TMEM and registers over the unit and is written once.
+// The state accumulates in TMEM over the unit and is written once.
 constexpr int kStateThreads = 416;
-constexpr uint32_t kColSS = 0;     // S, 64 columns per half
-constexpr uint32_t kColPS = 128;   // two 128-column fp32 projection buffers
-constexpr uint32_t kColAS = 384;   // two 64-column bf16 phi(k)^T buffers
+constexpr uint32_t kColSS = 0;     // [S|z], 80 columns per half
+constexpr uint32_t kColPS = 160;   // two 128-column projection buffers (exponent, then phi(k)^T in place)
+
+// Descriptor of K step k (16 token rows) of an MN-major [V|1] operand: the start
+// advances by 2048 B and the leading-dimension offset (bits 16..29, 16-byte units)
+// shrinks by the same amount, so that the second 64-column atom stays on the same
+// 16-row ones tile for every step.
+__device__ __forceinline__ uint64_t v_ones_desc(uint64_t d0, int k) {
+    return d0 + static_cast<uint64_t>(128 * k) - (static_cast<uint64_t>(128 * k) << 16);
+}
 
 
 // kFavor: FAVOR+ (projection by Omega' hi + lo and the offset step), else an
@@ -1343,7 +1259,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
-            mbar_init(&B.p_empty[i], 8);
             mbar_init(&B.a_full[i], 8);
             mbar_init(&B.a_empty[i], 1);
         }
@@ -1385,7 +1300,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = B.tmem_base;
-    float z0 = 0.f, z1 = 0.f;     // PE: this thread's share of z for its feature in halves 0 and 1
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
@@ -1428,7 +1342,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 // exponent of phi(k)^T, features 128h..: Omega' K^T, then one K step of
                 // ones x (-offset hi, -offset lo) per token
                 const int j = c * nhalves + h, b = j & 1;
-                if (j >= 2 && !(ok = warp_wait(&B.p_empty[b], ((j >> 1) - 1) & 1))) break;
+                if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
                 tc_fence_after();
                 const uint32_t d = tb + kColPS + 128 * b, fo = 16384u * h;
 #pragma unroll
@@ -1447,20 +1361,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp == 2) {
         // ------------------------------------------------------------ state-update MMAs (elected lane issues)
-        const uint32_t id_upd = idesc_bf16(128, 64, false, true);     // A from TMEM, B = V MN-major
+        const uint32_t id_upd = idesc_bf16(128, kNX, false, true);    // A from TMEM, B = [V|1] MN-major, N = 80
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
             if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
-            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv[st]), 16, 1024);   // MN-major, one 64-wide atom
+            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv[st]), smem_u32(s.ones) - smem_u32(s.tv[st]), 1024);
             for (int h = 0; h < nhalves && ok; ++h) {
                 const int j = c * nhalves + h, b = j & 1;
                 if (!(ok = warp_wait(&B.a_full[b], (j >> 1) & 1))) break;
                 tc_fence_after();
-                const uint32_t a0 = tb + kColAS + 64 * b;
+                // tokens 16k.. of phi(k)^T: warpgroup k / 4 wrote them to columns 64 (k / 4) + 8 (k % 4)
+                const uint32_t a0 = tb + kColPS + 128 * b;
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ts_w(tb + kColSS + 64 * h, a0 + 8 * k, sdesc_add(d_v, 2048 * k), id_upd,
+                    mma_ts_w(tb + kColSS + kNX * h, a0 + 64 * (k >> 2) + 8 * (k & 3), v_ones_desc(d_v, k), id_upd,
                              (c > 0 || k > 0) ? 1u : 0u);
                 mma_commit_w(&B.a_empty[b]);
             }
@@ -1474,7 +1389,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const int f = wl + lane;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c % kStateStages;
             const int nvalid = min(kC, un.end - (un.start + c * kC));
             for (int h = 0; h < nhalves && ok; ++h) {
                 const int j = c * nhalves + h, b = j & 1;
@@ -1483,12 +1397,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
-                tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg), v0);
-                tmem_ld32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg + 32), v1);
+                const uint32_t col = kColPS + 128 * b + 64 * wg;   // this warpgroup's 64 tokens
+                tmem_ld32(tmem_addr(tb, wl, col), v0);
+                tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
                 tmem_ld_wait();
-                warp_arrive(&B.p_empty[b], false);
-                // the update that read this phi buffer last must be done
-                if (j >= 2 && !(ok = warp_wait(&B.a_empty[b], ((j >> 1) - 1) & 1))) break;
                 if (favor) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -1514,21 +1426,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                         w[16 + e] = live ? pack_bf16x2(x0, x1) : 0u;
                     }
                 }
-                tmem_st32(tmem_addr(tb, wl, kColAS + 64 * b + 32 * wg), w);
-                float zs = 0.f;   // z from the same bf16 values the update multiplies
-#pragma unroll
-                for (int e = 0; e < 32; ++e) zs += bf16lo(w[e]) + bf16hi(w[e]);
-                if (h == 0) z0 += zs;
-                else z1 += zs;
+                tmem_st32(tmem_addr(tb, wl, col), w);   // phi(k)^T in place of the exponent it came from
                 tmem_st_wait();
                 warp_arrive(&B.a_full[b], false);
             }
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
-        if (wg == 1) {
-            s.zsum[f] = z0;
-            s.zsum[128 + f] = z1;
-        }
     } else {
         // ------------------------------------------------------------ NE: exponent offsets (warps 3, 12)
         const int tok0 = warp == 3 ? 0 : 64;      // this warp's 64 tokens
@@ -1561,23 +1464,23 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     __syncthreads();
     tc_fence_after();
-    if (warp >= 4 && warp < 8) {   // [S|z] rows of this thread's feature in each half
+    if (warp >= 4 && warp < 8) {   // [S|z] row of this thread's feature in each half
         const int f = t - 128;
         float* dst = p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65;
         for (int h = 0; h < nhalves; ++h) {
             const int feat = 128 * h + f;
-            for (int n0 = 0; n0 < 64; n0 += 16) {
+            for (int n0 = 0; n0 < 65; n0 += 16) {
                 uint32_t w[16] = {};
                 if (nchunks > 0) {
-                    tmem_ld16(tmem_addr(tb, (warp & 3) * 32, kColSS + 64 * h + n0), w);
+                    tmem_ld16(tmem_addr(tb, (warp & 3) * 32, kColSS + kNX * h + n0), w);
                     tmem_ld_wait();
                 }
                 if (feat < r) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) dst[(int64_t)feat * 65 + n0 + e] = __uint_as_float(w[e]);
+                    for (int e = 0; e < 16; ++e)
+                        if (n0 + e < 65) dst[(int64_t)feat * 65 + n0 + e] = __uint_as_float(w[e]);
                 }
             }
-            if (feat < r) dst[(int64_t)feat * 65 + 64] = (h == 0 ? z0 : z1) + s.zsum[128 * h + f];
         }
     }
     tc_fence_before();
