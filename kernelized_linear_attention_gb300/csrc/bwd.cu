@@ -162,75 +162,6 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
     }
 }
 
-// FAVOR+ features of nrows (<= CS) rows of x ([CS][d] in shared memory) with
-// Omega transposed in global memory (omt [d][r]): one thread per (feature, half
-// of the rows), eight rows at a time, so each Omega value (a coalesced load)
-// and each 4-wide read of x serve eight and four multiply-adds.  Rows past
-// nrows get 0.  Same arithmetic as compute_phi: exp(omega_f . x - |x|^2/2)/sqrt(r).
-__device__ void favor_features_tiled(float* phi, const float* x, float* half_sq, const float* omt, int nrows, int d,
-                                     int r) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int row = warp; row < CS; row += (blockDim.x >> 5)) {
-        float sq = 0.f;
-        for (int c = lane; c < d; c += 32) sq = fmaf(x[row * d + c], x[row * d + c], sq);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (lane == 0) half_sq[row] = 0.5f * sq;
-    }
-    __syncthreads();
-    const float inv_sqrt_r = rsqrtf((float)r);
-    const bool vec = (d & 3) == 0;
-    for (int it = threadIdx.x; it < 2 * r; it += blockDim.x) {
-        const int f = it % r, r0 = (it / r) * (CS / 2);
-        float acc[CS / 2];
-#pragma unroll
-        for (int j = 0; j < CS / 2; ++j) acc[j] = 0.f;
-        if (vec) {
-            for (int c = 0; c < d; c += 4) {
-                const float o0 = omt[(int64_t)c * r + f], o1 = omt[(int64_t)(c + 1) * r + f];
-                const float o2 = omt[(int64_t)(c + 2) * r + f], o3 = omt[(int64_t)(c + 3) * r + f];
-#pragma unroll
-                for (int j = 0; j < CS / 2; ++j) {
-                    const float4 xv = *reinterpret_cast<const float4*>(x + (r0 + j) * d + c);
-                    acc[j] = fmaf(xv.x, o0, fmaf(xv.y, o1, fmaf(xv.z, o2, fmaf(xv.w, o3, acc[j]))));
-                }
-            }
-        } else {
-            for (int c = 0; c < d; ++c) {
-                const float o = omt[(int64_t)c * r + f];
-#pragma unroll
-                for (int j = 0; j < CS / 2; ++j) acc[j] = fmaf(x[(r0 + j) * d + c], o, acc[j]);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < CS / 2; ++j) {
-            const int row = r0 + j;
-            phi[row * r + f] = row < nrows ? expf(acc[j] - half_sq[row]) * inv_sqrt_r : 0.f;
-        }
-    }
-}
-
-// acc[f][c] (+)= sum_i a[i][f] b[i][c] over the CS chunk rows, for the [r][dvx]
-// array acc (a: [CS][r], b: [CS][dvx], both in shared memory, r a multiple of
-// 4): each thread owns four consecutive features of one column, so a 128-bit
-// read of a and one read of b serve four multiply-adds.
-__device__ void rank_cs_update(float* acc, const float* a, const float* b, int r, int dvx) {
-    const int items = (r / 4) * dvx;
-    for (int w = threadIdx.x; w < items; w += blockDim.x) {
-        const int f0 = 4 * (w / dvx), c = w - (f0 / 4) * dvx;
-        float s0 = acc[(f0 + 0) * dvx + c], s1 = acc[(f0 + 1) * dvx + c];
-        float s2 = acc[(f0 + 2) * dvx + c], s3 = acc[(f0 + 3) * dvx + c];
-#pragma unroll
-        for (int i = 0; i < CS; ++i) {
-            const float4 av = *reinterpret_cast<const float4*>(a + i * r + f0);
-            const float bv = b[i * dvx + c];
-            s0 = fmaf(av.x, bv, s0); s1 = fmaf(av.y, bv, s1); s2 = fmaf(av.z, bv, s2); s3 = fmaf(av.w, bv, s3);
-        }
-        acc[(f0 + 0) * dvx + c] = s0; acc[(f0 + 1) * dvx + c] = s1;
-        acc[(f0 + 2) * dvx + c] = s2; acc[(f0 + 3) * dvx + c] = s3;
-    }
-}
-
 struct BwdView {
     float *st, *racc, *xq, *xk, *phq, *phk, *dph, *vx, *gg, *num, *go, *a, *gm, *hsq, *hsk, *sgq, *sgk, *su;
 };

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(NT) state_kernel(FwdParams p, int om_in_smem) 
     float* vx = sm + sp.vx / 4;
     float* hs = sm + sp.hsk / 4;
     const int r = p.r, dvx = p.dvx;
+    // Omega as [d][r] (staged in shared memory, or the backward's transposed copy): register-tiled features
+    const float* omt = (p.map != LA_MAP_FAVOR) ? nullptr : om_in_smem ? om.p : p.omega_t;
     const int E = r * dvx;
     for (int e = threadIdx.x; e < E; e += NT) S[e] = 0.f;
     const TIn* K = static_cast<const TIn*>(p.k);
@@ -117,18 +119,23 @@ __global__ void __launch_bounds__(NT) state_kernel(FwdParams p, int om_in_smem) 
         load_rows(xk, K, t0, n, p.H, h, p.dk);
         load_vx(vx, V, t0, n, p.H, h, p.dv);
         __syncthreads();
-        compute_phi(phk, xk, hs, om, n, p.map, p.dk, r);
+        if (omt) favor_features_tiled(phk, xk, hs, omt, n, p.dk, r);
+        else compute_phi(phk, xk, hs, om, n, p.map, p.dk, r);
         __syncthreads();
         if (p.norm == LA_NORM_SUM) {
             sum_normalise_rows(phk, n, r, p.eps);
             __syncthreads();
         }
-        for (int e = threadIdx.x; e < E; e += NT) {
-            const int f = e / dvx, c = e - f * dvx;
-            float acc = S[e];
+        if ((r & 3) == 0) {
+            rank_cs_update(S, phk, vx, r, dvx);
+        } else {
+            for (int e = threadIdx.x; e < E; e += NT) {
+                const int f = e / dvx, c = e - f * dvx;
+                float acc = S[e];
 #pragma unroll
-            for (int i = 0; i < CS; ++i) acc = fmaf(phk[i * r + f], vx[i * dvx + c], acc);
-            S[e] = acc;
+                for (int i = 0; i < CS; ++i) acc = fmaf(phk[i * r + f], vx[i * dvx + c], acc);
+                S[e] = acc;
+            }
         }
     }
     __syncthreads();
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(NT) out_kernel(FwdParams p, int om_in_smem, in
     float* hsk = sm + sp.hsk / 4;
     const int r = p.r, dv = p.dv, dvx = p.dvx;
     const int E = r * dvx;
+    const float* omt = (p.map == LA_MAP_FAVOR && om_in_smem) ? om.p : nullptr;   // [d][r]: register-tiled features
     const float* src = p.prefix + ((int64_t)u * p.H + h) * E;
     for (int e = threadIdx.x; e < E; e += NT) S[e] = prefix_is_zero ? 0.f : src[e];
     const TIn* Q = static_cast<const TIn*>(p.q);
@@ -175,8 +183,13 @@ __global__ void __launch_bounds__(NT) out_kernel(FwdParams p, int om_in_smem, in
             load_vx(vx, V, t0, n, p.H, h, dv);
         }
         __syncthreads();
-        compute_phi(phq, xq, hsq, om, n, p.map, p.dk, r);
-        if (p.causal) compute_phi(phk, xk, hsk, om, n, p.map, p.dk, r);
+        if (omt) {
+            favor_features_tiled(phq, xq, hsq, omt, n, p.dk, r);
+            if (p.causal) favor_features_tiled(phk, xk, hsk, omt, n, p.dk, r);
+        } else {
+            compute_phi(phq, xq, hsq, om, n, p.map, p.dk, r);
+            if (p.causal) compute_phi(phk, xk, hsk, om, n, p.map, p.dk, r);
+        }
         __syncthreads();
         if (p.norm == LA_NORM_SUM) {
             sum_normalise_rows(phq, n, r, p.eps);
@@ -209,7 +222,9 @@ __global__ void __launch_bounds__(NT) out_kernel(FwdParams p, int om_in_smem, in
             num[e] = acc;
         }
         __syncthreads();
-        if (p.causal) {
+        if (p.causal && (r & 3) == 0) {
+            rank_cs_update(S, phk, vx, r, dvx);
+        } else if (p.causal) {
             for (int e = threadIdx.x; e < E; e += NT) {
                 const int f = e / dvx, c = e - f * dvx;
                 float acc = S[e];
