@@ -126,11 +126,31 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
             if (lane == 0) su[row] = s;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < nrows * d; e += blockDim.x) {
-            const int row = e / d, c = e - row * d;
-            float acc = 0.f;
-            for (int f = 0; f < r; ++f) acc = fmaf(dph[row * r + f], om(c, f), acc);
-            store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, acc - x[row * d + c] * su[row]);
+        if ((r & 3) == 0) {
+            // two rows of one input column per thread: dph read four features at a time (broadcast),
+            // each Omega value (a coalesced load) serves two rows
+            for (int w = threadIdx.x; w < (CS / 2) * d; w += blockDim.x) {
+                const int rp = w / d, c = w - rp * d, ra = 2 * rp;
+                if (ra >= nrows) continue;
+                float a0 = 0.f, a1 = 0.f;
+                for (int f = 0; f < r; f += 4) {
+                    const float o0 = om(c, f), o1 = om(c, f + 1), o2 = om(c, f + 2), o3 = om(c, f + 3);
+                    const float4 u0 = *reinterpret_cast<const float4*>(dph + ra * r + f);
+                    const float4 u1 = *reinterpret_cast<const float4*>(dph + (ra + 1) * r + f);
+                    a0 = fmaf(u0.w, o3, fmaf(u0.z, o2, fmaf(u0.y, o1, fmaf(u0.x, o0, a0))));
+                    a1 = fmaf(u1.w, o3, fmaf(u1.z, o2, fmaf(u1.y, o1, fmaf(u1.x, o0, a1))));
+                }
+                store_elem(dst, ((row0 + ra) * p.H + h) * (int64_t)d + c, a0 - x[ra * d + c] * su[ra]);
+                if (ra + 1 < nrows)
+                    store_elem(dst, ((row0 + ra + 1) * p.H + h) * (int64_t)d + c, a1 - x[(ra + 1) * d + c] * su[ra + 1]);
+            }
+        } else {
+            for (int e = threadIdx.x; e < nrows * d; e += blockDim.x) {
+                const int row = e / d, c = e - row * d;
+                float acc = 0.f;
+                for (int f = 0; f < r; ++f) acc = fmaf(dph[row * r + f], om(c, f), acc);
+                store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, acc - x[row * d + c] * su[row]);
+            }
         }
     } else if (p.map == LA_MAP_DPFP) {
         const int d2 = 2 * d, nu = r / d2;
@@ -158,6 +178,80 @@ __device__ void features_vjp_rows(float* dph, float* phi, const float* x, const 
             const float xv = x[row * d + c], gv = dph[row * r + c];
             const float dxv = (p.map == LA_MAP_ELU1) ? gv * (xv > 0.f ? 1.f : expf(xv)) : gv;
             store_elem(dst, ((row0 + row) * p.H + h) * (int64_t)d + c, dxv);
+        }
+    }
+}
+
+// out[i][c] = sum_f a[i][f] M[f][c] (+ sum_s T(i, s) b[s][c] when T is given) for the CS
+// chunk rows i and the columns c < ncols; T(i, s) = T[i][s], or T[s][i] when kTT.  a is
+// [CS][r] (r a multiple of 4), M [r][dvx], T [CS][CS], b [CS][dvx], out rows ldo apart, all
+// in shared memory.  A thread computes rows 4 rb .. 4 rb + 3 of one column: a is read four
+// features at a time (a warp broadcast), M once per feature for four multiply-adds.
+template <bool kTT>
+__device__ void rows_times_state(float* out, int ldo, const float* a, const float* M, const float* T, const float* b,
+                                 int r, int dvx, int ncols) {
+    for (int w = threadIdx.x; w < 4 * ncols; w += blockDim.x) {
+        const int rb = w / ncols, c = w - rb * ncols, i0 = 4 * rb;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int f = 0; f < r; f += 4) {
+            const float m0 = M[f * dvx + c], m1 = M[(f + 1) * dvx + c];
+            const float m2 = M[(f + 2) * dvx + c], m3 = M[(f + 3) * dvx + c];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 av = *reinterpret_cast<const float4*>(a + (i0 + k) * r + f);
+                acc[k] = fmaf(av.w, m3, fmaf(av.z, m2, fmaf(av.y, m1, fmaf(av.x, m0, acc[k]))));
+            }
+        }
+        if (T) {
+#pragma unroll 4
+            for (int s = 0; s < CS; ++s) {
+                const float bv = b[s * dvx + c];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = fmaf(kTT ? T[s * CS + i0 + k] : T[(i0 + k) * CS + s], bv, acc[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[(i0 + k) * ldo + c] = acc[k];
+    }
+}
+
+// out[i][f] = sum_c M[f][c] b[i][c] (+ sum_s G(i, s) P[s][f] when G is given) for the CS
+// chunk rows i and the r features f (r even); G(i, s) = G[i][s], or G[s][i] when kGT.  M is
+// [r][dvx], b [CS][dvx], G [CS][CS], P [CS][r], out [CS][r], all in shared memory.  A thread
+// computes rows 4 rb .. 4 rb + 3 of features f and f + r / 2: the two reads of M are
+// 65-float strides across a warp (no bank conflicts), b and G reads are broadcasts.
+template <bool kGT>
+__device__ void state_times_rows(float* out, const float* M, const float* b, const float* G, const float* P, int r,
+                                 int dvx) {
+    const int half = r / 2;
+    for (int w = threadIdx.x; w < 4 * half; w += blockDim.x) {
+        const int rb = w / half, f0 = w - rb * half, f1 = f0 + half, i0 = 4 * rb;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < dvx; ++c) {
+            const float m0 = M[f0 * dvx + c], m1 = M[f1 * dvx + c];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float bv = b[(i0 + k) * dvx + c];
+                a0[k] = fmaf(m0, bv, a0[k]);
+                a1[k] = fmaf(m1, bv, a1[k]);
+            }
+        }
+        if (G) {
+#pragma unroll 4
+            for (int s = 0; s < CS; ++s) {
+                const float p0 = P[s * r + f0], p1 = P[s * r + f1];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float g = kGT ? G[s * CS + i0 + k] : G[(i0 + k) * CS + s];
+                    a0[k] = fmaf(g, p0, a0[k]);
+                    a1[k] = fmaf(g, p1, a1[k]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            out[(i0 + k) * r + f0] = a0[k];
+            out[(i0 + k) * r + f1] = a1[k];
         }
     }
 }
@@ -203,7 +297,7 @@ __device__ void causal_gv(float* Gm, const float* gg, const float* vx, int n, in
 // Forward walk of one segment: g of every row, dq, and the segment's sum of
 // phi(q_i) g_i^T (into p.partial).
 template <typename TIn>
-__global__ void __launch_bounds__(kBwdThreads) bwd_q_kernel(FwdParams p, int prefix_is_zero) {
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_q_kernel(FwdParams p, int prefix_is_zero) {
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
@@ -255,15 +349,19 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_q_kernel(FwdParams p, int pre
             __syncthreads();
         }
         // num | den of each row: phi(q_i) S (+ in-chunk terms)
-        for (int e = threadIdx.x; e < n * dvx; e += blockDim.x) {
-            const int i = e / dvx, c = e - i * dvx;
-            float acc = 0.f;
-            for (int f = 0; f < r; ++f) acc = fmaf(w.phq[i * r + f], w.st[f * dvx + c], acc);
-            if (p.causal) {
+        if ((r & 3) == 0) {
+            rows_times_state<false>(w.num, dvx, w.phq, w.st, p.causal ? w.a : nullptr, w.vx, r, dvx, dvx);
+        } else {
+            for (int e = threadIdx.x; e < n * dvx; e += blockDim.x) {
+                const int i = e / dvx, c = e - i * dvx;
+                float acc = 0.f;
+                for (int f = 0; f < r; ++f) acc = fmaf(w.phq[i * r + f], w.st[f * dvx + c], acc);
+                if (p.causal) {
 #pragma unroll
-                for (int j = 0; j < CS; ++j) acc = fmaf(w.a[i * CS + j], w.vx[j * dvx + c], acc);
+                    for (int j = 0; j < CS; ++j) acc = fmaf(w.a[i * CS + j], w.vx[j * dvx + c], acc);
+                }
+                w.num[e] = acc;
             }
-            w.num[e] = acc;
         }
         __syncthreads();
         // g_i = dL/d(num_i | den_i)
@@ -294,15 +392,19 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_q_kernel(FwdParams p, int pre
             __syncthreads();
         }
         // dphi(q_i) = S g_i (+ sum_{j<=i} (g_i . [v_j|1]) phi(k_j))
-        for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
-            const int i = e / r, f = e - i * r;
-            float acc = 0.f;
-            for (int c = 0; c < dvx; ++c) acc = fmaf(w.st[f * dvx + c], w.gg[i * dvx + c], acc);
-            if (p.causal) {
+        if ((r & 1) == 0) {
+            state_times_rows<false>(w.dph, w.st, w.gg, p.causal ? w.gm : nullptr, w.phk, r, dvx);
+        } else {
+            for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+                const int i = e / r, f = e - i * r;
+                float acc = 0.f;
+                for (int c = 0; c < dvx; ++c) acc = fmaf(w.st[f * dvx + c], w.gg[i * dvx + c], acc);
+                if (p.causal) {
 #pragma unroll
-                for (int j = 0; j < CS; ++j) acc = fmaf(w.gm[i * CS + j], w.phk[j * r + f], acc);
+                    for (int j = 0; j < CS; ++j) acc = fmaf(w.gm[i * CS + j], w.phk[j * r + f], acc);
+                }
+                w.dph[e] = acc;
             }
-            w.dph[e] = acc;
         }
         __syncthreads();   // the state is read above and updated below
         // the segment's sum of phi(q_i) g_i^T, and (causal) the state after the chunk
@@ -336,7 +438,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_q_kernel(FwdParams p, int pre
 // later segments (the whole sequence for the bidirectional form); writes dk
 // and dv.
 template <typename TIn>
-__global__ void __launch_bounds__(kBwdThreads) bwd_kv_kernel(FwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kv_kernel(FwdParams p) {
     const int u = blockIdx.x, h = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
@@ -386,26 +488,39 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kv_kernel(FwdParams p) {
             __syncthreads();
         }
         // dphi(k_j) = R [v_j | 1] (+ sum_{i>=j} (g_i . [v_j|1]) phi(q_i))
-        for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
-            const int j = e / r, f = e - j * r;
-            float acc = 0.f;
-            for (int c = 0; c < dvx; ++c) acc = fmaf(R[f * dvx + c], w.vx[j * dvx + c], acc);
-            if (p.causal) {
+        if ((r & 1) == 0) {
+            state_times_rows<true>(w.dph, R, w.vx, p.causal ? w.gm : nullptr, w.phq, r, dvx);
+        } else {
+            for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+                const int j = e / r, f = e - j * r;
+                float acc = 0.f;
+                for (int c = 0; c < dvx; ++c) acc = fmaf(R[f * dvx + c], w.vx[j * dvx + c], acc);
+                if (p.causal) {
 #pragma unroll
-                for (int i = 0; i < CS; ++i) acc = fmaf(w.gm[i * CS + j], w.phq[i * r + f], acc);
+                    for (int i = 0; i < CS; ++i) acc = fmaf(w.gm[i * CS + j], w.phq[i * r + f], acc);
+                }
+                w.dph[e] = acc;
             }
-            w.dph[e] = acc;
         }
         // dv_j = R^T phi(k_j) (+ sum_{i>=j} (phi(q_i) . phi(k_j)) g_i), first d_v entries
-        for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
-            const int j = e / dv, c = e - j * dv;
-            float acc = 0.f;
-            for (int f = 0; f < r; ++f) acc = fmaf(R[f * dvx + c], w.phk[j * r + f], acc);
-            if (p.causal) {
-#pragma unroll
-                for (int i = 0; i < CS; ++i) acc = fmaf(w.a[i * CS + j], w.gg[i * dvx + c], acc);
+        if ((r & 3) == 0) {
+            rows_times_state<true>(w.num, dvx, w.phk, R, p.causal ? w.a : nullptr, w.gg, r, dvx, dv);
+            __syncthreads();
+            for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
+                const int j = e / dv, c = e - j * dv;
+                store_elem(DV, ((t0 + j) * p.H + h) * (int64_t)dv + c, w.num[j * dvx + c]);
             }
-            store_elem(DV, ((t0 + j) * p.H + h) * (int64_t)dv + c, acc);
+        } else {
+            for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
+                const int j = e / dv, c = e - j * dv;
+                float acc = 0.f;
+                for (int f = 0; f < r; ++f) acc = fmaf(R[f * dvx + c], w.phk[j * r + f], acc);
+                if (p.causal) {
+#pragma unroll
+                    for (int i = 0; i < CS; ++i) acc = fmaf(w.a[i * CS + j], w.gg[i * dvx + c], acc);
+                }
+                store_elem(DV, ((t0 + j) * p.H + h) * (int64_t)dv + c, acc);
+            }
         }
         __syncthreads();   // R is read above and updated below
         if (p.causal) {
