@@ -46,20 +46,95 @@ __device__ __forceinline__ float phi_sum_row(float2 x, int map, int d, int r, in
     return acc;
 }
 
+constexpr int kRowsPerWarp = 4;   // rows whose loads a warp issues before it computes
+
 __global__ void __launch_bounds__(kNormThreads) sum_prologue_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                                                     const __nv_bfloat16* v, int map, int64_t rows,
                                                                     int r, float eps, float* sig_q,
                                                                     __nv_bfloat16* dst) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kNormThreads / 32);
-    for (int64_t row = (int64_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); row < rows; row += warps) {
-        const float2 xq = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(q + row * 64)[lane]);
-        const float2 xk = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(k + row * 64)[lane]);
-        const float2 xv = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(v + row * 64)[lane]);
-        const float sq = phi_sum_row(xq, map, 64, r, lane);
-        const float sk = fmaxf(phi_sum_row(xk, map, 64, r, lane), eps);
-        if (lane == 0) sig_q[row] = sq;
-        reinterpret_cast<__nv_bfloat162*>(dst + row * 64)[lane] = __floats2bfloat162_rn(xv.x / sk, xv.y / sk);
+    const int64_t first = ((int64_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5)) * kRowsPerWarp;
+    for (int64_t row0 = first; row0 < rows; row0 += warps * kRowsPerWarp) {
+        // every load of the warp's rows in flight before the first use
+        float2 xq[kRowsPerWarp], xk[kRowsPerWarp], xv[kRowsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int64_t row = row0 + i < rows ? row0 + i : row0;   // a past-the-end row repeats a valid one
+            xq[i] = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(q + row * 64)[lane]);
+            xk[i] = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(k + row * 64)[lane]);
+            xv[i] = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(v + row * 64)[lane]);
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int64_t row = row0 + i;
+            const float sq = phi_sum_row(xq[i], map, 64, r, lane);
+            const float sk = fmaxf(phi_sum_row(xk[i], map, 64, r, lane), eps);
+            if (row < rows) {
+                if (lane == 0) sig_q[row] = sq;
+                reinterpret_cast<__nv_bfloat162*>(dst + row * 64)[lane] = __floats2bfloat162_rn(xv[i].x / sk, xv[i].y / sk);
+            }
+        }
+    }
+}
+
+// The same for ELU+1 and identity, whose sums need no gather across the row: 16-byte
+// loads, eight lanes per row (a warp covers four rows per load) and kGroups such groups
+// of four rows in flight per warp; the row sums reduce over the eight lanes.
+template <int kGroups>
+__global__ void __launch_bounds__(kNormThreads) sum_prologue_vec_kernel(const __nv_bfloat16* q,
+                                                                        const __nv_bfloat16* k,
+                                                                        const __nv_bfloat16* v, int map,
+                                                                        int64_t rows, float eps, float* sig_q,
+                                                                        __nv_bfloat16* dst) {
+    const int lane = threadIdx.x & 31, sub = lane & 7, rr = lane >> 3;
+    const int64_t warps = (int64_t)gridDim.x * (kNormThreads / 32);
+    const int64_t first = ((int64_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5)) * (4 * kGroups);
+    const bool elu = map == LA_MAP_ELU1;
+    auto phi_sum8 = [&](const uint4& w) {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j]));
+            acc += elu ? (x.x > 0.f ? x.x + 1.f : expf(x.x)) : x.x;
+            acc += elu ? (x.y > 0.f ? x.y + 1.f : expf(x.y)) : x.y;
+        }
+        return acc;
+    };
+    for (int64_t row0 = first; row0 < rows; row0 += warps * (4 * kGroups)) {
+        uint4 aq[kGroups], ak[kGroups], av[kGroups];
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            int64_t row = row0 + 4 * g + rr;
+            row = row < rows ? row : rows - 1;   // a past-the-end row repeats the last one
+            aq[g] = reinterpret_cast<const uint4*>(q + row * 64)[sub];
+            ak[g] = reinterpret_cast<const uint4*>(k + row * 64)[sub];
+            av[g] = reinterpret_cast<const uint4*>(v + row * 64)[sub];
+        }
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            float sq = phi_sum8(aq[g]), sk = phi_sum8(ak[g]);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            sk = fmaxf(sk, eps);
+            const int64_t row = row0 + 4 * g + rr;
+            if (row < rows) {
+                if (sub == 0) sig_q[row] = sq;
+                const uint32_t u[4] = {av[g].x, av[g].y, av[g].z, av[g].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j]));
+                    const __nv_bfloat162 y = __floats2bfloat162_rn(x.x / sk, x.y / sk);
+                    o4[j] = *reinterpret_cast<const uint32_t*>(&y);
+                }
+                reinterpret_cast<uint4*>(dst + row * 64)[sub] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+        }
     }
 }
 
@@ -95,8 +170,18 @@ cudaError_t sum_prologue_elementwise(const void* q, const void* k, const void* v
                                      float eps, float* sig_q, void* dst, cudaStream_t s) {
     const int64_t rows = T * H;
     if (rows == 0) return cudaSuccess;
-    // one row per warp: every row's loads are in flight at once
-    const int64_t blocks = ceil_div(rows, kNormThreads / 32);
+    const bool vec = map != LA_MAP_DPFP && ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                                              reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0;
+    if (vec) {
+        constexpr int kGroups = 4;   // sixteen rows per warp
+        const int64_t blocks = ceil_div(rows, (int64_t)(kNormThreads / 32) * 4 * kGroups);
+        sum_prologue_vec_kernel<kGroups><<<(unsigned)(blocks < INT32_MAX ? blocks : INT32_MAX), kNormThreads, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+            static_cast<const __nv_bfloat16*>(v), map, rows, eps, sig_q, static_cast<__nv_bfloat16*>(dst));
+        return cudaGetLastError();
+    }
+    // four rows per warp, every row's loads in flight at once
+    const int64_t blocks = ceil_div(rows, (int64_t)(kNormThreads / 32) * kRowsPerWarp);
     sum_prologue_kernel<<<(unsigned)(blocks < INT32_MAX ? blocks : INT32_MAX), kNormThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         static_cast<const __nv_bfloat16*>(v), map, rows, r, eps, sig_q, static_cast<__nv_bfloat16*>(dst));
