@@ -111,12 +111,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
 
 constexpr int kScanThreads = 256;
 constexpr int kScanPerThread = 4;
+constexpr int kScanBatch = 8;   // units whose partial sums are in flight before they are added
 
 // grid: (ceil(E / (256*4)), nseq, H).  The result goes to p.prefix (the
 // backward pass points it at its suffix buffer and sets p.reverse).  Each
 // thread owns elements e of one
 // (sequence, head) state and walks the sequence's units in token order, so
 // state_in may alias state_out: it is read before the same thread writes it.
+// The units are taken kScanBatch at a time, their partial sums loaded before
+// any is added, so only the additions form a dependent chain.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
     const int s = blockIdx.y, h = blockIdx.z;
     const int u0 = p.seq_first[s], u1 = p.seq_first[s + 1];
@@ -129,41 +132,40 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(FwdParams p) {
         const int64_t e = e0 + j * kScanThreads;
         acc[j] = (p.state_in != nullptr && e < E) ? p.state_in[sbase + e] : 0.f;
     }
-    if (p.causal && p.reverse) {
-        // suffix: the sums of the units after u, walking the sequence backwards
-        for (int u = u1 - 1; u >= u0; --u) {
+    const bool rev = p.causal && p.reverse;
+    const int nu = u1 - u0;
+    for (int b0 = 0; b0 < nu; b0 += kScanBatch) {
+        // position b0 + i of the walk is unit u0 + (b0 + i), or u1 - 1 - (b0 + i) walking backwards
+        float part[kScanBatch][kScanPerThread];
+#pragma unroll
+        for (int i = 0; i < kScanBatch; ++i) {
+            const int w = b0 + i, u = rev ? u1 - 1 - w : u0 + w;
+            // causal forward: the last unit's sum exists only with keep_last
+            const bool add = w < nu && (rev || !p.causal || u + 1 < u1 || p.keep_last);
             const int64_t base = ((int64_t)u * p.H + h) * E;
 #pragma unroll
             for (int j = 0; j < kScanPerThread; ++j) {
                 const int64_t e = e0 + j * kScanThreads;
-                if (e < E) {
-                    p.prefix[base + e] = acc[j];
-                    acc[j] += p.partial[base + e];
+                part[i][j] = (add && e < E) ? p.partial[base + e] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kScanBatch; ++i) {
+            const int w = b0 + i, u = rev ? u1 - 1 - w : u0 + w;
+            if (w < nu) {
+                const int64_t base = ((int64_t)u * p.H + h) * E;
+#pragma unroll
+                for (int j = 0; j < kScanPerThread; ++j) {
+                    const int64_t e = e0 + j * kScanThreads;
+                    if (e < E) {
+                        if (p.causal) p.prefix[base + e] = acc[j];   // exclusive prefix (or suffix)
+                        acc[j] += part[i][j];
+                    }
                 }
             }
         }
-    } else if (p.causal) {
-        for (int u = u0; u < u1; ++u) {
-            const int64_t base = ((int64_t)u * p.H + h) * E;
-            const bool add = u + 1 < u1 || p.keep_last;   // the last unit's sum exists only with keep_last
-#pragma unroll
-            for (int j = 0; j < kScanPerThread; ++j) {
-                const int64_t e = e0 + j * kScanThreads;
-                if (e < E) {
-                    p.prefix[base + e] = acc[j];
-                    if (add) acc[j] += p.partial[base + e];
-                }
-            }
-        }
-    } else {
-        for (int u = u0; u < u1; ++u) {
-            const int64_t base = ((int64_t)u * p.H + h) * E;
-#pragma unroll
-            for (int j = 0; j < kScanPerThread; ++j) {
-                const int64_t e = e0 + j * kScanThreads;
-                if (e < E) acc[j] += p.partial[base + e];
-            }
-        }
+    }
+    if (!p.causal) {   // bidirectional: every unit of the sequence reads the whole-sequence sum
         for (int u = u0; u < u1; ++u) {
             const int64_t base = ((int64_t)u * p.H + h) * E;
 #pragma unroll

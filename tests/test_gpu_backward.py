@@ -78,7 +78,8 @@ def test_backward_identity_map_fp32(la, causal):
         assert_close(g, r_, "f32", f"identity {name}")
 
 
-@pytest.mark.parametrize("shape", [(16, 48, 96), (32, 16, 64)])
+# r = 30 (even, not a multiple of 4) and r = 33 (odd) take the backward's plain loops
+@pytest.mark.parametrize("shape", [(16, 48, 96), (32, 16, 64), (16, 48, 30), (32, 16, 33)])
 def test_backward_other_head_sizes_fp32(la, shape):
     dk, dv, r = shape
     inp = synthetic.random_inputs([90, 3, 250], H=2, dk=dk, dv=dv, dtype="f32", seed=53, qk_scale=dk ** -0.25)
