@@ -113,6 +113,8 @@ struct __align__(1024) StateSmem {
                                   // serve as the ones atom of the update's [V|1] (columns 64, 65)
     StateBars b;
 };
+// the [S|z] block of up to 256 features leaves through the k / v stages
+static_assert(256 * 65 * sizeof(float) <= 2 * kStateStages * sizeof(Tile), "state staging does not fit");
 
 // Feature-map kernel: 80 KB.
 struct __align__(1024) FmapSmem {
@@ -1464,9 +1466,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     __syncthreads();
     tc_fence_after();
-    if (warp >= 4 && warp < 8) {   // [S|z] row of this thread's feature in each half
+    // [S|z] as [r][65] fp32 rows: each thread's feature row into shared memory (the
+    // k / v stages, all consumed; a row stride of 65 words keeps the warp's stores
+    // on distinct banks), then one coalesced 16-byte copy of the whole block
+    float* stage = reinterpret_cast<float*>(s.tk[0]);
+    if (warp >= 4 && warp < 8) {
         const int f = t - 128;
-        float* dst = p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65;
         for (int h = 0; h < nhalves; ++h) {
             const int feat = 128 * h + f;
             for (int n0 = 0; n0 < 65; n0 += 16) {
@@ -1478,13 +1483,18 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 if (feat < r) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        if (n0 + e < 65) dst[(int64_t)feat * 65 + n0 + e] = __uint_as_float(w[e]);
+                        if (n0 + e < 65) stage[feat * 65 + n0 + e] = __uint_as_float(w[e]);
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    {
+        float4* dst = reinterpret_cast<float4*>(p.partial + ((int64_t)u * p.H + head) * (int64_t)r * 65);
+        const float4* src = reinterpret_cast<const float4*>(stage);
+        for (int i = t; i < r * 65 / 4; i += kStateThreads) dst[i] = src[i];
+    }
     if (warp == 1) tmem_dealloc(tb, kTmemCols);
 }
 
