@@ -143,21 +143,37 @@ struct TcParams {
 // ---------------------------------------------------------------------------
 // Omega' = log2(e) * Omega as bf16 hi + lo, [r][64] each, K-major swizzled
 // (the B operand of the projection).  lo = bf16(Omega' - hi).
-__device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* omega, int r) {
-    for (int i = threadIdx.x; i < r * 8; i += blockDim.x) {
-        const int row = i >> 3, c = i & 7;
-        const float4* src = reinterpret_cast<const float4*>(omega + row * 64 + c * 8);
-        const float4 a = src[0], b = src[1];
-        const float x[8] = {a.x * kLog2e, a.y * kLog2e, a.z * kLog2e, a.w * kLog2e,
-                            b.x * kLog2e, b.y * kLog2e, b.z * kLog2e, b.w * kLog2e};
-        uint32_t wh[4], wl[4];
+__device__ void stage_omega(unsigned char* hi, unsigned char* lo, const float* __restrict__ omega, int r) {
+    constexpr int kBatch = 4;   // 16-byte chunks per thread whose loads are in flight together
+    const int n = r * 8;
+    for (int i0 = threadIdx.x; i0 < n; i0 += kBatch * blockDim.x) {
+        float4 a[kBatch], b[kBatch];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            wh[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-            wl[j] = pack_bf16x2(x[2 * j] - bf16lo(wh[j]), x[2 * j + 1] - bf16hi(wh[j]));
+        for (int q = 0; q < kBatch; ++q) {
+            const int i = i0 + q * blockDim.x;
+            a[q] = b[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < n) {
+                const float4* src = reinterpret_cast<const float4*>(omega + (i >> 3) * 64 + (i & 7) * 8);
+                a[q] = __ldg(src);
+                b[q] = __ldg(src + 1);
+            }
         }
-        *reinterpret_cast<uint4*>(hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int i = i0 + q * blockDim.x;
+            if (i >= n) break;
+            const int row = i >> 3, c = i & 7;
+            const float x[8] = {a[q].x * kLog2e, a[q].y * kLog2e, a[q].z * kLog2e, a[q].w * kLog2e,
+                                b[q].x * kLog2e, b[q].y * kLog2e, b[q].z * kLog2e, b[q].w * kLog2e};
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wh[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+                wl[j] = pack_bf16x2(x[2 * j] - bf16lo(wh[j]), x[2 * j + 1] - bf16hi(wh[j]));
+            }
+            *reinterpret_cast<uint4*>(hi + sw128_chunk(row, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(lo + sw128_chunk(row, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
     }
 }
 
@@ -580,6 +596,13 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         mbar_init(&B.drain[0], 1);
         mbar_init(&B.drain[1], 1);
         fence_mbar_init();
+        if (nchunks > 0) {   // chunk 0's tiles go out before the set-up below (which does not touch them)
+            mbar_arrive_expect_tx(&B.qk_full, 2 * kTile);
+            tma_load_3d(s.tq, &map_q, 0, head, un.start, &B.qk_full);
+            tma_load_3d(s.tk, &map_k, 0, head, un.start, &B.qk_full);
+            mbar_arrive_expect_tx(&B.v_full, kTile);
+            tma_load_3d(s.tv, &map_v, 0, head, un.start, &B.v_full);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&B.tmem_base, kTmemCols);
@@ -622,7 +645,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = 1; c < nchunks; ++c) {   // chunk 0: issued at set-up
                 const int t0 = un.start + c * kC;
                 if (c > 0 && !mbar_wait(&B.qk_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
                 mbar_arrive_expect_tx(&B.qk_full, 2 * kTile);
@@ -1267,6 +1290,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         mbar_init(&B.drain[0], 1);
         mbar_init(&B.drain[1], 1);
         fence_mbar_init();
+        // the first stages' k / v tiles go out before the set-up below (nothing in it
+        // touches them), so that their DRAM latency overlaps the staging of Omega
+        for (int c = 0; c < nchunks && c < kStateStages; ++c) {
+            const int t0 = un.start + c * kC;
+            for (int a = (c == 0 ? 0 : kPrefetchAhead); a <= kPrefetchAhead; ++a)
+                if (c + a < nchunks) {
+                    tma_prefetch_3d(&map_k, 0, head, t0 + a * kC);
+                    tma_prefetch_3d(&map_v, 0, head, t0 + a * kC);
+                }
+            mbar_arrive_expect_tx(&B.k_full[c], kTile);
+            tma_load_3d(s.tk[c], &map_k, 0, head, t0, &B.k_full[c]);
+            mbar_arrive_expect_tx(&B.v_full[c], kTile);
+            tma_load_3d(s.tv[c], &map_v, 0, head, t0, &B.v_full[c]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&B.tmem_base, kTmemCols);
@@ -1306,7 +1343,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = kStateStages; c < nchunks; ++c) {   // chunks 0 .. kStateStages - 1: issued at set-up
                 const int st = c % kStateStages, ph = ((c / kStateStages) - 1) & 1, t0 = un.start + c * kC;
                 // into L2 ahead of the stages: the loads below then wait on L2, not DRAM
                 for (int a = (c == 0 ? 0 : kPrefetchAhead); a <= kPrefetchAhead; ++a)
