@@ -100,6 +100,7 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     size_t o = align_up(sizeof(WsHeader), kAlign);
     lo.units = o;     o = align_up(o + sizeof(Unit) * (size_t)U, kAlign);
     lo.seq_first = o; o = align_up(o + sizeof(int) * (size_t)(nseq + 1), kAlign);
+    lo.order = o;     o = align_up(o + sizeof(int) * (size_t)U, kAlign);
     const size_t state_bytes = sizeof(float) * (size_t)U * H * r * lo.dvx;
     lo.partial = o;   o = align_up(o + state_bytes, kAlign);
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
@@ -167,6 +168,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.units = reinterpret_cast<Unit*>(ws + lo.units);
     p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
+    p.order = reinterpret_cast<int*>(ws + lo.order);
     p.partial = reinterpret_cast<float*>(ws + lo.partial);
     p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
     p.sig_q = reinterpret_cast<float*>(ws + lo.sig_q);
@@ -268,6 +270,7 @@ la_status backward(int causal, int norm, const void* q, const void* k, const voi
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.units = reinterpret_cast<Unit*>(ws + lo.units);
     p.seq_first = reinterpret_cast<int*>(ws + lo.seq_first);
+    p.order = reinterpret_cast<int*>(ws + lo.order);
     p.partial = reinterpret_cast<float*>(ws + lo.partial);
     p.prefix = reinterpret_cast<float*>(ws + lo.prefix);
     p.suffix = reinterpret_cast<float*>(ws + lo.suffix);

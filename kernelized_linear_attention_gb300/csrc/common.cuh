@@ -32,6 +32,7 @@ struct WsHeader {
 struct Layout {
     size_t units;      // Unit[U]
     size_t seq_first;  // int[nseq + 1]: first unit of each sequence (+ total)
+    size_t order;      // int[U]: units by decreasing token count (packed batches), else 0, 1, ..
     size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
     size_t sig_q;      // float[T][H]: sum_f phi_f(q) (sum normalisation on the tensor-core path)
@@ -85,6 +86,7 @@ struct FwdParams {
     WsHeader* hdr;
     Unit* units;
     int* seq_first;
+    int* order;             // the tensor-core output kernels take units in this order (longest first)
     float* partial;
     float* prefix;
     int U, L;

@@ -15,6 +15,7 @@ namespace la {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kSortUnits = 1024;   // packed batches with more units keep the unit order
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int* warp_sums, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -106,6 +107,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
         p.seq_first[p.nseq] = min(total, p.U);
         p.hdr->n_units = min(total, p.U);
         p.hdr->error = (total > p.U) ? LA_DEVERR_CU_SEQLENS : LA_DEVERR_NONE;
+    }
+
+    // pass 3: the order in which the tensor-core output kernels take the units.
+    // Packed batches mix short and long units; launched longest first, the
+    // blocks of short units fill in behind the long ones instead of leaving a
+    // tail of long units on a few SMs.  Rank = number of units longer, ties by
+    // index (a permutation); equal-length batches keep 0, 1, ..
+    __shared__ int slen[kSortUnits];
+    const int nu = min(carry, p.U);
+    const bool sort = p.cu_seqlens != nullptr && nu <= kSortUnits;
+    if (sort)
+        for (int i = threadIdx.x; i < nu; i += blockDim.x) slen[i] = p.units[i].end - p.units[i].start;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nu; i += blockDim.x) {
+        int rank = i;
+        if (sort) {
+            const int li = slen[i];
+            rank = 0;
+            for (int j = 0; j < nu; ++j) {
+                const int lj = slen[j];
+                rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+            }
+        }
+        p.order[rank] = i;
     }
 }
 

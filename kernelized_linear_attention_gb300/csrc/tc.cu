@@ -558,8 +558,10 @@ __global__ void __launch_bounds__(kCausalThreads, 1)
 tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, const TcParams tp) {
     const FwdParams& p = tp.p;
-    const int u = blockIdx.x, head = blockIdx.y;
-    if (u >= p.hdr->n_units) return;
+    // one block per (unit, head), rank-major: all heads of the longest unit go out first
+    const int rank = blockIdx.x / p.H, head = blockIdx.x - rank * p.H;
+    if (rank >= p.hdr->n_units) return;
+    const int u = p.order[rank];
     const Unit un = p.units[u];
     CausalSmem& s = smem_ref<CausalSmem>();
     CausalBars& B = s.b;
@@ -987,8 +989,10 @@ template <bool kFavor>
 __global__ void __launch_bounds__(kBidirThreads, 1)
 tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp) {
     const FwdParams& p = tp.p;
-    const int u = blockIdx.x, head = blockIdx.y;
-    if (u >= p.hdr->n_units) return;
+    // one block per (unit, head), rank-major: all heads of the longest unit go out first
+    const int rank = blockIdx.x / p.H, head = blockIdx.x - rank * p.H;
+    if (rank >= p.hdr->n_units) return;
+    const int u = p.order[rank];
     const Unit un = p.units[u];
     BidirSmem& s = smem_ref<BidirSmem>();
     BidirBars& B = s.b;
@@ -1640,7 +1644,9 @@ cudaError_t tc_state(const FwdParams& p, cudaStream_t s) {
 }
 
 cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s) {
-    const dim3 grid((unsigned)p.U, (unsigned)p.H);
+    // one-dimensional grid of (unit rank, head) blocks, rank-major (see the kernels)
+    if ((int64_t)p.U * p.H > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)((int64_t)p.U * p.H));
     const TcParams tp{p, prefix_is_zero};
     CUtensorMap mq;
     if (!make_row_map(&mq, p.q, p.T, p.H)) return cudaErrorInvalidValue;
