@@ -282,6 +282,25 @@ def test_full_size_workload_sampled_rows(la, name):
     assert worst <= BF16_RMS_TOL, worst
 
 
+@pytest.mark.xfail(strict=False, reason="bf16 rounding of phi(q) and phi(k): on a 65536-token sequence about "
+                                        "0.3% of the rows exceed 2e-2 x RMS (the worst by up to 2.5x); fp16 "
+                                        "feature operands are the planned fix")
+def test_long_causal_sequence_every_row(la):
+    """Every row (not a sample) of a two-head causal FAVOR+ r = 256 problem with 65536 tokens,
+    q, k ~ N(0,1) * 64^-1/4, v ~ N(0,1), at the bf16 bar.  Measured on GB300 with the bf16
+    feature operands: 0.035 and 0.050 of the RMS over all rows, with 189 and 127 rows above
+    2e-2; the sampled-row test above holds the bar on the rows it checks."""
+    inp = synthetic.random_inputs([65536], H=2, dk=64, dv=64, dtype="bf16", seed=11, qk_scale=64 ** -0.25)
+    om = omega_for(256, 64)
+    got = _run(la, inp, "favor", True, om, cu=False)
+    worst = 0.0
+    for h in range(2):
+        ref = oracle.causal(inp.q[:, h:h + 1, :], inp.k[:, h:h + 1, :], inp.v[:, h:h + 1, :], "favor",
+                            omega=om.astype(np.float64))[:, 0, :]
+        worst = max(worst, abs_err_over_rms(got[:, h, :], ref))
+    assert worst <= BF16_RMS_TOL, worst
+
+
 # ----------------------------------------------------------------------------
 # Largest shapes
 # ----------------------------------------------------------------------------
