@@ -45,6 +45,8 @@ KERNEL_SOURCES = {"tc": {"output": "tc.cu", "state": "tc.cu", "scan": "plan.cu",
                            "decode": "decode.cu"}}
 # second measured line: the bidirectional state pass (phi(k)^T [v|1] over every token)
 BIDIR_WORKLOAD = "favor_bidir_b4h8n16384"
+# the other bf16 workloads of the benchmark plan, each timed as a whole forward
+CONFIG_WORKLOADS = ("elu_causal_b8h8n4096", "favor_bidir_b4h8n16384", "favor_causal_varlen64_h8")
 # the decode-step and backward lines of the default run
 DECODE_WORKLOAD = "favor_decode_b256h16"
 BACKWARD_WORKLOAD = "favor_causal_b4h8n4096_bwd"
@@ -82,6 +84,50 @@ def algorithmic(w: synthetic.Workload) -> dict:
     byts = (2 * w.dk + 2 * w.dv) * esz
     exps = 2 * w.r if w.map == "favor" else (2 * w.dk if w.map == "elu1" else 0)
     return {"flops": flops, "bytes": byts, "exps": exps}
+
+
+def roofline_of(w: synthetic.Workload, phase_ms: dict, peaks: dict) -> dict:
+    """Roofline of the dominant phase's kernel: algorithmic FLOPs or bytes of one
+    launch (the per-token-head figures of algorithmic() times the token-heads the
+    launch processes) over its measured duration, against the measured peak of
+    the roofline that bounds it (the larger of FLOPs / tensor peak and bytes /
+    HBM peak).  The output kernel performs the whole method for every token-head
+    (it reads q, k, v, writes out, computes both projections, the state terms
+    and the readout); the state kernel reads k and v of every token."""
+    alg = algorithmic(w)
+    token_heads = w.T * w.H
+    dom = max(phase_ms, key=phase_ms.get)
+    dom_ms = phase_ms[dom]
+    if dom == "state":
+        flops = (2 * w.dk * w.r * 2 if w.map == "favor" else 0) * token_heads // 2 + 2 * w.r * (w.dv + 1) * token_heads
+        byts = (w.dk + w.dv) * (2 if w.dtype == "bf16" else 4) * token_heads
+    else:
+        flops = alg["flops"] * token_heads
+        byts = alg["bytes"] * token_heads
+    tflop = peaks["bf16_tflops"] if w.dtype == "bf16" else FP32_ALU_TFLOPS
+    t_flop = flops / (tflop * 1e12)
+    t_byte = byts / (peaks["hbm_gbs"] * 1e9)
+    if dom in ("output", "state") and t_flop >= t_byte:
+        achieved = flops / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor" if w.dtype == "bf16" else "alu", "achieved": achieved, "peak": tflop,
+                "unit": "TFLOP/s"}
+    else:
+        achieved = byts / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["phase"] = dom
+    roof["kernel"] = {"output": "tc_causal_out_kernel" if w.causal else "tc_bidir_out_kernel",
+                      "state": "tc_state_kernel", "scan": "scan_kernel", "plan": "plan_kernel"}[dom]
+    roof["alg_flops_per_launch"] = flops
+    roof["alg_bytes_per_launch"] = byts
+    roof["peak_source"] = peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")
+    if "output" in phase_ms and phase_ms["output"] > 0:
+        roof["tensor_frac_of_output"] = alg["flops"] * token_heads / (phase_ms["output"] * 1e-3) / 1e12 / tflop
+        roof["hbm_frac_of_output"] = alg["bytes"] * token_heads / (phase_ms["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    roof["phase_ms"] = phase_ms
+    roof["kernel_timing"] = ("CUDA events between la_forward_phase calls on the launching stream, over as many "
+                             "forwards as the timed steps, right after them")
+    return roof
 
 
 def measured_peaks() -> dict:
@@ -208,16 +254,40 @@ def aggregate_value(tokens_per_step_per_rank: int, steps: int, world: int, max_m
 # ----------------------------------------------------------------------------
 # CPU baseline: the oracle, timed on a bounded sample of the workload
 # ----------------------------------------------------------------------------
-def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None) -> dict:
-    """Time the oracle, as it stands, on rows [0, n) of every head of the first
-    sequence (n sized from a calibration run so the sample takes ~`seconds`).
-    BLAS is limited to one thread; tokens/s = token-heads/s / H."""
+def _oracle_rows(job):
+    """Worker (spawned process, one BLAS thread): the oracle on one head's rows;
+    returns the seconds it took."""
     import oracle
     try:
         from threadpoolctl import threadpool_limits
-        limiter = threadpool_limits(limits=1)
+        threadpool_limits(limits=1)
     except Exception:
-        limiter = None
+        pass
+    causal, kind, q, k, v, om, eps, norm, state_in = job
+    f = oracle.causal if causal else oracle.bidir
+    t0 = time.perf_counter()
+    f(q, k, v, kind, omega=om, eps=eps, norm=norm, state_in=state_in)
+    return time.perf_counter() - t0
+
+
+def oracle_pool():
+    """Process pool for the CPU baseline: spawned (never forked after CUDA is
+    initialised), one worker per host core, each with one BLAS thread."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    n = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1))
+    return ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn")), n
+
+
+def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None, pool=None) -> dict:
+    """Time the oracle, as it stands, on rows [0, n) of every head of the first
+    sequence: one head per worker of `pool` (one process per host core, one
+    BLAS thread each), n sized from a single-core calibration run so that the
+    sample takes about `seconds` of CPU time.  tokens/s = token-heads/s / H,
+    with the wall time of the parallel sample."""
+    import oracle
     if inputs is None:
         inputs = synthetic.make_qkv(w)
     om = None
@@ -227,33 +297,34 @@ def cpu_baseline(w: synthetic.Workload, seconds: float, inputs=None) -> dict:
     if w.decode:
         return cpu_baseline_decode(w, seconds, inputs, om)
     a, b = int(inputs.cu_seqlens[0]), int(inputs.cu_seqlens[1])
-    f = oracle.causal if w.causal else oracle.bidir
     st = carried_state(w, 1) if w.carry else None
 
-    def run(h, n):
+    def job(h, n):
         sl = slice(a, a + n)
         state_in = None
         if st is not None:
             state_in = (st[:, h:h + 1, :, :-1].astype(np.float64), st[:, h:h + 1, :, -1].astype(np.float64))
-        f(inputs.q[sl, h:h + 1], inputs.k[sl, h:h + 1], inputs.v[sl, h:h + 1], w.map, omega=om, eps=w.eps,
-          norm=w.norm, state_in=state_in)
+        return (w.causal, w.map, np.ascontiguousarray(inputs.q[sl, h:h + 1]), np.ascontiguousarray(inputs.k[sl, h:h + 1]),
+                np.ascontiguousarray(inputs.v[sl, h:h + 1]), om, w.eps, w.norm, state_in)
 
-    n0 = min(2048, b - a)
-    t0 = time.perf_counter()
-    run(0, n0)
-    t_cal = time.perf_counter() - t0
-    n = int(min(b - a, max(n0, n0 * (seconds - t_cal) / max(1e-9, t_cal * max(1, w.H - 1)))))
+    n0 = min(1024, b - a)
+    t_cal = _oracle_rows(job(0, n0))
+    if pool is None:
+        pool, workers = oracle_pool()
+    else:
+        pool, workers = pool
+    used = min(workers, w.H)
+    # each worker gets ceil(H / used) heads; size n so that one worker's share takes ~seconds / used
+    per_worker = -(-w.H // used)
+    n = int(min(b - a, max(n0, n0 * (seconds / max(1, used)) / max(1e-9, t_cal * per_worker))))
     t1 = time.perf_counter()
-    for h in range(1, w.H):
-        run(h, n)
+    list(pool.map(_oracle_rows, [job(h, n) for h in range(w.H)]))
     el = time.perf_counter() - t1
-    th = n * (w.H - 1)
-    if el <= 0 or th == 0:
-        el, th = t_cal, n0
-    return {"value": th / w.H / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    th = n * w.H
+    return {"value": th / w.H / el, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"fp64 oracle ({'causal recurrence' if w.causal else 'bidirectional'}) on rows 0..{n - 1} "
-                      f"of heads 1..{w.H - 1} of sequence 0: {th} token-heads in {el:.1f} s, 1 BLAS thread; "
-                      f"tokens/s = token-heads/s / H"}
+                      f"of all {w.H} heads of sequence 0 ({th} token-heads) in {el:.1f} s wall, one head per "
+                      f"process on {used} host cores, 1 BLAS thread each; tokens/s = token-heads/s / H"}
 
 
 def carried_state(w: synthetic.Workload, nseq: int) -> np.ndarray:
@@ -317,10 +388,12 @@ def cpu_baseline_backward(w: synthetic.Workload, seconds: float) -> dict:
 # GPU arm
 # ----------------------------------------------------------------------------
 def run_ours(args):
+    world, rank, local = dist_env()
+    # the oracle's worker processes are spawned before CUDA is touched (rank 0, one GPU)
+    pool = oracle_pool() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     import torch
     import kernelized_linear_attention_gb300 as la
 
-    world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
@@ -363,25 +436,26 @@ def run_ours(args):
         state_out = torch.empty_like(state_in)
     state_kw = dict(norm=w.norm, state_in=ptr(state_in), state_out=ptr(state_out))
 
-    def step(evs=None):
-        n = 0
-        for ph in range(4):
-            if evs is not None:
-                evs[ph].record(stream)
-            n += la.la_forward_phase(w.causal, ph, *call_args, **state_kw)
-        if evs is not None:
-            evs[4].record(stream)
-        return n
+    plain = w.norm == "attention" and not w.carry
 
+    def step():
+        """One forward through the boundary entry point a user calls: la_forward_causal /
+        la_forward_bidir (la_forward for the norm and carried-state variants)."""
+        if plain:
+            la.forward_ptrs(w.causal, *call_args)
+        else:
+            la.forward_general_ptrs(w.causal, *call_args, **state_kw)
+        return launches_per_call
+
+    launches_per_call = sum(la.la_forward_phase(w.causal, ph, *call_args, **state_kw) for ph in range(4))
     warmup = max(args.warmup, 3)      # timing rules: at least 3 untimed warm-up steps
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     if la.la_workspace_error(ws) != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"device error {la.la_workspace_error(ws)} during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -392,7 +466,7 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(K):
-        launches += step(evs[i])
+        launches += step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -400,45 +474,20 @@ def run_ours(args):
     clocks = sampler.stop()
     ms_total = t_start.elapsed_time(t_end)
     ms_total_max = max_over_ranks(ms_total, world, dev)
-    phase_ms = {PHASE_NAMES[p]: statistics.mean(evs[i][p].elapsed_time(evs[i][p + 1]) for i in range(K))
-                for p in range(4)}
     if la.la_workspace_error(ws) != 0:
         raise RuntimeError("device error during the timed steps")
+    # the same forwards phase by phase (la_forward_phase runs exactly the kernels of the call
+    # above, in order), CUDA events between the phases on the launching stream: the duration
+    # of each kernel for the roofline
+    phase_ms, _ = _phase_timed(la, stream, K, (w.causal,) + call_args, **state_kw)
 
     tokens = T  # tokens per step per GPU (all heads)
     value = aggregate_value(tokens, K, world, ms_total_max)
-    alg = algorithmic(w)
     peaks = measured_peaks()
-    token_heads = T * H
-    dom = max(phase_ms, key=phase_ms.get)
-    dom_ms = phase_ms[dom]
-    # algorithmic work of one output-phase launch: the whole method for every
-    # token-head of the batch (it reads q, k, v, writes out, computes both
-    # projections, the state terms and the readout).
-    alg_flops = alg["flops"] * token_heads
-    alg_bytes = alg["bytes"] * token_heads
-    t_flop = alg_flops / (peaks["bf16_tflops"] * 1e12)
-    t_byte = alg_bytes / (peaks["hbm_gbs"] * 1e9)
-    if dom == "output":
-        if t_flop >= t_byte:
-            achieved = alg_flops / (dom_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-        else:
-            achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
-            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        byts = alg["bytes"] * token_heads / 2 if dom == "state" else alg_bytes
-        achieved = byts / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof = roofline_of(w, phase_ms, peaks)
     path = "tc" if la.la_selected_path(w.causal, w.map, tdt, dk, dv, r) == 1 and not (w.norm == "sum" and w.carry) \
         else "simt"
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(path, dom, w.name)
-    roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")
-    roof["tensor_frac_of_output"] = alg_flops / (phase_ms["output"] * 1e-3) / 1e12 / peaks["bf16_tflops"]
-    roof["hbm_frac_of_output"] = alg_bytes / (phase_ms["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
-    roof["phase_ms"] = phase_ms
+    roof["traffic"] = recorded_traffic(path, roof["phase"], w.name)
 
     # end to end through the C ABI with host buffers: every step copies its q, k, v from pinned host
     # memory, runs the forward and copies out back.  Pipelined over two device buffer sets on three
@@ -452,8 +501,10 @@ def run_ours(args):
     def forward_on(bset):
         a = (ptr(bset[0]), ptr(bset[1]), ptr(bset[2]), ptr(omega), w.map, tdt, ptr(cu), nseq, T, H, dk, dv, r,
              w.eps, ptr(bset[3]), ptr(ws), ws_bytes, stream.cuda_stream)
-        for ph in range(4):
-            la.la_forward_phase(w.causal, ph, *a, **state_kw)
+        if plain:
+            la.forward_ptrs(w.causal, *a)
+        else:
+            la.forward_general_ptrs(w.causal, *a, **state_kw)
 
     def pipelined(nsteps, e_begin=None, e_end=None):
         done, copied = [None, None], [None, None]
@@ -515,16 +566,22 @@ def run_ours(args):
         line["decode_step"] = decode_line(la, dev, stream, peaks, max(3, min(K, 20)), DECODE_WORKLOAD)
         line["backward"] = backward_line(la, dev, stream, max(3, min(K, 10)), BACKWARD_WORKLOAD)
         line["fp32_n1024"] = small_config_line(la, dev, stream, max(5, min(K, 20)))
+        line["configs"] = {name: config_line(la, dev, stream, peaks, K, name) for name in CONFIG_WORKLOADS}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, inputs, pool)
         if "variants" in line:
             # the oracle beside each further row, on a bounded sample of its workload
             secs = max(2.0, args.cpu_seconds / 4)
             for key, wname in (("none", "favor_causal_b1h16n65536_none"), ("carry", "favor_causal_b1h16n65536_carry"),
                                ("sum", "elu_causal_b8h8n4096_sum")):
-                line["variants"][key]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[wname], secs)
+                line["variants"][key]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[wname], secs, pool=pool)
+            for name in CONFIG_WORKLOADS:
+                line["configs"][name]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[name], secs, pool=pool)
+            line["fp32_n1024"]["cpu_baseline"] = cpu_baseline_single(synthetic.workloads()["fp32_n1024"])
             line["decode_step"]["cpu_baseline"] = cpu_baseline(synthetic.workloads()[DECODE_WORKLOAD], secs)
             line["backward"]["cpu_baseline"] = cpu_baseline_backward(synthetic.workloads()[BACKWARD_WORKLOAD], secs)
+    if pool is not None:
+        pool[0].shutdown()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -714,6 +771,75 @@ def decode_line(la, dev, stream, peaks, steps, name, warmup=3, world=1, e2e_step
             "roofline": roof, "e2e": e2e, "clocks": clocks}
 
 
+def config_line(la, dev, stream, peaks, steps, name) -> dict:
+    """One whole forward of a workload through la_forward_causal / la_forward_bidir
+    (cu_seqlens for packed workloads), timed with CUDA events on the launching
+    stream after 3 warm-up calls; then the same forwards phase by phase for the
+    roofline of the dominant kernel.  Inputs stay resident in HBM."""
+    import torch
+    w = synthetic.workloads()[name]
+    inputs = synthetic.make_qkv(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    qkv = []
+    for n in ("q", "k", "v"):
+        a = torch.from_numpy(np.ascontiguousarray(inputs.storage(n)))
+        qkv.append((a.view(torch.bfloat16) if w.dtype == "bf16" else a).to(dev))
+    omega = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        omega = la.la_orthogonal_features(torch.from_numpy(blocks).to(dev), torch.from_numpy(lengths).to(dev), w.r)
+    cu = None if w.equal_lengths else torch.from_numpy(inputs.cu_seqlens).to(dev)
+    out = torch.empty((w.T, w.H, w.dv), dtype=tdt, device=dev)
+    nb = la.la_workspace_bytes(w.causal, w.map, tdt, cu is not None, w.nseq, w.T, w.H, w.dk, w.dv, w.r)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    args = (ptr(qkv[0]), ptr(qkv[1]), ptr(qkv[2]), ptr(omega), w.map, tdt, ptr(cu), w.nseq, w.T, w.H, w.dk, w.dv,
+            w.r, w.eps, ptr(out), ptr(ws), nb, stream.cuda_stream)
+    for _ in range(3):
+        la.forward_ptrs(w.causal, *args)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        la.forward_ptrs(w.causal, *args)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if la.la_workspace_error(ws) != 0:
+        raise RuntimeError(f"device error in the {name} forward")
+    ms = e0.elapsed_time(e1) / steps
+    phase_ms, launches = _phase_timed(la, stream, steps, (w.causal,) + args)
+    roof = roofline_of(w, phase_ms, peaks)
+    roof["traffic"] = recorded_traffic("tc", roof["phase"], name)
+    alg = algorithmic(w)
+    return {"workload": name, "call": "la_forward_causal" if w.causal else "la_forward_bidir",
+            "B": w.nseq, "H": w.H, "N": w.lengths[0] if w.equal_lengths else "varlen",
+            "T": w.T, "map": w.map, "causal": w.causal, "r": w.r, "ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
+            "launches_per_call": launches, "roofline": roof,
+            "whole_forward": {"alg_bytes": alg["bytes"] * w.T * w.H, "alg_flops": alg["flops"] * w.T * w.H,
+                              "hbm_frac": alg["bytes"] * w.T * w.H / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                              "tensor_frac": alg["flops"] * w.T * w.H / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
+            "l2": "no flush: inputs exceed L2" if 3 * w.T * w.H * w.dk * 2 > (126 << 20)
+                  else "inputs below L2 (100 MB): consecutive forwards may hit L2",
+            "clocks": clocks}
+
+
+def cpu_baseline_single(w: synthetic.Workload) -> dict:
+    """The oracle on the whole (small) workload on one core, one BLAS thread."""
+    import oracle
+    inputs = synthetic.make_qkv(w)
+    om = None
+    if w.map == "favor":
+        blocks, lengths = synthetic.omega_gaussians(w.r, w.dk)
+        om = oracle.orthogonal_random_features(blocks, lengths, r=w.r).astype(np.float32)
+    el = _oracle_rows((w.causal, w.map, inputs.q, inputs.k, inputs.v, om, w.eps, w.norm, None))
+    return {"value": w.T / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle ({'causal recurrence' if w.causal else 'bidirectional'}) on the whole "
+                      f"{w.name} problem ({w.T} tokens x {w.H} head, {w.map}) in {el:.3f} s on one core, 1 BLAS thread"}
+
+
 def small_config_line(la, dev, stream, steps) -> dict:
     """Latency of the fp32 single-head N=1024 case (a parity configuration,
     reported as time only): whole forwards on the fp32 CUDA-core kernels, for
@@ -864,32 +990,40 @@ def run_reference(args):
         sample = (f"each step: fp64 oracle decode step of head 0 of the first {n_sample} sequences of the "
                   f"{w.name} workload (1 of {w.H} heads); tokens/s = (sequence, head) steps/s / H")
     else:
+        # each step: the oracle on the first n_sample tokens of every head, one head per
+        # process on the host's cores (spawned pool, one BLAS thread per process)
         n_sample = 2048
         sl = slice(0, n_sample)
-        state_in = None
-        if w.carry:
-            st = carried_state(w, 1)
-            state_in = (st[:, :1, :, :-1].astype(np.float64), st[:, :1, :, -1].astype(np.float64))
-        f = oracle.causal if w.causal else oracle.bidir
+        st = carried_state(w, 1) if w.carry else None
+        jobs = []
+        for h in range(w.H):
+            state_in = None
+            if st is not None:
+                state_in = (st[:, h:h + 1, :, :-1].astype(np.float64), st[:, h:h + 1, :, -1].astype(np.float64))
+            jobs.append((w.causal, w.map, np.ascontiguousarray(inputs.q[sl, h:h + 1]),
+                         np.ascontiguousarray(inputs.k[sl, h:h + 1]), np.ascontiguousarray(inputs.v[sl, h:h + 1]),
+                         om, w.eps, w.norm, state_in))
+        pool, workers = oracle_pool()
+        cores = min(workers, w.H)
 
         def one():
-            f(inputs.q[sl, :1], inputs.k[sl, :1], inputs.v[sl, :1], w.map, omega=om, eps=w.eps, norm=w.norm,
-              state_in=state_in)
-        sample = (f"each step: fp64 oracle on the first {n_sample} tokens of head 0 of the "
-                  f"{w.name} workload (1 of {w.H} heads); tokens/s = token-heads/s / H")
-
+            list(pool.map(_oracle_rows, jobs))
+        sample = (f"each step: fp64 oracle on the first {n_sample} tokens of all {w.H} heads of the "
+                  f"{w.name} workload, one head per process on {cores} host cores; tokens/s = token-heads/s / H")
     for _ in range(args.warmup):
         one()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one()
     el = time.perf_counter() - t0
-    value = n_sample * args.steps / w.H / el
+    heads_per_step = 1 if w.decode else w.H
+    value = n_sample * heads_per_step * args.steps / w.H / el
     line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1 if w.decode else cores,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -102,6 +102,10 @@ typedef enum { LA_NORM_ATTENTION = 0, LA_NORM_NONE = 1, LA_NORM_SUM = 2 } la_nor
 #define LA_DEVERR_NONE 0
 #define LA_DEVERR_CU_SEQLENS 1    /* cu_seqlens broke the packing rules: nothing computed */
 #define LA_DEVERR_WAIT_TIMEOUT 2  /* a bounded in-kernel wait ran out: output incomplete */
+#define LA_DEVERR_RANGE 3         /* tensor-core path: a value fell outside what its fp16
+                                     operands hold after scaling and was clamped; the result
+                                     is finite but may be less accurate (reported only when
+                                     neither error above was recorded) */
 
 /* Size limits (checked on the host). */
 #define LA_MAX_DK 256
@@ -277,13 +281,17 @@ LA_API la_status la_forward_phase(int causal, int phase, int norm, const void* q
  *   LA_NOALLOC_SCRATCH_BYTES (la_workspace_bytes(1, ...) gives the need).
  *   The first call on each device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
- *   stream capture.  Every call on a device uses the same array and leaves
- *   its contents behind; each call rewrites whatever it reads before reading
- *   it, so nothing needs clearing, but calls whose work overlaps on the GPU
- *   (different streams, or different host threads) race on the array and
- *   must be serialised by the caller.  Device-side errors are not reported
- *   (there is no workspace to read): check cu_seqlens with
- *   la_check_cu_seqlens beforehand where its contents are not trusted.
+ *   stream capture.  The cache lives as long as the process: cudaDeviceReset
+ *   destroys the context that holds the array, so a program that resets a
+ *   device must not call this entry point on that device afterwards (the
+ *   cached address would no longer be the array's).  Every call on a device
+ *   uses the same array and leaves its contents behind; each call rewrites
+ *   whatever it reads before reading it, so nothing needs clearing, but calls
+ *   whose work overlaps on the GPU (different streams, or different host
+ *   threads) race on the array and must be serialised by the caller.
+ *   Device-side errors of the latest call (cu_seqlens contents that break the
+ *   packing rules, a bounded wait that ran out, a value clamped into the f16
+ *   operand range) are read with la_noalloc_error.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -291,6 +299,16 @@ LA_API la_status la_forward_causal_noalloc(const void* q, const void* k, const v
                                     const float* omega, int map, int dtype,
                                     const int32_t* cu_seqlens, int nseq, int64_t T, int H,
                                     int d_k, int d_v, int r, float eps, void* out, void* stream);
+
+/*
+ * la_noalloc_error - the device error word that the latest
+ *   la_forward_causal_noalloc call on the current device left in the
+ *   library's scratch array, as la_workspace_error reports it for a
+ *   workspace: LA_OK, or LA_ERR_DEVICE with the LA_DEVERR_* code in *code
+ *   (host pointer, may be NULL).  Synchronises `stream` (pass the stream of
+ *   that call).  Not a counterpart of anything on the source pages.
+ */
+LA_API la_status la_noalloc_error(int* code, void* stream);
 
 /*
  * la_workspace_bytes - scratch size for a forward call on the current device.

@@ -55,6 +55,7 @@ def load_library():
         "la_decode_step": ([_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_float, _vp, _vp, _vp], _c_int),
         "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
+        "la_noalloc_error": ([ctypes.POINTER(_c_int), _vp], _c_int),
         "la_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_int],
                                _c_size),
         "la_check_cu_seqlens": ([_vp, _c_int, _c_i64, _vp], _c_int),
@@ -171,6 +172,16 @@ def forward_ptrs(causal: bool, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, 
                            out, workspace, workspace_bytes, _stream(stream)))
 
 
+def forward_general_ptrs(causal: bool, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r, eps,
+                         out, workspace, workspace_bytes, stream, norm="attention", state_in=None,
+                         state_out=None) -> None:
+    """Raw la_forward call with integer device pointers (state_in / state_out too)."""
+    dt = DTYPE_IDS[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    _check("la_forward", load_library().la_forward(int(causal), _norm_id(norm), q, k, v, omega, _map_id(map), dt,
+                                                   cu_seqlens, nseq, T, H, d_k, d_v, r, eps, state_in, state_out,
+                                                   out, workspace, workspace_bytes, _stream(stream)))
+
+
 def la_forward_phase(causal: bool, phase: int, q, k, v, omega, map, dtype, cu_seqlens, nseq, T, H, d_k, d_v, r,
                      eps, out, workspace, workspace_bytes, stream=None, norm="attention", state_in=None,
                      state_out=None) -> int:
@@ -209,6 +220,16 @@ def la_forward_causal_noalloc(q, k, v, map, omega=None, cu_seqlens=None, nseq=No
         _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype], _ptr(cu_seqlens), nseq, T, H, d_k, d_v, r,
         eps, _ptr(out), _stream(stream)))
     return out
+
+
+def la_noalloc_error(stream=None) -> int:
+    """Device error code the latest la_forward_causal_noalloc call on the current
+    device recorded in the library's scratch array (0 = none; synchronises)."""
+    code = _c_int(0)
+    st = load_library().la_noalloc_error(ctypes.byref(code), _stream(stream))
+    if st not in (LA_OK, 5):
+        raise LinAttnError("la_noalloc_error", st)
+    return code.value
 
 
 def _forward(causal, q, k, v, map, omega, cu_seqlens, nseq, eps, out, workspace, stream, norm="attention",

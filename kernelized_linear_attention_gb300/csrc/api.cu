@@ -96,6 +96,7 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     U = std::max<int64_t>(U, 1);
     lo.L = (int)std::min<int64_t>(L, INT32_MAX);
     lo.U = (int)U;
+    lo.Lc = (int)ceil_div(lo.L, 128);
     lo.dvx = dv + 1;
     size_t o = align_up(sizeof(WsHeader), kAlign);
     lo.units = o;     o = align_up(o + sizeof(Unit) * (size_t)U, kAlign);
@@ -104,6 +105,7 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     const size_t state_bytes = sizeof(float) * (size_t)U * H * r * lo.dvx;
     lo.partial = o;   o = align_up(o + state_bytes, kAlign);
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
+    lo.kscale = o;    o = align_up(o + (path == kPathTensor ? sizeof(int) * (size_t)U * H * lo.Lc : 0), kAlign);
     lo.sig_q = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     lo.sig_k = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     if (bwd) {
@@ -174,7 +176,11 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     p.sig_q = reinterpret_cast<float*>(ws + lo.sig_q);
     p.sig_k = reinterpret_cast<float*>(ws + lo.sig_k);
     if (tc_sum) p.div_rows = p.sig_q;   // the output kernels divide by max(sigma_q, eps)
-    p.U = lo.U; p.L = lo.L;
+    p.U = lo.U; p.L = lo.L; p.Lc = lo.Lc;
+    // The causal FAVOR+ output kernel scales each chunk's key features by the power of
+    // two the state kernel records per chunk: the state pass then covers every unit.
+    const bool want_kscale = path == kPathTensor && causal && map == LA_MAP_FAVOR;
+    if (want_kscale) p.kscale = reinterpret_cast<int*>(ws + lo.kscale);
 
     // A causal call whose sequences are all single segments starts every unit
     // from its sequence's state_in (or zero): unless the final state is
@@ -183,6 +189,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     // A final state needs every segment's sum, the last one included.
     const bool single_segments = !has_cu && lo.U == nseq;
     const bool need_state = !causal || !single_segments || state_out != nullptr;
+    const bool run_state = need_state || want_kscale;   // the scan only when need_state
     p.keep_last = state_out != nullptr ? 1 : 0;
     int prefix_is_zero = 0;
     if (!need_state) {
@@ -208,7 +215,7 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
                 }
                 break;
             case LA_PHASE_STATE:
-                if (T > 0 && need_state) {
+                if (T > 0 && run_state) {
                     e = (path == kPathTensor && map != LA_MAP_DPFP) ? tc_state(p, s) : simt_state(p, dtype, s);
                     ++n;
                 }
@@ -440,10 +447,11 @@ la_status la_check_cu_seqlens(const int32_t* cu_seqlens, int nseq, int64_t T, vo
 
 la_status la_workspace_error(const void* workspace, int* code, void* stream) {
     if (workspace == nullptr) return LA_ERR_INVALID_ARG;
-    int err = 0;
+    int words[3] = {0, 0, 0};   // WsHeader: error, n_units, range
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    const int err = words[0] != LA_DEVERR_NONE ? words[0] : (words[2] != 0 ? LA_DEVERR_RANGE : LA_DEVERR_NONE);
     if (code) *code = err;
     return err == LA_DEVERR_NONE ? LA_OK : LA_ERR_DEVICE;
 }

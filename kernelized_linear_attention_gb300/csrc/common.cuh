@@ -25,7 +25,10 @@ struct Unit {
 struct WsHeader {
     int error;     // LA_DEVERR_*; written with atomicMax, never cleared by kernels but the planner
     int n_units;   // units the planner produced
-    int pad[62];
+    int range;     // bits of the operands that had a value clamped into the fp16 range
+                   // (1 values, 2 key features, 4 query features, 8 element-wise features);
+                   // reported as LA_DEVERR_RANGE
+    int pad[61];
 };
 
 // Byte offsets of the workspace regions for one forward call.
@@ -35,6 +38,7 @@ struct Layout {
     size_t order;      // int[U]: units by decreasing token count (packed batches), else 0, 1, ..
     size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
+    size_t kscale;     // int[U][H][Lc]: power-of-two exponent of the keys' features in each chunk
     size_t sig_q;      // float[T][H]: sum_f phi_f(q) (sum normalisation on the tensor-core path)
     size_t sig_k;      // float[T][H]: sum_f phi_f(k)
     size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
@@ -43,6 +47,7 @@ struct Layout {
     size_t total;      // bytes
     int U;             // upper bound on units
     int L;             // segment length in tokens
+    int Lc;            // chunks of 128 tokens per segment (tensor-core path)
     int dvx;           // d_v + 1: the ones column carries z
 };
 
@@ -89,7 +94,11 @@ struct FwdParams {
     int* order;             // the tensor-core output kernels take units in this order (longest first)
     float* partial;
     float* prefix;
-    int U, L;
+    // Tensor-core path: for every (unit, head, chunk of 128 tokens) the exponent e such that
+    // the chunk's FAVOR+ key features times 2^-e lie below 2^15 (written by the state kernel,
+    // read by the causal output kernel).
+    int* kscale;
+    int U, L, Lc;
 };
 
 // ---------------------------------------------------------------------------
@@ -106,6 +115,11 @@ __device__ __forceinline__ void store_elem(__nv_bfloat16* p, int64_t i, float x)
 
 __device__ __forceinline__ void record_error(WsHeader* hdr, int code) {
     atomicMax(&hdr->error, code);
+}
+// A value outside the range the fp16 tensor-core operands hold was clamped.
+constexpr int kRangeV = 1, kRangeK = 2, kRangeQ = 4, kRangeElementwise = 8;
+__device__ __forceinline__ void record_range(WsHeader* hdr, int bits) {
+    if ((hdr->range & bits) != bits) atomicOr(&hdr->range, bits);
 }
 
 }  // namespace la

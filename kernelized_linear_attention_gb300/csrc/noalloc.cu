@@ -42,6 +42,13 @@ la_status scratch_address(void** addr) {
 }  // namespace
 }  // namespace la
 
+extern "C" la_status la_noalloc_error(int* code, void* stream) {
+    void* scratch = nullptr;
+    const la_status st = la::scratch_address(&scratch);
+    if (st != LA_OK) return st;
+    return la_workspace_error(scratch, code, stream);
+}
+
 extern "C" la_status la_forward_causal_noalloc(const void* q, const void* k, const void* v, const float* omega,
                                                int map, int dtype, const int32_t* cu_seqlens, int nseq, int64_t T,
                                                int H, int d_k, int d_v, int r, float eps, void* out,

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
         if (threadIdx.x == 0) {
             p.hdr->n_units = 0;
             p.hdr->error = LA_DEVERR_CU_SEQLENS;
+            p.hdr->range = 0;
         }
         for (int s = threadIdx.x; s <= p.nseq; s += blockDim.x) p.seq_first[s] = 0;
         return;
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
         p.seq_first[p.nseq] = min(total, p.U);
         p.hdr->n_units = min(total, p.U);
         p.hdr->error = (total > p.U) ? LA_DEVERR_CU_SEQLENS : LA_DEVERR_NONE;
+        p.hdr->range = 0;
     }
 
     // pass 3: the order in which the tensor-core output kernels take the units.

@@ -54,6 +54,8 @@ constexpr uint32_t kColP = 368;   // projection of up to 128 features [128][128]
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
+// bound on the exit-time wait for a TMA load the CTA issued (it completes in microseconds)
+constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 typedef unsigned char Tile[kTile];
 
@@ -72,8 +74,10 @@ struct BidirBars {
     uint64_t q_full[2], q_empty[2];   // TMA -> NE, projection issuer;  (projection commit + 2 NE) -> TMA
     uint64_t cx_full[2];              // NE (2 warps) -> projection issuer: offsets of the stage's queries staged
     uint64_t p_full[2], p_empty[2];   // projection commit -> PE: exponent of a feature half;  PE (8 warps) -> issuer
-    uint64_t a_full[2], a_empty[2];   // PE (8 warps) -> readout issuer: phi(q) bf16 in TMEM;  readout commit -> PE
+    uint64_t a_full[2], a_empty[2];   // PE (8 warps) -> readout issuer: phi(q) f16 in TMEM;  readout commit -> PE
     uint64_t o_full, o_empty;         // readout commit -> OE: numerator/denominator;  OE (4 warps) -> readout issuer
+    uint64_t rx_full[2];              // PE (8 warps) -> PE: per-row maxima of a chunk posted (two slots)
+    uint64_t srow_free[2];            // OE (4 warps) -> PE: the row scales of a chunk read (two slots)
     uint64_t drain[2];
     uint32_t tmem_base;
     int pad;
@@ -85,17 +89,22 @@ struct __align__(1024) BidirSmem {
     Tile tq[2];                       // two stages
     Tile bias;                        // K-major [query][64]: columns 16 st, 16 st + 1 = -offset (hi, lo)
     Tile ones;                        // K-major [feature][64]: columns 16 i, 16 i + 1 = 1
-    unsigned char shi[4][kSbfBlock];  // whole-sequence [S|z]^T, bf16 high part
-    unsigned char slo[4][kSbfBlock];  // and the bf16 rounding remainder
+    unsigned char sf16[4][kSbfBlock]; // whole-sequence [S|z]^T 2^-g as f16: rows 0..63 S, 64 z (hi), 65 z (lo)
+    float rowmax[2][2][kC];           // per chunk slot, warpgroup and query row: the maximum it saw
+    int srow[2][kC];                  // per chunk slot and query row: the exponent of its phi(q) scale
+    int gexp;                         // exponent g of the state copy's scale
+    float red[8];
     BidirBars b;
 };
 
-// Segment-state kernel: 226 KB.
-constexpr int kStateStages = 4;
+// Segment-state kernel: 196 KB.
+constexpr int kStateStages = 3;
 struct StateBars {
     uint64_t k_full[kStateStages], k_empty[kStateStages];   // TMA -> NE / PE;  (projection commit + NE) / 8 PE warps -> TMA
-    uint64_t v_full[kStateStages], v_empty[kStateStages];   // TMA -> update issuer;  its commit -> TMA
+    uint64_t v_full[kStateStages], v_empty[kStateStages];   // TMA -> NE;  update commit -> TMA
+    uint64_t vh_full[kStateStages];   // NE (2 warps) -> update issuer: the stage's V converted to f16
     uint64_t cx_full[kStateStages];   // NE -> projection issuer: exponent offsets of the stage's tokens staged
+    uint64_t red_full[2];    // PE (8 warps) -> PE: per-warp maxima of a job posted
     uint64_t p_full[2];      // projection commit -> PE: phi exponent of a feature half in buffer b
     uint64_t a_full[2];      // PE (8 warps) -> update issuer: phi(k)^T of that half in buffer b (bf16)
     uint64_t a_empty[2];     // update commit -> projection issuer: buffer b read
@@ -109,8 +118,11 @@ struct __align__(1024) StateSmem {
     unsigned char omg_lo[kOmgBytes];
     Tile tk[kStateStages], tv[kStateStages];
     Tile bias;                    // K-major [token][64]: columns 16 st, 16 st + 1 = -offset (hi, lo) of stage st
-    Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1; rows 0..15 also
-                                  // serve as the ones atom of the update's [V|1] (columns 64, 65)
+    Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1 (bf16)
+    unsigned char ones16[2048];   // f16 ones atom of the update's [V|1]: (row, 0) = 1 (column 64 = z)
+    float red[2][8];              // PE maxima per warp (two slots)
+    int kmx[4];                   // per chunk (ring of 4): largest key exponent e over the features
+    int rsf[256];                 // each feature's final state scale exponent
     StateBars b;
 };
 // the [S|z] block of up to 256 features leaves through the k / v stages
@@ -394,6 +406,75 @@ __device__ __forceinline__ void store_output_row(const uint32_t (&a)[32], const 
     }
 }
 
+// One output row from registers as bf16 to global: out = O[0..63] * mult.
+__device__ __forceinline__ void store_output_row_f(const uint32_t (&a)[32], const uint32_t (&b)[32], float mult,
+                                                   __nv_bfloat16* dst_row) {
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t* x = q < 4 ? a + 8 * q : b + 8 * (q - 4);
+        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(x[0]) * mult, __uint_as_float(x[1]) * mult),
+                            pack_bf16x2(__uint_as_float(x[2]) * mult, __uint_as_float(x[3]) * mult),
+                            pack_bf16x2(__uint_as_float(x[4]) * mult, __uint_as_float(x[5]) * mult),
+                            pack_bf16x2(__uint_as_float(x[6]) * mult, __uint_as_float(x[7]) * mult));
+    }
+}
+
+// Factor that turns a row's scaled numerator O (the true one times 2^-e) into the
+// output: attention normalisation divides by max(den 2^e, eps) ("Performer" §3
+// sketch clamp), none multiplies by 2^e, sum normalisation divides the true
+// numerator by max(sigma_q, eps) of the row.
+__device__ __forceinline__ float row_multiplier(float den, int e, const FwdParams& p, int64_t orow) {
+    if (p.div_rows) return exp2i(e) / fmaxf(p.div_rows[orow], p.eps);
+    if (p.norm != LA_NORM_ATTENTION) return exp2i(e);
+    return den >= p.eps * exp2i(-e) && den > 0.f ? 1.0f / den : exp2i(e) / p.eps;
+}
+
+// The whole-sequence state [r][65] (fp32, true scale) as the f16 B operand of the
+// bidirectional readout: K-major blocks [80 rows][64 features], row n < 64 = S[:, n],
+// row 64 = z, row 65 = the f16 remainder of z, other rows 0; all times 2^-g with g
+// chosen so that the largest entry lies in (2^13, 2^14].  Called by every thread of
+// the block during set-up (it synchronises); writes g to *gexp.
+__device__ void load_state_f16(unsigned char (*dst)[kSbfBlock], const float* src, int r, int nhalves, float* red,
+                               int* gexp) {
+    const int t = threadIdx.x;
+    float m = 0.f;
+    if (t < 128) {
+        for (int h = 0; h < nhalves; ++h) {
+            const int feat = 128 * h + t;
+            if (feat >= r) continue;
+            for (int n = 0; n < 65; ++n) m = fmaxf(m, fabsf(src[(int64_t)feat * 65 + n]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (t < 128 && (t & 31) == 0) red[t >> 5] = m;
+    __syncthreads();
+    if (t == 0) {
+        const float mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        *gexp = mx > 0.f && mx < INFINITY ? (int)ceilf(__log2f(mx)) - 14 : 0;
+    }
+    __syncthreads();
+    const float mul = exp2i(-*gexp);
+    if (t < 128) {
+        for (int h = 0; h < nhalves; ++h) {
+            const int feat = 128 * h + t;
+            const bool have = feat < r;
+            unsigned char* blk = dst[2 * h + (t >> 6)];
+            for (int n = 0; n < kNX; ++n) {
+                float x = 0.f;
+                if (have && n < 64) x = src[(int64_t)feat * 65 + n] * mul;
+                if (have && n >= 64 && n < 66) {
+                    const float z = src[(int64_t)feat * 65 + 64] * mul;
+                    const float zh = __half2float(__float2half_rn(z));
+                    x = n == 64 ? zh : z - zh;
+                }
+                *reinterpret_cast<__half*>(blk + sw128_off(n, t & 63)) = __float2half_rn(x);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Synchronisation and MMA helpers
 // ---------------------------------------------------------------------------
@@ -471,59 +552,143 @@ struct Phase {
     }
 };
 
+// Descriptor of K step k (16 token rows) of an MN-major [V|1] operand: the start
+// advances by 2048 B and the leading-dimension offset (bits 16..29, 16-byte units)
+// shrinks by the same amount, so that the second 64-column atom stays on the same
+// 16-row ones tile for every step.
+__device__ __forceinline__ uint64_t v_ones_desc(uint64_t d0, int k) {
+    return d0 + static_cast<uint64_t>(128 * k) - (static_cast<uint64_t>(128 * k) << 16);
+}
+
+// The 16-row f16 ones atom of an MN-major [V|1] operand: element (row, 0) = 1.
+__device__ void fill_ones_atom_f16(unsigned char* tile, int tid, int nthreads) {
+    for (int i = tid; i < 16 * 8; i += nthreads) {
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, c)) =
+            c == 0 ? make_uint4(0x3C00u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Two bf16 values (one word) as two f16 values: exact for |v| in [2^-14, 65504]
+// (f16 keeps more significant bits than bf16), rounded in f16's subnormal range,
+// |v| > 65504 saturated to 65504 (satfinite).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+// Nonzero when either bf16 half of w is beyond the f16 range (|v| >= 65536, or NaN / inf).
+__device__ __forceinline__ uint32_t bf16x2_beyond_f16(uint32_t w) {
+    return __vcmpgtu2(w & 0x7FFF7FFFu, 0x477F477Fu);
+}
+
+// Rows row0 .. row0 + nrows - 1 of a [128][64] bf16 tile converted in place to f16
+// by `nthreads` cooperating threads (index tid); values beyond the f16 range are
+// saturated and, for real tokens (rows < nvalid), reported.  Returns the largest
+// |v| among the rows < nvalid this thread converted (for bounds on the state).
+__device__ float v_tile_to_f16(unsigned char* tile, int row0, int nrows, int nvalid, WsHeader* hdr, int tid,
+                               int nthreads) {
+    uint32_t bad = 0u, vmax = 0u;
+#pragma unroll 4
+    for (int i = tid; i < nrows * 8; i += nthreads) {
+        const int row = row0 + (i >> 3);
+        uint4* p = reinterpret_cast<uint4*>(tile + row * 128 + (i & 7) * 16);
+        const uint4 w = *p;
+        if (row < nvalid) {
+            bad |= bf16x2_beyond_f16(w.x) | bf16x2_beyond_f16(w.y) | bf16x2_beyond_f16(w.z) | bf16x2_beyond_f16(w.w);
+            vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                           __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+        }
+        *p = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+    }
+    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0) record_range(hdr, kRangeV);
+    // the largest magnitude as bf16 bits orders like the value (non-negative, finite or saturated)
+    const uint32_t m = max(vmax & 0xFFFFu, vmax >> 16);
+    return __uint_as_float(min(m, 0x4780u) << 16);
+}
+
 // ---------------------------------------------------------------------------
 // Causal output kernel (warp-specialised)
 // ---------------------------------------------------------------------------
+// Operands of the feature products are f16 (11 significant bits) with exact
+// power-of-two scales, so that every value the products depend on is a normal
+// f16 number:
+//   phi(k)   2^-e_c for the chunk (e_c from the state kernel: the chunk's largest
+//            key feature lands in (2^14, 2^15]); the state [S|z] is held in TMEM
+//            times 2^-e_c and rescaled exactly when the chunk's e changes;
+//   phi(q)   2^-s_i per query row (s_i from the row's first 64 features: their
+//            largest becomes 2^-10, later ones may exceed it by up to 2^26); the
+//            factor is common to the row's numerator and denominator;
+//   scores   A_i. 2^-t_i per row (largest in (2^13, 2^14]), causal mask applied;
+//   state    the copy the readout reads is [S|z] 2^-g_c (largest in (2^13, 2^14]),
+//            z also as its f16 remainder;
+//   V        converted to f16 in place (|v| <= 65504, else clamped).
+// The in-chunk numerator O_in = tril(A) [V|1] and the cross-chunk numerator
+// O_cross = Phi_Q [S|z] accumulate in separate TMEM blocks (their scales
+// differ) and are combined in fp32: num = 2^t_i O_in + 2^g_c O_cross, likewise
+// the denominator, all times 2^(s_i + e_c).  Values clamped into the f16 range
+// are reported as LA_DEVERR_RANGE.
 // Roles (512 threads):
 //   warp 0 lane 0      TMA: q, k tiles and the v tile of each chunk
 //   warp 1             projection MMAs, one elected lane (warp 1 also owns the TMEM
 //                      allocation); runs ahead, throttled by the two projection buffers
 //   warp 2             product MMAs (scores, readout, denominator, state update, A V)
+//   warp 3             the chunk's V tile as f16, in place
 //   warps 4..11 (PE)   projection epilogue in two warpgroups, each converting 32 of
 //                      the 64 columns of every job: phi(k), phi(q) of each quarter
 //                      of the features into shared memory (token t = TMEM lane t)
-//   warps 12..15 (TE)  chunk tail: masked scores as bf16 hi + lo in TMEM, then (while
-//                      A V runs) the bf16 copy of the state for the next chunk's
-//                      readout, then the output rows
+//   warps 12..15 (TE)  chunk tail: masked scores as f16 in TMEM, then (while A V
+//                      runs) the f16 copy of the state for the next chunk's readout,
+//                      then the output rows
 // Per chunk the projection warp runs, for each quarter q of the features, the
 // projections of k and q (Omega hi + lo) into two TMEM buffers; once the PE has
 // written phi, the product warp runs the products of that quarter:
-//   A (+)= Phi_Q Phi_K^T,  O (+)= Phi_Q [S|z]_bf16,  and after the last quarter
+//   A (+)= Phi_Q Phi_K^T,  O_cross (+)= Phi_Q [S|z],  and after the last quarter
 //   of each half [S|z] += Phi_K^T [V|1];
-// then, once the OE has split A, O += tril(A) [V|1].  All hand-offs are
+// then, once the TE has converted A, O_in = tril(A) [V|1].  All hand-offs are
 // mbarriers.  The next chunk's projections overlap this chunk's tail; its
-// first products wait only until O has been read out and the SE has written
+// first products wait only until O has been read out and the TE has written
 // the state of the chunks so far.
 constexpr int kCausalThreads = 512;
 
+// Tensor-memory columns of the causal kernel (512 allocated).
+constexpr uint32_t kColCS = 0;     // state, one 80-column block per feature half (lanes = features)
+constexpr uint32_t kColCP = 160;   // two 64-column projection buffers
+constexpr uint32_t kColCA = 288;   // scores [128 q][128 k] fp32; then f16 in [288, 352)
+constexpr uint32_t kColCI = 352;   // O_in [128][80]: reuses the scores' columns 64.. once converted
+constexpr uint32_t kColCX = 432;   // O_cross [128][80]
+
 struct CausalBars {
     uint64_t qk_full, qk_empty;     // TMA -> (MMA, PE);  (MMA commit + 4 PE warps) -> TMA
-    uint64_t v_full, v_empty;       // TMA -> MMA;        MMA commit -> TMA
+    uint64_t v_full, v_empty;       // TMA -> warp 3;     MMA commit -> TMA
+    uint64_t vh_full;               // warp 3 -> MMA: V as f16
     uint64_t p_full[2];             // MMA commit -> PE: projection in TMEM buffer b
     uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
     uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
     uint64_t phiq_full[2];          // PE (8 warps) -> MMA: phi(q) of global quarter g in smem (g & 1)
     uint64_t upd_done;              // MMA commit -> PE: a state update has read phi(k) of its half
     uint64_t phq_free[2];           // MMA commit -> PE: products of global quarter g done (g & 1)
-    uint64_t a_full;                // MMA commit -> SE, OE: scores, readout, state update of the chunk done
-    uint64_t ahl_full;              // OE (4 warps) -> MMA: masked scores hi/lo in TMEM
-    uint64_t o_full;                // MMA commit -> OE: numerator/denominator complete
-    uint64_t o_empty;               // OE (4 warps) -> MMA: O read out of TMEM
-    uint64_t sbf_full;              // SE (4 warps) -> MMA, PE: bf16 state and fp32 z of the previous chunks in smem
+    uint64_t a_full;                // MMA commit -> TE: scores, readout, state update of the chunk done
+    uint64_t ahl_full;              // TE (4 warps) -> MMA: masked scores as f16 in TMEM
+    uint64_t o_full;                // MMA commit -> TE: O_in complete
+    uint64_t o_empty;               // TE (4 warps) -> MMA: O_in and O_cross read out of TMEM
+    uint64_t sbf_full;              // TE (4 warps) -> MMA, PE: f16 state copy of the previous chunks in smem
+    uint64_t rx_full[2];            // PE (8 warps) -> PE: row maxima of phi(q), quarter 0, posted (two slots)
+    uint64_t tx_full[2];            // TE (4 warps) -> TE: maxima of the state posted (two slots)
+    uint64_t srow_free[2];          // TE (4 warps) -> PE: a chunk's row scales read (two slots)
     uint64_t drain[2];              // one per MMA-issuing warp
     uint32_t tmem_base;
     int pad;
 };
 
-// z of feature f (0..63 within its quarter) as bf16 hi (row 0) + lo (row 1) of
-// the quarter's 16-row K-major tile: the denominator MMA then yields
-// phi(q) . z_hi and phi(q) . z_lo in two columns.  A single bf16 z was the
-// largest error of long causal rows (its rounding no longer matched the
-// numerator's).
-__device__ __forceinline__ void store_z_hilo(unsigned char* tile, int f, float z) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(z);
-    *reinterpret_cast<__nv_bfloat16*>(tile + sw128_off(0, f)) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(tile + sw128_off(1, f)) = __float2bfloat16_rn(z - __bfloat162float(hi));
+// z of feature f (0..63 within its quarter) as f16 (row 0) and its f16 remainder
+// (row 1) of the quarter's 16-row K-major tile: the denominator MMA then yields
+// both parts of phi(q) . z in two columns.
+__device__ __forceinline__ void store_z_f16(unsigned char* tile, int f, float z) {
+    const __half hi = __float2half_rn(z);
+    *reinterpret_cast<__half*>(tile + sw128_off(0, f)) = hi;
+    *reinterpret_cast<__half*>(tile + sw128_off(1, f)) = __float2half_rn(z - __half2float(hi));
 }
 
 struct __align__(1024) CausalSmem {
@@ -532,11 +697,25 @@ struct __align__(1024) CausalSmem {
     Tile tq, tk, tv;
     Tile phq[2];                      // Phi_Q of one quarter (64 features), two buffers
     Tile phk[2];                      // Phi_K of one half (two quarters)
-    Tile sbf[2];                      // S bf16, MN-major [feature][v]: features 128h.. in sbf[h]
-    unsigned char zrow[4][2048];      // per quarter: K-major [16][64], rows 0, 1 = z as bf16 hi, lo; rows 2..15 = 0
-    unsigned char zones[2][2048];     // K-major [16][64] x 2 (tokens 0..63, 64..127): row 0 = 1, rest 0
+    Tile sbf[2];                      // S 2^-g f16, MN-major [feature][v]: features 128h.. in sbf[h]
+    unsigned char zrow[4][2048];      // per quarter: K-major [16][64], rows 0, 1 = z 2^-g as f16 + remainder
+    unsigned char ones16[2048];       // f16 ones atom of [V|1]: (row, 0) = 1
+    float rowmax[2][2][kC];           // phi(q) row maxima per slot and warpgroup
+    int srow[2][kC];                  // per slot and query row: s_i
+    float qsum[2][2][kC];             // per slot, warpgroup and query row: sum of |phi(q) 2^-s_i| it wrote
+    float tred[2][4];                 // TE maxima per slot and warp
+    float vmax;                       // largest |v| of the unit's chunks converted so far (warp 3)
     CausalBars b;
 };
+
+// Power-of-two exponent R of the keys' scale for a chunk whose largest key feature
+// exponent bound is e (e = ceil(max) - 15, from the state kernel): the previous R is
+// kept while the chunk's largest feature stays within (2^7, 2^15] of the scale, so
+// that the state is rescaled only when the keys' magnitude moves; a new R puts the
+// largest feature at 2^13.
+__device__ __forceinline__ int next_key_scale(int R, int e, bool first) {
+    return (first || e > R || e < R - 8) ? e + 2 : R;
+}
 
 // Bounded wait of every lane of a warp; false for the whole warp if any lane timed out.
 // Epilogue warps proceed independently and meet only through mbarriers.
@@ -550,6 +729,112 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, bool smem_written) {
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Element-wise phi (ELU+1 or identity) of row t of a tile as f16 into the same
+// position of dst (zero when the row is past the unit's end); |phi| > 65504 is
+// clamped.  Adds sum |phi| of the row to `sum`; returns true when it clamped.
+__device__ bool elementwise_phi_row_f16(const unsigned char* tile, unsigned char* dst, int t, bool valid, int map,
+                                        float& sum) {
+    bool big = false;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo = bf16lo(ws[j]), hi = bf16hi(ws[j]);
+                if (map == LA_MAP_ELU1) {   // exponentials unconditional, so that the choices are selects
+                    const float el = ex2_approx(lo * kLog2e), eh = ex2_approx(hi * kLog2e);
+                    lo = lo > 0.f ? lo + 1.f : el;
+                    hi = hi > 0.f ? hi + 1.f : eh;
+                }
+                big |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+                lo = fminf(fmaxf(lo, -65504.f), 65504.f);
+                hi = fminf(fmaxf(hi, -65504.f), 65504.f);
+                sum += fabsf(lo) + fabsf(hi);
+                ws[j] = pack_f16x2(lo, hi);
+            }
+            o = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, c)) = o;
+    }
+    return big;
+}
+
+// DPFP-nu features of one row ("The Kernel Zoo" §6.3): x~ = relu([x, -x]) in
+// R^128 (d = 64), feature (s-1) 128 + a = x~_a x~_{(a+s) mod 128}, as f16 pairs
+// (features A0 .. A0 + 31 of shift S); products beyond 65504 are clamped (big).
+template <int S, int A0>
+__device__ __forceinline__ void dpfp_features32_f16(const uint32_t (&xw)[32], uint32_t (&out)[16], bool& big,
+                                                    float& sum) {
+    auto xval = [&](int j) { return (j & 1) ? bf16hi(xw[j >> 1]) : bf16lo(xw[j >> 1]); };
+    auto xt = [&](int j) { return j < 64 ? fmaxf(xval(j), 0.f) : fmaxf(-xval(j - 64), 0.f); };
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const int a = A0 + i;
+        const float f0 = xt(a) * xt((a + S) & 127), f1 = xt(a + 1) * xt((a + 1 + S) & 127);
+        big |= !(f0 <= 65504.f) || !(f1 <= 65504.f);
+        sum += fminf(f0, 65504.f) + fminf(f1, 65504.f);
+        out[i >> 1] = pack_f16x2(fminf(f0, 65504.f), fminf(f1, 65504.f));
+    }
+}
+
+// Features 64 quarter + 32 half .. + 31 of row t of a [128][64] bf16 input tile,
+// as f16 into the same row of dst at columns 32 half .. (zero past the unit's end).
+// r = 128 nu: quarters 0, 1 are shift 1, quarters 2, 3 shift 2.  Adds the features'
+// sum to `sum`; returns true when a feature was clamped.
+__device__ bool dpfp_phi_row32_f16(const unsigned char* tile, unsigned char* dst, int t, bool valid, int quarter,
+                                   int half, float& sum) {
+    uint32_t xw[32], w[16];
+    bool big = false;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
+        xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
+    }
+    switch (quarter * 2 + half) {
+        case 0: dpfp_features32_f16<1, 0>(xw, w, big, acc); break;
+        case 1: dpfp_features32_f16<1, 32>(xw, w, big, acc); break;
+        case 2: dpfp_features32_f16<1, 64>(xw, w, big, acc); break;
+        case 3: dpfp_features32_f16<1, 96>(xw, w, big, acc); break;
+        case 4: dpfp_features32_f16<2, 0>(xw, w, big, acc); break;
+        case 5: dpfp_features32_f16<2, 32>(xw, w, big, acc); break;
+        case 6: dpfp_features32_f16<2, 64>(xw, w, big, acc); break;
+        default: dpfp_features32_f16<2, 96>(xw, w, big, acc); break;
+    }
+    if (!valid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = 0u;
+        big = false;
+        acc = 0.f;
+    }
+    sum += acc;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, 4 * half + q)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    return big;
+}
+
+// Maximum over the four TE warps for use j (bounded mbarrier exchange, two slots).
+__device__ __forceinline__ bool group_max4(float& m, float (*red)[4], uint64_t* bar, int j, int warp0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int slot = j & 1;
+    if ((threadIdx.x & 31) == 0) red[slot][(threadIdx.x >> 5) - warp0] = m;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[slot]);
+    if (!warp_wait(&bar[slot], (j >> 1) & 1)) return false;
+    m = fmaxf(fmaxf(red[slot][0], red[slot][1]), fmaxf(red[slot][2], red[slot][3]));
+    return true;
+}
+
+// Exponent g with max * 2^-g in (2^13, 2^14] (0 for max = 0 or not finite).
+__device__ __forceinline__ int copy_exponent(float mx) {
+    return (mx > 0.f && mx < INFINITY) ? (int)ceilf(__log2f(mx)) - 14 : 0;
 }
 
 // kFavor: FAVOR+ projections, else element-wise maps of q and k; one instantiation per kind.
@@ -571,6 +856,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     const int nq = r / 64;                        // feature quarters (1, 2 or 4)
     const int nhalves = (r + 127) / 128;
     const int nchunks = (un.end - un.start + kC - 1) / kC;
+    // exponent of the keys' scale in chunk c (FAVOR+: recorded by the state kernel)
+    const int* kscale = favor ? p.kscale + ((int64_t)u * p.H + head) * p.Lc : nullptr;
+    auto key_exp = [&](int c) -> int { return favor ? kscale[c] : 0; };
 
     if (t == 0) {
         prefetch_tensormap(&map_q);
@@ -580,14 +868,16 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         mbar_init(&B.qk_empty, 9);      // MMA commit + one arrival per projection-epilogue warp
         mbar_init(&B.v_full, 1);
         mbar_init(&B.v_empty, 1);
+        mbar_init(&B.vh_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
             mbar_init(&B.p_empty[i], 8);
             mbar_init(&B.phik_full[i], 8);
-        }
-        for (int i = 0; i < 2; ++i) {
             mbar_init(&B.phiq_full[i], 8);
             mbar_init(&B.phq_free[i], 1);
+            mbar_init(&B.rx_full[i], 8);
+            mbar_init(&B.tx_full[i], 4);
+            mbar_init(&B.srow_free[i], 4);
         }
         mbar_init(&B.upd_done, 1);
         mbar_init(&B.a_full, 1);
@@ -604,7 +894,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             tma_load_3d(s.tk, &map_k, 0, head, un.start, &B.qk_full);
             mbar_arrive_expect_tx(&B.v_full, kTile);
             tma_load_3d(s.tv, &map_v, 0, head, un.start, &B.v_full);
+            if (nchunks > 1) tma_prefetch_3d(&map_v, 0, head, un.start + kC);
         }
+        s.vmax = 0.f;
     }
     if (warp == 1) {
         tmem_alloc(&B.tmem_base, kTmemCols);
@@ -628,11 +920,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     }
     for (int i = t; i < 4 * 2048 / 16; i += kCausalThreads)
         reinterpret_cast<uint4*>(s.zrow)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = t; i < 2 * 16 * 8; i += kCausalThreads) {   // row 0 of both 16 x 64 ones blocks = 1
-        const int blk = i >> 7, row = (i >> 3) & 15, c = i & 7;
-        *reinterpret_cast<uint4*>(s.zones[blk] + sw128_chunk(row, c)) =
-            row == 0 ? make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    fill_ones_atom_f16(s.ones16, t, kCausalThreads);
     for (int i = t; i < kC * 8; i += kCausalThreads) {
         const int row = i >> 3, c = i & 7;
         if (nq == 1)   // feature rows 64..127 of the state update stay zero
@@ -647,16 +935,24 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            for (int c = 1; c < nchunks; ++c) {   // chunk 0: issued at set-up
+            int nqk = nchunks > 0 ? 1 : 0, nv = nqk;   // chunks whose loads were issued (chunk 0 at set-up)
+            for (int c = 1; c < nchunks; ++c) {
                 const int t0 = un.start + c * kC;
                 if (c > 0 && !mbar_wait(&B.qk_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
                 mbar_arrive_expect_tx(&B.qk_full, 2 * kTile);
                 tma_load_3d(s.tq, &map_q, 0, head, t0, &B.qk_full);
                 tma_load_3d(s.tk, &map_k, 0, head, t0, &B.qk_full);
+                ++nqk;
+                if (c + 1 < nchunks) tma_prefetch_3d(&map_v, 0, head, t0 + kC);   // into L2 before it is needed
                 if (c > 0 && !mbar_wait(&B.v_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
                 mbar_arrive_expect_tx(&B.v_full, kTile);
                 tma_load_3d(s.tv, &map_v, 0, head, t0, &B.v_full);
+                ++nv;
             }
+            // a consumer may have given up on a wait: the CTA must not exit while a load it issued
+            // can still write shared memory (bounded; completed loads return at once)
+            if (nqk > 0 && !mbar_wait(&B.qk_full, (nqk - 1) & 1, kDrainLimitNs)) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+            if (nv > 0 && !mbar_wait(&B.v_full, (nv - 1) & 1, kDrainLimitNs)) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
         }
     }
     else if (warp == 1) {
@@ -675,7 +971,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             ++jobs[b];
             tc_fence_after();
             const uint64_t dx = b ? d_tq : d_tk;
-            const uint32_t d = tb + kColP + 64 * b, fo = 8192u * quarter;
+            const uint32_t d = tb + kColCP + 64 * b, fo = 8192u * quarter;
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
 #pragma unroll
@@ -683,8 +979,20 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mma_commit_w(&B.p_full[b]);
             return true;
         };
+        // the hi part alone of a q job: for the rows' largest exponents (buffer 1)
+        auto issue_max_job = [&](int quarter) -> bool {
+            if (!warp_wait(&B.p_empty[1], jobs[1] & 1u)) return false;
+            ++jobs[1];
+            tc_fence_after();
+            const uint32_t d = tb + kColCP + 64, fo = 8192u * quarter;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(d_tq, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+            mma_commit_w(&B.p_full[1]);
+            return true;
+        };
         for (int c = 0; c < nchunks && ok; ++c) {
             if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
+            for (int q = 0; favor && q < nq && ok; ++q) ok = issue_max_job(q);
             for (int q = 0; favor && q < nq && ok; ++q) ok = issue_job(0, q) && issue_job(1, q);
             if (ok) mma_commit_w(&B.qk_empty);   // every projection of this chunk issued
         }
@@ -693,76 +1001,51 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     else if (warp == 2) {
         // ------------------------------------------------------------ product MMAs (elected lane issues)
         const uint64_t d_phq = sdesc_sw128(smem_u32(s.phq[0]), 16, 1024);
-        const uint64_t d_zones = sdesc_sw128(smem_u32(s.zones[0]), 16, 1024);
-        const uint32_t id_z = idesc_bf16(128, 16, true, false);
         const uint64_t d_phk = sdesc_sw128(smem_u32(s.phk[0]), 16, 1024);
         const uint64_t d_sbf = sdesc_sw128(smem_u32(s.sbf[0]), kTile, 1024);                 // MN-major
-        const uint64_t d_v = sdesc_sw128(smem_u32(s.tv), kTile, 1024);                       // MN-major, V only
+        // [V|1]: V MN-major with the f16 ones atom as the second 64-column atom
+        const uint64_t d_v1 = sdesc_sw128(smem_u32(s.tv), smem_u32(s.ones16) - smem_u32(s.tv), 1024);
         const uint64_t d_zrow = sdesc_sw128(smem_u32(s.zrow[0]), 16, 1024);
-        const uint32_t id_den = idesc_bf16(128, 16, false, false);
         const uint64_t d_upd_a = sdesc_sw128(smem_u32(s.phk[0]), kTile, 1024);              // MN-major
-        const uint32_t id_scores = idesc_bf16(128, 128, false, false);
-        const uint32_t id_read = idesc_bf16(128, 64, false, true);
-        const uint32_t id_upd = idesc_bf16(128, 64, true, true);
-        const uint32_t id_av = idesc_bf16(128, 64, false, true);
-        // DPFP: phi(k) is held as hi + lo (lo tiles in the Omega area): every product with phi(k)
-        // runs once more with the lo part
-        const bool klo = !favor && p.map == LA_MAP_DPFP;   // compile-time false for FAVOR+
-        const uint64_t d_phk_lo = sdesc_sw128(smem_u32(s.omg_hi), 16, 1024);
-        const uint64_t d_upd_a_lo = sdesc_sw128(smem_u32(s.omg_hi), kTile, 1024);   // MN-major
+        const uint32_t id_den = idesc_f16(128, 16, false, false);
+        const uint32_t id_scores = idesc_f16(128, 128, false, false);
+        const uint32_t id_read = idesc_f16(128, 64, false, true);
+        const uint32_t id_upd = idesc_f16(128, kNX, true, true);
+        const uint32_t id_av = idesc_f16(128, kNX, false, true);
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             bool v_ready = false;
             for (int q = 0; q < nq; ++q) {
                 const int g = c * nq + q;
                 if (!(ok = warp_wait(&B.phik_full[g & 1], (g >> 1) & 1))) break;
-                if (q == 0) {   // O and the scores of chunk c-1 read out; the state of chunks < c copied
+                if (q == 0) {   // O of chunk c-1 read out; the state of chunks < c copied (and rescaled)
                     if (!(ok = (c == 0 || warp_wait(&B.o_empty, (c - 1) & 1)) && warp_wait(&B.sbf_full, c & 1))) break;
                 }
                 tc_fence_after();
                 if ((q & 1) || q == nq - 1) {   // phi(k) of the half complete: update now, ahead of the scores
-                    if (!v_ready && !(ok = warp_wait(&B.v_full, c & 1))) break;
+                    if (!v_ready && !(ok = warp_wait(&B.vh_full, c & 1))) break;
                     v_ready = true;
-                    const uint32_t ds = tb + kColS + 80 * (q >> 1);
+                    // [S|z] += phi(k)^T [V|1]: z from the ones column (column 64)
+                    const uint32_t ds = tb + kColCS + kNX * (q >> 1);
 #pragma unroll
                     for (int k = 0; k < kC / 16; ++k)
-                        mma_ss_w(ds, sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_v, 2048 * k), id_upd, 1u);
-                    // z += phi(k)^T 1 into column 64 (the only non-zero row of a 16-row operand)
-#pragma unroll
-                    for (int k = 0; k < kC / 16; ++k)
-                        mma_ss_w(ds + 64, sdesc_add(d_upd_a, 2048 * k), sdesc_add(d_zones, 2048 * (k >> 2) + 32 * (k & 3)), id_z, 1u);
-                    if (klo) {
-#pragma unroll
-                        for (int k = 0; k < kC / 16; ++k)
-                            mma_ss_w(ds, sdesc_add(d_upd_a_lo, 2048 * k), sdesc_add(d_v, 2048 * k), id_upd, 1u);
-#pragma unroll
-                        for (int k = 0; k < kC / 16; ++k)
-                            mma_ss_w(ds + 64, sdesc_add(d_upd_a_lo, 2048 * k),
-                                     sdesc_add(d_zones, 2048 * (k >> 2) + 32 * (k & 3)), id_z, 1u);
-                    }
+                        mma_ss_w(ds, sdesc_add(d_upd_a, 2048 * k), v_ones_desc(d_v1, k), id_upd, 1u);
                     mma_commit_w(&B.upd_done);
                 }
                 if (!(ok = warp_wait(&B.phiq_full[g & 1], (g >> 1) & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
+                    mma_ss_w(tb + kColCA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_phk, kTile * (q & 1) + 32 * k), id_scores,
                              (q > 0 || k > 0) ? 1u : 0u);
-                if (klo) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss_w(tb + kColA, sdesc_add(d_phq, kTile * (g & 1) + 32 * k),
-                                 sdesc_add(d_phk_lo, kTile * (q & 1) + 32 * k), id_scores, 1u);
-                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColO, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
+                    mma_ss_w(tb + kColCX, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_sbf, 8192 * q + 2048 * k), id_read,
                              (q > 0 || k > 0) ? 1u : 0u);
-                // denominator terms phi(q) . z_hi, phi(q) . z_lo into columns 64, 65 of O
-                // (z as the two non-zero rows of a 16-row operand)
+                // denominator terms phi(q) . z (f16 and its remainder) into columns 64, 65 of O_cross
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss_w(tb + kColO + 64, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
+                    mma_ss_w(tb + kColCX + 64, sdesc_add(d_phq, kTile * (g & 1) + 32 * k), sdesc_add(d_zrow, 2048 * q + 32 * k), id_den,
                              (q > 0 || k > 0) ? 1u : 0u);
                 mma_commit_w(&B.phq_free[g & 1]);   // this phi(q) buffer may be rewritten
             }
@@ -770,15 +1053,27 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mma_commit_w(&B.a_full);
             if (!(ok = warp_wait(&B.ahl_full, c & 1))) break;
             tc_fence_after();
-            // scores in TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127], 32 columns each
+            // O_in = tril(A) [V|1]: scores as f16 in TMEM, keys 2c, 2c + 1 in column c
 #pragma unroll
             for (int k = 0; k < kC / 16; ++k)
-                mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
-#pragma unroll
-            for (int k = 0; k < kC / 16; ++k)
-                mma_ts_w(tb + kColO, tb + kColA + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_add(d_v, 2048 * k), id_av, 1u);
+                mma_ts_w(tb + kColCI, tb + kColCA + 8 * k, v_ones_desc(d_v1, k), id_av, k > 0 ? 1u : 0u);
             mma_commit_w(&B.o_full);
             mma_commit_w(&B.v_empty);
+        }
+        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+    }
+    else if (warp == 3) {
+        // ------------------------------------------------------------ V as f16, in place
+        bool ok = true;
+        float vm = 0.f;   // running largest |v| of the unit
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int nvalid = min(kC, un.end - (un.start + c * kC));
+            if (!(ok = warp_wait(&B.v_full, c & 1))) break;
+            vm = fmaxf(vm, v_tile_to_f16(s.tv, 0, kC, nvalid, p.hdr, lane, 32));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+            if (lane == 0) s.vmax = vm;   // read by the TE for the bound on the state copy
+            warp_arrive(&B.vh_full, true);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -792,21 +1087,56 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             warp_arrive(&B.p_empty[1], false);
         }
         bool ok = true;
+        bool bigk = false, bigq = false;
+        int R = 0;                                        // the keys' scale exponent of the chunk
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             const bool valid = tr < min(kC, un.end - t0);
+            R = favor ? next_key_scale(R, key_exp(c), c == 0) : 0;
+            // the TE has read the row scales and sums of chunk c - 2 (same slot)
+            if (c >= 2 && !(ok = warp_wait(&B.srow_free[c & 1], ((c >> 1) - 1) & 1))) break;
             if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
             const float cq = favor ? favor_offset(s.tq, tr, r) : 0.f;
-            const float ck = favor ? favor_offset(s.tk, tr, r) : 0.f;
+            const float ck = favor ? favor_offset(s.tk, tr, r) + (float)R : 0.f;
             if (favor) warp_arrive(&B.qk_empty, false);   // this warp no longer reads the tiles
+            float cqs = cq;                               // + s_i
+            float qs = 0.f;                               // sum of |phi(q) 2^-s_i| this thread wrote
+            if (favor) {
+                // s_i from the row's largest exponent over all r features, taken from Q Omega'_hi^T
+                // (four jobs of the hi part alone, which errs by less than 2^-8 |Omega' x|): the row's
+                // largest phi(q) 2^-s_i lies below 2^14 times 2 to that error, well inside f16
+                float m = -INFINITY;
+                for (int q = 0; q < nq && ok; ++q) {
+                    if (!(ok = warp_wait(&B.p_full[1], (c * 2 * nq + q) & 1))) break;
+                    tc_fence_after();
+                    uint32_t v0[32];
+                    tmem_ld32(tmem_addr(tb, wl, kColCP + 64 + 32 * half_cols), v0);
+                    tmem_ld_wait();
+                    warp_arrive(&B.p_empty[1], false);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(v0[j]));
+                }
+                if (!ok) break;
+                // the other warpgroup holds the other 32 columns of every job
+                const int slot = c & 1;
+                s.rowmax[slot][half_cols][tr] = m;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.rx_full[slot]);
+                if (!(ok = warp_wait(&B.rx_full[slot], (c >> 1) & 1))) break;
+                const float mm = fmaxf(s.rowmax[slot][0][tr], s.rowmax[slot][1][tr]) - cq;
+                const int si = (valid && mm > -1e30f) ? (int)ceilf(mm) - 14 : 0;
+                cqs = cq + (float)si;
+                if (half_cols == 0) s.srow[slot][tr] = si;   // for the TE: the row's factor
+            }
             for (int q = 0; q < nq && ok; ++q) {
                 const int g = c * nq + q;
                 for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
                     uint32_t v0[32];
                     if (favor) {
-                        if (!(ok = warp_wait(&B.p_full[kind], g & 1))) break;
+                        // buffer 0: the k jobs; buffer 1: per chunk the nq max jobs, then the q jobs
+                        if (!(ok = warp_wait(&B.p_full[kind], (kind == 0 ? g : c * 2 * nq + nq + q) & 1))) break;
                         tc_fence_after();
-                        tmem_ld32(tmem_addr(tb, wl, kColP + 64 * kind + 32 * half_cols), v0);
+                        tmem_ld32(tmem_addr(tb, wl, kColCP + 64 * kind + 32 * half_cols), v0);
                         tmem_ld_wait();
                         warp_arrive(&B.p_empty[kind], false);
                     }
@@ -824,27 +1154,39 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                     unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq[g & 1];
                     if (favor) {
                         // rows past the unit's end: 2^(p - inf) = 0
-                        const float cx = valid ? (kind == 0 ? ck : cq) : __int_as_float(0x7f800000);
+                        const float cx = valid ? (kind == 0 ? ck : cqs) : __int_as_float(0x7f800000);
                         uint32_t w[16];
+                        bool big = false;
+                        float sum = 0.f;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            w[j] = pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * j]) - cx),
-                                               ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx));
+                        for (int j = 0; j < 16; ++j) {
+                            const float a = fminf(ex2_approx(__uint_as_float(v0[2 * j]) - cx), 65504.f);
+                            const float b = fminf(ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx), 65504.f);
+                            big |= !(a < 65504.f) || !(b < 65504.f);
+                            sum += a + b;
+                            w[j] = pack_f16x2(a, b);
+                        }
+                        (kind == 0 ? bigk : bigq) |= big;
+                        if (kind == 1) qs += sum;
                         store_row32_bf16(dst, tr, 32 * half_cols, w);
                     } else if (p.map == LA_MAP_DPFP) {
-                        // phi(k) also as hi + lo: its rounding is what the outputs feel (phi(q)'s
-                        // largely cancels between numerator and denominator); the lo tiles use
-                        // the Omega area, which element-wise maps leave free
-                        dpfp_phi_row32(kind == 0 ? s.tk : s.tq, dst, kind == 0 ? s.omg_hi + kTile * (q & 1) : nullptr,
-                                       tr, valid, q, half_cols);
+                        float sum = 0.f;
+                        (kind == 0 ? bigk : bigq) |= dpfp_phi_row32_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, q, half_cols, sum);
+                        if (kind == 1) qs += sum;
                     } else if (half_cols == 0) {
-                        elementwise_phi_row(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map);
+                        float sum = 0.f;
+                        (kind == 0 ? bigk : bigq) |= elementwise_phi_row_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map, sum);
+                        if (kind == 1) qs += sum;
                     }
+                    // the row's sum of |phi(q)|, for the bound that scales its scores
+                    if (kind == 1 && q == nq - 1) s.qsum[c & 1][half_cols][tr] = qs;
                     warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full[g & 1], true);
                 }
             }
             if (ok && !favor) warp_arrive(&B.qk_empty, false);
         }
+        if (__any_sync(0xffffffffu, bigk) && lane == 0) record_range(p.hdr, kRangeK);
+        if (__any_sync(0xffffffffu, bigq) && lane == 0) record_range(p.hdr, kRangeQ);
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp >= 12) {
         // ------------------------------------------------------------ TE: chunk tail
@@ -853,97 +1195,214 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         const int64_t E = (int64_t)r * 65;
         const float* src = p.prefix + ((int64_t)u * p.H + head) * E;
         const bool zero = tp.prefix_is_zero != 0;
-        for (int half = 0; half < nhalves; ++half) {   // the entering state: TMEM, bf16 rows, z
-            const int feat = 128 * half + tr;
-            const bool have = !zero && feat < r;
-            uint32_t w[32];
-#pragma unroll
-            for (int n0 = 0; n0 < kNX; n0 += 16) {
-                uint32_t x[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    x[j] = __float_as_uint((have && n0 + j < 65) ? src[(int64_t)feat * 65 + n0 + j] : 0.f);
-                tmem_st16(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + n0), x);
-                if (n0 < 64) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) w[n0 / 2 + j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-                } else if (feat < r) {
-                    store_z_hilo(s.zrow[feat >> 6], feat & 63, __uint_as_float(x[0]));
-                }
-            }
-            state_row_bf16(s.sbf[half], tr, w);
-        }
-        tmem_st_wait();
-        warp_arrive(&B.sbf_full, true);
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        // the identity map has features of either sign: |S| has no bound from z, so its copy
+        // takes the exact largest |entry| (one more pass over the state)
+        const bool exact_copy = p.map == LA_MAP_IDENTITY;
+        int uses = 0;                             // group_max4 uses (slot alternation)
         bool ok = true;
+        // The state the unit starts from (true scale) into TMEM times 2^-R_0, and its f16
+        // copy times 2^-(R_0 + g_0) for chunk 0's readout.  min holds the largest |entry|
+        // of that entering state in the current TMEM scale (part of the copy's bound).
+        int Rcur = favor && nchunks > 0 ? next_key_scale(0, key_exp(0), true) : 0;
+        int gcur = 0;
+        float min_ = 0.f;
+        {
+            const float fe = exp2i(-Rcur);
+            float m = 0.f;
+            for (int half = 0; half < nhalves; ++half) {
+                const int feat = 128 * half + tr;
+                if (zero || feat >= r) continue;
+                for (int n = 0; n < 65; ++n) m = fmaxf(m, fabsf(src[(int64_t)feat * 65 + n] * fe));
+            }
+            ok = group_max4(m, s.tred, B.tx_full, uses++, 12);
+            min_ = m;
+            gcur = copy_exponent(m);
+            const float fg = exp2i(-gcur);
+            for (int half = 0; half < nhalves && ok; ++half) {   // the entering state: TMEM, f16 rows, z
+                const int feat = 128 * half + tr;
+                const bool have = !zero && feat < r;
+                uint32_t w[32];
+#pragma unroll
+                for (int n0 = 0; n0 < kNX; n0 += 16) {
+                    uint32_t x[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        x[j] = __float_as_uint((have && n0 + j < 65) ? src[(int64_t)feat * 65 + n0 + j] * fe : 0.f);
+                    tmem_st16(tmem_addr(tb, wl, kColCS + kNX * half + n0), x);
+                    if (n0 < 64) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            w[n0 / 2 + j] = pack_f16x2(__uint_as_float(x[2 * j]) * fg, __uint_as_float(x[2 * j + 1]) * fg);
+                    } else if (feat < r) {
+                        store_z_f16(s.zrow[feat >> 6], feat & 63, __uint_as_float(x[0]) * fg);
+                    }
+                }
+                state_row_bf16(s.sbf[half], tr, w);
+            }
+            tmem_st_wait();
+            if (ok) warp_arrive(&B.sbf_full, true);
+        }
+        // bound on |phi(k) 2^-R| of the chunk's keys: FAVOR+ 2^15 (the state kernel's chunk
+        // maximum), element-wise maps the f16 limit
+        const float kmax = favor ? 32768.f : 65504.f;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             const bool valid = tr < min(kC, un.end - t0);
             if (!(ok = warp_wait(&B.a_full, c & 1))) break;
             tc_fence_after();
-            // masked scores (key j <= query tr) as bf16 hi + lo, two keys per column, in
-            // TMEM as [hi keys 0..63 | lo 0..63 | hi 64..127 | lo 64..127]: each group of
-            // 64 keys is read whole before its 64 columns are overwritten
-            float dsum = 0.f;   // sum_{j <= i} A_ij: the in-chunk part of the denominator
-            // key blocks of 32: above this warp's rows all masked (no load), below kept
-            // whole, on the diagonal masked per element
+            // masked scores (key j <= query tr) as f16 times 2^-t_i in TMEM: A_ij <= (sum_f
+            // |phi(q)_if|) max |phi(k)| bounds the row, so A 2^-t_i <= 2^14; keys 0..63 go to
+            // columns 0..31 (read before written), keys 64..127 to columns 32..63
             const int wq = warp & 3;                  // rows 32 wq .. 32 wq + 31
+            const int ti = copy_exponent((s.qsum[c & 1][0][tr] + s.qsum[c & 1][1][tr]) * kmax);
+            const int si = favor ? s.srow[c & 1][tr] : 0;
+            warp_arrive(&B.srow_free[c & 1], false);   // the PE may rewrite this slot (chunk c + 2)
+            const float ft = exp2i(-ti);
             for (int part = 0; part < 2; ++part) {
-                const uint32_t cb = kColA + 64 * part;
                 const int x0 = 2 * part, x1 = 2 * part + 1;
-                uint32_t hv0[16], lv0[16], hv1[16], lv1[16];
+                uint32_t h0[16], h1[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) hv0[j] = lv0[j] = hv1[j] = lv1[j] = 0u;
+                for (int j = 0; j < 16; ++j) h0[j] = h1[j] = 0u;
                 if (x0 <= wq) {
                     uint32_t v0[32], v1[32];
-                    tmem_ld32(tmem_addr(tb, wl, cb), v0);
-                    if (x1 <= wq) tmem_ld32(tmem_addr(tb, wl, cb + 32), v1);
+                    tmem_ld32(tmem_addr(tb, wl, kColCA + 64 * part), v0);
+                    if (x1 <= wq) tmem_ld32(tmem_addr(tb, wl, kColCA + 64 * part + 32), v1);
                     tmem_ld_wait();
-                    split_scores32(v0, 32 * x0, x0 == wq, tr, dsum, hv0, lv0);
-                    if (x1 <= wq) split_scores32(v1, 32 * x1, x1 == wq, tr, dsum, hv1, lv1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int k0 = 32 * x0 + 2 * j;
+                        const float a = (x0 < wq || k0 <= tr) ? __uint_as_float(v0[2 * j]) * ft : 0.f;
+                        const float b = (x0 < wq || k0 + 1 <= tr) ? __uint_as_float(v0[2 * j + 1]) * ft : 0.f;
+                        h0[j] = pack_f16x2(a, b);
+                    }
+                    if (x1 <= wq) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int k0 = 32 * x1 + 2 * j;
+                            const float a = (x1 < wq || k0 <= tr) ? __uint_as_float(v1[2 * j]) * ft : 0.f;
+                            const float b = (x1 < wq || k0 + 1 <= tr) ? __uint_as_float(v1[2 * j + 1]) * ft : 0.f;
+                            h1[j] = pack_f16x2(a, b);
+                        }
+                    }
                 }
-                tmem_st16(tmem_addr(tb, wl, cb), hv0);
-                tmem_st16(tmem_addr(tb, wl, cb + 32), lv0);
-                tmem_st16(tmem_addr(tb, wl, cb + 16), hv1);
-                tmem_st16(tmem_addr(tb, wl, cb + 48), lv1);
+                tmem_st16(tmem_addr(tb, wl, kColCA + 32 * part), h0);
+                tmem_st16(tmem_addr(tb, wl, kColCA + 32 * part + 16), h1);
             }
             tmem_st_wait();
             warp_arrive(&B.ahl_full, false);
-            if (c + 1 < nchunks) {   // the state after this chunk, while A V runs
+            int gnext = gcur, Rnext = Rcur;
+            if (c + 1 < nchunks) {
+                // the state after this chunk, while A V runs: rescaled exactly (a power of two)
+                // when the next chunk's key scale differs, then its f16 copy times 2^-g, g from
+                // |S| <= max|S_in| + z max|v| (non-negative features) or the exact maximum
+                Rnext = favor ? next_key_scale(Rcur, key_exp(c + 1), false) : 0;
+                const float fe = exp2i(Rcur - Rnext);
+                float m = 0.f;
+                for (int half = 0; half < nhalves; ++half) {
+                    const uint32_t col = kColCS + kNX * half;
+                    const bool live = 128 * half + tr < r;
+                    if (Rnext != Rcur || exact_copy) {
+                        uint32_t a0[32], a1[32], zc;
+                        tmem_ld32(tmem_addr(tb, wl, col), a0);
+                        tmem_ld32(tmem_addr(tb, wl, col + 32), a1);
+                        tmem_ld1(tmem_addr(tb, wl, col + 64), zc);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            a0[j] = __float_as_uint(__uint_as_float(a0[j]) * fe);
+                            a1[j] = __float_as_uint(__uint_as_float(a1[j]) * fe);
+                            if (exact_copy && live)
+                                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(a0[j])), fabsf(__uint_as_float(a1[j]))));
+                        }
+                        zc = __float_as_uint(__uint_as_float(zc) * fe);
+                        if (live) m = fmaxf(m, fabsf(__uint_as_float(zc)));
+                        if (Rnext != Rcur) {
+                            tmem_st32(tmem_addr(tb, wl, col), a0);
+                            tmem_st32(tmem_addr(tb, wl, col + 32), a1);
+                            asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
+                                         ::"r"(tmem_addr(tb, wl, col + 64)), "r"(zc) : "memory");
+                        }
+                    } else {
+                        uint32_t zc;
+                        tmem_ld1(tmem_addr(tb, wl, col + 64), zc);
+                        tmem_ld_wait();
+                        if (live) m = fmaxf(m, fabsf(__uint_as_float(zc)));
+                    }
+                }
+                if (Rnext != Rcur) tmem_st_wait();
+                if (!(ok = group_max4(m, s.tred, B.tx_full, uses++, 12))) break;
+                min_ *= fe;
+                // largest |v| of the chunks so far (warp 3 publishes it before the updates use V)
+                gnext = copy_exponent(exact_copy ? m : fmaxf(m, min_ + m * s.vmax));
+                const float fg = exp2i(-gnext);
                 for (int half = 0; half < nhalves; ++half) {
                     uint32_t a0[32], a1[32], zc;
-                    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half), a0);
-                    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 32), a1);
-                    tmem_ld1(tmem_addr(tb, (warp & 3) * 32, kColS + 80 * half + 64), zc);
+                    const uint32_t col = kColCS + kNX * half;
+                    tmem_ld32(tmem_addr(tb, wl, col), a0);
+                    tmem_ld32(tmem_addr(tb, wl, col + 32), a1);
+                    tmem_ld1(tmem_addr(tb, wl, col + 64), zc);
                     tmem_ld_wait();
                     uint32_t w[32];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        w[j] = pack_bf16x2(__uint_as_float(a0[2 * j]), __uint_as_float(a0[2 * j + 1]));
-                        w[16 + j] = pack_bf16x2(__uint_as_float(a1[2 * j]), __uint_as_float(a1[2 * j + 1]));
+                        w[j] = pack_f16x2(__uint_as_float(a0[2 * j]) * fg, __uint_as_float(a0[2 * j + 1]) * fg);
+                        w[16 + j] = pack_f16x2(__uint_as_float(a1[2 * j]) * fg, __uint_as_float(a1[2 * j + 1]) * fg);
                     }
                     state_row_bf16(s.sbf[half], tr, w);
                     const int feat = 128 * half + tr;
-                    if (feat < r) store_z_hilo(s.zrow[feat >> 6], feat & 63, __uint_as_float(zc));
+                    if (feat < r) store_z_f16(s.zrow[feat >> 6], feat & 63, __uint_as_float(zc) * fg);
                 }
                 warp_arrive(&B.sbf_full, true);
             }
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            uint32_t o0[32], o1[32], dz, dzl;
-            tmem_ld32(tmem_addr(tb, wl, kColO), o0);
-            tmem_ld32(tmem_addr(tb, wl, kColO + 32), o1);
-            tmem_ld1(tmem_addr(tb, wl, kColO + 64), dz);    // phi(q) . z_hi
-            tmem_ld1(tmem_addr(tb, wl, kColO + 65), dzl);   // phi(q) . z_lo
-            tmem_ld_wait();
-            const float den = dsum + (__uint_as_float(dz) + __uint_as_float(dzl));
-            warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O and the scores
-            const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
-            // sum normalisation divides by sigma_q of the row instead of the attention denominator
-            const float dv_ = p.div_rows ? (valid ? p.div_rows[orow] : 1.f) : den;
-            if (valid) store_output_row(o0, o1, __float_as_uint(dv_), p.eps, p.norm == LA_NORM_ATTENTION || p.div_rows,
-                                        out + orow * 64);
+            // num = 2^t_i O_in + 2^g O_cross (and the denominators), all times 2^(s_i + R_c)
+            float num[64];
+            float den;
+            {
+                uint32_t o0[32], o1[32], di;
+                tmem_ld32(tmem_addr(tb, wl, kColCI), o0);
+                tmem_ld32(tmem_addr(tb, wl, kColCI + 32), o1);
+                tmem_ld1(tmem_addr(tb, wl, kColCI + 64), di);
+                tmem_ld_wait();
+                const float f2t = exp2i(ti);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    num[j] = __uint_as_float(o0[j]) * f2t;
+                    num[32 + j] = __uint_as_float(o1[j]) * f2t;
+                }
+                den = __uint_as_float(di) * f2t;
+            }
+            {
+                const float f2g = exp2i(gcur);
+                uint32_t x[32], dh, dl;
+                tmem_ld32(tmem_addr(tb, wl, kColCX), x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) num[j] = fmaf(__uint_as_float(x[j]), f2g, num[j]);
+                tmem_ld32(tmem_addr(tb, wl, kColCX + 32), x);
+                tmem_ld1(tmem_addr(tb, wl, kColCX + 64), dh);
+                tmem_ld1(tmem_addr(tb, wl, kColCX + 65), dl);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) num[32 + j] = fmaf(__uint_as_float(x[j]), f2g, num[32 + j]);
+                den = fmaf(__uint_as_float(dh) + __uint_as_float(dl), f2g, den);
+            }
+            warp_arrive(&B.o_empty, false);           // the next chunk may overwrite O_in, O_cross and the scores
+            if (valid) {
+                const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
+                const float mult = row_multiplier(den, si + Rcur, p, orow);
+                uint4* dst = reinterpret_cast<uint4*>(out + orow * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_uint4(pack_bf16x2(num[8 * q] * mult, num[8 * q + 1] * mult),
+                                        pack_bf16x2(num[8 * q + 2] * mult, num[8 * q + 3] * mult),
+                                        pack_bf16x2(num[8 * q + 4] * mult, num[8 * q + 5] * mult),
+                                        pack_bf16x2(num[8 * q + 6] * mult, num[8 * q + 7] * mult));
+            }
+            gcur = gnext;
+            Rcur = Rnext;
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1016,6 +1475,10 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         }
         mbar_init(&B.o_full, 1);
         mbar_init(&B.o_empty, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B.rx_full[i], 8);
+            mbar_init(&B.srow_free[i], 4);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1047,9 +1510,9 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) =
             make_uint4((c & 1) == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
     }
-    if (t < 128)   // the whole-sequence state as bf16 hi + lo readout blocks
-        load_state(s.shi, s.slo, 0u, false, p.prefix + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves,
-                   false, t);
+    // the whole-sequence state as one f16 readout operand, scaled by 2^-g so that its
+    // largest entry lies in (2^13, 2^14] (z also as the f16 remainder, row 65)
+    load_state_f16(s.sf16, p.prefix + ((int64_t)u * p.H + head) * (int64_t)r * 65, r, nhalves, s.red, &s.gexp);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1059,6 +1522,7 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
+            int nq = 0;   // chunks whose loads were issued
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1, t0 = un.start + c * kC;
                 for (int a = (c == 0 ? 0 : kPrefetchAhead); a <= kPrefetchAhead; ++a)
@@ -1069,6 +1533,13 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
                 }
                 mbar_arrive_expect_tx(&B.q_full[st], kTile);
                 tma_load_3d(s.tq[st], &map_q, 0, head, t0, &B.q_full[st]);
+                ++nq;
+            }
+            // no exit while an issued load can still write shared memory (bounded)
+            for (int st = 0; st < 2; ++st) {
+                const int last = nq - 1 - ((nq - 1 - st) & 1);   // last chunk issued into stage st
+                if (last >= 0 && !mbar_wait(&B.q_full[st], (last >> 1) & 1, kDrainLimitNs))
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
             }
         }
     } else if (warp == 1) {
@@ -1104,7 +1575,7 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp == 2) {
         // ------------------------------------------------------------ readout MMAs (elected lane issues)
-        const uint32_t id_read = idesc_bf16(128, kNX, false, false);   // A from TMEM, B K-major
+        const uint32_t id_read = idesc_f16(128, kNX, false, false);   // A f16 from TMEM, B f16 K-major
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             for (int h = 0; h < nhalves && ok; ++h) {
@@ -1116,10 +1587,8 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
                 const int nk = min(r - 128 * h, 128) / 16;
                 for (int k = 0; k < nk; ++k) {
                     const int blk = 2 * h + (k >> 2);
-                    mma_ts_w(tb + kColBO, a0 + 8 * k, sdesc_sw128(smem_u32(s.shi[blk]) + 32u * (k & 3), 16, 1024),
+                    mma_ts_w(tb + kColBO, a0 + 8 * k, sdesc_sw128(smem_u32(s.sf16[blk]) + 32u * (k & 3), 16, 1024),
                              id_read, (h > 0 || k > 0) ? 1u : 0u);
-                    mma_ts_w(tb + kColBO, a0 + 8 * k, sdesc_sw128(smem_u32(s.slo[blk]) + 32u * (k & 3), 16, 1024),
-                             id_read, 1u);
                 }
                 mma_commit_w(&B.a_empty[b]);
             }
@@ -1128,15 +1597,52 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ PE: phi(q)
+        // per chunk: the exact maximum of each query row over all its features (both
+        // halves, both warpgroups), then phi(q) 2^-s_i as f16 (largest in (2^14, 2^15]);
+        // the factor 2^-s_i is common to the row's numerator and denominator
         const int wg = (warp - 4) >> 2;           // features 64 wg .. of every half
         const int wl = (warp & 3) * 32;           // TMEM lane base: queries wl ..
+        const int row = wl + lane;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
+            float m = -INFINITY;
+            for (int h = 0; h < nhalves && ok; ++h) {
+                const int j = c * nhalves + h, b = j & 1;
+                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
+                tc_fence_after();
+                if (128 * h + 64 * wg >= r) continue;   // these 64 features do not exist
+#pragma unroll
+                for (int piece = 0; piece < 2; ++piece) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg + 32 * piece), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = __uint_as_float(v[e]);
+                        m = fmaxf(m, favor ? x : fabsf(phi_elementwise(x, p.map)));
+                    }
+                }
+            }
+            if (!ok) break;
+            // the other warpgroup holds the rest of the row
+            const int slot = c & 1;
+            s.rowmax[slot][wg][row] = m;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.rx_full[slot]);
+            if (!(ok = warp_wait(&B.rx_full[slot], (c >> 1) & 1))) break;
+            m = fmaxf(s.rowmax[slot][0][row], s.rowmax[slot][1][row]);
+            // FAVOR+: m is the row's largest exponent; element-wise maps: its largest |phi|
+            int sx = 0;
+            if (favor) sx = m > -1e30f ? (int)ceilf(m) - 15 : 0;
+            else sx = m > 0.f ? (int)ceilf(__log2f(m)) - 15 : 0;
+            if (wg == 0) {   // for the OE (denominator clamp, unnormalised output)
+                if (c >= 2 && !(ok = warp_wait(&B.srow_free[slot], ((c >> 1) - 1) & 1))) break;
+                s.srow[slot][row] = sx;
+            }
+            const float fs = (float)sx, mul = exp2i(-sx);
             for (int h = 0; h < nhalves && ok; ++h) {
                 const int j = c * nhalves + h, b = j & 1;
                 const bool live = 128 * h + 64 * wg < r;   // these 64 features exist
-                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
-                tc_fence_after();
                 uint32_t v0[32], v1[32], w[32];
                 tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg), v0);
                 tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg + 32), v1);
@@ -1147,15 +1653,15 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float a0 = __uint_as_float(v0[2 * e]), a1 = __uint_as_float(v0[2 * e + 1]);
-                    w[e] = live ? (favor ? pack_bf16x2(ex2_approx(a0), ex2_approx(a1))
-                                         : pack_bf16x2(phi_elementwise(a0, p.map), phi_elementwise(a1, p.map)))
+                    w[e] = live ? (favor ? pack_f16x2(ex2_approx(a0 - fs), ex2_approx(a1 - fs))
+                                         : pack_f16x2(phi_elementwise(a0, p.map) * mul, phi_elementwise(a1, p.map) * mul))
                                 : 0u;
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float a0 = __uint_as_float(v1[2 * e]), a1 = __uint_as_float(v1[2 * e + 1]);
-                    w[16 + e] = live ? (favor ? pack_bf16x2(ex2_approx(a0), ex2_approx(a1))
-                                              : pack_bf16x2(phi_elementwise(a0, p.map), phi_elementwise(a1, p.map)))
+                    w[16 + e] = live ? (favor ? pack_f16x2(ex2_approx(a0 - fs), ex2_approx(a1 - fs))
+                                              : pack_f16x2(phi_elementwise(a0, p.map) * mul, phi_elementwise(a1, p.map) * mul))
                                      : 0u;
                 }
                 tmem_st32(tmem_addr(tb, wl, kColBA + 64 * b + 32 * wg), w);
@@ -1187,21 +1693,26 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         const int wl = (warp & 3) * 32;
         const int tr = wl + lane;                 // query row = TMEM lane
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        const int g = s.gexp;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            uint32_t o0[32], o1[32], den;
+            uint32_t o0[32], o1[32], dh, dl;
             tmem_ld32(tmem_addr(tb, wl, kColBO), o0);
             tmem_ld32(tmem_addr(tb, wl, kColBO + 32), o1);
-            tmem_ld1(tmem_addr(tb, wl, kColBO + 64), den);
+            tmem_ld1(tmem_addr(tb, wl, kColBO + 64), dh);   // phi(q) . z (f16 part)
+            tmem_ld1(tmem_addr(tb, wl, kColBO + 65), dl);   // phi(q) . z (f16 remainder)
             tmem_ld_wait();
-            warp_arrive(&B.o_empty, false);   // the next chunk may overwrite O
+            const int sx = s.srow[c & 1][tr];
+            warp_arrive(&B.o_empty, false);     // the next chunk may overwrite O
+            warp_arrive(&B.srow_free[c & 1], false);
             if (tr < min(kC, un.end - t0)) {
                 const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
-                const uint32_t dv_ = p.div_rows ? __float_as_uint(p.div_rows[orow]) : den;
-                store_output_row(o0, o1, dv_, p.eps, p.norm == LA_NORM_ATTENTION || p.div_rows, out + orow * 64);
+                // O and the denominator are the true values times 2^-(s_i + g)
+                const float den = __uint_as_float(dh) + __uint_as_float(dl);
+                store_output_row_f(o0, o1, row_multiplier(den, sx + g, p, orow), out + orow * 64);
             }
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
@@ -1223,37 +1734,55 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // The projection is computed transposed, P^T = Omega' K^T (TMEM lanes = features,
 // columns = tokens); one more K step adds each token's exponent offset -(log2(e)
 // |k|^2 / 2 + log2(sqrt r)) as bf16 hi + lo, so that phi = 2^P^T element-wise.
-// The PE warps turn it into phi(k)^T as bf16 and write it back into the same
-// buffer (the first 32 of each warpgroup's 64 columns); [S|z] += phi(k)^T [V|1]
-// takes its A operand from there and its B operand from V with a ones tile as the
-// second 64-column atom, so z = sum_t phi(k_t) (column 64) comes from the same bf16
-// values as S.  Neither phi(k) nor the update's A operand passes through shared memory.
+//
+// fp16 features with an exact power-of-two scale per (chunk, feature half): the
+// PE warps first reduce the maximum of the half's 128 x 128 exponents, take
+// e = ceil(max) - 15, and write phi(k)^T 2^-e as f16 (11 significant bits; every
+// feature within 2^-29 of the chunk's largest is a normal number) back into the
+// buffer it came from.  The state of each half is accumulated in TMEM in the
+// scale 2^-e of the latest chunk: when e changes, the PE rescales that half
+// exactly (a power of two) before the chunk's update, and the state leaves in
+// true scale.  V is converted to f16 in place by the NE warps (values beyond
+// 65504 are clamped and reported as LA_DEVERR_RANGE); [S|z] += phi(k)^T [V|1]
+// takes its A operand from TMEM and its B operand from V with an f16 ones tile as
+// the second 64-column atom, so z (column 64) comes from the same features as S.
+// The chunk's key exponent (the larger of the two halves) is recorded in
+// p.kscale for the causal output kernel.
 // TMEM: [S|z] [0, 160) (80 columns per 128-feature half), two fp32 projection
 // buffers [160, 416).
 // Roles (416 threads):
-//   warp 0 lane 0     TMA: k and v tiles of each chunk into four stages (and L2 prefetch)
+//   warp 0 lane 0     TMA: k and v tiles of each chunk into three stages (and L2 prefetch)
 //   warp 1            projection MMAs (one elected lane; warp 1 owns the TMEM
 //                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the
 //                     update has read that buffer's previous phi(k)^T
 //   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T
 //   warps 3, 12 (NE)  the exponent offset of every token of a stage (FAVOR+), into
-//                     the bias operand of the projection (64 tokens each, on two
-//                     different SM sub-partitions)
+//                     the bias operand of the projection, and the stage's V as f16
+//                     (64 tokens each, on two different SM sub-partitions)
 //   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
 //                     every half (lane = feature)
-// The state accumulates in TMEM over the unit and is written once.
 constexpr int kStateThreads = 416;
 constexpr uint32_t kColSS = 0;     // [S|z], 80 columns per half
 constexpr uint32_t kColPS = 160;   // two 128-column projection buffers (exponent, then phi(k)^T in place)
 
-// Descriptor of K step k (16 token rows) of an MN-major [V|1] operand: the start
-// advances by 2048 B and the leading-dimension offset (bits 16..29, 16-byte units)
-// shrinks by the same amount, so that the second 64-column atom stays on the same
-// 16-row ones tile for every step.
-__device__ __forceinline__ uint64_t v_ones_desc(uint64_t d0, int k) {
-    return d0 + static_cast<uint64_t>(128 * k) - (static_cast<uint64_t>(128 * k) << 16);
+// Maximum over the eight warps warp0 .. warp0 + 7 for use j: each warp posts its
+// maximum and arrives on bar[j & 1] (count 8), then waits for the others (bounded:
+// false if the wait ran out).  Two slots: a warp cannot post use j + 2 before every
+// warp has arrived for use j + 1, i.e. finished reading use j.
+__device__ __forceinline__ bool group_max8(float& m, float (*red)[8], uint64_t* bar, int j, int warp0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int slot = j & 1;
+    if ((threadIdx.x & 31) == 0) red[slot][(threadIdx.x >> 5) - warp0] = m;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[slot]);
+    if (!warp_wait(&bar[slot], (j >> 1) & 1)) return false;
+    float r = red[slot][0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[slot][i]);
+    m = r;
+    return true;
 }
-
 
 // kFavor: FAVOR+ (projection by Omega' hi + lo and the offset step), else an
 // element-wise map of k (identity projection); one instantiation per kind.
@@ -1265,9 +1794,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int u = blockIdx.x, head = blockIdx.y;
     if (u >= p.hdr->n_units) return;
     const Unit un = p.units[u];
-    // causal: no later segment adds the last segment of a sequence to its
-    // prefix; only a final state needs its sum
-    if (p.causal && !p.keep_last && u + 1 == p.seq_first[un.seq + 1]) return;
+    // causal: no later segment adds the last segment of a sequence to its prefix;
+    // only a final state or the key exponents of the output kernel need it
+    const bool last = p.causal && u + 1 == p.seq_first[un.seq + 1];
+    if (last && !p.keep_last && p.kscale == nullptr) return;
     StateSmem& s = smem_ref<StateSmem>();
     StateBars& B = s.b;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -1275,21 +1805,26 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     constexpr bool favor = kFavor;
     const int nhalves = (r + 127) / 128;
     const int nchunks = (un.end - un.start + kC - 1) / kC;
+    // r = 256 FAVOR+: one warpgroup per feature half, a scale per feature (see the PE)
+    const bool per_feature = favor && nhalves == 2;
 
     if (t == 0) {
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
+        for (int i = 0; i < 4; ++i) s.kmx[i] = INT_MIN;
         for (int i = 0; i < kStateStages; ++i) {
             mbar_init(&B.k_full[i], 1);
             mbar_init(&B.k_empty[i], 3);   // projection commit + 2 NE warps
             mbar_init(&B.v_full[i], 1);
             mbar_init(&B.v_empty[i], 1);
             mbar_init(&B.cx_full[i], 2);
+            mbar_init(&B.vh_full[i], 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
-            mbar_init(&B.a_full[i], 8);
+            mbar_init(&B.a_full[i], per_feature ? 4 : 8);
             mbar_init(&B.a_empty[i], 1);
+            mbar_init(&B.red_full[i], 8);
         }
         mbar_init(&B.drain[0], 1);
         mbar_init(&B.drain[1], 1);
@@ -1338,6 +1873,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         *reinterpret_cast<uint4*>(s.ones + sw128_chunk(row, c)) =
             make_uint4((c & 1) == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
     }
+    fill_ones_atom_f16(s.ones16, t, kStateThreads);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1347,6 +1883,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
+            int nk = min(nchunks, kStateStages), nv = nk;   // chunks whose loads were issued
             for (int c = kStateStages; c < nchunks; ++c) {   // chunks 0 .. kStateStages - 1: issued at set-up
                 const int st = c % kStateStages, ph = ((c / kStateStages) - 1) & 1, t0 = un.start + c * kC;
                 // into L2 ahead of the stages: the loads below then wait on L2, not DRAM
@@ -1361,12 +1898,23 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 }
                 mbar_arrive_expect_tx(&B.k_full[st], kTile);
                 tma_load_3d(s.tk[st], &map_k, 0, head, t0, &B.k_full[st]);
+                ++nk;
                 if (c >= kStateStages && !mbar_wait(&B.v_empty[st], ph)) {
                     record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
                 mbar_arrive_expect_tx(&B.v_full[st], kTile);
                 tma_load_3d(s.tv[st], &map_v, 0, head, t0, &B.v_full[st]);
+                ++nv;
+            }
+            // no exit while an issued load can still write shared memory (bounded)
+            for (int st = 0; st < kStateStages; ++st) {
+                const int lk = nk - 1 - ((nk - 1 - st) % kStateStages + kStateStages) % kStateStages;
+                const int lv = nv - 1 - ((nv - 1 - st) % kStateStages + kStateStages) % kStateStages;
+                if (lk >= 0 && !mbar_wait(&B.k_full[st], (lk / kStateStages) & 1, kDrainLimitNs))
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
+                if (lv >= 0 && !mbar_wait(&B.v_full[st], (lv / kStateStages) & 1, kDrainLimitNs))
+                    record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
             }
         }
     } else if (warp == 1) {
@@ -1404,17 +1952,22 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp == 2) {
         // ------------------------------------------------------------ state-update MMAs (elected lane issues)
-        const uint32_t id_upd = idesc_bf16(128, kNX, false, true);    // A from TMEM, B = [V|1] MN-major, N = 80
+        const uint32_t id_upd = idesc_f16(128, kNX, false, true);    // A f16 from TMEM, B = [V|1] f16 MN-major, N = 80
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
-            if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
-            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv[st]), smem_u32(s.ones) - smem_u32(s.tv[st]), 1024);
+            if (!(ok = warp_wait(&B.vh_full[st], (c / kStateStages) & 1))) break;   // V as f16
+            const uint64_t d_v = sdesc_sw128(smem_u32(s.tv[st]), smem_u32(s.ones16) - smem_u32(s.tv[st]), 1024);
             for (int h = 0; h < nhalves && ok; ++h) {
                 const int j = c * nhalves + h, b = j & 1;
                 if (!(ok = warp_wait(&B.a_full[b], (j >> 1) & 1))) break;
                 tc_fence_after();
-                // tokens 16k.. of phi(k)^T: warpgroup k / 4 wrote them to columns 64 (k / 4) + 8 (k % 4)
+                if (per_feature && h == 1 && lane == 0 && p.kscale != nullptr) {
+                    // both halves' features have posted their exponents: the chunk's key scale
+                    p.kscale[((int64_t)u * p.H + head) * p.Lc + c] = s.kmx[c & 3];
+                    s.kmx[c & 3] = INT_MIN;
+                }
+                // tokens 16k.. of phi(k)^T: columns 64 (k / 4) + 8 (k % 4) of the buffer
                 const uint32_t a0 = tb + kColPS + 128 * b;
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
@@ -1427,56 +1980,159 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ PE: phi(k)^T
-        const int wg = (warp - 4) >> 2;           // tokens 64 wg .. 64 wg + 63
+        const int wg = (warp - 4) >> 2;
         const int wl = (warp & 3) * 32;           // TMEM lane base: features wl .. wl + 31 of a half
         const int f = wl + lane;
         bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int nvalid = min(kC, un.end - (un.start + c * kC));
-            for (int h = 0; h < nhalves && ok; ++h) {
-                const int j = c * nhalves + h, b = j & 1;
-                const bool live = 128 * h + f < r;
-                uint32_t w[32];
+        if (per_feature) {
+            // r = 256: warpgroup wg owns feature half wg (jobs 2c + wg, always buffer wg) and each
+            // thread one feature over all 128 tokens: phi(k)_f 2^-R_f with R_f from the feature's
+            // own largest exponent in the chunk (hysteresis: next_key_scale), no exchange
+            const int feat = 128 * wg + f, b = wg;
+            const bool live = feat < r;
+            int R = 0;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int j = 2 * c + wg;
                 if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
                 tc_fence_after();
-                uint32_t v0[32], v1[32];
-                const uint32_t col = kColPS + 128 * b + 64 * wg;   // this warpgroup's 64 tokens
-                tmem_ld32(tmem_addr(tb, wl, col), v0);
-                tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
-                tmem_ld_wait();
-                if (favor) {
+                const uint32_t col = kColPS + 128 * b;
+                float m = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v0[2 * e])),
-                                                  ex2_approx(__uint_as_float(v0[2 * e + 1]))) : 0u;
+                for (int piece = 0; piece < 4; ++piece) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_addr(tb, wl, col + 32 * piece), v);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[16 + e] = live ? pack_bf16x2(ex2_approx(__uint_as_float(v1[2 * e])),
-                                                       ex2_approx(__uint_as_float(v1[2 * e + 1]))) : 0u;
-                } else {
-                    // k^T element-wise; tokens past the unit's end give phi = 0
-                    const int tbase = 64 * wg;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float x0 = tbase + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v0[2 * e]), p.map) : 0.f;
-                        const float x1 = tbase + 2 * e + 1 < nvalid ? phi_elementwise(__uint_as_float(v0[2 * e + 1]), p.map) : 0.f;
-                        w[e] = live ? pack_bf16x2(x0, x1) : 0u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float x0 = tbase + 32 + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v1[2 * e]), p.map) : 0.f;
-                        const float x1 = tbase + 33 + 2 * e < nvalid ? phi_elementwise(__uint_as_float(v1[2 * e + 1]), p.map) : 0.f;
-                        w[16 + e] = live ? pack_bf16x2(x0, x1) : 0u;
-                    }
+                    for (int e = 0; e < 32; ++e) m = fmaxf(m, __uint_as_float(v[e]));
                 }
-                tmem_st32(tmem_addr(tb, wl, col), w);   // phi(k)^T in place of the exponent it came from
+                const int e = (live && m > -1e30f) ? (int)ceilf(m) - 15 : R;
+                const int Rn = next_key_scale(R, e, c == 0);
+                if (live) atomicMax(&s.kmx[c & 3], e);
+                // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp takes the branch
+                // when any of its features changes scale (the others multiply by exactly 1)
+                if (c > 0 && __any_sync(0xffffffffu, Rn != R)) {
+                    // the previous update of this half is complete (this job's projection waited for
+                    // it): the feature's state row times 2^(R - Rn), exactly
+                    const float fct = exp2i(R - Rn);
+                    uint32_t w0[32], w1[32], zc;
+                    const uint32_t sc = kColSS + kNX * wg;
+                    tmem_ld32(tmem_addr(tb, wl, sc), w0);
+                    tmem_ld32(tmem_addr(tb, wl, sc + 32), w1);
+                    tmem_ld1(tmem_addr(tb, wl, sc + 64), zc);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        w0[i] = __float_as_uint(__uint_as_float(w0[i]) * fct);
+                        w1[i] = __float_as_uint(__uint_as_float(w1[i]) * fct);
+                    }
+                    zc = __float_as_uint(__uint_as_float(zc) * fct);
+                    tmem_st32(tmem_addr(tb, wl, sc), w0);
+                    tmem_st32(tmem_addr(tb, wl, sc + 32), w1);
+                    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
+                                 ::"r"(tmem_addr(tb, wl, sc + 64)), "r"(zc) : "memory");
+                    tmem_st_wait();
+                }
+                R = Rn;
+                const float fe = (float)R;
+                for (int hh = 0; hh < 2; ++hh) {   // tokens 64 hh ..: read whole, then packed into 64 hh ..
+                    uint32_t v0[32], v1[32], w[32];
+                    tmem_ld32(tmem_addr(tb, wl, col + 64 * hh), v0);
+                    tmem_ld32(tmem_addr(tb, wl, col + 64 * hh + 32), v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        w[i] = live ? pack_f16x2(ex2_approx(__uint_as_float(v0[2 * i]) - fe),
+                                                 ex2_approx(__uint_as_float(v0[2 * i + 1]) - fe)) : 0u;
+                        w[16 + i] = live ? pack_f16x2(ex2_approx(__uint_as_float(v1[2 * i]) - fe),
+                                                      ex2_approx(__uint_as_float(v1[2 * i + 1]) - fe)) : 0u;
+                    }
+                    tmem_st32(tmem_addr(tb, wl, col + 64 * hh), w);
+                }
                 tmem_st_wait();
                 warp_arrive(&B.a_full[b], false);
             }
+            s.rsf[feat] = R;
+        } else {
+            // r <= 128 (one half) and element-wise maps: both warpgroups convert every job, tokens
+            // 64 wg .. 64 wg + 63; FAVOR+ takes one scale per chunk from the exact maximum over the
+            // eight warps (group_max8), element-wise features keep their own scale
+            int R = 0;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int nvalid = min(kC, un.end - (un.start + c * kC));
+                const int j = c, b = j & 1;
+                const bool live = f < r;
+                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
+                tc_fence_after();
+                float x[64];
+                {
+                    uint32_t v0[32], v1[32];
+                    const uint32_t col = kColPS + 128 * b + 64 * wg;   // this warpgroup's 64 tokens
+                    tmem_ld32(tmem_addr(tb, wl, col), v0);
+                    tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) { x[e] = __uint_as_float(v0[e]); x[32 + e] = __uint_as_float(v1[e]); }
+                }
+                // FAVOR+: x is the exponent (log2) of phi; element-wise maps: phi itself, kept in
+                // its own scale (|phi| <= 65504 for |k| below that; larger values are clamped)
+                float m = -INFINITY;
+                const int tbase = 64 * wg;
+                bool big = false;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    if (!favor) {
+                        const float ph = tbase + e < nvalid ? phi_elementwise(x[e], p.map) : 0.f;
+                        big |= live && !(fabsf(ph) <= 65504.f);
+                        x[e] = fminf(fmaxf(ph, -65504.f), 65504.f);
+                    } else if (live) {
+                        m = fmaxf(m, x[e]);
+                    }
+                }
+                if (!favor && __any_sync(0xffffffffu, big) && lane == 0) record_range(p.hdr, kRangeElementwise);
+                if (favor && !(ok = group_max8(m, s.red, B.red_full, j, 4))) break;
+                const int e = (favor && m > -1e30f) ? (int)ceilf(m) - 15 : 0;
+                const int Rn = favor ? next_key_scale(R, e, c == 0) : 0;
+                if (c > 0 && Rn != R) {
+                    // the previous chunk's update must be complete: rescale exactly
+                    if (!(ok = warp_wait(&B.a_empty[b ^ 1], (((j - 1) >> 1)) & 1))) break;
+                    const float fct = exp2i(R - Rn);
+                    uint32_t w[32];
+                    const uint32_t sc = kColSS + 32 * wg;   // columns 0..31 (wg 0), 32..63 (wg 1)
+                    tmem_ld32(tmem_addr(tb, wl, sc), w);
+                    uint32_t zc = 0u;
+                    if (wg == 1) tmem_ld1(tmem_addr(tb, wl, kColSS + 64), zc);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * fct);
+                    tmem_st32(tmem_addr(tb, wl, sc), w);
+                    if (wg == 1) {
+                        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
+                                     ::"r"(tmem_addr(tb, wl, kColSS + 64)),
+                                       "r"(__float_as_uint(__uint_as_float(zc) * fct)) : "memory");
+                    }
+                    tmem_st_wait();
+                }
+                R = Rn;
+                uint32_t w[32];
+                if (favor) {
+                    const float fe = (float)R;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        w[i] = live ? pack_f16x2(ex2_approx(x[2 * i] - fe), ex2_approx(x[2 * i + 1] - fe)) : 0u;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = live ? pack_f16x2(x[2 * i], x[2 * i + 1]) : 0u;
+                }
+                tmem_st32(tmem_addr(tb, wl, kColPS + 128 * b + 64 * wg), w);   // phi(k)^T in place
+                tmem_st_wait();
+                warp_arrive(&B.a_full[b], false);
+                if (favor && p.kscale != nullptr && t == 128) p.kscale[((int64_t)u * p.H + head) * p.Lc + c] = e;
+            }
+            if (wg == 0) s.rsf[f] = R;
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else {
-        // ------------------------------------------------------------ NE: exponent offsets (warps 3, 12)
+        // ------------------------------------------------------------ NE: exponent offsets, V as f16 (warps 3, 12)
         const int tok0 = warp == 3 ? 0 : 64;      // this warp's 64 tokens
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -1495,6 +2151,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             }
             warp_arrive(&B.cx_full[st], true);
             warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
+            if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
+            v_tile_to_f16(s.tv[st], tok0, 64, nvalid, p.hdr, lane, 32);
+            warp_arrive(&B.vh_full[st], true);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
@@ -1507,14 +2166,19 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     __syncthreads();
     tc_fence_after();
-    // [S|z] as [r][65] fp32 rows: each thread's feature row into shared memory (the
-    // k / v stages, all consumed; a row stride of 65 words keeps the warp's stores
-    // on distinct banks), then one coalesced 16-byte copy of the whole block
+    if (last && !p.keep_last) {   // only the key exponents were wanted
+        if (warp == 1) tmem_dealloc(tb, kTmemCols);
+        return;
+    }
+    // [S|z] as [r][65] fp32 rows in true scale: each thread's feature row into shared
+    // memory (the k / v stages, all consumed; a row stride of 65 words keeps the warp's
+    // stores on distinct banks), then one coalesced 16-byte copy of the whole block
     float* stage = reinterpret_cast<float*>(s.tk[0]);
     if (warp >= 4 && warp < 8) {
         const int f = t - 128;
         for (int h = 0; h < nhalves; ++h) {
             const int feat = 128 * h + f;
+            const float fct = exp2i(feat < r ? s.rsf[feat] : 0);
             for (int n0 = 0; n0 < 65; n0 += 16) {
                 uint32_t w[16] = {};
                 if (nchunks > 0) {
@@ -1524,7 +2188,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 if (feat < r) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        if (n0 + e < 65) stage[feat * 65 + n0 + e] = __uint_as_float(w[e]);
+                        if (n0 + e < 65) stage[feat * 65 + n0 + e] = __uint_as_float(w[e]) * fct;
                 }
             }
         }

@@ -18,6 +18,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace la {
@@ -236,6 +237,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            | ((static_cast<uint32_t>(N) >> 3) << 17)   // N / 8
            | ((static_cast<uint32_t>(M) >> 4) << 24);  // M / 16
 }
+// The same with f16 A and B (formats 0): both operands of one MMA must share the type.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                   // D: f32; A, B: f16
+           | ((a_mn_major ? 1u : 0u) << 15)
+           | ((b_mn_major ? 1u : 0u) << 16)
+           | ((static_cast<uint32_t>(N) >> 3) << 17)
+           | ((static_cast<uint32_t>(M) >> 4) << 24);
+}
 
 // D (+)= A * B^T, A and B from shared memory.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -327,6 +336,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+// Two fp32 values as f16 (round to nearest even) in one word, lo in the low half.
+// fp16 keeps 11 significant bits (bf16: 8) over 2^-14 .. 65504 (subnormals to 2^-24);
+// callers scale by powers of two so that the values they care about stay in range.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+// 2^k for an integer k, exact, for |k| <= 252 (two exponent-field multiplies).
+__device__ __forceinline__ float exp2i(int k) {
+    k = max(-252, min(252, k));
+    const int a = k / 2, b = k - a;
+    return __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
 }
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -4,30 +4,18 @@ Tolerances (written out here and asserted in the tests):
 * fp32 path: max over elements of |gpu - oracle| / max(|oracle|, RMS(oracle))
   <= 1e-4 (relative error, with the output RMS as the floor below which an
   element's size does not shrink the allowance);
-* bf16 inputs, fp32 accumulation, bf16 output: |gpu - oracle| <= 2e-2 * RMS(oracle)
-  + 2^-8 * |oracle| for every element.  The second term is the rounding of the
-  stored bf16 output itself (at most half an ulp, 2^-8 of the value): early
-  causal rows average few values and sit far above the RMS, so the storage
-  rounding alone can exceed 2e-2 * RMS there.
-
-Bounds from the arithmetic, for results the output-RMS rule does not fit.
-bf16 keeps 8 significant bits, so one rounding has relative error at most
-u = 2^-8.  The tensor-core path rounds phi(q) and phi(k) to bf16 once each and
-rounds every in-chunk score, or the carried state it reads, once more; sums
-are fp32.  With non-negative features every weight w_ij = phi(q_i) . phi(k_j)
-it effectively uses is within 3u of the exact one.  Hence, with
-M_ic = sum_j w_ij |v_jc| (plus phi(q_i) . |S_in[:, c]| for a carried state):
-* unnormalised output (norm "none"), whose rows span orders of magnitude
-  (FAVOR+ weights are heavy-tailed), so one global RMS means little:
-  |error| <= 3u M_ic;
-* normalised output: |error| <= 3u (M_ic / den_i + |out_ic|), the worst case
-  for rows with a long history (a carried state, or far into a sequence),
-  where outputs are small averages and bf16 noise is a larger part of them;
-* a state (a sum, no normalisation): one rounding of phi(k), so
-  |error| <= u M with M the state computed with |v| (z: M = z).
-The tests allow 3.25u instead of 3u (0.25u for the fp32 exponentials, sums and
-the 1 / (1 - 3u) of the division) and 1.25u instead of u, plus u |ref| for the
-rounding of a stored bf16 output.
+* bf16 inputs, fp32 accumulation, bf16 output: for every element,
+  |gpu - oracle| - |bf16(oracle) - oracle| <= 2e-2 * RMS(oracle).  The only
+  allowance beyond 2e-2 RMS is the rounding of that element's exact value to
+  the stored bf16 output (an oracle-side quantity): early causal rows average
+  few values and sit far above the RMS, where that rounding alone can exceed
+  2e-2 RMS.
+* results whose rows span orders of magnitude (the unnormalised fast-weight
+  output, the sum-normalised output, whose rows grow with the number of keys
+  they sum): the same rule row by row, each row against the RMS of its own
+  oracle values;
+* states (fp32 sums [S|z] of one sequence and head): S and z each against
+  2e-2 of the RMS of their own oracle values.
 """
 import numpy as np
 
@@ -46,19 +34,44 @@ def rel_err_rms_floor(got, ref):
     return float(np.max(np.abs(got - ref) / denom)) if ref.size else 0.0
 
 
-BF16_STORE_REL = 2.0 ** -8
+def bf16_round(x):
+    """Values rounded to bf16 (round to nearest even), as float64."""
+    return synthetic.bf16_to_f32(synthetic.bf16_bits(np.asarray(x, np.float32))).astype(np.float64)
+
+
+def store_excess(got, ref):
+    """|got - ref| beyond the bf16 rounding of the exact value: |got - ref| - |bf16(ref) - ref|."""
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    return np.abs(got - ref) - np.abs(bf16_round(ref) - ref)
 
 
 def abs_err_over_rms(got, ref, rms=None):
-    """max over elements of (|got - ref| - 2^-8 |ref|) / RMS(ref): the error
-    beyond the bf16 rounding of the stored output, in units of the RMS."""
-    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    """max over elements of (|got - ref| - |bf16(ref) - ref|) / RMS(ref)."""
+    ref = np.asarray(ref, np.float64)
     if ref.size == 0:
         return 0.0
     if rms is None:
         rms = np.sqrt(np.mean(ref * ref))
-    excess = np.abs(got - ref) - BF16_STORE_REL * np.abs(ref)
-    return float(max(0.0, np.max(excess)) / (rms if rms > 0 else 1.0))
+    return float(max(0.0, np.max(store_excess(got, ref))) / (rms if rms > 0 else 1.0))
+
+
+def rows_over_bar(got, ref, rms=None, tol=BF16_RMS_TOL):
+    """Number of rows (last axis = channels) with an element beyond the bar."""
+    ref = np.asarray(ref, np.float64)
+    if rms is None:
+        rms = np.sqrt(np.mean(ref * ref))
+    return int(np.sum(np.max(store_excess(got, ref), axis=-1) > tol * rms))
+
+
+def rowwise_err_over_rms(got, ref):
+    """max over rows (last axis = channels) of the bf16 rule against the row's own RMS."""
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    ex = store_excess(got, ref)
+    ratio = np.where(rms > 0, ex / np.where(rms > 0, rms, 1.0), np.where(ex > 0, np.inf, 0.0))
+    return float(max(0.0, np.max(ratio)))
 
 
 def assert_close(got, ref, dtype, what=""):
@@ -71,36 +84,26 @@ def assert_close(got, ref, dtype, what=""):
     return e
 
 
-BF16_U = 2.0 ** -8
+def assert_rowwise_close(got, ref, what=""):
+    e = rowwise_err_over_rms(got, ref)
+    assert e <= BF16_RMS_TOL, f"{what}: bf16 abs error / row RMS {e:.3e} > {BF16_RMS_TOL}"
+    return e
 
 
-def _bound_ratio(got, ref, scale, stored_bf16):
-    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64); scale = np.asarray(scale, np.float64)
-    excess = np.abs(got - ref) - (BF16_U * np.abs(ref) if stored_bf16 else 0.0)
-    return float(np.max(excess / np.where(scale > 0, scale, 1.0))) / BF16_U if ref.size else 0.0
-
-
-def assert_within_rounding_bound(got, ref, M, what="", units=3.25):
-    """Unnormalised bf16-path output: |got - ref| <= 3.25u M + u |ref|.  Under sum
-    normalisation on tensor cores the values enter as bf16(v / sigma_k), one
-    rounding more: units = 4.25, M the sum-normalised output for |v|."""
-    k = _bound_ratio(got, ref, M, True)
-    assert k <= units, f"{what}: error {k:.2f} u M > {units} u M"
-    return k
-
-
-def assert_normalised_within_rounding_bound(got, ref, Mbar, what=""):
-    """Normalised bf16-path output: |got - ref| <= 3.25u (Mbar + |ref|) + u |ref|, Mbar = M / den."""
-    k = _bound_ratio(got, ref, np.asarray(Mbar, np.float64) + np.abs(np.asarray(ref, np.float64)), True)
-    assert k <= 3.25, f"{what}: error {k:.2f} u (M/den + |out|) > 3.25 u"
-    return k
-
-
-def assert_state_within_rounding_bound(got, ref, M, what=""):
-    """bf16-path state (fp32 sums of bf16 features): |got - ref| <= 1.25u M."""
-    k = _bound_ratio(got, ref, M, False)
-    assert k <= 1.25, f"{what}: state error {k:.2f} u M > 1.25 u M"
-    return k
+def assert_state_close(got, ref, what=""):
+    """[.., r, dv + 1] states: per leading index (sequence, head), S and z each
+    within 2e-2 of the RMS of their own oracle values (fp32, nothing stored in bf16)."""
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    g2 = got.reshape(-1, *got.shape[-2:]); r2 = ref.reshape(-1, *ref.shape[-2:])
+    worst = 0.0
+    for gs, rs in zip(g2, r2):
+        for part in (np.s_[:, :-1], np.s_[:, -1]):
+            rp = rs[part]
+            rms = np.sqrt(np.mean(rp * rp))
+            err = np.max(np.abs(gs[part] - rp)) if rp.size else 0.0
+            worst = max(worst, err / rms if rms > 0 else (np.inf if err > 0 else 0.0))
+    assert worst <= BF16_RMS_TOL, f"{what}: state abs error / RMS {worst:.3e} > {BF16_RMS_TOL}"
+    return worst
 
 
 def omega_for(r, d, seed=synthetic.OMEGA_SEED):

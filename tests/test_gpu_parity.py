@@ -12,7 +12,7 @@ import pytest
 import oracle
 import synthetic
 from parity_util import (BF16_RMS_TOL, FP32_REL_TOL, abs_err_over_rms, assert_close, from_torch,
-                         omega_for, rel_err_rms_floor, to_torch)
+                         omega_for, rel_err_rms_floor, rows_over_bar, to_torch)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -35,13 +35,21 @@ def _tensor(a, dtype):
 
 
 def _run(la, inputs, kind, causal, omega=None, eps=1e-6, cu=True):
+    """One forward through the C ABI; the device error word must stay clear (no
+    timed-out wait, no value clamped into the f16 operand range)."""
     q, k, v = to_torch(inputs)
     om = torch.from_numpy(omega).cuda() if omega is not None else None
     cu_t = torch.from_numpy(inputs.cu_seqlens).cuda() if cu else None
     nseq = len(inputs.cu_seqlens) - 1
+    T, H, dk = q.shape
+    r = omega.shape[0] if omega is not None else (2 * dk * int(kind[4:]) if kind.startswith("dpfp") else dk)
+    nb = la.la_workspace_bytes(causal, kind, q.dtype, cu, nseq, T, H, dk, v.shape[2], r)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
     fn = la.la_forward_causal if causal else la.la_forward_bidir
-    out = fn(q, k, v, kind, omega=om, cu_seqlens=cu_t, nseq=nseq, eps=eps)
+    out = fn(q, k, v, kind, omega=om, cu_seqlens=cu_t, nseq=nseq, eps=eps, workspace=ws)
     torch.cuda.synchronize()
+    code = la.la_workspace_error(ws)
+    assert code == 0, f"device error word {code} after the forward"
     return from_torch(out)
 
 
@@ -282,23 +290,58 @@ def test_full_size_workload_sampled_rows(la, name):
     assert worst <= BF16_RMS_TOL, worst
 
 
-@pytest.mark.xfail(strict=False, reason="bf16 rounding of phi(q) and phi(k): on a 65536-token sequence about "
-                                        "0.3% of the rows exceed 2e-2 x RMS (the worst by up to 2.5x); fp16 "
-                                        "feature operands are the planned fix")
+def _every_row(got, ref, what):
+    rms = np.sqrt(np.mean(ref ** 2))
+    e = abs_err_over_rms(got, ref, rms)
+    assert e <= BF16_RMS_TOL, f"{what}: bf16 abs error / RMS {e:.3e} > {BF16_RMS_TOL} " \
+                              f"({rows_over_bar(got, ref, rms)} rows over)"
+    return e
+
+
 def test_long_causal_sequence_every_row(la):
     """Every row (not a sample) of a two-head causal FAVOR+ r = 256 problem with 65536 tokens,
-    q, k ~ N(0,1) * 64^-1/4, v ~ N(0,1), at the bf16 bar.  Measured on GB300 with the bf16
-    feature operands: 0.035 and 0.050 of the RMS over all rows, with 189 and 127 rows above
-    2e-2; the sampled-row test above holds the bar on the rows it checks."""
+    q, k ~ N(0,1) * 64^-1/4, v ~ N(0,1), at the bf16 bar.  Long causal rows average many
+    values and are small, early rows few and large: both must hold 2e-2 of the one RMS."""
     inp = synthetic.random_inputs([65536], H=2, dk=64, dv=64, dtype="bf16", seed=11, qk_scale=64 ** -0.25)
     om = omega_for(256, 64)
     got = _run(la, inp, "favor", True, om, cu=False)
-    worst = 0.0
     for h in range(2):
         ref = oracle.causal(inp.q[:, h:h + 1, :], inp.k[:, h:h + 1, :], inp.v[:, h:h + 1, :], "favor",
                             omega=om.astype(np.float64))[:, 0, :]
-        worst = max(worst, abs_err_over_rms(got[:, h, :], ref))
-    assert worst <= BF16_RMS_TOL, worst
+        _every_row(got[:, h, :], ref, f"causal N=65536 head {h}")
+
+
+def test_bidir_full_size_every_row(la):
+    """Every row of two (sequence, head) pairs of the bidirectional FAVOR+ workload
+    B = 4, H = 8, N = 16384, r = 256, run whole in the benchmark's configuration."""
+    w = synthetic.workloads()["favor_bidir_b4h8n16384"]
+    inp = synthetic.make_qkv(w)
+    om = omega_for(w.r, w.dk)
+    got = _run(la, inp, "favor", False, om, cu=False)
+    for s, h in ((0, 0), (3, 7)):
+        a, b = s * 16384, (s + 1) * 16384
+        ref = oracle.bidir(inp.q[a:b, h:h + 1], inp.k[a:b, h:h + 1], inp.v[a:b, h:h + 1], "favor",
+                           omega=om.astype(np.float64))[:, 0, :]
+        _every_row(got[a:b, h, :], ref, f"bidir sequence {s} head {h}")
+
+
+def test_varlen_full_size_every_row(la):
+    """Every row of four sequences (every head) of the packed workload: 64 causal FAVOR+
+    sequences of 128..8192 tokens, H = 8, run whole in the benchmark's configuration;
+    each sequence's outputs against the oracle over that sequence alone (the state resets
+    at every boundary)."""
+    w = synthetic.workloads()["favor_causal_varlen64_h8"]
+    inp = synthetic.make_qkv(w)
+    om = omega_for(w.r, w.dk)
+    got = _run(la, inp, "favor", True, om, cu=True)
+    cu = inp.cu_seqlens
+    lens = np.diff(cu)
+    for s in sorted({0, int(np.argmax(lens)), int(np.argmin(lens)), len(lens) - 1}):
+        a, b = int(cu[s]), int(cu[s + 1])
+        for h in range(w.H):
+            ref = oracle.causal(inp.q[a:b, h:h + 1], inp.k[a:b, h:h + 1], inp.v[a:b, h:h + 1], "favor",
+                                omega=om.astype(np.float64))[:, 0, :]
+            _every_row(got[a:b, h, :], ref, f"varlen sequence {s} ({b - a} tokens) head {h}")
 
 
 # ----------------------------------------------------------------------------

@@ -1,4 +1,5 @@
-"""The no-allocation causal entry point against the workspace entry point.
+"""The no-allocation causal entry point against the workspace entry point and
+the oracle.
 
 la_forward_causal_noalloc serves callers that may not allocate device memory
 on their hot path (a serving loop with a fixed memory budget, a plug-in inside
@@ -12,6 +13,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import synthetic
 from parity_util import assert_close, from_torch, omega_for, to_torch
 
@@ -54,17 +56,43 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(la):
                            64, 64, r, out)
         assert st == 0, la.la_status_string(st)
         torch.cuda.synchronize()
+        assert la.la_noalloc_error() == 0
         assert_close(from_torch(out), from_torch(ref), dtype, f"no-alloc {kind} {dtype}")
+        exact = oracle.forward(inp.q, inp.k, inp.v, kind, True, omega=omega_for(256, 64) if kind == "favor" else None,
+                               cu_seqlens=inp.cu_seqlens)
+        assert_close(from_torch(out), exact, dtype, f"no-alloc {kind} {dtype} against the oracle")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(la):
     lib = la.load_library()
-    # 20000 packed sequences x 16 heads x r=256 states do not fit in the fixed scratch
-    nseq, T, H = 20000, 20000 * 4, 16
-    need = la.la_workspace_bytes(True, "favor", torch.bfloat16, True, nseq, T, H, 64, 64, 256)
+    # 16 sequences x 16 heads of r = 256 states need more than the fixed scratch; the
+    # buffers are sized for the call, so that it would stay in bounds even if it ran
+    nseq, H = 16, 16
+    T = nseq * 128
+    need = la.la_workspace_bytes(True, "favor", torch.bfloat16, False, nseq, T, H, 64, 64, 256)
     assert need > (32 << 20)
-    z = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((T, H, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(q, 7.0)
     om = torch.zeros((256, 64), dtype=torch.float32, device="cuda")
-    cu = torch.zeros(nseq + 1, dtype=torch.int32, device="cuda")
-    st = _call_noalloc(lib, z, z, z, om, "favor", 1, cu, nseq, T, H, 64, 64, 256, z)
+    st = _call_noalloc(lib, q, q, q, om, "favor", 1, None, nseq, T, H, 64, 64, 256, out)
     assert st == LA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+def test_noalloc_reports_bad_cu_seqlens_through_its_error_accessor(la):
+    """cu_seqlens that decrease: the planner records LA_DEVERR_CU_SEQLENS in the
+    fixed scratch's error word and every kernel skips its work (nothing faults);
+    la_noalloc_error reads it, and the next valid call clears it."""
+    lib = la.load_library()
+    inp = synthetic.random_inputs([100, 50, 80], H=2, dk=64, dv=64, dtype="bf16", seed=27, qk_scale=1.0)
+    q, k, v = to_torch(inp)
+    bad = torch.tensor([0, 120, 60, 230], dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(q)
+    assert _call_noalloc(lib, q, k, v, None, "elu1", 1, bad, 3, q.shape[0], 2, 64, 64, 64, out) == 0
+    torch.cuda.synchronize()
+    assert la.la_noalloc_error() == 1
+    good = torch.from_numpy(inp.cu_seqlens).cuda()
+    assert _call_noalloc(lib, q, k, v, None, "elu1", 1, good, 3, q.shape[0], 2, 64, 64, 64, out) == 0
+    torch.cuda.synchronize()
+    assert la.la_noalloc_error() == 0
