@@ -45,6 +45,8 @@ int select_path(int causal, int map, int dtype, int dk, int dv, int r, int norm 
 // DPFP on tensor cores runs every sequence as one unit: its state pass (CUDA
 // cores) then only has work when a final state is wanted.
 bool whole_sequences(int path, int map) { return path == kPathTensor && map == LA_MAP_DPFP; }
+// The causal FAVOR+ tensor-core route passes V as f16 from the state kernel to the output kernel.
+bool vtables(int path, int causal, int map) { return path == kPathTensor && causal && map == LA_MAP_FAVOR; }
 
 // Normalisation variants; sum normalisation needs non-negative features.
 la_status check_norm(int norm, int map) {
@@ -64,7 +66,7 @@ la_status path_supported(int path, int map, int dk, int dv, int r) {
 // into the same number of segments so that units * heads fills the SMs;
 // packed batches (lengths only known on the device) use one length for all.
 Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, int r, int nsm, bool bwd = false,
-                   bool whole = false) {
+                   bool whole = false, bool vtables = false) {
     Layout lo{};
     const int64_t C = path_chunk(path);
     int64_t L, U;
@@ -106,6 +108,8 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     lo.partial = o;   o = align_up(o + state_bytes, kAlign);
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
     lo.kscale = o;    o = align_up(o + (path == kPathTensor ? sizeof(int) * (size_t)U * H * lo.Lc : 0), kAlign);
+    lo.v16 = o;       o = align_up(o + (vtables ? (size_t)16384 * U * H * lo.Lc : 0), kAlign);
+    lo.vmax = o;      o = align_up(o + (vtables ? sizeof(float) * 2 * (size_t)U * H * lo.Lc : 0), kAlign);
     lo.sig_q = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     lo.sig_k = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     if (bwd) {
@@ -148,7 +152,8 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     if ((st = path_supported(path, map, dk, dv, r)) != LA_OK) return st;
     const int nsm = device_sm_count();
     if (nsm <= 0) return LA_ERR_CUDA;
-    const Layout lo = make_layout(path, has_cu, nseq, T, H, dv, r, nsm, false, whole_sequences(path, map));
+    const Layout lo = make_layout(path, has_cu, nseq, T, H, dv, r, nsm, false, whole_sequences(path, map),
+                                  vtables(path, causal, map));
     if (workspace_bytes < lo.total) return LA_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -180,7 +185,12 @@ la_status forward(int causal, int phase_lo, int phase_hi, const void* q, const v
     // The causal FAVOR+ output kernel scales each chunk's key features by the power of
     // two the state kernel records per chunk: the state pass then covers every unit.
     const bool want_kscale = path == kPathTensor && causal && map == LA_MAP_FAVOR;
-    if (want_kscale) p.kscale = reinterpret_cast<int*>(ws + lo.kscale);
+    if (want_kscale) {
+        p.kscale = reinterpret_cast<int*>(ws + lo.kscale);
+        // and hands it each chunk's V as f16 with the chunk's largest |v|
+        p.v16 = ws + lo.v16;
+        p.vmax = reinterpret_cast<float*>(ws + lo.vmax);
+    }
 
     // A causal call whose sequences are all single segments starts every unit
     // from its sequence's state_in (or zero): unless the final state is
@@ -424,7 +434,7 @@ size_t la_workspace_bytes(int causal, int map, int dtype, int has_cu_seqlens, in
     const int nsm = device_sm_count();
     if (nsm <= 0) return 0;
     size_t bytes = make_layout(path, has_cu_seqlens != 0, nseq, T, H, d_v, r, nsm, false,
-                               whole_sequences(path, map)).total;
+                               whole_sequences(path, map), vtables(path, causal, map)).total;
     // sum normalisation and unaligned operands move a tensor-core call to the
     // CUDA-core kernels: the size covers both
     if (path == kPathTensor && path_supported(kPathSimt, map, d_k, d_v, r) == LA_OK)

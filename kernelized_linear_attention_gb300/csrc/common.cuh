@@ -39,6 +39,8 @@ struct Layout {
     size_t partial;    // float[U][H][r][dvx]: per-unit state sum_j phi(k_j) [v_j | 1]^T
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
     size_t kscale;     // int[U][H][Lc]: power-of-two exponent of the keys' features in each chunk
+    size_t v16;        // causal FAVOR+ tensor path: [U][H][Lc] tiles of 128 x 64 f16 V (128B-swizzled rows)
+    size_t vmax;       // float[U][H][Lc][2]: largest |v| of each 64-row half of a chunk's valid rows
     size_t sig_q;      // float[T][H]: sum_f phi_f(q) (sum normalisation on the tensor-core path)
     size_t sig_k;      // float[T][H]: sum_f phi_f(k)
     size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
@@ -98,6 +100,12 @@ struct FwdParams {
     // the chunk's FAVOR+ key features times 2^-e lie below 2^15 (written by the state kernel,
     // read by the causal output kernel).
     int* kscale;
+    // Causal FAVOR+ tensor path: every chunk's V tile as f16 in the shared-memory layout of the
+    // kernels (rows of 128 bytes, 16-byte pieces swizzled within 1024-byte groups), one 16 KB
+    // tile per (unit, head, chunk), and the largest |v| of each 64-row half of its valid rows
+    // (written by the state kernel, read by the causal output kernel); else NULL.
+    void* v16;
+    float* vmax;
     int U, L, Lc;
 };
 

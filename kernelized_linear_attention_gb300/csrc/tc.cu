@@ -211,6 +211,29 @@ __device__ __forceinline__ float favor_offset(const unsigned char* tile, int t, 
     return row_sq_norm(tile, t) * (0.5f * kLog2e) + 0.5f * __log2f((float)r);
 }
 
+// FAVOR+ exponent offsets of row t of the q and k tiles (as favor_offset, two
+// independent sums so that their latencies overlap).
+__device__ __forceinline__ void favor_offsets2(const unsigned char* tq, const unsigned char* tk, int t, int r,
+                                               float& oq, float& ok) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 a = *reinterpret_cast<const uint4*>(tq + sw128_chunk(t, c));
+        const uint4 b = *reinterpret_cast<const uint4*>(tk + sw128_chunk(t, c));
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            sq = fmaf(bf16lo(wa[j]), bf16lo(wa[j]), sq);
+            sq = fmaf(bf16hi(wa[j]), bf16hi(wa[j]), sq);
+            sk = fmaf(bf16lo(wb[j]), bf16lo(wb[j]), sk);
+            sk = fmaf(bf16hi(wb[j]), bf16hi(wb[j]), sk);
+        }
+    }
+    const float lr = 0.5f * __log2f((float)r);
+    oq = sq * (0.5f * kLog2e) + lr;
+    ok = sk * (0.5f * kLog2e) + lr;
+}
+
 // Element-wise phi (ELU+1 or identity) of row t of a tile into the same
 // position of dst (row t; zero when the row is past the unit's end).
 __device__ void elementwise_phi_row(const unsigned char* tile, unsigned char* dst, int t, bool valid, int map) {
@@ -634,11 +657,13 @@ __device__ float v_tile_to_f16(unsigned char* tile, int row0, int nrows, int nva
 //   warp 1             projection MMAs, one elected lane (warp 1 also owns the TMEM
 //                      allocation); runs ahead, throttled by the two projection buffers
 //   warp 2             product MMAs (scores, readout, denominator, state update, A V)
-//   warp 3             the chunk's V tile as f16, in place
+//   warp 3             idle (holds no role)
 //   warps 4..11 (PE)   projection epilogue in two warpgroups, each converting 32 of
 //                      the 64 columns of every job: phi(k), phi(q) of each quarter
 //                      of the features into shared memory (token t = TMEM lane t)
-//   warps 12..15 (TE)  chunk tail: masked scores as f16 in TMEM, then (while A V
+//   warps 12..15 (TE)  chunk tail: the chunk's V tile as f16 in place (before its first
+//                      state update), FAVOR+: the next chunk's row offsets (once its
+//                      tiles land), masked scores as f16 in TMEM, then (while A V
 //                      runs) the f16 copy of the state for the next chunk's readout,
 //                      then the output rows
 // Per chunk the projection warp runs, for each quarter q of the features, the
@@ -660,9 +685,10 @@ constexpr uint32_t kColCI = 352;   // O_in [128][80]: reuses the scores' columns
 constexpr uint32_t kColCX = 432;   // O_cross [128][80]
 
 struct CausalBars {
-    uint64_t qk_full, qk_empty;     // TMA -> (MMA, PE);  (MMA commit + 4 PE warps) -> TMA
-    uint64_t v_full, v_empty;       // TMA -> warp 3;     MMA commit -> TMA
-    uint64_t vh_full;               // warp 3 -> MMA: V as f16
+    uint64_t qk_full, qk_empty;     // TMA -> (MMA, TE or PE);  (MMA commit + 4 TE or 8 PE warps) -> TMA
+    uint64_t v_full, v_empty;       // TMA -> TE;         MMA commit -> TMA
+    uint64_t vh_full;               // TE (4 warps) -> MMA: V as f16
+    uint64_t off_full[2];           // TE (4 warps) -> PE: FAVOR+ offsets of a chunk (slot c & 1)
     uint64_t p_full[2];             // MMA commit -> PE: projection in TMEM buffer b
     uint64_t p_empty[2];            // PE (4 warps) -> MMA: buffer b drained
     uint64_t phik_full[2];          // PE (4 warps) -> MMA: phi(k) of global quarter g in smem (g & 1)
@@ -704,9 +730,11 @@ struct __align__(1024) CausalSmem {
     int srow[2][kC];                  // per slot and query row: s_i
     float qsum[2][2][kC];             // per slot, warpgroup and query row: sum of |phi(q) 2^-s_i| it wrote
     float tred[2][4];                 // TE maxima per slot and warp
-    float vmax;                       // largest |v| of the unit's chunks converted so far (warp 3)
+    float vt[2][4];                   // per slot (chunk & 1) and TE warp: largest |v| of its rows
+    float offq[2][kC], offk[2][kC];   // per slot: FAVOR+ exponent offsets of the query / key rows
     CausalBars b;
 };
+static_assert(sizeof(CausalSmem) + 1024 <= 232448, "causal kernel shared memory exceeds 227 KB");
 
 // Power-of-two exponent R of the keys' scale for a chunk whose largest key feature
 // exponent bound is e (e = ceil(max) - 15, from the state kernel): the previous R is
@@ -837,6 +865,35 @@ __device__ __forceinline__ int copy_exponent(float mx) {
     return (mx > 0.f && mx < INFINITY) ? (int)ceilf(__log2f(mx)) - 14 : 0;
 }
 
+// FAVOR+ projection schedule of a chunk, in steps of two jobs: one in each TMEM
+// projection buffer (kind 0 none, 1 max job, 2 k job, 3 q job; and its quarter).
+// The epilogue reads both jobs of a step, frees both buffers, then converts, so
+// that the next step's projections run meanwhile.  The q jobs need the rows'
+// largest exponents (all max jobs) first; the k jobs do not, and hide the max
+// jobs' latency.  Each quarter's k job precedes its q job (the products' order).
+struct ProjStep { int kind[2], quarter[2]; };
+__device__ __forceinline__ int proj_steps(int nq) { return nq == 4 ? 6 : nq == 2 ? 3 : 2; }
+__device__ __forceinline__ ProjStep proj_step(int nq, int i) {
+    if (nq == 4) {
+        switch (i) {
+            case 0: return {{1, 1}, {0, 1}};
+            case 1: return {{2, 1}, {0, 2}};
+            case 2: return {{2, 1}, {1, 3}};
+            case 3: return {{3, 3}, {0, 1}};
+            case 4: return {{2, 3}, {2, 2}};
+            default: return {{2, 3}, {3, 3}};
+        }
+    }
+    if (nq == 2) {
+        switch (i) {
+            case 0: return {{1, 1}, {0, 1}};
+            case 1: return {{2, 3}, {0, 0}};
+            default: return {{2, 3}, {1, 1}};
+        }
+    }
+    return i == 0 ? ProjStep{{1, 0}, {0, 0}} : ProjStep{{2, 3}, {0, 0}};
+}
+
 // kFavor: FAVOR+ projections, else element-wise maps of q and k; one instantiation per kind.
 template <bool kFavor>
 __global__ void __launch_bounds__(kCausalThreads, 1)
@@ -859,16 +916,29 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     // exponent of the keys' scale in chunk c (FAVOR+: recorded by the state kernel)
     const int* kscale = favor ? p.kscale + ((int64_t)u * p.H + head) * p.Lc : nullptr;
     auto key_exp = [&](int c) -> int { return favor ? kscale[c] : 0; };
+    // V of chunk c into s.tv: FAVOR+ the f16 tile the state kernel wrote (one bulk copy), else the
+    // bf16 input tile (the TE converts it in place)
+    const unsigned char* v16 = favor ? static_cast<const unsigned char*>(p.v16) + ((int64_t)u * p.H + head) * p.Lc * (int64_t)kTile
+                                     : nullptr;
+    const float* vmx = favor ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * 2 : nullptr;
+    auto load_v = [&](int c) {
+        if (favor) bulk_load(s.tv, v16 + (int64_t)c * kTile, kTile, &B.v_full);
+        else tma_load_3d(s.tv, &map_v, 0, head, un.start + c * kC, &B.v_full);
+    };
+    auto prefetch_v = [&](int c) {
+        if (favor) bulk_prefetch_l2(v16 + (int64_t)c * kTile, kTile);
+        else tma_prefetch_3d(&map_v, 0, head, un.start + c * kC);
+    };
 
     if (t == 0) {
         prefetch_tensormap(&map_q);
         prefetch_tensormap(&map_k);
         prefetch_tensormap(&map_v);
         mbar_init(&B.qk_full, 1);
-        mbar_init(&B.qk_empty, 9);      // MMA commit + one arrival per projection-epilogue warp
+        mbar_init(&B.qk_empty, favor ? 5 : 9);   // MMA commit + the 4 TE warps (FAVOR+) or the 8 PE warps
         mbar_init(&B.v_full, 1);
         mbar_init(&B.v_empty, 1);
-        mbar_init(&B.vh_full, 1);
+        mbar_init(&B.vh_full, 4);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
             mbar_init(&B.p_empty[i], 8);
@@ -876,6 +946,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(&B.phiq_full[i], 8);
             mbar_init(&B.phq_free[i], 1);
             mbar_init(&B.rx_full[i], 8);
+            mbar_init(&B.off_full[i], 4);
             mbar_init(&B.tx_full[i], 4);
             mbar_init(&B.srow_free[i], 4);
         }
@@ -893,10 +964,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             tma_load_3d(s.tq, &map_q, 0, head, un.start, &B.qk_full);
             tma_load_3d(s.tk, &map_k, 0, head, un.start, &B.qk_full);
             mbar_arrive_expect_tx(&B.v_full, kTile);
-            tma_load_3d(s.tv, &map_v, 0, head, un.start, &B.v_full);
-            if (nchunks > 1) tma_prefetch_3d(&map_v, 0, head, un.start + kC);
+            load_v(0);
+            if (nchunks > 1) prefetch_v(1);
         }
-        s.vmax = 0.f;
     }
     if (warp == 1) {
         tmem_alloc(&B.tmem_base, kTmemCols);
@@ -943,10 +1013,10 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 tma_load_3d(s.tq, &map_q, 0, head, t0, &B.qk_full);
                 tma_load_3d(s.tk, &map_k, 0, head, t0, &B.qk_full);
                 ++nqk;
-                if (c + 1 < nchunks) tma_prefetch_3d(&map_v, 0, head, t0 + kC);   // into L2 before it is needed
+                if (c + 1 < nchunks) prefetch_v(c + 1);   // into L2 before it is needed
                 if (c > 0 && !mbar_wait(&B.v_empty, (c - 1) & 1)) { record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT); break; }
                 mbar_arrive_expect_tx(&B.v_full, kTile);
-                tma_load_3d(s.tv, &map_v, 0, head, t0, &B.v_full);
+                load_v(c);
                 ++nv;
             }
             // a consumer may have given up on a wait: the CTA must not exit while a load it issued
@@ -964,36 +1034,32 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         const uint32_t id_proj = idesc_bf16(128, 64, false, false);
         uint32_t jobs[2] = {0u, 0u};
         bool ok = true;
-        // projection of the k (b = 0) or q (b = 1) tile, features 64*quarter.., into buffer b;
-        // runs ahead of the products, throttled by the epilogue draining each buffer
-        auto issue_job = [&](int b, int quarter) -> bool {
+        // job of the given kind (1 max: the hi part of Q Omega'^T alone, for the rows' largest
+        // exponents; 2 k, 3 q: hi + lo) for features 64 quarter .. into buffer b; waits until the
+        // epilogue has read the buffer's previous job
+        auto issue = [&](int b, int kind, int quarter) -> bool {
             if (!warp_wait(&B.p_empty[b], jobs[b] & 1u)) return false;
             ++jobs[b];
             tc_fence_after();
-            const uint64_t dx = b ? d_tq : d_tk;
+            const uint64_t dx = kind == 2 ? d_tk : d_tq;
             const uint32_t d = tb + kColCP + 64 * b, fo = 8192u * quarter;
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
+            if (kind != 1) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+                for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(dx, 32 * k), sdesc_add(d_omg_lo, fo + 32 * k), id_proj, 1u);
+            }
             mma_commit_w(&B.p_full[b]);
             return true;
         };
-        // the hi part alone of a q job: for the rows' largest exponents (buffer 1)
-        auto issue_max_job = [&](int quarter) -> bool {
-            if (!warp_wait(&B.p_empty[1], jobs[1] & 1u)) return false;
-            ++jobs[1];
-            tc_fence_after();
-            const uint32_t d = tb + kColCP + 64, fo = 8192u * quarter;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss_w(d, sdesc_add(d_tq, 32 * k), sdesc_add(d_omg_hi, fo + 32 * k), id_proj, k > 0);
-            mma_commit_w(&B.p_full[1]);
-            return true;
-        };
+        const int nsteps = proj_steps(nq);
         for (int c = 0; c < nchunks && ok; ++c) {
             if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
-            for (int q = 0; favor && q < nq && ok; ++q) ok = issue_max_job(q);
-            for (int q = 0; favor && q < nq && ok; ++q) ok = issue_job(0, q) && issue_job(1, q);
+            for (int i = 0; favor && i < nsteps && ok; ++i) {
+                const ProjStep st = proj_step(nq, i);
+                for (int b = 0; b < 2 && ok; ++b)
+                    if (st.kind[b] != 0) ok = issue(b, st.kind[b], st.quarter[b]);
+            }
             if (ok) mma_commit_w(&B.qk_empty);   // every projection of this chunk issued
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
@@ -1023,7 +1089,8 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 }
                 tc_fence_after();
                 if ((q & 1) || q == nq - 1) {   // phi(k) of the half complete: update now, ahead of the scores
-                    if (!v_ready && !(ok = warp_wait(&B.vh_full, c & 1))) break;
+                    // V as f16: FAVOR+ loaded so, else converted by the TE
+                    if (!v_ready && !(ok = warp_wait(favor ? &B.v_full : &B.vh_full, c & 1))) break;
                     v_ready = true;
                     // [S|z] += phi(k)^T [V|1]: z from the ones column (column 64)
                     const uint32_t ds = tb + kColCS + kNX * (q >> 1);
@@ -1063,19 +1130,6 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     else if (warp == 3) {
-        // ------------------------------------------------------------ V as f16, in place
-        bool ok = true;
-        float vm = 0.f;   // running largest |v| of the unit
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int nvalid = min(kC, un.end - (un.start + c * kC));
-            if (!(ok = warp_wait(&B.v_full, c & 1))) break;
-            vm = fmaxf(vm, v_tile_to_f16(s.tv, 0, kC, nvalid, p.hdr, lane, 32));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-            if (lane == 0) s.vmax = vm;   // read by the TE for the bound on the state copy
-            warp_arrive(&B.vh_full, true);
-        }
-        if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
     else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ PE: phi(k), phi(q)
@@ -1089,101 +1143,128 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         bool ok = true;
         bool bigk = false, bigq = false;
         int R = 0;                                        // the keys' scale exponent of the chunk
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int t0 = un.start + c * kC;
-            const bool valid = tr < min(kC, un.end - t0);
-            R = favor ? next_key_scale(R, key_exp(c), c == 0) : 0;
-            // the TE has read the row scales and sums of chunk c - 2 (same slot)
-            if (c >= 2 && !(ok = warp_wait(&B.srow_free[c & 1], ((c >> 1) - 1) & 1))) break;
-            if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
-            const float cq = favor ? favor_offset(s.tq, tr, r) : 0.f;
-            const float ck = favor ? favor_offset(s.tk, tr, r) + (float)R : 0.f;
-            if (favor) warp_arrive(&B.qk_empty, false);   // this warp no longer reads the tiles
-            float cqs = cq;                               // + s_i
-            float qs = 0.f;                               // sum of |phi(q) 2^-s_i| this thread wrote
-            if (favor) {
-                // s_i from the row's largest exponent over all r features, taken from Q Omega'_hi^T
-                // (four jobs of the hi part alone, which errs by less than 2^-8 |Omega' x|): the row's
-                // largest phi(q) 2^-s_i lies below 2^14 times 2 to that error, well inside f16
-                float m = -INFINITY;
-                for (int q = 0; q < nq && ok; ++q) {
-                    if (!(ok = warp_wait(&B.p_full[1], (c * 2 * nq + q) & 1))) break;
-                    tc_fence_after();
-                    uint32_t v0[32];
-                    tmem_ld32(tmem_addr(tb, wl, kColCP + 64 + 32 * half_cols), v0);
-                    tmem_ld_wait();
-                    warp_arrive(&B.p_empty[1], false);
+        uint32_t njob[2] = {0u, 0u};                      // jobs read from each projection buffer
+        // Projection job in buffer b (the buffer's next), columns 32 half_cols .. + 31.
+        auto fetch = [&](int b, uint32_t (&v)[32]) -> bool {
+            if (!warp_wait(&B.p_full[b], njob[b]++ & 1u)) return false;
+            tc_fence_after();
+            tmem_ld32(tmem_addr(tb, wl, kColCP + 64 * b + 32 * half_cols), v);
+            return true;
+        };
+        // phi of one 32-column block of a job into dst (FAVOR+): 2^(p - cx), cx = inf past the end
+        auto favor_phi = [&](const uint32_t (&v)[32], float cx, unsigned char* dst, bool& big) -> float {
+            uint32_t w[16];
+            bool bg = false;
+            float sum = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(v0[j]));
-                }
-                if (!ok) break;
-                // the other warpgroup holds the other 32 columns of every job
+            for (int j = 0; j < 16; ++j) {
+                const float a = fminf(ex2_approx(__uint_as_float(v[2 * j]) - cx), 65504.f);
+                const float b = fminf(ex2_approx(__uint_as_float(v[2 * j + 1]) - cx), 65504.f);
+                bg |= !(a < 65504.f) || !(b < 65504.f);
+                sum += a + b;
+                w[j] = pack_f16x2(a, b);
+            }
+            big |= bg;
+            store_row32_bf16(dst, tr, 32 * half_cols, w);
+            return sum;
+        };
+        // the MMAs that read a phi buffer last must be done before it is rewritten: for phi(q)
+        // of global quarter g the products of quarter g - 2 (same buffer); for phi(k) the scores
+        // of the previous quarter using that buffer and the state update of its half
+        auto phq_writable = [&](int g) -> bool {
+            return g < 2 || warp_wait(&B.phq_free[g & 1], ((g >> 1) - 1) & 1);
+        };
+        auto phk_writable = [&](int g) -> bool {
+            const int gw = g - (nq >= 2 ? 2 : 1);
+            const int uw = (gw / nq) * nhalves + ((gw % nq) >> 1);   // that update's index
+            return gw < 0 || (warp_wait(&B.upd_done, uw & 1) && warp_wait(&B.phq_free[gw & 1], (gw >> 1) & 1));
+        };
+        if (favor) {
+            int e_next = nchunks > 0 ? key_exp(0) : 0;   // the table is read a chunk ahead of its use
+            for (int c = 0; c < nchunks && ok; ++c) {
                 const int slot = c & 1;
-                s.rowmax[slot][half_cols][tr] = m;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&B.rx_full[slot]);
-                if (!(ok = warp_wait(&B.rx_full[slot], (c >> 1) & 1))) break;
-                const float mm = fmaxf(s.rowmax[slot][0][tr], s.rowmax[slot][1][tr]) - cq;
-                const int si = (valid && mm > -1e30f) ? (int)ceilf(mm) - 14 : 0;
-                cqs = cq + (float)si;
-                if (half_cols == 0) s.srow[slot][tr] = si;   // for the TE: the row's factor
-            }
-            for (int q = 0; q < nq && ok; ++q) {
-                const int g = c * nq + q;
-                for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
-                    uint32_t v0[32];
-                    if (favor) {
-                        // buffer 0: the k jobs; buffer 1: per chunk the nq max jobs, then the q jobs
-                        if (!(ok = warp_wait(&B.p_full[kind], (kind == 0 ? g : c * 2 * nq + nq + q) & 1))) break;
-                        tc_fence_after();
-                        tmem_ld32(tmem_addr(tb, wl, kColCP + 64 * kind + 32 * half_cols), v0);
-                        tmem_ld_wait();
-                        warp_arrive(&B.p_empty[kind], false);
-                    }
-                    // the MMAs that read the destination buffer last must be done: for phi(q) the
-                    // products of the quarter two before (same buffer); for phi(k) the scores of
-                    // the previous quarter using this buffer and the update of its half
-                    if (kind == 1) {
-                        if (g >= 2 && !(ok = warp_wait(&B.phq_free[g & 1], ((g >> 1) - 1) & 1))) break;
-                    } else {
-                        const int gw = g - (nq >= 2 ? 2 : 1);
-                        const int uw = (gw / nq) * nhalves + ((gw % nq) >> 1);   // that update's index
-                        if (gw >= 0 && !(ok = warp_wait(&B.upd_done, uw & 1) &&
-                                              warp_wait(&B.phq_free[gw & 1], (gw >> 1) & 1))) break;
-                    }
-                    unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq[g & 1];
-                    if (favor) {
-                        // rows past the unit's end: 2^(p - inf) = 0
-                        const float cx = valid ? (kind == 0 ? ck : cqs) : __int_as_float(0x7f800000);
-                        uint32_t w[16];
-                        bool big = false;
-                        float sum = 0.f;
+                const bool valid = tr < min(kC, un.end - (un.start + c * kC));
+                R = next_key_scale(R, e_next, c == 0);
+                e_next = c + 1 < nchunks ? key_exp(c + 1) : 0;
+                // the TE has read the row scales and sums of chunk c - 2 (same slot)
+                if (c >= 2 && !(ok = warp_wait(&B.srow_free[slot], ((c >> 1) - 1) & 1))) break;
+                if (!(ok = warp_wait(&B.off_full[slot], (c >> 1) & 1))) break;
+                const float cq = s.offq[slot][tr];
+                const float ck = s.offk[slot][tr] + (float)R;
+                const float cxk = valid ? ck : __int_as_float(0x7f800000);   // rows past the end: 2^-inf = 0
+                // s_i from the row's largest exponent over all r features, taken from Q Omega'_hi^T
+                // (the max jobs: the hi part alone, which errs by less than 2^-8 |Omega' x|): the
+                // row's largest phi(q) 2^-s_i lies below 2^14 times 2 to that error, inside f16
+                float m = -INFINITY;
+                float cxq = 0.f;                             // cq + s_i once the maxima are in
+                bool have_si = false;
+                float qs = 0.f;                              // sum of |phi(q) 2^-s_i| this thread wrote
+                const int nsteps = proj_steps(nq);
+                for (int i = 0; i < nsteps && ok; ++i) {
+                    const ProjStep st = proj_step(nq, i);
+                    // both jobs of the step at once: each buffer takes its next job while this warp converts
+                    uint32_t v[2][32];
+                    if (!(ok = fetch(0, v[0]) && (st.kind[1] == 0 || fetch(1, v[1])))) break;
+                    tmem_ld_wait();
+                    warp_arrive(&B.p_empty[0], false);
+                    if (st.kind[1] != 0) warp_arrive(&B.p_empty[1], false);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float a = fminf(ex2_approx(__uint_as_float(v0[2 * j]) - cx), 65504.f);
-                            const float b = fminf(ex2_approx(__uint_as_float(v0[2 * j + 1]) - cx), 65504.f);
-                            big |= !(a < 65504.f) || !(b < 65504.f);
-                            sum += a + b;
-                            w[j] = pack_f16x2(a, b);
+                    for (int b = 0; b < 2; ++b) {
+                        const int kind = st.kind[b], q = st.quarter[b], g = c * nq + q;
+                        if (kind == 1) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(v[b][j]));
+                        } else if (kind == 2) {
+                            if (!(ok = phk_writable(g))) break;
+                            favor_phi(v[b], cxk, s.phk[q & 1], bigk);
+                            warp_arrive(&B.phik_full[g & 1], true);
+                        } else if (kind == 3) {
+                            if (!have_si) {
+                                // the other warpgroup holds the other 32 columns of every job
+                                s.rowmax[slot][half_cols][tr] = m;
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&B.rx_full[slot]);
+                                if (!(ok = warp_wait(&B.rx_full[slot], (c >> 1) & 1))) break;
+                                const float mm = fmaxf(s.rowmax[slot][0][tr], s.rowmax[slot][1][tr]) - cq;
+                                const int si = (valid && mm > -1e30f) ? (int)ceilf(mm) - 14 : 0;
+                                if (half_cols == 0) s.srow[slot][tr] = si;   // for the TE: the row's factor
+                                cxq = valid ? cq + (float)si : __int_as_float(0x7f800000);
+                                have_si = true;
+                            }
+                            if (!(ok = phq_writable(g))) break;
+                            qs += favor_phi(v[b], cxq, s.phq[g & 1], bigq);
+                            // the row's sum of |phi(q)|, for the bound that scales its scores
+                            if (q == nq - 1) s.qsum[slot][half_cols][tr] = qs;
+                            warp_arrive(&B.phiq_full[g & 1], true);
                         }
-                        (kind == 0 ? bigk : bigq) |= big;
-                        if (kind == 1) qs += sum;
-                        store_row32_bf16(dst, tr, 32 * half_cols, w);
-                    } else if (p.map == LA_MAP_DPFP) {
-                        float sum = 0.f;
-                        (kind == 0 ? bigk : bigq) |= dpfp_phi_row32_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, q, half_cols, sum);
-                        if (kind == 1) qs += sum;
-                    } else if (half_cols == 0) {
-                        float sum = 0.f;
-                        (kind == 0 ? bigk : bigq) |= elementwise_phi_row_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map, sum);
-                        if (kind == 1) qs += sum;
                     }
-                    // the row's sum of |phi(q)|, for the bound that scales its scores
-                    if (kind == 1 && q == nq - 1) s.qsum[c & 1][half_cols][tr] = qs;
-                    warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full[g & 1], true);
                 }
             }
-            if (ok && !favor) warp_arrive(&B.qk_empty, false);
+        } else {
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int t0 = un.start + c * kC;
+                const bool valid = tr < min(kC, un.end - t0);
+                if (c >= 2 && !(ok = warp_wait(&B.srow_free[c & 1], ((c >> 1) - 1) & 1))) break;
+                if (!(ok = warp_wait(&B.qk_full, c & 1))) break;
+                float qs = 0.f;
+                for (int q = 0; q < nq && ok; ++q) {
+                    const int g = c * nq + q;
+                    for (int kind = 0; kind < 2; ++kind) {   // 0: phi(k) of quarter q, 1: phi(q)
+                        if (!(ok = kind == 0 ? phk_writable(g) : phq_writable(g))) break;
+                        unsigned char* dst = kind == 0 ? s.phk[q & 1] : s.phq[g & 1];
+                        float sum = 0.f;
+                        if (p.map == LA_MAP_DPFP) {
+                            (kind == 0 ? bigk : bigq) |= dpfp_phi_row32_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, q, half_cols, sum);
+                        } else if (half_cols == 0) {
+                            (kind == 0 ? bigk : bigq) |= elementwise_phi_row_f16(kind == 0 ? s.tk : s.tq, dst, tr, valid, p.map, sum);
+                        }
+                        if (kind == 1) qs += sum;
+                        if (kind == 1 && q == nq - 1) s.qsum[c & 1][half_cols][tr] = qs;
+                        warp_arrive(kind == 0 ? &B.phik_full[g & 1] : &B.phiq_full[g & 1], true);
+                    }
+                }
+                if (ok) warp_arrive(&B.qk_empty, false);
+            }
         }
         if (__any_sync(0xffffffffu, bigk) && lane == 0) record_range(p.hdr, kRangeK);
         if (__any_sync(0xffffffffu, bigq) && lane == 0) record_range(p.hdr, kRangeQ);
@@ -1246,9 +1327,34 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         // maximum), element-wise maps the f16 limit
         const float kmax = favor ? 32768.f : 65504.f;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+        // FAVOR+: the exponent offsets of chunk c's query and key rows (one row per thread, slot
+        // c & 1), computed while the TE waits for the chunk before; the PE starts chunk c on them
+        auto post_offsets = [&](int c) -> bool {
+            if (!warp_wait(&B.qk_full, c & 1)) return false;
+            favor_offsets2(s.tq, s.tk, tr, r, s.offq[c & 1][tr], s.offk[c & 1][tr]);
+            warp_arrive(&B.qk_empty, false);      // the tiles are no longer read by this warp
+            warp_arrive(&B.off_full[c & 1], false);
+            return true;
+        };
+        if (favor && nchunks > 0 && ok) ok = post_offsets(0);
+        float vrun = 0.f;                         // largest |v| of the unit's chunks so far
         for (int c = 0; c < nchunks && ok; ++c) {
             const int t0 = un.start + c * kC;
             const bool valid = tr < min(kC, un.end - t0);
+            const int e_next = favor && c + 1 < nchunks ? key_exp(c + 1) : 0;   // read well before its use
+            // the state copy's bound takes the chunk's largest |v| (FAVOR+: from the state kernel's table)
+            const float vm_c = favor ? fmaxf(vmx[2 * c], vmx[2 * c + 1]) : 0.f;
+            if (!favor) {
+                // the chunk's V tile as f16, in place, rows 32 wq ..: the first state update of
+                // the chunk waits for all four warps; each posts its rows' largest |v|
+                if (!(ok = warp_wait(&B.v_full, c & 1))) break;
+                float vm = v_tile_to_f16(s.tv, 32 * (warp & 3), 32, min(kC, un.end - t0), p.hdr, lane, 32);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+                if (lane == 0) s.vt[c & 1][warp & 3] = vm;
+                warp_arrive(&B.vh_full, true);
+            }
+            if (favor && c + 1 < nchunks && !(ok = post_offsets(c + 1))) break;
             if (!(ok = warp_wait(&B.a_full, c & 1))) break;
             tc_fence_after();
             // masked scores (key j <= query tr) as f16 times 2^-t_i in TMEM: A_ij <= (sum_f
@@ -1296,7 +1402,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 // the state after this chunk, while A V runs: rescaled exactly (a power of two)
                 // when the next chunk's key scale differs, then its f16 copy times 2^-g, g from
                 // |S| <= max|S_in| + z max|v| (non-negative features) or the exact maximum
-                Rnext = favor ? next_key_scale(Rcur, key_exp(c + 1), false) : 0;
+                Rnext = favor ? next_key_scale(Rcur, e_next, false) : 0;
                 const float fe = exp2i(Rcur - Rnext);
                 float m = 0.f;
                 for (int half = 0; half < nhalves; ++half) {
@@ -1333,8 +1439,10 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 if (Rnext != Rcur) tmem_st_wait();
                 if (!(ok = group_max4(m, s.tred, B.tx_full, uses++, 12))) break;
                 min_ *= fe;
-                // largest |v| of the chunks so far (warp 3 publishes it before the updates use V)
-                gnext = copy_exponent(exact_copy ? m : fmaxf(m, min_ + m * s.vmax));
+                // every TE warp posted its rows' largest |v| before the exchange above
+                vrun = fmaxf(vrun, favor ? vm_c : fmaxf(fmaxf(s.vt[c & 1][0], s.vt[c & 1][1]),
+                                                        fmaxf(s.vt[c & 1][2], s.vt[c & 1][3])));
+                gnext = copy_exponent(exact_copy ? m : fmaxf(m, min_ + m * vrun));
                 const float fg = exp2i(-gnext);
                 for (int half = 0; half < nhalves; ++half) {
                     uint32_t a0[32], a1[32], zc;
@@ -1816,7 +1924,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             mbar_init(&B.k_full[i], 1);
             mbar_init(&B.k_empty[i], 3);   // projection commit + 2 NE warps
             mbar_init(&B.v_full[i], 1);
-            mbar_init(&B.v_empty[i], 1);
+            // update commit, and with the f16 copy of V going out the two NE warps once it has read the stage
+            mbar_init(&B.v_empty[i], p.v16 != nullptr ? 3 : 1);
             mbar_init(&B.cx_full[i], 2);
             mbar_init(&B.vh_full[i], 2);
         }
@@ -2134,6 +2243,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     } else {
         // ------------------------------------------------------------ NE: exponent offsets, V as f16 (warps 3, 12)
         const int tok0 = warp == 3 ? 0 : 64;      // this warp's 64 tokens
+        // the f16 V tiles of this (unit, head) for the causal output kernel, and their |v| maxima
+        unsigned char* v16 = p.v16 != nullptr
+                                 ? static_cast<unsigned char*>(p.v16) + ((int64_t)u * p.H + head) * p.Lc * (int64_t)kTile
+                                 : nullptr;
+        float* vmx = p.v16 != nullptr ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * 2 : nullptr;
+        int pending = -1;                         // stage whose f16 rows are being copied out
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
@@ -2152,8 +2267,34 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             warp_arrive(&B.cx_full[st], true);
             warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
             if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
-            v_tile_to_f16(s.tv[st], tok0, 64, nvalid, p.hdr, lane, 32);
+            float vm = v_tile_to_f16(s.tv[st], tok0, 64, nvalid, p.hdr, lane, 32);
+            if (v16 != nullptr) {
+                // the 64 rows out as they lie in shared memory (8 KB, one bulk copy), and their largest |v|
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_store(v16 + (int64_t)c * kTile + tok0 * 128, s.tv[st] + tok0 * 128, 64 * 128);
+                    bulk_commit();
+                    vmx[2 * c + (tok0 >> 6)] = vm;
+                }
+            }
             warp_arrive(&B.vh_full[st], true);
+            if (v16 != nullptr) {
+                // the previous chunk's copy has read its stage: the TMA warp may refill it
+                if (pending >= 0) {
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    warp_arrive(&B.v_empty[pending], false);
+                }
+                pending = st;
+            }
+        }
+        if (v16 != nullptr) {   // every copy complete before the block exits (and its stage released)
+            if (lane == 0) bulk_wait_all<0>();
+            __syncwarp();
+            if (pending >= 0) warp_arrive(&B.v_empty[pending], false);
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     }
