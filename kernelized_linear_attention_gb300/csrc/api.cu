@@ -109,7 +109,7 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
     lo.prefix = o;    o = align_up(o + state_bytes, kAlign);
     lo.kscale = o;    o = align_up(o + (path == kPathTensor ? sizeof(int) * (size_t)U * H * lo.Lc : 0), kAlign);
     lo.v16 = o;       o = align_up(o + (vtables ? (size_t)16384 * U * H * lo.Lc : 0), kAlign);
-    lo.vmax = o;      o = align_up(o + (vtables ? sizeof(float) * 2 * (size_t)U * H * lo.Lc : 0), kAlign);
+    lo.vmax = o;      o = align_up(o + (vtables ? sizeof(float) * kVmaxParts * (size_t)U * H * lo.Lc : 0), kAlign);
     lo.sig_q = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     lo.sig_k = o;     o = align_up(o + sizeof(float) * (size_t)T * H, kAlign);
     if (bwd) {

@@ -32,6 +32,9 @@ struct WsHeader {
 };
 
 // Byte offsets of the workspace regions for one forward call.
+// Parts (32-row quarters) of a chunk whose largest |v| the state kernel records.
+constexpr int kVmaxParts = 4;
+
 struct Layout {
     size_t units;      // Unit[U]
     size_t seq_first;  // int[nseq + 1]: first unit of each sequence (+ total)
@@ -40,7 +43,7 @@ struct Layout {
     size_t prefix;     // float[U][H][r][dvx]: state entering the unit (causal) / whole-sequence state (bidir)
     size_t kscale;     // int[U][H][Lc]: power-of-two exponent of the keys' features in each chunk
     size_t v16;        // causal FAVOR+ tensor path: [U][H][Lc] tiles of 128 x 64 f16 V (128B-swizzled rows)
-    size_t vmax;       // float[U][H][Lc][2]: largest |v| of each 64-row half of a chunk's valid rows
+    size_t vmax;       // float[U][H][Lc][kVmaxParts]: largest |v| of each 32-row quarter of a chunk's valid rows
     size_t sig_q;      // float[T][H]: sum_f phi_f(q) (sum normalisation on the tensor-core path)
     size_t sig_k;      // float[T][H]: sum_f phi_f(k)
     size_t suffix;     // backward: float[U][H][r][dvx], sum of phi(q) g^T over later units (or the sequence)
@@ -102,8 +105,8 @@ struct FwdParams {
     int* kscale;
     // Causal FAVOR+ tensor path: every chunk's V tile as f16 in the shared-memory layout of the
     // kernels (rows of 128 bytes, 16-byte pieces swizzled within 1024-byte groups), one 16 KB
-    // tile per (unit, head, chunk), and the largest |v| of each 64-row half of its valid rows
-    // (written by the state kernel, read by the causal output kernel); else NULL.
+    // tile per (unit, head, chunk), and the largest |v| of its valid rows
+    // (per 32-row quarter; written by the state kernel, read by the causal output kernel); else NULL.
     void* v16;
     float* vmax;
     int U, L, Lc;

@@ -206,6 +206,27 @@ __device__ float row_sq_norm(const unsigned char* tile, int t) {
     return s;
 }
 
+// |x|^2 of rows t0 and t1 of a tile: four independent partial sums, so that the
+// FMA latencies overlap (the sums differ from row_sq_norm's in rounding order only).
+__device__ __forceinline__ void row_sq_norm2(const unsigned char* tile, int t0, int t1, float& n0, float& n1) {
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t0, c));
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t1, c));
+        const uint32_t wu[4] = {u.x, u.y, u.z, u.w}, wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            a0 = fmaf(bf16lo(wu[j]), bf16lo(wu[j]), a0);
+            a1 = fmaf(bf16hi(wu[j]), bf16hi(wu[j]), a1);
+            b0 = fmaf(bf16lo(wv[j]), bf16lo(wv[j]), b0);
+            b1 = fmaf(bf16hi(wv[j]), bf16hi(wv[j]), b1);
+        }
+    }
+    n0 = a0 + a1;
+    n1 = b0 + b1;
+}
+
 // Exponent offset of the FAVOR+ epilogue for row t: log2(e) |x|^2 / 2 + log2(sqrt r).
 __device__ __forceinline__ float favor_offset(const unsigned char* tile, int t, int r) {
     return row_sq_norm(tile, t) * (0.5f * kLog2e) + 0.5f * __log2f((float)r);
@@ -601,10 +622,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
         : "=r"(r) : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
     return r;
 }
-// Nonzero when either bf16 half of w is beyond the f16 range (|v| >= 65536, or NaN / inf).
-__device__ __forceinline__ uint32_t bf16x2_beyond_f16(uint32_t w) {
-    return __vcmpgtu2(w & 0x7FFF7FFFu, 0x477F477Fu);
-}
 
 // Rows row0 .. row0 + nrows - 1 of a [128][64] bf16 tile converted in place to f16
 // by `nthreads` cooperating threads (index tid); values beyond the f16 range are
@@ -612,22 +629,21 @@ __device__ __forceinline__ uint32_t bf16x2_beyond_f16(uint32_t w) {
 // |v| among the rows < nvalid this thread converted (for bounds on the state).
 __device__ float v_tile_to_f16(unsigned char* tile, int row0, int nrows, int nvalid, WsHeader* hdr, int tid,
                                int nthreads) {
-    uint32_t bad = 0u, vmax = 0u;
+    uint32_t vmax = 0u;
 #pragma unroll 4
     for (int i = tid; i < nrows * 8; i += nthreads) {
         const int row = row0 + (i >> 3);
         uint4* p = reinterpret_cast<uint4*>(tile + row * 128 + (i & 7) * 16);
         const uint4 w = *p;
-        if (row < nvalid) {
-            bad |= bf16x2_beyond_f16(w.x) | bf16x2_beyond_f16(w.y) | bf16x2_beyond_f16(w.z) | bf16x2_beyond_f16(w.w);
+        if (row < nvalid)
             vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
                                            __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
-        }
         *p = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
     }
-    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0) record_range(hdr, kRangeV);
-    // the largest magnitude as bf16 bits orders like the value (non-negative, finite or saturated)
+    // |v| as bf16 bits orders like the value for every non-negative pattern (infinities and NaNs
+    // lie above the largest finite): a valid element beyond 65504 shows in the maximum
     const uint32_t m = max(vmax & 0xFFFFu, vmax >> 16);
+    if (__any_sync(0xffffffffu, m > 0x477Fu) && (threadIdx.x & 31) == 0) record_range(hdr, kRangeV);
     return __uint_as_float(min(m, 0x4780u) << 16);
 }
 
@@ -920,7 +936,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     // bf16 input tile (the TE converts it in place)
     const unsigned char* v16 = favor ? static_cast<const unsigned char*>(p.v16) + ((int64_t)u * p.H + head) * p.Lc * (int64_t)kTile
                                      : nullptr;
-    const float* vmx = favor ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * 2 : nullptr;
+    const float* vmx = favor ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * kVmaxParts : nullptr;
     auto load_v = [&](int c) {
         if (favor) bulk_load(s.tv, v16 + (int64_t)c * kTile, kTile, &B.v_full);
         else tma_load_3d(s.tv, &map_v, 0, head, un.start + c * kC, &B.v_full);
@@ -1343,7 +1359,9 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             const bool valid = tr < min(kC, un.end - t0);
             const int e_next = favor && c + 1 < nchunks ? key_exp(c + 1) : 0;   // read well before its use
             // the state copy's bound takes the chunk's largest |v| (FAVOR+: from the state kernel's table)
-            const float vm_c = favor ? fmaxf(vmx[2 * c], vmx[2 * c + 1]) : 0.f;
+            const float vm_c = favor ? fmaxf(fmaxf(vmx[kVmaxParts * c], vmx[kVmaxParts * c + 1]),
+                                             fmaxf(vmx[kVmaxParts * c + 2], vmx[kVmaxParts * c + 3]))
+                                     : 0.f;
             if (!favor) {
                 // the chunk's V tile as f16, in place, rows 32 wq ..: the first state update of
                 // the chunk waits for all four warps; each posts its rows' largest |v|
@@ -1785,12 +1803,16 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1;
             if (!(ok = warp_wait(&B.q_full[st], (c >> 1) & 1))) break;
+            if (favor) {
+                float nx[2];
+                row_sq_norm2(s.tq[st], tok0 + lane, tok0 + lane + 32, nx[0], nx[1]);
 #pragma unroll
-            for (int x = 0; x < 2 && favor; ++x) {
-                const int tok = tok0 + lane + 32 * x;
-                const float o = -(row_sq_norm(s.tq[st], tok) * (0.5f * kLog2e) + 0.5f * __log2f((float)r));
-                const uint32_t hl = pack_bf16x2(o, 0.f);
-                *reinterpret_cast<uint32_t*>(s.bias + sw128_off(tok, 16 * st)) = pack_bf16x2(o, o - bf16lo(hl));
+                for (int x = 0; x < 2; ++x) {
+                    const int tok = tok0 + lane + 32 * x;
+                    const float o = -(nx[x] * (0.5f * kLog2e) + 0.5f * __log2f((float)r));
+                    const uint32_t hl = pack_bf16x2(o, 0.f);
+                    *reinterpret_cast<uint32_t*>(s.bias + sw128_off(tok, 16 * st)) = pack_bf16x2(o, o - bf16lo(hl));
+                }
             }
             warp_arrive(&B.cx_full[st], true);
             warp_arrive(&B.q_empty[st], false);   // this warp no longer reads the tile
@@ -1858,18 +1880,21 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // p.kscale for the causal output kernel.
 // TMEM: [S|z] [0, 160) (80 columns per 128-feature half), two fp32 projection
 // buffers [160, 416).
-// Roles (416 threads):
+// Roles (480 threads):
 //   warp 0 lane 0     TMA: k and v tiles of each chunk into three stages (and L2 prefetch)
 //   warp 1            projection MMAs (one elected lane; warp 1 owns the TMEM
 //                     allocation): (c, h) into buffer (c nhalves + h) & 1 once the
 //                     update has read that buffer's previous phi(k)^T
 //   warp 2            state-update MMAs: (c, h) once the PE has written phi(k)^T
-//   warps 3, 12 (NE)  the exponent offset of every token of a stage (FAVOR+), into
-//                     the bias operand of the projection, and the stage's V as f16
-//                     (64 tokens each, on two different SM sub-partitions)
+//   warps 3, 12..14   (NE) the exponent offset of every token of a stage (FAVOR+),
+//                     into the bias operand of the projection, and the stage's V as
+//                     f16 (32 tokens each, on all four SM sub-partitions); with the
+//                     causal FAVOR+ output kernel to follow, the f16 rows also go to
+//                     the workspace with their largest |v|
 //   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
 //                     every half (lane = feature)
-constexpr int kStateThreads = 416;
+constexpr int kStateThreads = 480;
+constexpr int kStateNE = 4;        // NE warps: 3, 12, 13, 14
 constexpr uint32_t kColSS = 0;     // [S|z], 80 columns per half
 constexpr uint32_t kColPS = 160;   // two 128-column projection buffers (exponent, then phi(k)^T in place)
 
@@ -1922,12 +1947,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         for (int i = 0; i < 4; ++i) s.kmx[i] = INT_MIN;
         for (int i = 0; i < kStateStages; ++i) {
             mbar_init(&B.k_full[i], 1);
-            mbar_init(&B.k_empty[i], 3);   // projection commit + 2 NE warps
+            mbar_init(&B.k_empty[i], 1 + kStateNE);   // projection commit + the NE warps
             mbar_init(&B.v_full[i], 1);
             // update commit, and with the f16 copy of V going out the two NE warps once it has read the stage
-            mbar_init(&B.v_empty[i], p.v16 != nullptr ? 3 : 1);
-            mbar_init(&B.cx_full[i], 2);
-            mbar_init(&B.vh_full[i], 2);
+            mbar_init(&B.v_empty[i], p.v16 != nullptr ? 1 + kStateNE : 1);
+            mbar_init(&B.cx_full[i], kStateNE);
+            mbar_init(&B.vh_full[i], kStateNE);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
@@ -2241,43 +2266,45 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
         if (!ok && lane == 0) record_error(p.hdr, LA_DEVERR_WAIT_TIMEOUT);
     } else {
-        // ------------------------------------------------------------ NE: exponent offsets, V as f16 (warps 3, 12)
-        const int tok0 = warp == 3 ? 0 : 64;      // this warp's 64 tokens
+        // ------------------------------------------------------------ NE: exponent offsets, V as f16 (warps 3, 12..14)
+        const int ne = warp == 3 ? 0 : warp - 11;
+        const int tok0 = 32 * ne;                 // this warp's 32 tokens
         // the f16 V tiles of this (unit, head) for the causal output kernel, and their |v| maxima
         unsigned char* v16 = p.v16 != nullptr
                                  ? static_cast<unsigned char*>(p.v16) + ((int64_t)u * p.H + head) * p.Lc * (int64_t)kTile
                                  : nullptr;
-        float* vmx = p.v16 != nullptr ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * 2 : nullptr;
+        float* vmx = p.v16 != nullptr ? p.vmax + ((int64_t)u * p.H + head) * p.Lc * kVmaxParts : nullptr;
         int pending = -1;                         // stage whose f16 rows are being copied out
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c % kStateStages;
             const int nvalid = min(kC, un.end - (un.start + c * kC));
             if (!(ok = warp_wait(&B.k_full[st], (c / kStateStages) & 1))) break;
-#pragma unroll
-            for (int x = 0; x < 2 && favor; ++x) {
-                const int tok = tok0 + lane + 32 * x;
+            if (favor) {
                 // -offset as bf16 hi + lo into the stage's bias columns; past the unit's
-                // end a large negative exponent makes phi = 0
-                const float o = tok < nvalid ? -(row_sq_norm(s.tk[st], tok) * (0.5f * kLog2e) + 0.5f * __log2f((float)r))
-                                             : -32768.f;
+                // end a large negative exponent makes phi = 0.  Token tok0 + lane; the partner
+                // row is only there to share the loop (its sum is the same token's)
+                const int tok = tok0 + lane;
+                float n, n_unused;
+                row_sq_norm2(s.tk[st], tok, tok, n, n_unused);
+                const float o = tok < nvalid ? -(n * (0.5f * kLog2e) + 0.5f * __log2f((float)r)) : -32768.f;
                 const uint32_t hl = pack_bf16x2(o, 0.f);
                 *reinterpret_cast<uint32_t*>(s.bias + sw128_off(tok, 16 * st)) = pack_bf16x2(o, o - bf16lo(hl));
             }
             warp_arrive(&B.cx_full[st], true);
             warp_arrive(&B.k_empty[st], false);   // this warp no longer reads the tile
             if (!(ok = warp_wait(&B.v_full[st], (c / kStateStages) & 1))) break;
-            float vm = v_tile_to_f16(s.tv[st], tok0, 64, nvalid, p.hdr, lane, 32);
+            float vm = v_tile_to_f16(s.tv[st], tok0, 32, nvalid, p.hdr, lane, 32);
             if (v16 != nullptr) {
-                // the 64 rows out as they lie in shared memory (8 KB, one bulk copy), and their largest |v|
+                // the 32 rows out as they lie in shared memory (4 KB, one bulk copy), and their largest |v|
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    bulk_store(v16 + (int64_t)c * kTile + tok0 * 128, s.tv[st] + tok0 * 128, 64 * 128);
+                    bulk_store(v16 + (int64_t)c * kTile + tok0 * 128, s.tv[st] + tok0 * 128, 32 * 128);
                     bulk_commit();
-                    vmx[2 * c + (tok0 >> 6)] = vm;
+                    vmx[kVmaxParts * c + ne] = vm;
                 }
             }
             warp_arrive(&B.vh_full[st], true);
