@@ -1168,19 +1168,21 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             return true;
         };
         // phi of one 32-column block of a job into dst (FAVOR+): 2^(p - cx), cx = inf past the end
+        // (values at or beyond the f16 limit saturate to 65504 and are reported: the largest
+        // exponent argument of the block decides that, one maximum per element)
         auto favor_phi = [&](const uint32_t (&v)[32], float cx, unsigned char* dst, bool& big) -> float {
             uint32_t w[16];
-            bool bg = false;
+            float mx = -INFINITY;
             float sum = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float a = fminf(ex2_approx(__uint_as_float(v[2 * j]) - cx), 65504.f);
-                const float b = fminf(ex2_approx(__uint_as_float(v[2 * j + 1]) - cx), 65504.f);
-                bg |= !(a < 65504.f) || !(b < 65504.f);
+                const float xa = __uint_as_float(v[2 * j]) - cx, xb = __uint_as_float(v[2 * j + 1]) - cx;
+                mx = fmaxf(mx, fmaxf(xa, xb));
+                const float a = ex2_approx(xa), b = ex2_approx(xb);
                 sum += a + b;
-                w[j] = pack_f16x2(a, b);
+                w[j] = pack_f16x2_sat(a, b);
             }
-            big |= bg;
+            big |= mx >= 15.9997f;   // 2^15.9997 > 65503
             store_row32_bf16(dst, tr, 32 * half_cols, w);
             return sum;
         };
