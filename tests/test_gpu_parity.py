@@ -293,6 +293,10 @@ def test_full_size_workload_sampled_rows(la, name):
 def _every_row(got, ref, what):
     rms = np.sqrt(np.mean(ref ** 2))
     e = abs_err_over_rms(got, ref, rms)
+    # reported beside the gated figure: the plain max |gpu - ref| / RMS (the bf16 storage
+    # rounding of each exact value included)
+    plain = float(np.max(np.abs(np.asarray(got, np.float64) - ref)) / rms)
+    print(f"every-row {what}: {e:.4f} of RMS beyond the storage rounding, {plain:.4f} plain")
     assert e <= BF16_RMS_TOL, f"{what}: bf16 abs error / RMS {e:.3e} > {BF16_RMS_TOL} " \
                               f"({rows_over_bar(got, ref, rms)} rows over)"
     return e
