@@ -91,19 +91,27 @@ def roofline_of(w: synthetic.Workload, phase_ms: dict, peaks: dict) -> dict:
     launch (the per-token-head figures of algorithmic() times the token-heads the
     launch processes) over its measured duration, against the measured peak of
     the roofline that bounds it (the larger of FLOPs / tensor peak and bytes /
-    HBM peak).  The output kernel performs the whole method for every token-head
-    (it reads q, k, v, writes out, computes both projections, the state terms
-    and the readout); the state kernel reads k and v of every token."""
-    alg = algorithmic(w)
+    HBM peak).  The causal output kernel performs the whole method for every
+    token-head (it reads q, k, v, writes out, computes both projections, the state
+    terms and the readout); the bidirectional output kernel reads q and writes out
+    (the q projection and the readout); the state kernel reads k and v of every
+    token (the k projection and the state update)."""
     token_heads = w.T * w.H
+    esz = 2 if w.dtype == "bf16" else 4
+    proj1 = 2 * w.dk * w.r if w.map == "favor" else 0     # one projection (q or k)
+    term = 2 * w.r * (w.dv + 1)                            # the state update or the readout
+    if w.causal:
+        out_flops, out_bytes = algorithmic(w)["flops"], algorithmic(w)["bytes"]
+    else:
+        out_flops, out_bytes = proj1 + term, (w.dk + w.dv) * esz
     dom = max(phase_ms, key=phase_ms.get)
     dom_ms = phase_ms[dom]
     if dom == "state":
-        flops = (2 * w.dk * w.r * 2 if w.map == "favor" else 0) * token_heads // 2 + 2 * w.r * (w.dv + 1) * token_heads
-        byts = (w.dk + w.dv) * (2 if w.dtype == "bf16" else 4) * token_heads
+        flops = (proj1 + term) * token_heads
+        byts = (w.dk + w.dv) * esz * token_heads
     else:
-        flops = alg["flops"] * token_heads
-        byts = alg["bytes"] * token_heads
+        flops = out_flops * token_heads
+        byts = out_bytes * token_heads
     tflop = peaks["bf16_tflops"] if w.dtype == "bf16" else FP32_ALU_TFLOPS
     t_flop = flops / (tflop * 1e12)
     t_byte = byts / (peaks["hbm_gbs"] * 1e9)
@@ -122,8 +130,8 @@ def roofline_of(w: synthetic.Workload, phase_ms: dict, peaks: dict) -> dict:
     roof["alg_bytes_per_launch"] = byts
     roof["peak_source"] = peaks["source"] + (" (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "")
     if "output" in phase_ms and phase_ms["output"] > 0:
-        roof["tensor_frac_of_output"] = alg["flops"] * token_heads / (phase_ms["output"] * 1e-3) / 1e12 / tflop
-        roof["hbm_frac_of_output"] = alg["bytes"] * token_heads / (phase_ms["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+        roof["tensor_frac_of_output"] = out_flops * token_heads / (phase_ms["output"] * 1e-3) / 1e12 / tflop
+        roof["hbm_frac_of_output"] = out_bytes * token_heads / (phase_ms["output"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
     roof["phase_ms"] = phase_ms
     roof["kernel_timing"] = ("CUDA events between la_forward_phase calls on the launching stream, over as many "
                              "forwards as the timed steps, right after them")
