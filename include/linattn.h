@@ -311,6 +311,20 @@ LA_API la_status la_forward_causal_noalloc(const void* q, const void* k, const v
 LA_API la_status la_noalloc_error(int* code, void* stream);
 
 /*
+ * la_test_force_wait_timeout - test hook for the bounded waits (not part of
+ *   the method).  With enable = 1, every later launch of the causal tensor-core
+ *   output kernel on the current device makes its projection epilogue first
+ *   wait on a barrier that nothing arrives at, with a 1 ms limit; the wait runs
+ *   out, the kernel records LA_DEVERR_WAIT_TIMEOUT in the workspace error word,
+ *   every role gives up on its own bounded waits (2 s each), drains the copies
+ *   and MMAs it started, frees its tensor memory and returns: the outputs of that
+ *   call are incomplete and the context stays usable.  enable = 0 restores normal
+ *   operation.  Device-wide; not for concurrent use with other calls.  Returns
+ *   LA_OK, or LA_ERR_CUDA when the device flag cannot be written.
+ */
+LA_API la_status la_test_force_wait_timeout(int enable);
+
+/*
  * la_workspace_bytes - scratch size for a forward call on the current device.
  *   causal: 1 for la_forward_causal, 0 for la_forward_bidir; `has_cu_seqlens`:
  *   1 when a cu_seqlens array will be passed.  Returns 0 for arguments the

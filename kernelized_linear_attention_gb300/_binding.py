@@ -56,6 +56,7 @@ def load_library():
                             _c_float, _vp, _vp, _vp], _c_int),
         "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
         "la_noalloc_error": ([ctypes.POINTER(_c_int), _vp], _c_int),
+        "la_test_force_wait_timeout": ([_c_int], _c_int),
         "la_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_int],
                                _c_size),
         "la_check_cu_seqlens": ([_vp, _c_int, _c_i64, _vp], _c_int),
@@ -220,6 +221,14 @@ def la_forward_causal_noalloc(q, k, v, map, omega=None, cu_seqlens=None, nseq=No
         _ptr(q), _ptr(k), _ptr(v), _ptr(omega), m, DTYPE_IDS[q.dtype], _ptr(cu_seqlens), nseq, T, H, d_k, d_v, r,
         eps, _ptr(out), _stream(stream)))
     return out
+
+
+def la_test_force_wait_timeout(enable: bool) -> None:
+    """Test hook: while enabled, the causal tensor-core output kernel's bounded waits are made
+    to run out (it records LA_DEVERR_WAIT_TIMEOUT and returns); see include/linattn.h."""
+    st = load_library().la_test_force_wait_timeout(1 if enable else 0)
+    if st != LA_OK:
+        raise LinAttnError("la_test_force_wait_timeout", st)
 
 
 def la_noalloc_error(stream=None) -> int:

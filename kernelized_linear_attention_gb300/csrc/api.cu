@@ -466,6 +466,10 @@ la_status la_workspace_error(const void* workspace, int* code, void* stream) {
     return err == LA_DEVERR_NONE ? LA_OK : LA_ERR_DEVICE;
 }
 
+la_status la_test_force_wait_timeout(int enable) {
+    return la::tc_force_wait_timeout(enable ? 1 : 0) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
 la_status la_orthogonal_features(const double* gauss_blocks, const double* gauss_lengths, int r, int d,
                                  float* omega, void* stream) {
     if (!gauss_blocks || !gauss_lengths || !omega) return LA_ERR_INVALID_ARG;

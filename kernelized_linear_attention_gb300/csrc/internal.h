@@ -35,6 +35,9 @@ la_status forward_entry(int causal, int phase_lo, int phase_hi, const void* q, c
 // (DPFP-1, -2: whole sequences per unit, state pass on CUDA cores); 16-byte
 // aligned operands.
 bool tc_supported(int map, int dk, int dv, int r, int causal);
+// Test hook behind la_test_force_wait_timeout: sets the causal output kernel's flag on the
+// current device.
+cudaError_t tc_force_wait_timeout(int enable);
 cudaError_t tc_state(const FwdParams& p, cudaStream_t s);
 cudaError_t tc_out(const FwdParams& p, int prefix_is_zero, cudaStream_t s);
 cudaError_t tc_feature_map(const void* x, const float* omega, int64_t T, int H, int r, float* phi, int* err,

@@ -46,16 +46,17 @@ constexpr uint32_t kOmgBytes = 256 * 128;        // Omega' part [256][64] bf16 =
 constexpr int kNX = 80;                          // d_v + ones column, padded to a multiple of 16
 constexpr uint32_t kSbfBlock = kNX * 128;        // [80][64] bf16 = 10 KB
 
-// Tensor-memory columns (512 allocated).
-constexpr uint32_t kColS = 0;     // state, one 80-column block per feature half (lanes = features)
-constexpr uint32_t kColA = 160;   // causal scores [128 q][128 k]
-constexpr uint32_t kColO = 288;   // numerator | denominator [128][80]
+// Tensor-memory columns of the feature-map kernel (512 allocated by every kernel).
 constexpr uint32_t kColP = 368;   // projection of up to 128 features [128][128]
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 // bound on the exit-time wait for a TMA load the CTA issued (it completes in microseconds)
 constexpr uint64_t kDrainLimitNs = 100000000ull;
+// Test hook (la_test_force_wait_timeout): nonzero makes the causal output kernel's projection
+// epilogue wait on a barrier that nothing arrives at, with kForcedWaitLimitNs.
+__device__ int g_force_wait_timeout = 0;
+constexpr uint64_t kForcedWaitLimitNs = 1000000ull;
 
 typedef unsigned char Tile[kTile];
 
@@ -255,31 +256,6 @@ __device__ __forceinline__ void favor_offsets2(const unsigned char* tq, const un
     ok = sk * (0.5f * kLog2e) + lr;
 }
 
-// Element-wise phi (ELU+1 or identity) of row t of a tile into the same
-// position of dst (row t; zero when the row is past the unit's end).
-__device__ void elementwise_phi_row(const unsigned char* tile, unsigned char* dst, int t, bool valid, int map) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float lo = bf16lo(ws[j]), hi = bf16hi(ws[j]);
-                if (map == LA_MAP_ELU1) {   // exponentials unconditional, so that the choices are selects
-                    const float el = ex2_approx(lo * kLog2e), eh = ex2_approx(hi * kLog2e);
-                    lo = lo > 0.f ? lo + 1.f : el;
-                    hi = hi > 0.f ? hi + 1.f : eh;
-                }
-                ws[j] = pack_bf16x2(lo, hi);
-            }
-            o = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-        }
-        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, c)) = o;
-    }
-}
-
 // DPFP-nu features of one row ("The Kernel Zoo" §6.3): x~ = relu([x, -x]) in
 // R^128 (d = 64), feature (s-1) 128 + a = x~_a x~_{(a+s) mod 128}.  xw holds
 // the row's 64 bf16 inputs in pairs (element j in half j & 1 of xw[j >> 1]);
@@ -297,42 +273,6 @@ __device__ __forceinline__ void dpfp_features32(const uint32_t (&xw)[32], uint32
         const uint32_t h = pack_bf16x2(f0, f1);
         hi[i >> 1] = h;
         lo[i >> 1] = pack_bf16x2(f0 - bf16lo(h), f1 - bf16hi(h));
-    }
-}
-
-// Features 64 quarter + 32 half .. + 31 of row t of a [128][64] bf16 input
-// tile, as bf16 into the same row of dst at columns 32 half .. (zero past the
-// unit's end), and their bf16 remainders into dst_lo when it is given.
-// r = 128 nu: quarters 0, 1 are shift 1, quarters 2, 3 shift 2.
-__device__ void dpfp_phi_row32(const unsigned char* tile, unsigned char* dst, unsigned char* dst_lo, int t, bool valid,
-                               int quarter, int half) {
-    uint32_t xw[32], hi[16], lo[16];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_chunk(t, c));
-        xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
-    }
-    switch (quarter * 2 + half) {
-        case 0: dpfp_features32<1, 0>(xw, hi, lo); break;
-        case 1: dpfp_features32<1, 32>(xw, hi, lo); break;
-        case 2: dpfp_features32<1, 64>(xw, hi, lo); break;
-        case 3: dpfp_features32<1, 96>(xw, hi, lo); break;
-        case 4: dpfp_features32<2, 0>(xw, hi, lo); break;
-        case 5: dpfp_features32<2, 32>(xw, hi, lo); break;
-        case 6: dpfp_features32<2, 64>(xw, hi, lo); break;
-        default: dpfp_features32<2, 96>(xw, hi, lo); break;
-    }
-    if (!valid) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) { hi[j] = 0u; lo[j] = 0u; }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        *reinterpret_cast<uint4*>(dst + sw128_chunk(t, 4 * half + q)) =
-            make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-        if (dst_lo)
-            *reinterpret_cast<uint4*>(dst_lo + sw128_chunk(t, 4 * half + q)) =
-                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
     }
 }
 
@@ -380,74 +320,11 @@ __device__ float projection_rowsum(uint32_t tbase, int nf, float c) {
     return acc;
 }
 
-// The fp32 state a unit starts from ([r][65] in global; zero if `zero`):
-// into TMEM (tmem_base != 0xFFFFFFFF) and into bf16 readout blocks hi (and the
-// rounding remainder into lo when lo != nullptr).
-__device__ void load_state(unsigned char (*hi)[kSbfBlock], unsigned char (*lo)[kSbfBlock], uint32_t tbase,
-                           bool to_tmem, const float* src, int r, int nhalves, bool zero, int f = threadIdx.x,
-                           int only_half = -1) {
-    const int warp = f >> 5;
-    for (int half = 0; half < nhalves; ++half) {
-        if (only_half >= 0 && half != only_half) continue;
-        const int feat = 128 * half + f;
-        const bool have = !zero && feat < r;
-        const int blk = 2 * half + (f >> 6);
-        for (int n0 = 0; n0 < kNX; n0 += 16) {
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int n = n0 + j;
-                const float x = (have && n < 65) ? src[(int64_t)feat * 65 + n] : 0.f;
-                w[j] = __float_as_uint(x);
-                const __nv_bfloat16 xh = __float2bfloat16_rn(x);
-                *reinterpret_cast<__nv_bfloat16*>(hi[blk] + sw128_off(n, f & 63)) = xh;
-                if (lo != nullptr)
-                    *reinterpret_cast<__nv_bfloat16*>(lo[blk] + sw128_off(n, f & 63)) =
-                        __float2bfloat16_rn(x - __bfloat162float(xh));
-            }
-            if (to_tmem) tmem_st16(tmem_addr(tbase, warp * 32, kColS + 80 * half + n0), w);
-        }
-    }
-    if (to_tmem) tmem_st_wait();
-}
-
-// 32 scores of one row (keys key0 .. key0 + 31) as bf16 hi + lo, two keys per word;
-// keys after `row` are zeroed when the block is on the diagonal.  Adds the kept
-// scores to dsum.
-__device__ __forceinline__ void split_scores32(const uint32_t (&v)[32], int key0, bool diag, int row, float& dsum,
-                                               uint32_t (&hv)[16], uint32_t (&lv)[16]) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int c0 = key0 + 2 * j;
-        const float a = (!diag || c0 <= row) ? __uint_as_float(v[2 * j]) : 0.f;
-        const float b = (!diag || c0 + 1 <= row) ? __uint_as_float(v[2 * j + 1]) : 0.f;
-        dsum += a + b;
-        hv[j] = pack_bf16x2(a, b);
-        lv[j] = pack_bf16x2(a - bf16lo(hv[j]), b - bf16hi(hv[j]));
-    }
-}
-
 // 64 bf16 (packed in pairs) as row `row` of a 128-byte-swizzled tile.
 __device__ __forceinline__ void state_row_bf16(unsigned char* tile, int row, const uint32_t (&w)[32]) {
 #pragma unroll
     for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, c)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-}
-
-// One output row from registers as bf16 to global: O[0..63] / max(den, eps)
-// under attention normalisation, O[0..63] itself without it.
-__device__ __forceinline__ void store_output_row(const uint32_t (&a)[32], const uint32_t (&b)[32], uint32_t den,
-                                                 float eps, bool normalise, __nv_bfloat16* dst_row) {
-    const float inv = normalise ? 1.0f / fmaxf(__uint_as_float(den), eps) : 1.0f;
-    uint4* dst = reinterpret_cast<uint4*>(dst_row);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint32_t* x = q < 4 ? a + 8 * q : b + 8 * (q - 4);
-        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                            pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                            pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                            pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
-    }
 }
 
 // One output row from registers as bf16 to global: out = O[0..63] * mult.
@@ -719,6 +596,7 @@ struct CausalBars {
     uint64_t rx_full[2];            // PE (8 warps) -> PE: row maxima of phi(q), quarter 0, posted (two slots)
     uint64_t tx_full[2];            // TE (4 warps) -> TE: maxima of the state posted (two slots)
     uint64_t srow_free[2];          // TE (4 warps) -> PE: a chunk's row scales read (two slots)
+    uint64_t never;                 // no arrivals: the wait la_test_force_wait_timeout makes run out
     uint64_t drain[2];              // one per MMA-issuing warp
     uint32_t tmem_base;
     int pad;
@@ -972,6 +850,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         mbar_init(&B.o_full, 1);
         mbar_init(&B.o_empty, 4);
         mbar_init(&B.sbf_full, 4);
+        mbar_init(&B.never, 1);
         mbar_init(&B.drain[0], 1);
         mbar_init(&B.drain[1], 1);
         fence_mbar_init();
@@ -1199,6 +1078,12 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         };
         if (favor) {
             int e_next = nchunks > 0 ? key_exp(0) : 0;   // the table is read a chunk ahead of its use
+            if (g_force_wait_timeout != 0) {
+                // test hook: a wait on a barrier that nothing arrives at runs out, as a lost
+                // hand-off would; the other roles then give up on their own bounded waits
+                const bool got = mbar_wait(&B.never, 0, kForcedWaitLimitNs);
+                ok = !__any_sync(0xffffffffu, !got);
+            }
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int slot = c & 1;
                 const bool valid = tr < min(kC, un.end - (un.start + c * kC));
@@ -2456,6 +2341,10 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 }  // namespace
+
+cudaError_t tc_force_wait_timeout(int enable) {
+    return cudaMemcpyToSymbol(g_force_wait_timeout, &enable, sizeof(int));
+}
 
 bool tc_supported(int map, int dk, int dv, int r, int causal) {
     if (dk != 64 || dv != 64) return false;
