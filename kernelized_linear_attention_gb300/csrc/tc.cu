@@ -1052,15 +1052,18 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         auto favor_phi = [&](const uint32_t (&v)[32], float cx, unsigned char* dst, bool& big) -> float {
             uint32_t w[16];
             float mx = -INFINITY;
-            float sum = 0.f;
+            uint64_t sum2 = f32x2_splat(0.f);             // two partial sums (even, odd columns)
+            const uint64_t ncx = f32x2_splat(-cx);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float xa = __uint_as_float(v[2 * j]) - cx, xb = __uint_as_float(v[2 * j + 1]) - cx;
+                const uint64_t x2 = f32x2_add(f32x2_of(v[2 * j], v[2 * j + 1]), ncx);
+                const float xa = f32x2_lo(x2), xb = f32x2_hi(x2);
                 mx = fmaxf(mx, fmaxf(xa, xb));
                 const float a = ex2_approx(xa), b = ex2_approx(xb);
-                sum += a + b;
+                sum2 = f32x2_add(sum2, f32x2_of(__float_as_uint(a), __float_as_uint(b)));
                 w[j] = pack_f16x2_sat(a, b);
             }
+            const float sum = f32x2_lo(sum2) + f32x2_hi(sum2);
             big |= mx >= 15.9997f;   // 2^15.9997 > 65503
             store_row32_bf16(dst, tr, 32 * half_cols, w);
             return sum;
@@ -1370,49 +1373,39 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             }
             if (!(ok = warp_wait(&B.o_full, c & 1))) break;
             tc_fence_after();
-            // num = 2^t_i O_in + 2^g O_cross (and the denominators), all times 2^(s_i + R_c)
-            float num[64];
-            float den;
-            {
-                uint32_t o0[32], o1[32], di;
-                tmem_ld32(tmem_addr(tb, wl, kColCI), o0);
-                tmem_ld32(tmem_addr(tb, wl, kColCI + 32), o1);
-                tmem_ld1(tmem_addr(tb, wl, kColCI + 64), di);
-                tmem_ld_wait();
-                const float f2t = exp2i(ti);
+            // out = (2^t_i O_in + 2^g O_cross) times the row's multiplier (all in the scale
+            // 2^(s_i + R_c)); the denominator first, since it sets the multiplier, then both
+            // scales folded into it (exact powers of two), one packed multiply and one packed FMA
+            // per pair of columns
+            uint32_t di, dh, dl;
+            tmem_ld1(tmem_addr(tb, wl, kColCI + 64), di);
+            tmem_ld1(tmem_addr(tb, wl, kColCX + 64), dh);
+            tmem_ld1(tmem_addr(tb, wl, kColCX + 65), dl);
+            tmem_ld_wait();
+            const float f2t = exp2i(ti), f2g = exp2i(gcur);
+            const float den = fmaf(__uint_as_float(dh) + __uint_as_float(dl), f2g, __uint_as_float(di) * f2t);
+            const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
+            const float mult = valid ? row_multiplier(den, si + Rcur, p, orow) : 0.f;
+            const uint64_t ma = f32x2_splat(f2t * mult), mb = f32x2_splat(f2g * mult);
+            uint4* dst = reinterpret_cast<uint4*>(out + orow * 64);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    num[j] = __uint_as_float(o0[j]) * f2t;
-                    num[32 + j] = __uint_as_float(o1[j]) * f2t;
+            for (int piece = 0; piece < 2; ++piece) {
+                uint32_t a[32], x[32];
+                tmem_ld32(tmem_addr(tb, wl, kColCI + 32 * piece), a);
+                tmem_ld32(tmem_addr(tb, wl, kColCX + 32 * piece), x);
+                tmem_ld_wait();
+                // the next chunk may overwrite O_in, O_cross and the scores
+                if (piece == 1) warp_arrive(&B.o_empty, false);
+                if (valid) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = f32x2_to_bf16x2(f32x2_fma(f32x2_of(x[2 * j], x[2 * j + 1]), mb,
+                                                         f32x2_mul(f32x2_of(a[2 * j], a[2 * j + 1]), ma)));
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        dst[4 * piece + qq] = make_uint4(w[4 * qq], w[4 * qq + 1], w[4 * qq + 2], w[4 * qq + 3]);
                 }
-                den = __uint_as_float(di) * f2t;
-            }
-            {
-                const float f2g = exp2i(gcur);
-                uint32_t x[32], dh, dl;
-                tmem_ld32(tmem_addr(tb, wl, kColCX), x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) num[j] = fmaf(__uint_as_float(x[j]), f2g, num[j]);
-                tmem_ld32(tmem_addr(tb, wl, kColCX + 32), x);
-                tmem_ld1(tmem_addr(tb, wl, kColCX + 64), dh);
-                tmem_ld1(tmem_addr(tb, wl, kColCX + 65), dl);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) num[32 + j] = fmaf(__uint_as_float(x[j]), f2g, num[32 + j]);
-                den = fmaf(__uint_as_float(dh) + __uint_as_float(dl), f2g, den);
-            }
-            warp_arrive(&B.o_empty, false);           // the next chunk may overwrite O_in, O_cross and the scores
-            if (valid) {
-                const int64_t orow = (int64_t)(t0 + tr) * p.H + head;
-                const float mult = row_multiplier(den, si + Rcur, p, orow);
-                uint4* dst = reinterpret_cast<uint4*>(out + orow * 64);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_uint4(pack_bf16x2(num[8 * q] * mult, num[8 * q + 1] * mult),
-                                        pack_bf16x2(num[8 * q + 2] * mult, num[8 * q + 3] * mult),
-                                        pack_bf16x2(num[8 * q + 4] * mult, num[8 * q + 5] * mult),
-                                        pack_bf16x2(num[8 * q + 6] * mult, num[8 * q + 7] * mult));
             }
             gcur = gnext;
             Rcur = Rnext;
