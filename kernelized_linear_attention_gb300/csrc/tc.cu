@@ -94,7 +94,7 @@ struct __align__(1024) BidirSmem {
     float rowmax[2][2][kC];           // per chunk slot, warpgroup and query row: the maximum it saw
     int srow[2][kC];                  // per chunk slot and query row: the exponent of its phi(q) scale
     int gexp;                         // exponent g of the state copy's scale
-    float red[8];
+    float red[32];                    // per-warp maxima of the set-up
     BidirBars b;
 };
 
@@ -358,40 +358,45 @@ __device__ __forceinline__ float row_multiplier(float den, int e, const FwdParam
 // the block during set-up (it synchronises); writes g to *gexp.
 __device__ void load_state_f16(unsigned char (*dst)[kSbfBlock], const float* src, int r, int nhalves, float* red,
                                int* gexp) {
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, nthreads = blockDim.x;
+    // the largest |entry|: 16-byte loads over the contiguous [r][65] block (r * 65 is a
+    // multiple of 4 and the block starts 16-byte aligned), every thread of the block
     float m = 0.f;
-    if (t < 128) {
-        for (int h = 0; h < nhalves; ++h) {
-            const int feat = 128 * h + t;
-            if (feat >= r) continue;
-            for (int n = 0; n < 65; ++n) m = fmaxf(m, fabsf(src[(int64_t)feat * 65 + n]));
-        }
+    const float4* src4 = reinterpret_cast<const float4*>(src);
+    for (int i = t; i < r * 65 / 4; i += nthreads) {
+        const float4 x = src4[i];
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (t < 128 && (t & 31) == 0) red[t >> 5] = m;
+    if ((t & 31) == 0) red[t >> 5] = m;
     __syncthreads();
     if (t == 0) {
-        const float mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        float mx = 0.f;
+        for (int w = 0; w < nthreads / 32; ++w) mx = fmaxf(mx, red[w]);
         *gexp = mx > 0.f && mx < INFINITY ? (int)ceilf(__log2f(mx)) - 14 : 0;
     }
     __syncthreads();
     const float mul = exp2i(-*gexp);
-    if (t < 128) {
-        for (int h = 0; h < nhalves; ++h) {
-            const int feat = 128 * h + t;
-            const bool have = feat < r;
-            unsigned char* blk = dst[2 * h + (t >> 6)];
-            for (int n = 0; n < kNX; ++n) {
-                float x = 0.f;
-                if (have && n < 64) x = src[(int64_t)feat * 65 + n] * mul;
-                if (have && n >= 64 && n < 66) {
-                    const float z = src[(int64_t)feat * 65 + 64] * mul;
-                    const float zh = __half2float(__float2half_rn(z));
-                    x = n == 64 ? zh : z - zh;
-                }
-                *reinterpret_cast<__half*>(blk + sw128_off(n, t & 63)) = __float2half_rn(x);
-            }
+    // rows 66..79 of every block and the blocks of features r.. are zero
+    const int nblk = 2 * nhalves;
+    for (int i = t; i < nblk * kSbfBlock / 16; i += nthreads) {
+        const int blk = i / (kSbfBlock / 16), off = (i - blk * (kSbfBlock / 16)) * 16;
+        if (off >= 66 * 128 || 64 * blk >= r)
+            *reinterpret_cast<uint4*>(dst[blk] + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // entry (f, n) of the state, in its own (contiguous) order, to row n (64, 65: z as f16 and
+    // its remainder), column f of the K-major operand blocks [80][64]
+    for (int e = t; e < r * 65; e += nthreads) {
+        const int f = e / 65, n = e - 65 * f;
+        const float x = src[e] * mul;
+        unsigned char* blk = dst[f >> 6];
+        if (n < 64) {
+            *reinterpret_cast<__half*>(blk + sw128_off(n, f & 63)) = __float2half_rn(x);
+        } else {
+            const __half zh = __float2half_rn(x);
+            *reinterpret_cast<__half*>(blk + sw128_off(64, f & 63)) = zh;
+            *reinterpret_cast<__half*>(blk + sw128_off(65, f & 63)) = __float2half_rn(x - __half2float(zh));
         }
     }
 }
