@@ -109,6 +109,7 @@ struct StateBars {
     uint64_t p_full[2];      // projection commit -> PE: phi exponent of a feature half in buffer b
     uint64_t a_full[2];      // PE (8 warps) -> update issuer: phi(k)^T of that half in buffer b (bf16)
     uint64_t a_empty[2];     // update commit -> projection issuer: buffer b read
+    uint64_t pmx_full[4][2]; // r = 256: the two PE warps of a TMEM lane quarter -> each other: maxima of half h posted
     uint64_t drain[2];
     uint32_t tmem_base;
     int pad;
@@ -122,6 +123,7 @@ struct __align__(1024) StateSmem {
     Tile ones;                    // K-major [feature][64]: columns 16 i, 16 i + 1 = 1 (bf16)
     unsigned char ones16[2048];   // f16 ones atom of the update's [V|1]: (row, 0) = 1 (column 64 = z)
     float red[2][8];              // PE maxima per warp (two slots)
+    float pmx[2][2][128];         // r = 256: per-feature maxima of half h over tokens 64 wg .. 64 wg + 63
     int kmx[4];                   // per chunk (ring of 4): largest key exponent e over the features
     int rsf[256];                 // each feature's final state scale exponent
     StateBars b;
@@ -1841,9 +1843,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.p_full[i], 1);
-            mbar_init(&B.a_full[i], per_feature ? 4 : 8);
+            mbar_init(&B.a_full[i], 8);
             mbar_init(&B.a_empty[i], 1);
             mbar_init(&B.red_full[i], 8);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&B.pmx_full[i][0], 2);
+            mbar_init(&B.pmx_full[i][1], 2);
         }
         mbar_init(&B.drain[0], 1);
         mbar_init(&B.drain[1], 1);
@@ -2004,73 +2010,80 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const int f = wl + lane;
         bool ok = true;
         if (per_feature) {
-            // r = 256: warpgroup wg owns feature half wg (jobs 2c + wg, always buffer wg) and each
-            // thread one feature over all 128 tokens: phi(k)_f 2^-R_f with R_f from the feature's
-            // own largest exponent in the chunk (hysteresis: next_key_scale), no exchange
-            const int feat = 128 * wg + f, b = wg;
-            const bool live = feat < r;
-            int R = 0;
+            // r = 256: both warpgroups convert every job (c, h) in turn, warpgroup wg tokens
+            // 64 wg .. 64 wg + 63 (lane = feature 128 h + f), so that one half's conversion has
+            // all eight warps while the other half's update and next projection run on the
+            // tensor pipe.  phi(k)_f 2^-R_f with R_f from the feature's own largest exponent
+            // over the chunk's 128 tokens (hysteresis: next_key_scale): the two warps holding a
+            // feature's token halves (warps 4 + q and 8 + q) exchange their maxima
+            const int q4 = warp & 3;
+            int Rh[2] = {0, 0};
             for (int c = 0; c < nchunks && ok; ++c) {
-                const int j = 2 * c + wg;
-                if (!(ok = warp_wait(&B.p_full[b], (j >> 1) & 1))) break;
-                tc_fence_after();
-                const uint32_t col = kColPS + 128 * b;
-                float m = -INFINITY;
-#pragma unroll
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem_addr(tb, wl, col + 32 * piece), v);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    const int b = h;                      // job 2c + h uses buffer (2c + h) & 1
+                    const bool live = 128 * h + f < r;
+                    if (!(ok = warp_wait(&B.p_full[b], c & 1))) break;
+                    tc_fence_after();
+                    const uint32_t col = kColPS + 128 * b + 64 * wg;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem_addr(tb, wl, col), v0);
+                    tmem_ld32(tmem_addr(tb, wl, col + 32), v1);
                     tmem_ld_wait();
+                    float m = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) m = fmaxf(m, __uint_as_float(v[e]));
-                }
-                const int e = (live && m > -1e30f) ? (int)ceilf(m) - 15 : R;
-                const int Rn = next_key_scale(R, e, c == 0);
-                if (live) atomicMax(&s.kmx[c & 3], e);
-                // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp takes the branch
-                // when any of its features changes scale (the others multiply by exactly 1)
-                if (c > 0 && __any_sync(0xffffffffu, Rn != R)) {
-                    // the previous update of this half is complete (this job's projection waited for
-                    // it): the feature's state row times 2^(R - Rn), exactly
-                    const float fct = exp2i(R - Rn);
-                    uint32_t w0[32], w1[32], zc;
-                    const uint32_t sc = kColSS + kNX * wg;
-                    tmem_ld32(tmem_addr(tb, wl, sc), w0);
-                    tmem_ld32(tmem_addr(tb, wl, sc + 32), w1);
-                    tmem_ld1(tmem_addr(tb, wl, sc + 64), zc);
-                    tmem_ld_wait();
+                    for (int e = 0; e < 32; ++e) m = fmaxf(m, fmaxf(__uint_as_float(v0[e]), __uint_as_float(v1[e])));
+                    // slot h: a warp posts the next chunk's maximum of this half only after its
+                    // wait for half h ^ 1, i.e. after the partner has read this one
+                    s.pmx[h][wg][32 * q4 + lane] = m;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&B.pmx_full[q4][h]);
+                    if (!(ok = warp_wait(&B.pmx_full[q4][h], c & 1))) break;
+                    m = fmaxf(m, s.pmx[h][wg ^ 1][32 * q4 + lane]);
+                    const int R = Rh[h];
+                    const int e = (live && m > -1e30f) ? (int)ceilf(m) - 15 : R;
+                    const int Rn = next_key_scale(R, e, c == 0);
+                    if (live) atomicMax(&s.kmx[c & 3], e);
+                    // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp takes the
+                    // branch when any of its features changes scale (the others multiply by exactly 1)
+                    if (c > 0 && __any_sync(0xffffffffu, Rn != R)) {
+                        // the previous update of this half is complete (this job's projection waited
+                        // for it): the feature's state row times 2^(R - Rn), exactly; warpgroup 0
+                        // takes columns 0..31 and z, warpgroup 1 columns 32..63
+                        const float fct = exp2i(R - Rn);
+                        const uint32_t sc = kColSS + kNX * h;
+                        uint32_t w[32], zc = 0u;
+                        tmem_ld32(tmem_addr(tb, wl, sc + 32 * wg), w);
+                        if (wg == 0) tmem_ld1(tmem_addr(tb, wl, sc + 64), zc);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        w0[i] = __float_as_uint(__uint_as_float(w0[i]) * fct);
-                        w1[i] = __float_as_uint(__uint_as_float(w1[i]) * fct);
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * fct);
+                        tmem_st32(tmem_addr(tb, wl, sc + 32 * wg), w);
+                        if (wg == 0) {
+                            asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
+                                         ::"r"(tmem_addr(tb, wl, sc + 64)),
+                                           "r"(__float_as_uint(__uint_as_float(zc) * fct)) : "memory");
+                        }
+                        tmem_st_wait();
                     }
-                    zc = __float_as_uint(__uint_as_float(zc) * fct);
-                    tmem_st32(tmem_addr(tb, wl, sc), w0);
-                    tmem_st32(tmem_addr(tb, wl, sc + 32), w1);
-                    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};"
-                                 ::"r"(tmem_addr(tb, wl, sc + 64)), "r"(zc) : "memory");
-                    tmem_st_wait();
-                }
-                R = Rn;
-                const float fe = (float)R;
-                for (int hh = 0; hh < 2; ++hh) {   // tokens 64 hh ..: read whole, then packed into 64 hh ..
-                    uint32_t v0[32], v1[32], w[32];
-                    tmem_ld32(tmem_addr(tb, wl, col + 64 * hh), v0);
-                    tmem_ld32(tmem_addr(tb, wl, col + 64 * hh + 32), v1);
-                    tmem_ld_wait();
+                    Rh[h] = Rn;
+                    const uint64_t nfe = f32x2_splat(-(float)Rn);
+                    uint32_t w[32];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        w[i] = live ? pack_f16x2(ex2_approx(__uint_as_float(v0[2 * i]) - fe),
-                                                 ex2_approx(__uint_as_float(v0[2 * i + 1]) - fe)) : 0u;
-                        w[16 + i] = live ? pack_f16x2(ex2_approx(__uint_as_float(v1[2 * i]) - fe),
-                                                      ex2_approx(__uint_as_float(v1[2 * i + 1]) - fe)) : 0u;
+                        const uint64_t x0 = f32x2_add(f32x2_of(v0[2 * i], v0[2 * i + 1]), nfe);
+                        const uint64_t x1 = f32x2_add(f32x2_of(v1[2 * i], v1[2 * i + 1]), nfe);
+                        w[i] = live ? pack_f16x2(ex2_approx(f32x2_lo(x0)), ex2_approx(f32x2_hi(x0))) : 0u;
+                        w[16 + i] = live ? pack_f16x2(ex2_approx(f32x2_lo(x1)), ex2_approx(f32x2_hi(x1))) : 0u;
                     }
-                    tmem_st32(tmem_addr(tb, wl, col + 64 * hh), w);
+                    tmem_st32(tmem_addr(tb, wl, col), w);   // tokens 64 wg .. packed into columns 64 wg ..
+                    tmem_st_wait();
+                    warp_arrive(&B.a_full[b], false);
                 }
-                tmem_st_wait();
-                warp_arrive(&B.a_full[b], false);
             }
-            s.rsf[feat] = R;
+            if (wg == 0) {
+                s.rsf[f] = Rh[0];
+                s.rsf[128 + f] = Rh[1];
+            }
         } else {
             // r <= 128 (one half) and element-wise maps: both warpgroups convert every job, tokens
             // 64 wg .. 64 wg + 63; FAVOR+ takes one scale per chunk from the exact maximum over the
