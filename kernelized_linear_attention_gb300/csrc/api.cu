@@ -2,6 +2,10 @@
 // The operation each entry point computes is specified in include/linattn.h.
 #include <algorithm>
 #include <cmath>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "internal.h"
@@ -62,6 +66,50 @@ la_status path_supported(int path, int map, int dk, int dv, int r) {
     return LA_OK;
 }
 
+// Finish time, in chunk times, of nbig blocks of big chunks and nsmall of small
+// chunks started longest first (the order in which the tensor-core kernels map
+// block indices to units) on nsm SMs, each block as its SM frees up and each
+// paying one chunk of set-up.
+int64_t block_makespan(int64_t nbig, int64_t big, int64_t nsmall, int64_t small, int nsm) {
+    std::vector<int64_t> free_at((size_t)std::max(1, nsm), 0);   // min-heap of SM free times
+    int64_t end = 0;
+    for (int64_t i = 0; i < nbig + nsmall; ++i) {
+        std::pop_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+        free_at.back() += (i < nbig ? big : small) + 1;
+        end = std::max(end, free_at.back());
+        std::push_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+    }
+    return end;
+}
+
+// Tensor-core path, equal-length batches: the segment length in chunks whose blocks
+// (pairs (sequence, head) pairs x segments, the last segment of a sequence shorter)
+// finish soonest, among those giving between half a wave and two waves of blocks;
+// ties go to the longer segment.  B=1 H=16 N=65536 on 152 SMs: 54 chunks (144 blocks
+// of 54 and 16 of 26, the second eight of which start where the first eight end)
+// instead of 57 in one wave of 144.  Zero: no candidate (the caller keeps its length).
+int64_t tensor_segment_chunks(int64_t nchunks, int64_t pairs, int nsm) {
+    static std::mutex mu;
+    static std::map<std::tuple<int64_t, int64_t, int>, int64_t> memo;
+    const auto key = std::make_tuple(nchunks, pairs, nsm);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = memo.find(key);
+        if (it != memo.end()) return it->second;
+    }
+    const int64_t min_segs = std::max<int64_t>(1, ceil_div((int64_t)nsm, 2 * pairs));
+    int64_t best = -1, best_lc = 0;
+    for (int64_t lc = ceil_div(nchunks, min_segs); lc >= 1; --lc) {
+        const int64_t segs = ceil_div(nchunks, lc);
+        if (segs * pairs > 2 * (int64_t)nsm) break;   // segs only grows as lc falls
+        const int64_t t = block_makespan((segs - 1) * pairs, lc, pairs, nchunks - (segs - 1) * lc, nsm);
+        if (best < 0 || t < best) { best = t; best_lc = lc; }
+    }
+    std::lock_guard<std::mutex> g(mu);
+    memo[key] = best_lc;
+    return best_lc;
+}
+
 // Segment length and unit bound.  Equal-length batches split every sequence
 // into the same number of segments so that units * heads fills the SMs;
 // packed batches (lengths only known on the device) use one length for all.
@@ -90,6 +138,10 @@ Layout make_layout(int path, bool has_cu, int nseq, int64_t T, int H, int dv, in
             }
         }
         L = std::max<int64_t>(C, ceil_div(ceil_div(len, per), C) * C);
+        if (path == kPathTensor && !bwd) {
+            const int64_t lc = tensor_segment_chunks(ceil_div(len, C), pairs, nsm);
+            if (lc > 0) L = lc * C;
+        }
         U = (int64_t)nseq * ceil_div(len, L);
     } else {
         L = std::max<int64_t>(C, ceil_div(ceil_div(T * H, std::max(1, nsm)), C) * C);

@@ -111,14 +111,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(FwdParams p) {
         p.hdr->range = 0;
     }
 
-    // pass 3: the order in which the tensor-core output kernels take the units.
-    // Packed batches mix short and long units; launched longest first, the
-    // blocks of short units fill in behind the long ones instead of leaving a
-    // tail of long units on a few SMs.  Rank = number of units longer, ties by
-    // index (a permutation); equal-length batches keep 0, 1, ..
+    // pass 3: the order in which the tensor-core kernels take the units.
+    // Packed batches mix short and long units, and an equal-length batch's last
+    // segments are shorter; launched longest first, the blocks of short units
+    // fill in behind the long ones instead of leaving a tail of long units on a
+    // few SMs.  Rank = number of units longer, ties by index (a permutation);
+    // batches of more than kSortUnits units keep 0, 1, ..
     __shared__ int slen[kSortUnits];
     const int nu = min(carry, p.U);
-    const bool sort = p.cu_seqlens != nullptr && nu <= kSortUnits;
+    const bool sort = nu <= kSortUnits;
     if (sort)
         for (int i = threadIdx.x; i < nu; i += blockDim.x) slen[i] = p.units[i].end - p.units[i].start;
     __syncthreads();

@@ -1811,8 +1811,11 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const TcParams tp) {
     const FwdParams& p = tp.p;
-    const int u = blockIdx.x, head = blockIdx.y;
-    if (u >= p.hdr->n_units) return;
+    // one block per (unit, head), rank-major as in the output kernels: all heads of the
+    // longest unit first, so that blocks past the first wave are those of short units
+    const int rank = blockIdx.x / p.H, head = blockIdx.x - rank * p.H;
+    if (rank >= p.hdr->n_units) return;
+    const int u = p.order[rank];
     const Unit un = p.units[u];
     // causal: no later segment adds the last segment of a sequence to its prefix;
     // only a final state or the key exponents of the output kernel need it
@@ -2372,8 +2375,10 @@ cudaError_t tc_state(const FwdParams& p, cudaStream_t s) {
     const bool favor = p.map == LA_MAP_FAVOR;
     cudaError_t e = favor ? set_smem(tc_state_kernel<true>, bytes) : set_smem(tc_state_kernel<false>, bytes);
     if (e != cudaSuccess) return e;
-    if (favor) tc_state_kernel<true><<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
-    else tc_state_kernel<false><<<dim3((unsigned)p.U, (unsigned)p.H), kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    if ((int64_t)p.U * p.H > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)((int64_t)p.U * p.H));
+    if (favor) tc_state_kernel<true><<<grid, kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
+    else tc_state_kernel<false><<<grid, kStateThreads, bytes, s>>>(mk, mv, TcParams{p, 0});
     return cudaGetLastError();
 }
 
