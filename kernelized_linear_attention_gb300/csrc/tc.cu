@@ -646,6 +646,27 @@ __device__ __forceinline__ int next_key_scale(int R, int e, bool first) {
     return (first || e > R || e < R - 8) ? e + 2 : R;
 }
 
+// Largest of N values as a balanced tree: depth log2 N instead of a chain of N dependent
+// maxima, whose latency the few warps of an epilogue cannot hide.
+template <int N>
+__device__ __forceinline__ float max_tree(const float (&x)[N]) {
+    static_assert(N >= 2 && (N & (N - 1)) == 0, "power of two");
+    float a[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) a[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int n = N / 4; n > 0; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n; ++i) a[i] = fmaxf(a[i], a[i + n]);
+    return a[0];
+}
+__device__ __forceinline__ float max_tree32(const uint32_t (&v)[32]) {
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+    return max_tree(x);
+}
+
 // Bounded wait of every lane of a warp; false for the whole warp if any lane timed out.
 // Epilogue warps proceed independently and meet only through mbarriers.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -1629,10 +1650,11 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
                     uint32_t v[32];
                     tmem_ld32(tmem_addr(tb, wl, kColBP + 128 * b + 64 * wg + 32 * piece), v);
                     tmem_ld_wait();
+                    if (favor) {
+                        m = fmaxf(m, max_tree32(v));
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = __uint_as_float(v[e]);
-                        m = fmaxf(m, favor ? x : fabsf(phi_elementwise(x, p.map)));
+                        for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(phi_elementwise(__uint_as_float(v[e]), p.map)));
                     }
                 }
             }
