@@ -1076,8 +1076,12 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         };
         // phi of one 32-column block of a job into dst (FAVOR+): 2^(p - cx), cx = inf past the end
         // (values at or beyond the f16 limit saturate to 65504 and are reported: the largest
-        // exponent argument of the block decides that, one maximum per element)
-        auto favor_phi = [&](const uint32_t (&v)[32], float cx, unsigned char* dst, bool& big) -> float {
+        // exponent argument of the block decides that, one maximum per element).  Keys skip the
+        // check: the chunk's scale R is at least the state kernel's exact e = ceil(max) - 15 over
+        // the same projection, so p - R stays below 15 plus the two passes' rounding difference
+        // for finite keys; the state kernel reports non-finite ones
+        auto favor_phi = [&](const uint32_t (&v)[32], float cx, unsigned char* dst, bool& big,
+                             bool check) -> float {
             uint32_t w[16];
             float mx = -INFINITY;
             uint64_t sum2 = f32x2_splat(0.f);             // two partial sums (even, odd columns)
@@ -1086,7 +1090,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             for (int j = 0; j < 16; ++j) {
                 const uint64_t x2 = f32x2_add(f32x2_of(v[2 * j], v[2 * j + 1]), ncx);
                 const float xa = f32x2_lo(x2), xb = f32x2_hi(x2);
-                mx = fmaxf(mx, fmaxf(xa, xb));
+                if (check) mx = fmaxf(mx, fmaxf(xa, xb));
                 const float a = ex2_approx(xa), b = ex2_approx(xb);
                 sum2 = f32x2_add(sum2, f32x2_of(__float_as_uint(a), __float_as_uint(b)));
                 w[j] = pack_f16x2_sat(a, b);
@@ -1150,7 +1154,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                             for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(v[b][j]));
                         } else if (kind == 2) {
                             if (!(ok = phk_writable(g))) break;
-                            favor_phi(v[b], cxk, s.phk[q & 1], bigk);
+                            favor_phi(v[b], cxk, s.phk[q & 1], bigk, false);
                             warp_arrive(&B.phik_full[g & 1], true);
                         } else if (kind == 3) {
                             if (!have_si) {
@@ -1166,7 +1170,7 @@ tc_causal_out_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                                 have_si = true;
                             }
                             if (!(ok = phq_writable(g))) break;
-                            qs += favor_phi(v[b], cxq, s.phq[g & 1], bigq);
+                            qs += favor_phi(v[b], cxq, s.phq[g & 1], bigq, true);
                             // the row's sum of |phi(q)|, for the bound that scales its scores
                             if (q == nq - 1) s.qsum[slot][half_cols][tr] = qs;
                             warp_arrive(&B.phiq_full[g & 1], true);
@@ -1803,6 +1807,9 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 //   warps 4..11 (PE)  two warpgroups; warpgroup w converts tokens 64w..64w+63 of
 //                     every half (lane = feature)
 constexpr int kStateThreads = 480;
+// Largest key exponent the chunk scales handle (e = ceil(max) - 15 and the rescales stay far
+// inside int and the float exponent); beyond it the state kernel reports LA_DEVERR_RANGE.
+constexpr float kKeyExpLimit = 1.0e9f;
 constexpr int kStateNE = 4;        // NE warps: 3, 12, 13, 14
 constexpr uint32_t kColSS = 0;     // [S|z], 80 columns per half
 constexpr uint32_t kColPS = 160;   // two 128-column projection buffers (exponent, then phi(k)^T in place)
@@ -2043,6 +2050,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             // feature's token halves (warps 4 + q and 8 + q) exchange their maxima
             const int q4 = warp & 3;
             int Rh[2] = {0, 0};
+            // an exponent beyond the integer scale arithmetic is the one way phi(k) 2^-R can leave
+            // the f16 range (the output kernel relies on that and does not check keys): reported
+            // once, after the unit
+            bool kbig = false;
             for (int c = 0; c < nchunks && ok; ++c) {
                 for (int h = 0; h < 2 && ok; ++h) {
                     const int b = h;                      // job 2c + h uses buffer (2c + h) & 1
@@ -2064,6 +2075,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                     if (lane == 0) mbar_arrive(&B.pmx_full[q4][h]);
                     if (!(ok = warp_wait(&B.pmx_full[q4][h], c & 1))) break;
                     m = fmaxf(m, s.pmx[h][wg ^ 1][32 * q4 + lane]);
+                    kbig |= live && !(m <= kKeyExpLimit);
                     const int R = Rh[h];
                     const int e = (live && m > -1e30f) ? (int)ceilf(m) - 15 : R;
                     const int Rn = next_key_scale(R, e, c == 0);
@@ -2109,6 +2121,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 s.rsf[f] = Rh[0];
                 s.rsf[128 + f] = Rh[1];
             }
+            if (__any_sync(0xffffffffu, kbig) && lane == 0) record_range(p.hdr, kRangeK);
         } else {
             // r <= 128 (one half) and element-wise maps: both warpgroups convert every job, tokens
             // 64 wg .. 64 wg + 63; FAVOR+ takes one scale per chunk from the exact maximum over the
@@ -2147,6 +2160,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 }
                 if (!favor && __any_sync(0xffffffffu, big) && lane == 0) record_range(p.hdr, kRangeElementwise);
                 if (favor && !(ok = group_max8(m, s.red, B.red_full, j, 4))) break;
+                // as in the per-feature branch (the maximum is the same in every warp)
+                if (favor && wg == 0 && warp == 4 && lane == 0 && !(m <= kKeyExpLimit)) record_range(p.hdr, kRangeK);
                 const int e = (favor && m > -1e30f) ? (int)ceilf(m) - 15 : 0;
                 const int Rn = favor ? next_key_scale(R, e, c == 0) : 0;
                 if (c > 0 && Rn != R) {

@@ -249,6 +249,21 @@ def test_bad_cu_seqlens_is_reported_not_faulted(la):
         assert torch.all(o == 7.0)     # nothing was computed
 
 
+def test_key_exponent_beyond_the_scale_range_is_reported(la):
+    """Causal FAVOR+ on tensor cores: key projections so large (Omega times 1e12; the queries
+    times 1e-12, so that theirs stay ordinary and raise nothing) that a chunk's key exponent
+    leaves what the power-of-two chunk scales handle; the state pass reports LA_DEVERR_RANGE
+    (3) (the output kernel relies on it and does not check keys), and nothing faults.
+    Realistic keys stay far inside: the every-row tests see no report."""
+    inp = synthetic.random_inputs([700], H=2, dk=64, dv=64, dtype="bf16", seed=31)
+    inp.q = (inp.q * np.float32(1e-12)).astype(np.float32)
+    om = (omega_for(256, 64) * 1e12).astype(np.float32)
+    q, k, v = to_torch(inp)
+    o, ws = la.attention(q, k, v, "favor", causal=True, omega=torch.from_numpy(om).cuda(), return_workspace=True)
+    torch.cuda.synchronize()
+    assert la.la_workspace_error(ws) == 3
+
+
 def test_empty_batch(la):
     z = torch.empty((0, 2, 64), dtype=torch.bfloat16, device="cuda")
     out = la.la_forward_causal(z, z, z, "elu1", nseq=1)
