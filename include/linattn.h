@@ -325,6 +325,21 @@ LA_API la_status la_noalloc_error(int* code, void* stream);
 LA_API la_status la_test_force_wait_timeout(int enable);
 
 /*
+ * la_test_segment_plan - test hook for the planner's host logic (not part of the
+ *   method; no device needed).  For an equal-length batch on the tensor-core path
+ *   whose sequences have `nchunks` chunks of 128 tokens each, with `pairs`
+ *   (sequence, head) pairs on `nsm` SMs: with force_chunks = 0, returns the segment
+ *   length in chunks the forward call uses (0: no candidate, the call then keeps
+ *   one wave of nsm / pairs segments per sequence); with force_chunks > 0, returns
+ *   force_chunks.  *makespan (if not null) receives the simulated finish time, in
+ *   chunk times, of the returned length's blocks: blocks taken longest first, each
+ *   starting as an SM frees up, one chunk of set-up each.  Returns -1 for
+ *   nchunks, pairs or nsm below 1.
+ */
+LA_API int64_t la_test_segment_plan(int64_t nchunks, int64_t pairs, int nsm, int64_t force_chunks,
+                                    int64_t* makespan);
+
+/*
  * la_workspace_bytes - scratch size for a forward call on the current device.
  *   causal: 1 for la_forward_causal, 0 for la_forward_bidir; `has_cu_seqlens`:
  *   1 when a cu_seqlens array will be passed.  Returns 0 for arguments the

@@ -57,6 +57,7 @@ def load_library():
         "la_forward_causal_noalloc": (fwd_args[:15] + [_vp], _c_int),
         "la_noalloc_error": ([ctypes.POINTER(_c_int), _vp], _c_int),
         "la_test_force_wait_timeout": ([_c_int], _c_int),
+        "la_test_segment_plan": ([_c_i64, _c_i64, _c_int, _c_i64, ctypes.POINTER(_c_i64)], _c_i64),
         "la_workspace_bytes": ([_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_int],
                                _c_size),
         "la_check_cu_seqlens": ([_vp, _c_int, _c_i64, _vp], _c_int),
@@ -229,6 +230,16 @@ def la_test_force_wait_timeout(enable: bool) -> None:
     st = load_library().la_test_force_wait_timeout(1 if enable else 0)
     if st != LA_OK:
         raise LinAttnError("la_test_force_wait_timeout", st)
+
+
+def la_test_segment_plan(nchunks: int, pairs: int, nsm: int, force_chunks: int = 0):
+    """Test hook (host only): (segment length in chunks, simulated makespan in chunk times)
+    the tensor-core planner chooses, or evaluates for force_chunks; see include/linattn.h."""
+    ms = _c_i64(0)
+    lc = load_library().la_test_segment_plan(nchunks, pairs, nsm, force_chunks, ctypes.byref(ms))
+    if lc < 0:
+        raise ValueError("la_test_segment_plan: nchunks, pairs and nsm must be at least 1")
+    return int(lc), int(ms.value)
 
 
 def la_noalloc_error(stream=None) -> int:

@@ -99,9 +99,10 @@ int64_t tensor_segment_chunks(int64_t nchunks, int64_t pairs, int nsm) {
     }
     const int64_t min_segs = std::max<int64_t>(1, ceil_div((int64_t)nsm, 2 * pairs));
     int64_t best = -1, best_lc = 0;
-    for (int64_t lc = ceil_div(nchunks, min_segs); lc >= 1; --lc) {
+    for (int64_t lc = nchunks; lc >= 1; --lc) {
         const int64_t segs = ceil_div(nchunks, lc);
         if (segs * pairs > 2 * (int64_t)nsm) break;   // segs only grows as lc falls
+        if (segs < min_segs) continue;
         const int64_t t = block_makespan((segs - 1) * pairs, lc, pairs, nchunks - (segs - 1) * lc, nsm);
         if (best < 0 || t < best) { best = t; best_lc = lc; }
     }
@@ -520,6 +521,19 @@ la_status la_workspace_error(const void* workspace, int* code, void* stream) {
 
 la_status la_test_force_wait_timeout(int enable) {
     return la::tc_force_wait_timeout(enable ? 1 : 0) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+int64_t la_test_segment_plan(int64_t nchunks, int64_t pairs, int nsm, int64_t force_chunks, int64_t* makespan) {
+    if (nchunks < 1 || pairs < 1 || nsm < 1) return -1;
+    const int64_t lc = force_chunks > 0 ? force_chunks : tensor_segment_chunks(nchunks, pairs, nsm);
+    if (makespan) {
+        *makespan = 0;
+        if (lc > 0) {
+            const int64_t segs = ceil_div(nchunks, lc);
+            *makespan = block_makespan((segs - 1) * pairs, lc, pairs, nchunks - (segs - 1) * lc, nsm);
+        }
+    }
+    return lc;
 }
 
 la_status la_orthogonal_features(const double* gauss_blocks, const double* gauss_lengths, int r, int d,
