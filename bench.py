@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -150,10 +151,24 @@ def measured_peaks() -> dict:
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def code_only(text: str) -> str:
+    """C++/CUDA source with its comments removed and whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(path: str, phase: str) -> str:
-    p = os.path.join(ROOT, "kernelized_linear_attention_gb300", "csrc", KERNEL_SOURCES[path][phase])
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Fingerprint of a kernel's source as compiled: its .cu file and every header of the
+    library, comments and whitespace removed (an edit of comments alone leaves a capture
+    valid; any change of code, in the file or a header, invalidates it)."""
+    csrc = os.path.join(ROOT, "kernelized_linear_attention_gb300", "csrc")
+    names = [KERNEL_SOURCES[path][phase]] + sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(csrc, n)) as f:
+            h.update(code_only(f.read()).encode())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(path: str, phase: str, workload: str):
