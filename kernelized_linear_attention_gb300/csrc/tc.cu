@@ -5,31 +5,40 @@
 //
 //   FAVOR+ projection   P = X Omega'^T with Omega' = log2(e) Omega held as two
 //                       bf16 parts (hi + lo, ~16 significant bits), so the
-//                       exponent carries no bf16 rounding of Omega; epilogue
-//                       phi = 2^(P - c), c = log2(e) |x|^2/2 + log2(sqrt r)
-//                       ("The Kernel Zoo" §4.2, "Performer" §2 Step 3), rounded
-//                       to bf16 as the operand of the next products
-//   ELU+1 / identity    phi computed element-wise from the staged tile
+//                       exponent carries no bf16 rounding of Omega; one more K
+//                       step adds each row's offset -c, c = log2(e) |x|^2/2 +
+//                       log2(sqrt r) ("The Kernel Zoo" §4.2, "Performer" §2
+//                       Step 3); the epilogue writes phi = 2^(P - c) times an
+//                       exact power of two as f16, the operand of the products
+//   ELU+1 / identity    the same MMA with an identity "projection", phi
+//                       element-wise in the epilogue
 //   causal scores       A (+)= Phi_Q Phi_K^T                  (TMEM, fp32)
-//   cross-chunk readout O (+)= Phi_Q [S|z]  (state before this chunk, bf16;
-//                       hi + lo parts in the bidirectional kernel)
+//   cross-chunk readout O_x (+)= Phi_Q [S|z]  (state before this chunk, an f16
+//                       copy with z also as its f16 remainder)
 //   state update        [S|z] += Phi_K^T [V|1]                (TMEM, fp32, carried)
-//   causal in-chunk     O += tril(A) [V|1]  (diagonal included, "The Kernel Zoo" §1.3),
-//                       A as bf16 hi + lo parts from tensor memory
-//   store               out = O[:, :64] / max(O[:, 64], eps)  ("Performer" §3 sketch clamp)
+//   causal in-chunk     O_in = tril(A) [V|1]  (diagonal included, "The Kernel Zoo"
+//                       §1.3), A as f16 from tensor memory
+//   store               out = num / max(den, eps)  ("Performer" §3 sketch clamp),
+//                       num | den = 2^t O_in + 2^g O_x in fp32
 //
-// The ones column of [V|1] makes column 64 of every state z and of every
-// numerator the denominator, so numerator and denominator see the same
-// rounded weights.  The causal kernel processes the feature dimension in
-// halves of 128 (keys) and quarters of 64 (queries) so that its operands fit
-// in shared memory; the bidirectional output kernel reads the whole-sequence
-// state; the state kernel only projects k and updates the state.
+// Every product is tcgen05.mma kind::f16 with both operands f16 and fp32
+// accumulation; each operand carries an exact power-of-two scale (per query row,
+// per key chunk or feature, per score row, per state copy) that keeps the values
+// that matter normal f16 numbers and is undone in fp32.  The ones column of
+// [V|1] makes column 64 of every state z and of every numerator the denominator,
+// so numerator and denominator see the same rounded weights.  The causal kernel
+// processes the feature dimension in halves of 128 (keys) and quarters of 64
+// (queries) so that its operands fit in shared memory; the bidirectional output
+// kernel reads the whole-sequence state; the state kernel only projects k and
+// updates the state.
 //
 // Shared-memory operands use the 128-byte-swizzled [rows][64] layout of
-// tc_ptx.cuh.  One thread issues TMA and MMA; all 4 warps run the epilogues
-// (warp w owns TMEM lanes 32w..32w+31).  Waits are bounded: a wait that runs
-// out records LA_DEVERR_WAIT_TIMEOUT in the workspace, drains outstanding
-// MMAs, frees TMEM and returns.
+// tc_ptx.cuh.  The kernels are warp-specialised (each kernel's roles are listed
+// above it): one elected thread issues the TMA loads, one the projection MMAs and
+// one the product MMAs; epilogue warps own TMEM lanes 32 (w mod 4) .. + 31.  Waits
+// are bounded: a wait that runs out records LA_DEVERR_WAIT_TIMEOUT in the
+// workspace, and the CTA drains its outstanding copies and MMAs, frees TMEM and
+// returns.
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -540,9 +549,10 @@ __device__ float v_tile_to_f16(unsigned char* tile, int row0, int nrows, int nva
 //   phi(k)   2^-e_c for the chunk (e_c from the state kernel: the chunk's largest
 //            key feature lands in (2^14, 2^15]); the state [S|z] is held in TMEM
 //            times 2^-e_c and rescaled exactly when the chunk's e changes;
-//   phi(q)   2^-s_i per query row (s_i from the row's first 64 features: their
-//            largest becomes 2^-10, later ones may exceed it by up to 2^26); the
-//            factor is common to the row's numerator and denominator;
+//   phi(q)   2^-s_i per query row (s_i from the row's largest exponent over all r
+//            features, taken from hi-only projections, so that its largest feature
+//            lies just below 2^14); the factor is common to the row's numerator
+//            and denominator;
 //   scores   A_i. 2^-t_i per row (largest in (2^13, 2^14]), causal mask applied;
 //   state    the copy the readout reads is [S|z] 2^-g_c (largest in (2^13, 2^14]),
 //            z also as its f16 remainder;
@@ -1466,16 +1476,17 @@ __device__ __forceinline__ float phi_elementwise(float x, int map) {
 
 // ---------------------------------------------------------------------------
 // Bidirectional output kernel (warp-specialised): out = phi(q)^T [S|z] / max(phi(q)^T z, eps)
-// with [S|z] the whole-sequence state (bf16 hi + lo in shared memory)
+// with [S|z] the whole-sequence state (in shared memory as f16 times 2^-g, z also as its
+// f16 remainder)
 // ---------------------------------------------------------------------------
-// TMEM: two fp32 projection buffers [0, 256) (one 128-feature half each), two bf16
+// TMEM: two fp32 projection buffers [0, 256) (one 128-feature half each), two f16
 // phi(q) buffers [256, 384), O = numerator | denominator [384, 464).
 // Roles (544 threads):
 //   warp 0 lane 0      TMA: the q tile of each chunk into two stages (and L2 prefetch)
 //   warp 1             projection MMAs (elected lane; warp 1 owns the TMEM allocation):
 //                      Q Omega'^T (hi, lo) plus one K step adding each query's
 //                      exponent offset (FAVOR+), or Q itself (identity, element-wise maps)
-//   warp 2             readout MMAs: O (+)= phi(q) [S|z]_hi + phi(q) [S|z]_lo, A from TMEM
+//   warp 2             readout MMAs: O (+)= phi(q) [S|z]_f16 (one MMA per K step), A from TMEM
 //   warps 3, 12 (NE)   per-query exponent offsets into the bias operand (FAVOR+)
 //   warps 4..11 (PE)   phi(q) of each half: warpgroup w converts features 64w.. (lane = query)
 //   warps 13..16 (OE)  out rows = O[0..63] / max(O[64], eps), after releasing O
@@ -1778,14 +1789,15 @@ tc_bidir_out_kernel(const __grid_constant__ CUtensorMap map_q, const TcParams tp
 // columns = tokens); one more K step adds each token's exponent offset -(log2(e)
 // |k|^2 / 2 + log2(sqrt r)) as bf16 hi + lo, so that phi = 2^P^T element-wise.
 //
-// fp16 features with an exact power-of-two scale per (chunk, feature half): the
-// PE warps first reduce the maximum of the half's 128 x 128 exponents, take
-// e = ceil(max) - 15, and write phi(k)^T 2^-e as f16 (11 significant bits; every
-// feature within 2^-29 of the chunk's largest is a normal number) back into the
-// buffer it came from.  The state of each half is accumulated in TMEM in the
-// scale 2^-e of the latest chunk: when e changes, the PE rescales that half
-// exactly (a power of two) before the chunk's update, and the state leaves in
-// true scale.  V is converted to f16 in place by the NE warps (values beyond
+// fp16 features with exact power-of-two scales: the PE warps reduce the largest
+// exponent, take e = ceil(max) - 15 and write phi(k)^T 2^-R as f16 (11 significant
+// bits) back into the buffer it came from, R following e with hysteresis
+// (next_key_scale).  For r = 256 the scale is per feature (its own maximum over
+// the chunk's 128 tokens, the two warps holding its token halves exchanging
+// theirs); for r <= 128 and the element-wise maps one scale per chunk (the
+// maximum over all eight warps).  The state is accumulated in TMEM in the latest
+// scale: when it changes, the PE rescales the state rows exactly (a power of two)
+// before the chunk's update, and the state leaves in true scale.  V is converted to f16 in place by the NE warps (values beyond
 // 65504 are clamped and reported as LA_DEVERR_RANGE); [S|z] += phi(k)^T [V|1]
 // takes its A operand from TMEM and its B operand from V with an f16 ones tile as
 // the second 64-column atom, so z (column 64) comes from the same features as S.
